@@ -1,0 +1,201 @@
+"""GB300 dynamic draft-tree hot path: Python binding of the libdt C ABI.
+
+Every function here has the name of the C entry point it calls and only
+marshals arguments (torch CUDA tensors -> device pointers, the current CUDA
+stream); all work runs in libdt's sm_103a kernels. See include/dt.h for the
+semantics, layouts and error behaviour of each call.
+"""
+import ctypes
+
+import torch
+
+from ._lib import (lib, check, DtError, DtConfig, DtTreeView, DtPruneParams, DtPruneOut, DtTemplate,  # noqa
+                   DtTreeMeta, EXPORTS, DT_OK, DT_ERR_ARG, DT_ERR_CUDA, DT_ERR_DEVICE,
+                   DT_ERR_DEVICE_TIMEOUT, DT_BF16, DT_F32, DT_GREEDY, DT_SAMPLE,
+                   DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT,
+                   DT_DEV_BAD_LOGITS, DT_DEV_BAD_TOKEN, DT_DEV_BAD_TREE, DT_DEV_TIMEOUT, DT_DEV_INTERNAL,
+                   DT_FLAG_TEST_TIMEOUT, LIB_PATH)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensor required")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor required")
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+
+
+class Handle:
+    """An open libdt handle (one draft tree in flight) and its configuration."""
+
+    def __init__(self, B_max, V, K, W, D_max, P_max, dtype=DT_BF16, flags=0):
+        self.cfg = DtConfig(B_max, V, K, W, D_max, P_max, dtype, flags)
+        self.h = ctypes.c_void_p()
+        check(lib.dt_create(ctypes.byref(self.cfg), ctypes.byref(self.h)))
+
+    def close(self):
+        if self.h:
+            check(lib.dt_destroy(self.h))
+            self.h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class _DevArray:
+    """Zero-copy view of a library-owned device array, for torch.as_tensor."""
+
+    def __init__(self, ptr, shape, typestr):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (ptr, True), "version": 3, "strides": None}
+
+
+def dt_create(B_max, V, K, W, D_max, P_max, dtype=DT_BF16, flags=0):
+    return Handle(B_max, V, K, W, D_max, P_max, dtype, flags)
+
+
+def dt_destroy(h):
+    h.close()
+
+
+def dt_get_tree(h):
+    """The tree arrays as torch tensors viewing the handle's workspace (valid until the next call)."""
+    v = DtTreeView()
+    check(lib.dt_get_tree(h.h, ctypes.byref(v)))
+    Bm, N, D, LW, W = h.cfg.B_max, v.N, v.D_max, v.LW, v.W
+
+    def view(ptr, shape, ts):
+        return torch.as_tensor(_DevArray(ptr, shape, ts), device="cuda")
+
+    return dict(B=v.B, K=v.K, W=W, D_max=D, N=N, LW=LW, depth=v.depth,
+                token=view(v.token, (Bm, N), "<i4"), parent=view(v.parent, (Bm, N), "<i4"),
+                node_depth=view(v.node_depth, (Bm, N), "<i4"), logc=view(v.logc, (Bm, N), "<f4"),
+                value=view(v.value, (Bm, N), "<f4"),
+                layer_order=view(v.layer_order, (Bm, D + 1, LW), "<i4"),
+                layer_count=view(v.layer_count, (Bm, D + 1), "<i4"),
+                frontier=view(v.frontier, (Bm, W), "<i4"),
+                frontier_count=view(v.frontier_count, (Bm,), "<i4"))
+
+
+def dt_get_status(h, stream=None):
+    """Synchronises the stream; returns the device status bits (0 = clean)."""
+    bits = ctypes.c_int32(0)
+    rc = lib.dt_get_status(h.h, _stream(stream), ctypes.byref(bits))
+    if rc not in (DT_OK, DT_ERR_DEVICE, DT_ERR_DEVICE_TIMEOUT):
+        check(rc)
+    return bits.value
+
+
+def dt_clear_status(h, stream=None):
+    check(lib.dt_clear_status(h.h, _stream(stream)))
+
+
+def dt_tree_reset(h, root_token, stream=None):
+    check(lib.dt_tree_reset(h.h, root_token.numel(), _ptr(root_token), _stream(stream)))
+
+
+def dt_select_frontier(h, width=None, stop=None, frontier_token=None, stream=None):
+    wl = 0 if width is None else width.numel()
+    check(lib.dt_select_frontier(h.h, _ptr(width), wl, _ptr(stop), _ptr(frontier_token), _stream(stream)))
+
+
+def dt_expand_layer(h, logits, F, ld=None, stream=None):
+    ld = logits.shape[-1] if ld is None else ld
+    check(lib.dt_expand_layer(h.h, _ptr(logits), ld, F, _stream(stream)))
+
+
+def dt_cast_prune(h, policy, params, out, stream=None):
+    check(lib.dt_cast_prune(h.h, policy, ctypes.byref(params), ctypes.byref(out), _stream(stream)))
+
+
+def dt_rerank(h, m, m_cap, selected, stream=None):
+    ml = 0 if m is None else m.numel()
+    check(lib.dt_rerank(h.h, _ptr(m), ml, m_cap, _ptr(selected), _stream(stream)))
+
+
+def dt_graft_retrieve(h, M, m_draft, K_total, template, R_cap, ret_token, ret_parent, ret_count, stream=None):
+    check(lib.dt_graft_retrieve(h.h, _ptr(M), _ptr(m_draft), K_total, ctypes.byref(template.c), R_cap,
+                                _ptr(ret_token), _ptr(ret_parent), _ptr(ret_count), _stream(stream)))
+
+
+def dt_build_tree_meta(h, selected, m_cap, meta, pos_offset=None, ret_token=None, ret_parent=None,
+                       ret_count=None, R_cap=0, stream=None):
+    check(lib.dt_build_tree_meta(h.h, _ptr(selected), m_cap, _ptr(ret_token), _ptr(ret_parent),
+                                 _ptr(ret_count), R_cap, _ptr(pos_offset), ctypes.byref(meta.c),
+                                 _stream(stream)))
+
+
+def dt_verify(h, meta, logits, mode, seed, round_, accept_len, accept_path, bonus, top8=None, ld=None,
+              stream=None):
+    ld = logits.shape[-1] if ld is None else ld
+    check(lib.dt_verify(h.h, ctypes.byref(meta.c), _ptr(logits), ld, mode, seed, round_, _ptr(accept_len),
+                        _ptr(accept_path), _ptr(bonus), _ptr(top8), _stream(stream)))
+
+
+def dt_adj_update(h, M, meta, top8, stream=None):
+    check(lib.dt_adj_update(h.h, _ptr(M), ctypes.byref(meta.c), _ptr(top8), _stream(stream)))
+
+
+class Meta:
+    """Caller-owned device arrays of a flattened verify tree (dt_tree_meta)."""
+
+    def __init__(self, B, P, D_path, device="cuda"):
+        i32 = dict(dtype=torch.int32, device=device)
+        self.P, self.D_path = P, D_path
+        self.tokens = torch.empty((B, P), **i32)
+        self.parents = torch.empty((B, P), **i32)
+        self.depth = torch.empty((B, P), **i32)
+        self.node_id = torch.empty((B, P), **i32)
+        self.mask = torch.empty((B, P, P), dtype=torch.uint8, device=device)
+        self.position_ids = torch.empty((B, P), **i32)
+        self.retrieve = torch.empty((B, P, D_path), **i32)
+        self.n_leaves = torch.empty((B,), **i32)
+        self.n_pos = torch.empty((B,), **i32)
+        self.c = DtTreeMeta(P, D_path, *[_ptr(t) for t in (self.tokens, self.parents, self.depth, self.node_id,
+                                                            self.mask, self.position_ids, self.retrieve,
+                                                            self.n_leaves, self.n_pos)])
+
+    def numpy(self):
+        return {k: getattr(self, k).cpu().numpy() for k in
+                ("tokens", "parents", "depth", "node_id", "mask", "position_ids", "retrieve", "n_leaves",
+                 "n_pos")}
+
+
+def make_prune_params(S_T=None, S_D=None, L=512.0, n0=0, C1=0.0, C2=0.0, C3=0.0, R=3, width_cap=1, m_cap=1,
+                      D_max=1, ckpt_layers=(), tau=(), k_draft=(), K_total=0):
+    """dt_prune_params from device tables (float64 tensors [M_rows][N_cols]) and scalars."""
+    p = DtPruneParams()
+    p.S_T = _ptr(S_T)
+    p.S_D = _ptr(S_D)
+    if S_T is not None:
+        p.M_rows, p.N_cols = S_T.shape
+    p.L, p.n0, p.C1, p.C2, p.C3, p.R = L, n0, C1, C2, C3, R
+    p.width_cap, p.m_cap, p.D_max = width_cap, m_cap, D_max
+    p.n_ckpt = len(ckpt_layers)
+    for i, (c, t, k) in enumerate(zip(ckpt_layers, tau, k_draft)):
+        p.ckpt_layer[i], p.tau[i], p.k_draft[i] = c, t, k
+    p.K_total = K_total
+    return p
+
+
+def make_prune_out(width=None, stop=None, m=None, stage=None):
+    return DtPruneOut(_ptr(width), _ptr(stop), _ptr(m), _ptr(stage))
+
+
+class Template:
+    """Host-side retrieval template (parent, rank) in breadth-first order."""
+
+    def __init__(self, parent, rank):
+        self.n = len(parent)
+        self._p = (ctypes.c_int32 * max(1, self.n))(*parent)
+        self._r = (ctypes.c_int32 * max(1, self.n))(*rank)
+        self.c = DtTemplate(self.n, ctypes.cast(self._p, ctypes.c_void_p), ctypes.cast(self._r, ctypes.c_void_p))

@@ -1,0 +1,213 @@
+// Internal declarations shared by the libdt translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dt.h"
+
+namespace dt {
+
+constexpr int kMaxK = 32;
+constexpr int kMaxW = 32;
+constexpr int kMaxD = 16;
+constexpr int kMaxP = 512;
+constexpr int kMaxFifo = 16;
+constexpr int kRowThreads = 256;
+constexpr int kTileBytes = 16384;   // one TMA bulk tile
+constexpr int kStages = 4;          // tiles in flight per CTA
+constexpr int kCandCap = 1024;      // candidate keys buffered per CTA
+
+// Per-(row, segment) partial result of a row scan.
+struct Partial {
+  float m;           // segment max (or -inf)
+  int32_t pad;
+  double s;          // sum exp(x - m) over the segment
+  uint64_t keys[kMaxK];  // segment top-K keys, descending; 0 = empty
+};
+
+// Per-row statistics left by the verify row pass.
+struct RowStat {
+  float m;       // row max
+  int32_t amax;  // argmax token (lowest id among maxima)
+  double s;      // sum exp(x - m)
+};
+
+// CAST running state of the tree in flight.
+struct CastState {
+  double fifo[kMaxFifo];
+  int32_t fifo_len;
+  int32_t pad;
+  double u_prev;
+  int64_t ctx_sum;
+  double u_layer;     // u_{n_d} of the newest pruned layer
+};
+
+// Sampled walk result handed to the bonus kernel.
+struct WalkState {
+  int32_t cur;        // position whose residual is sampled
+  int32_t n_rej;      // rejected tokens at that position
+  int32_t rej[kMaxP];
+};
+
+struct Workspace {
+  // tree
+  int32_t* token;
+  int32_t* parent;
+  int32_t* node_depth;
+  float* logc;
+  float* value;
+  int32_t* layer_order;
+  int32_t* layer_count;
+  int32_t* frontier;
+  int32_t* frontier_count;
+  // row scans
+  Partial* partials;
+  int64_t partial_cap;
+  int32_t* row_counter;
+  int64_t row_counter_cap;
+  int32_t* req_counter;
+  RowStat* row_stats;
+  // selection scratch
+  double* sorted_lin;    // [B_max][P_max] linear values of each request's top nodes
+  int32_t* sorted_cnt;   // [B_max]
+  CastState* cast;
+  WalkState* walk;
+  unsigned long long* bonus_key;  // [B_max]
+  int32_t* bonus_counter;         // [B_max]
+  int32_t* status;
+};
+
+}  // namespace dt
+
+struct dt_handle {
+  dt_config cfg;
+  int32_t N;       // nodes per request
+  int32_t LW;      // slots per layer
+  int32_t B;       // batch of the tree in flight
+  int32_t depth;   // layers built
+  int num_sms;
+  dt::Workspace ws;
+  void* alloc;     // single device allocation backing the workspace
+  size_t alloc_bytes;
+};
+
+namespace dt {
+
+// ---- launchers implemented in the kernel translation units (host functions) ----
+cudaError_t launch_tree_reset(dt_handle* h, const int32_t* root, cudaStream_t s);
+cudaError_t launch_select_frontier(dt_handle* h, const int32_t* width, int width_len, const int32_t* stop,
+                                   int32_t* frontier_token, cudaStream_t s);
+cudaError_t launch_expand(dt_handle* h, const void* logits, int64_t ld, int F, cudaStream_t s);
+cudaError_t launch_cast_prune(dt_handle* h, int policy, const dt_prune_params* p, const dt_prune_out* out,
+                              cudaStream_t s);
+cudaError_t launch_rerank(dt_handle* h, const int32_t* m, int m_len, int m_cap, int32_t* selected,
+                          cudaStream_t s);
+cudaError_t launch_graft_retrieve(dt_handle* h, const int32_t* M, const int32_t* m_draft, int K_total,
+                                  const dt_template* tpl, int R_cap, int32_t* ret_token,
+                                  int32_t* ret_parent, int32_t* ret_count, cudaStream_t s);
+cudaError_t launch_build_meta(dt_handle* h, const int32_t* selected, int m_cap, const int32_t* ret_token,
+                              const int32_t* ret_parent, const int32_t* ret_count, int R_cap,
+                              const int32_t* pos_offset, const dt_tree_meta* meta, cudaStream_t s);
+cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int mode,
+                          uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path,
+                          int32_t* bonus, int32_t* top8, cudaStream_t s);
+cudaError_t launch_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta, const int32_t* top8,
+                              cudaStream_t s);
+
+// Segments per row for a row-scan launch of `rows` rows of V elements.
+int choose_segments(const dt_handle* h, int64_t rows, int64_t V, int elt_bytes);
+
+}  // namespace dt
+
+// ---------------------------------------------------------------- device helpers ----
+#ifdef __CUDACC__
+namespace dt {
+
+__device__ __forceinline__ uint32_t f2ord(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;  // -0 orders as +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ord2f(uint32_t o) {
+  uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+  return __uint_as_float(u);
+}
+// Total-order key: larger key = larger value, then smaller id. 0 is below every real key.
+__device__ __forceinline__ uint64_t make_key(float v, uint32_t id) {
+  return ((uint64_t)f2ord(v) << 32) | (uint64_t)(~id);
+}
+__device__ __forceinline__ float key_value(uint64_t k) { return ord2f((uint32_t)(k >> 32)); }
+__device__ __forceinline__ uint32_t key_id(uint64_t k) { return ~(uint32_t)k; }
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// 2^x on the SFU (ex2.approx, flushes subnormal results to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void set_status(int32_t* status, int32_t bits) { atomicOr(status, bits); }
+
+__device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
+  uint32_t lo = __shfl_sync(0xFFFFFFFFu, (uint32_t)v, src);
+  uint32_t hi = __shfl_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), src);
+  return ((uint64_t)hi << 32) | lo;
+}
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+  uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)v, m);
+  uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), m);
+  return ((uint64_t)hi << 32) | lo;
+}
+
+// Descending bitonic sort of one 64-bit key per lane across a warp.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t k) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      uint64_t o = shfl_xor_u64(k, stride);
+      bool up = ((lane & size) == 0);        // this block sorts descending
+      bool lower = ((lane & stride) == 0);   // lower index of the pair
+      bool take_max = (lower == up);
+      k = take_max ? (k > o ? k : o) : (k < o ? k : o);
+    }
+  }
+  return k;
+}
+
+// Philox4x32-10 (Salmon et al., SC'11), written from the published round function.
+struct Philox4 {
+  uint32_t v[4];
+};
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                 uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+  }
+  Philox4 out;
+  out.v[0] = c0;
+  out.v[1] = c1;
+  out.v[2] = c2;
+  out.v[3] = c3;
+  return out;
+}
+
+}  // namespace dt
+#endif

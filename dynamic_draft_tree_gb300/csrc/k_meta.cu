@@ -1,0 +1,201 @@
+// Flattening and tree-attention metadata.
+//
+// EAGLE-2 page §"重排阶段": the selected connected subtree is flattened to a token list and a
+// tree attention mask lets each node see only its ancestors. Graft page step (3): the kept draft
+// nodes and the grafted retrieval nodes are flattened to K_max tokens with standard position IDs,
+// ancestor mask and candidate path (retrieve) indices.
+#include <algorithm>
+
+#include "dt_internal.cuh"
+
+namespace dt {
+namespace {
+
+struct MetaArgs {
+  Workspace ws;
+  int N, m_cap, R_cap;
+  const int32_t* selected;
+  const int32_t* ret_token;
+  const int32_t* ret_parent;
+  const int32_t* ret_count;
+  const int32_t* pos_offset;
+  dt_tree_meta meta;
+};
+
+constexpr int kMetaThreads = 512;
+constexpr int kWords = kMaxP / 32;
+
+// One CTA per request.
+__global__ void __launch_bounds__(kMetaThreads) build_meta_kernel(MetaArgs a) {
+  extern __shared__ __align__(16) int16_t pos_of[];  // [N] node id -> position, -1 if not placed
+  __shared__ int32_t tok[kMaxP], par[kMaxP], dep[kMaxP], nid[kMaxP];
+  __shared__ uint32_t anc[kMaxP][kWords];
+  __shared__ int32_t has_child[kMaxP];
+  __shared__ int32_t leaf_idx[kMaxP];
+  __shared__ int32_t s_nsel, s_npos, s_bad;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const Workspace& ws = a.ws;
+  const int P = a.meta.P;
+  const int Dp = a.meta.D_path;
+
+  for (int i = tid; i < a.N; i += blockDim.x) pos_of[i] = -1;
+  if (tid == 0) {
+    int n = 0;
+    while (n < a.m_cap && a.selected[(int64_t)b * a.m_cap + n] >= 0) ++n;
+    s_nsel = n;
+    int rc = a.ret_count ? a.ret_count[b] : 0;
+    rc = max(0, min(rc, a.R_cap));
+    s_npos = min(P, 1 + n + rc);
+    s_bad = (1 + n + rc > P) ? 1 : 0;  // positions would not fit: flagged, the extra ones dropped
+  }
+  for (int i = tid; i < P; i += blockDim.x) has_child[i] = 0;
+  __syncthreads();
+  const int nsel = s_nsel, npos = s_npos;
+  if (tid == 0) pos_of[0] = 0;
+  for (int j = tid; j < nsel; j += blockDim.x) {
+    const int id = a.selected[(int64_t)b * a.m_cap + j];
+    if (id > 0 && id < a.N) pos_of[id] = (int16_t)(1 + j);
+  }
+  __syncthreads();
+
+  // token, parent position, node id
+  for (int p = tid; p < P; p += blockDim.x) {
+    int t = -1, pp = -1, id = -1;
+    if (p == 0) {
+      t = ws.token[(int64_t)b * a.N];
+      id = 0;
+    } else if (p <= nsel) {
+      id = a.selected[(int64_t)b * a.m_cap + (p - 1)];
+      if (id > 0 && id < a.N) {
+        t = ws.token[(int64_t)b * a.N + id];
+        const int parent_id = ws.parent[(int64_t)b * a.N + id];
+        pp = parent_id >= 0 ? pos_of[parent_id] : -1;
+        if (pp < 0 || pp >= p) {  // selection is not parent-closed
+          s_bad = 1;
+          pp = 0;
+        }
+      } else {
+        s_bad = 1;
+        pp = 0;
+      }
+    } else if (p < npos) {
+      const int u = p - nsel - 1;
+      t = a.ret_token[(int64_t)b * a.R_cap + u];
+      const int rp = a.ret_parent[(int64_t)b * a.R_cap + u];
+      pp = rp < 0 ? 0 : nsel + 1 + rp;
+      if (pp >= p) {
+        s_bad = 1;
+        pp = 0;
+      }
+    }
+    tok[p] = t;
+    par[p] = pp;
+    nid[p] = id;
+  }
+  __syncthreads();
+  // depth and ancestor bitset by walking to the root (parents precede children)
+  for (int p = tid; p < P; p += blockDim.x) {
+#pragma unroll
+    for (int w = 0; w < kWords; ++w) anc[p][w] = 0u;
+    if (p >= npos) {
+      dep[p] = -1;
+      continue;
+    }
+    int q = p, d = 0;
+    while (true) {
+      anc[p][q >> 5] |= 1u << (q & 31);
+      if (q == 0) break;
+      q = par[q];
+      ++d;
+      if (d > kMaxP) {
+        s_bad = 1;
+        break;
+      }
+    }
+    dep[p] = d;
+    if (p > 0) atomicOr(&has_child[par[p]], 1);
+  }
+  __syncthreads();
+  // leaves in increasing position: exclusive prefix count of leaf flags (serial over <= 512 flags
+  // by warp 0 with ballots)
+  if (tid < 32) {
+    int base = 0;
+    for (int c = 0; c < P; c += 32) {
+      const int p = c + tid;
+      const bool leaf = p < npos && !has_child[p];
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, leaf);
+      if (leaf) leaf_idx[p] = base + __popc(m & ((1u << tid) - 1u));
+      else if (p < P) leaf_idx[p] = -1;
+      base += __popc(m);
+    }
+    if (tid == 0) a.meta.n_leaves[b] = base;
+  }
+  __syncthreads();
+
+  // ---- outputs ----
+  const int64_t rb = (int64_t)b * P;
+  const int po = a.pos_offset ? a.pos_offset[b] : 0;
+  for (int p = tid; p < P; p += blockDim.x) {
+    a.meta.tokens[rb + p] = p < npos ? tok[p] : -1;
+    a.meta.parents[rb + p] = p < npos ? par[p] : -1;
+    a.meta.depth[rb + p] = dep[p];
+    a.meta.node_id[rb + p] = p < npos ? nid[p] : -1;
+    a.meta.position_ids[rb + p] = p < npos ? po + dep[p] : -1;
+  }
+  // mask [P][P] bytes
+  uint8_t* mask = a.meta.mask + rb * P;
+  const int64_t mbytes = (int64_t)P * P;
+  for (int64_t e = tid; e < mbytes; e += blockDim.x) {
+    const int i = (int)(e / P), j = (int)(e % P);
+    mask[e] = (uint8_t)((anc[i][j >> 5] >> (j & 31)) & 1u);
+  }
+  // retrieve rows
+  int32_t* ret = a.meta.retrieve + rb * Dp;
+  for (int64_t e = tid; e < (int64_t)P * Dp; e += blockDim.x) ret[e] = -1;
+  __syncthreads();
+  for (int p = tid; p < npos; p += blockDim.x) {
+    const int li = leaf_idx[p];
+    if (li < 0) continue;
+    const int d = dep[p];
+    if (d + 1 > Dp) {
+      s_bad = 1;
+      continue;
+    }
+    int q = p;
+    for (int k = d; k >= 0; --k) {
+      ret[(int64_t)li * Dp + k] = q;
+      q = par[q];
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    a.meta.n_pos[b] = npos;
+    if (s_bad) set_status(ws.status, DT_DEV_BAD_TREE);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_build_meta(dt_handle* h, const int32_t* selected, int m_cap, const int32_t* ret_token,
+                              const int32_t* ret_parent, const int32_t* ret_count, int R_cap,
+                              const int32_t* pos_offset, const dt_tree_meta* meta, cudaStream_t s) {
+  MetaArgs a;
+  a.ws = h->ws;
+  a.N = h->N;
+  a.m_cap = m_cap;
+  a.R_cap = R_cap;
+  a.selected = selected;
+  a.ret_token = ret_token;
+  a.ret_parent = ret_parent;
+  a.ret_count = ret_token ? ret_count : nullptr;
+  a.pos_offset = pos_offset;
+  a.meta = *meta;
+  const size_t smem = ((size_t)h->N * sizeof(int16_t) + 15) / 16 * 16;
+  cudaError_t e = cudaFuncSetAttribute(build_meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  build_meta_kernel<<<h->B, kMetaThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dt

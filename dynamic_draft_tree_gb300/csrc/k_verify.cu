@@ -1,0 +1,436 @@
+// Tree verification: one read of the target rows, then the acceptance walk.
+//
+// EAGLE-2 page §"先把投机解码的账本摆清楚": accept the candidate with probability
+// min(1, p/q), on rejection resample from norm(max(0, p - q)); §"无损性为什么没有被动态树破坏":
+// the tree only changes the proposals, the rule keeps the target distribution; greedy decoding
+// is deterministic. The candidates here are deterministic (top-K / top-m), so each candidate's
+// proposal is a point mass: accept x with probability P_res(x), drop x from the residual on a
+// rejection. Graft page step (3): every verified row also yields its top-k successor ids.
+#include <algorithm>
+
+#include "rowscan.cuh"
+
+namespace dt {
+namespace {
+
+struct RowPassArgs {
+  Workspace ws;
+  const void* logits;
+  int64_t ld;
+  int P, S, V, K;
+  int64_t seg_len;
+  const int32_t* tokens;  // meta [B][P]
+  const int32_t* n_pos;   // meta [B]
+  int32_t* top8;          // [B][P][8] or null
+  uint32_t first_wait_cap;
+};
+
+template <typename T, bool SOFTMAX>
+__global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(RowPassArgs a) {
+  extern __shared__ __align__(128) uint8_t dyn_smem[];
+  __shared__ ScanSmem sm;
+  const int r = blockIdx.x / a.S;
+  const int seg = blockIdx.x % a.S;
+  const int b = r / a.P, i = r % a.P;
+  const int tid = threadIdx.x;
+  Workspace& ws = a.ws;
+  if (i >= a.n_pos[b] || a.tokens[r] < 0) return;  // unused position or invalid token: row not needed
+
+  const T* row = reinterpret_cast<const T*>(a.logits) + (int64_t)r * a.ld;
+  const int64_t s0 = (int64_t)seg * a.seg_len;
+  const int64_t s1 = min((int64_t)a.V, s0 + a.seg_len);
+  SegOut so = scan_segment<T, SOFTMAX>(row, s0, s1, a.K, sm, dyn_smem, a.first_wait_cap);
+
+  Partial* part = ws.partials + (int64_t)r * a.S;
+  for (int k = tid; k < a.K; k += blockDim.x) part[seg].keys[k] = k < so.nkeys ? sm.cand[k] : 0ull;
+  if (tid == 0) {
+    part[seg].m = so.m;
+    part[seg].s = so.s;
+    if (so.timed_out) set_status(ws.status, DT_DEV_TIMEOUT);
+    if (so.internal) set_status(ws.status, DT_DEV_INTERNAL);
+    if (so.bad) set_status(ws.status, DT_DEV_BAD_LOGITS);
+    __threadfence();
+    const int prev = atomicAdd(&ws.row_counter[r], 1);
+    sm.last = (prev == a.S - 1);
+  }
+  __syncthreads();
+  if (!sm.last) return;
+
+  __threadfence();
+  if (tid == 0) ws.row_counter[r] = 0;
+  const int nk = a.S * a.K;
+  for (int k = tid; k < nk; k += blockDim.x) sm.cand[k] = __ldcg(&part[k / a.K].keys[k % a.K]);
+  if (tid < kMaxK) sm.topk[tid] = 0ull;
+  __syncthreads();
+  select_topk(sm, nk, a.K);
+  if (tid == 0) {
+    RowStat st;
+    st.amax = (int32_t)key_id(sm.topk[0]);
+    if (SOFTMAX) {
+      float M = -INFINITY;
+      for (int s = 0; s < a.S; ++s) M = fmaxf(M, __ldcg(&part[s].m));
+      double S = 0.0;
+      bool nan = false;
+      for (int s = 0; s < a.S; ++s) {
+        const float ms = __ldcg(&part[s].m);
+        const double ss = __ldcg(&part[s].s);
+        if (ss != ss) nan = true;
+        if (ms == -INFINITY) continue;
+        S += ss * (double)ex2((ms - M) * kLog2e);
+      }
+      if (nan || !(M > -INFINITY) || M == INFINITY || !(S > 0.0)) set_status(ws.status, DT_DEV_BAD_LOGITS);
+      st.m = M;
+      st.s = S;
+    } else {
+      st.m = key_value(sm.topk[0]);
+      st.s = 0.0;
+      if (sm.topk[0] == 0ull || !(st.m > -INFINITY)) set_status(ws.status, DT_DEV_BAD_LOGITS);
+    }
+    ws.row_stats[r] = st;
+  }
+  if (a.top8 && tid < 8) {
+    const uint64_t k = sm.topk[tid];
+    a.top8[(int64_t)r * 8 + tid] = (tid < a.K && k != 0ull) ? (int32_t)key_id(k) : -1;
+  }
+}
+
+struct WalkArgs {
+  Workspace ws;
+  dt_tree_meta meta;
+  const void* logits;
+  int64_t ld;
+  int P, V, dtype, mode;
+  uint32_t key0, key1, r0, r1;
+  int32_t* accept_len;
+  int32_t* accept_path;
+  int32_t* bonus;
+};
+
+__device__ __forceinline__ float load_logit(const void* logits, int dtype, int64_t idx) {
+  if (dtype == DT_BF16)
+    return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const uint16_t*>(logits) + idx) << 16);
+  return __ldg(reinterpret_cast<const float*>(logits) + idx);
+}
+
+constexpr int kWalkThreads = 256;
+
+// Exact residual mass of row `r` without the tokens rej[0..n_rej): fixed-point sum of
+// exp(x - M) (2^-46 units), so that subtracting the rejected terms cannot cancel.
+__device__ double residual_rescan(const WalkArgs& a, int64_t r, float M, const int32_t* rej, int n_rej) {
+  __shared__ unsigned long long acc;
+  if (threadIdx.x == 0) acc = 0ull;
+  __syncthreads();
+  unsigned long long part = 0ull;
+  const float scale = 70368744177664.0f;  // 2^46
+  for (int64_t v = threadIdx.x; v < a.V; v += blockDim.x) {
+    const float e = ex2((load_logit(a.logits, a.dtype, r * a.ld + v) - M) * kLog2e);
+    part += (unsigned long long)__float2ull_rn(e * scale);
+  }
+  atomicAdd(&acc, part);
+  __syncthreads();
+  unsigned long long tot = acc;
+  for (int j = 0; j < n_rej; ++j) {
+    const float e = ex2((load_logit(a.logits, a.dtype, r * a.ld + rej[j]) - M) * kLog2e);
+    tot -= (unsigned long long)__float2ull_rn(e * scale);
+  }
+  __syncthreads();
+  return (double)tot * 1.4210854715202004e-14;  // 2^-46
+}
+
+// One CTA per request.
+__global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
+  __shared__ int32_t s_first_child[kMaxP], s_next_sib[kMaxP];
+  __shared__ int32_t s_path[kMaxP];
+  __shared__ int32_t s_rej[kMaxP];
+  __shared__ unsigned long long s_best;
+  __shared__ int32_t s_cur, s_len, s_nrej, s_state;
+  __shared__ double s_sres;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int P = a.P;
+  const int Dp = a.meta.D_path;
+  const Workspace& ws = a.ws;
+  const int64_t rb = (int64_t)b * P;
+  const int npos = a.meta.n_pos[b];
+
+  if (a.mode == DT_GREEDY) {
+    if (tid == 0) s_best = 0ull;
+    __syncthreads();
+    const int nl = a.meta.n_leaves[b];
+    for (int l = tid; l < nl; l += blockDim.x) {
+      const int32_t* row = a.meta.retrieve + (rb + l) * Dp;
+      int cnt = 0;
+      for (int j = 1; j < Dp; ++j) {
+        const int p = row[j];
+        if (p < 0) break;
+        const int t = a.meta.tokens[rb + p];
+        if (t >= 0 && t == ws.row_stats[rb + row[j - 1]].amax) ++cnt;
+        else break;
+      }
+      // larger count wins, then the earlier row
+      const unsigned long long key = ((unsigned long long)(cnt + 1) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)l);
+      atomicMax(&s_best, key);
+    }
+    __syncthreads();
+    const int cnt = (int)(s_best >> 32) - 1;
+    const int l = (int)(0xFFFFFFFFu - (uint32_t)(s_best & 0xFFFFFFFFull));
+    const int32_t* row = a.meta.retrieve + (rb + l) * Dp;
+    for (int j = tid; j < Dp; j += blockDim.x) a.accept_path[(int64_t)b * Dp + j] = j <= cnt ? row[j] : -1;
+    if (tid == 0) {
+      a.accept_len[b] = cnt;
+      a.bonus[b] = ws.row_stats[rb + row[cnt]].amax;
+    }
+    return;
+  }
+
+  // ---- speculative sampling walk ----
+  if (tid == 0) {
+    for (int p = 0; p < P; ++p) {
+      s_first_child[p] = -1;
+      s_next_sib[p] = -1;
+    }
+    for (int p = npos - 1; p >= 1; --p) {  // children in increasing position
+      const int q = a.meta.parents[rb + p];
+      if (q >= 0 && q < P) {
+        s_next_sib[p] = s_first_child[q];
+        s_first_child[q] = p;
+      }
+    }
+    s_cur = 0;
+    s_len = 0;
+    s_path[0] = 0;
+  }
+  __syncthreads();
+  for (int guard = 0; guard < kMaxP; ++guard) {
+    const int cur = s_cur;
+    const RowStat st = ws.row_stats[rb + cur];
+    const double S = st.s;
+    __syncthreads();
+    if (tid == 0) {
+      s_nrej = 0;
+      s_sres = S;
+    }
+    double s_ref = S;
+    int child = s_first_child[cur];
+    bool moved = false;
+    while (child >= 0) {
+      __syncthreads();  // every thread is done with the previous step's shared state
+      if (tid == 0) {
+        const int t = a.meta.tokens[rb + child];
+        bool skip = t < 0;
+        if (t >= a.V) {
+          set_status(ws.status, DT_DEV_BAD_TOKEN);
+          skip = true;
+        }
+        for (int j = 0; j < s_nrej && !skip; ++j) skip = s_rej[j] == t;
+        s_state = skip ? 3 : (s_sres < s_ref * 0.125 ? 4 : 0);
+      }
+      __syncthreads();
+      const int st0 = s_state;
+      if (st0 == 4) {  // the running residual lost too much to cancellation: recompute it exactly
+        const double v = residual_rescan(a, rb + cur, st.m, s_rej, s_nrej);
+        if (tid == 0) s_sres = v;
+        s_ref = v;
+      }
+      __syncthreads();
+      if (tid == 0 && st0 != 3) {
+        const int t = a.meta.tokens[rb + child];
+        const float x = load_logit(a.logits, a.dtype, (rb + cur) * a.ld + t);
+        const float e = ex2((x - st.m) * kLog2e);
+        const double p = (double)e / s_sres;
+        const Philox4 w = philox4x32_10(a.r0, a.r1, (uint32_t)(512 * b + child), 0x80000000u, a.key0, a.key1);
+        const double u = (double)(w.v[0] >> 8) * 5.9604644775390625e-08;  // 2^-24
+        if (u < p) {
+          s_state = 1;
+        } else {
+          s_rej[s_nrej] = t;
+          s_nrej = s_nrej + 1;
+          s_sres = s_sres - (double)e;
+        }
+      }
+      __syncthreads();
+      if (s_state == 1) {
+        moved = true;
+        break;
+      }
+      child = s_next_sib[child];
+    }
+    if (moved) {
+      if (tid == 0) {
+        s_len = s_len + 1;
+        s_path[s_len] = child;
+        s_cur = child;
+      }
+      __syncthreads();
+      continue;
+    }
+    // residual draw happens in the bonus kernel
+    if (tid == 0) {
+      WalkState* wsb = ws.walk + b;
+      wsb->cur = cur;
+      wsb->n_rej = s_nrej;
+      for (int j = 0; j < s_nrej; ++j) wsb->rej[j] = s_rej[j];
+      ws.bonus_key[b] = 0ull;
+      a.accept_len[b] = s_len;
+    }
+    __syncthreads();
+    for (int j = tid; j < Dp; j += blockDim.x) a.accept_path[(int64_t)b * Dp + j] = j <= s_len ? s_path[j] : -1;
+    return;
+  }
+  if (tid == 0) set_status(ws.status, DT_DEV_INTERNAL);
+}
+
+struct BonusArgs {
+  Workspace ws;
+  const void* logits;
+  int64_t ld;
+  int P, V, dtype, S;
+  int64_t seg_len;
+  uint32_t key0, key1, r0, r1;
+  int32_t* bonus;
+};
+
+constexpr int kBonusThreads = 256;
+
+// Gumbel-max draw from the final residual: argmax over tokens not rejected at that position of
+// x_v - log(-log(u_v)). Grid: B * S CTAs, each a segment of the row.
+__global__ void __launch_bounds__(kBonusThreads) verify_bonus_kernel(BonusArgs a) {
+  __shared__ unsigned long long s_best;
+  __shared__ int32_t s_rej[kMaxP];
+  __shared__ int32_t s_last;
+  const int b = blockIdx.x / a.S, seg = blockIdx.x % a.S;
+  const int tid = threadIdx.x;
+  Workspace& ws = a.ws;
+  const WalkState* wsb = ws.walk + b;
+  const int cur = wsb->cur;
+  const int n_rej = wsb->n_rej;
+  for (int j = tid; j < n_rej; j += blockDim.x) s_rej[j] = wsb->rej[j];
+  if (tid == 0) s_best = 0ull;
+  __syncthreads();
+  const int64_t r = (int64_t)b * a.P + cur;
+  const int64_t v0 = (int64_t)seg * a.seg_len;
+  const int64_t v1 = min((int64_t)a.V, v0 + a.seg_len);
+  unsigned long long best = 0ull;
+  // groups of 4 consecutive tokens share one Philox call
+  for (int64_t g = v0 / 4 + tid; g * 4 < v1; g += blockDim.x) {
+    const Philox4 w = philox4x32_10(a.r0, a.r1, (uint32_t)(512 * b + cur), (uint32_t)g, a.key0, a.key1);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t v = g * 4 + e;
+      if (v < v0 || v >= v1) continue;
+      const float u = ((float)(w.v[e] >> 9) + 0.5f) * 1.1920928955078125e-07f;  // 2^-23
+      const float gmb = -logf(-logf(u));
+      const float y = load_logit(a.logits, a.dtype, r * a.ld + v) + gmb;
+      const unsigned long long k = make_key(y, (uint32_t)v);
+      if (k > best) {
+        bool rej = false;
+        for (int j = 0; j < n_rej; ++j) rej |= (s_rej[j] == (int32_t)v);
+        if (!rej) best = k;
+      }
+    }
+  }
+  atomicMax(&s_best, best);
+  __syncthreads();
+  if (tid == 0) {
+    atomicMax(&ws.bonus_key[b], s_best);
+    __threadfence();
+    const int prev = atomicAdd(&ws.bonus_counter[b], 1);
+    s_last = prev == a.S - 1;
+  }
+  __syncthreads();
+  if (s_last && tid == 0) {
+    __threadfence();
+    const unsigned long long k = atomicAdd(&ws.bonus_key[b], 0ull);
+    a.bonus[b] = k ? (int32_t)key_id(k) : -1;
+    ws.bonus_counter[b] = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int mode,
+                          uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path,
+                          int32_t* bonus, int32_t* top8, cudaStream_t s) {
+  const int P = meta->P;
+  const int V = h->cfg.V;
+  const int esz = h->cfg.dtype == DT_BF16 ? 2 : 4;
+  const int64_t rows = (int64_t)h->B * P;
+  RowPassArgs ra;
+  ra.ws = h->ws;
+  ra.logits = logits;
+  ra.ld = ld;
+  ra.P = P;
+  ra.V = V;
+  ra.K = top8 ? 8 : 1;
+  ra.S = choose_segments(h, rows, V, esz);
+  if (ra.S * ra.K > kCandCap) ra.S = kCandCap / ra.K;
+  int64_t L = (V + ra.S - 1) / ra.S;
+  ra.seg_len = (L + 7) / 8 * 8;
+  ra.tokens = meta->tokens;
+  ra.n_pos = meta->n_pos;
+  ra.top8 = top8;
+  ra.first_wait_cap = (h->cfg.flags & DT_FLAG_TEST_TIMEOUT) ? 0u : kSpinCap;
+  const unsigned grid = (unsigned)(rows * ra.S);
+  const size_t smem = (size_t)kStages * kTileBytes;
+  cudaError_t e;
+#define DT_LAUNCH_ROWS(T, SM)                                                                            \
+  do {                                                                                                   \
+    e = cudaFuncSetAttribute(verify_rows_kernel<T, SM>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
+                             (int)smem);                                                                 \
+    if (e != cudaSuccess) return e;                                                                      \
+    verify_rows_kernel<T, SM><<<grid, kRowThreads, smem, s>>>(ra);                                       \
+  } while (0)
+  const bool sm_on = mode == DT_SAMPLE;
+  if (h->cfg.dtype == DT_BF16) {
+    if (sm_on) DT_LAUNCH_ROWS(uint16_t, true);
+    else DT_LAUNCH_ROWS(uint16_t, false);
+  } else {
+    if (sm_on) DT_LAUNCH_ROWS(float, true);
+    else DT_LAUNCH_ROWS(float, false);
+  }
+#undef DT_LAUNCH_ROWS
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  WalkArgs wa;
+  wa.ws = h->ws;
+  wa.meta = *meta;
+  wa.logits = logits;
+  wa.ld = ld;
+  wa.P = P;
+  wa.V = V;
+  wa.dtype = h->cfg.dtype;
+  wa.mode = mode;
+  wa.key0 = (uint32_t)seed;
+  wa.key1 = (uint32_t)(seed >> 32);
+  wa.r0 = (uint32_t)round;
+  wa.r1 = (uint32_t)(round >> 32);
+  wa.accept_len = accept_len;
+  wa.accept_path = accept_path;
+  wa.bonus = bonus;
+  verify_walk_kernel<<<h->B, kWalkThreads, 0, s>>>(wa);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || mode != DT_SAMPLE) return e;
+
+  BonusArgs ba;
+  ba.ws = h->ws;
+  ba.logits = logits;
+  ba.ld = ld;
+  ba.P = P;
+  ba.V = V;
+  ba.dtype = h->cfg.dtype;
+  const int64_t target = (int64_t)h->num_sms * 4;
+  int Sb = (int)std::max<int64_t>(1, std::min<int64_t>((target + h->B - 1) / h->B, (V + 4095) / 4096));
+  ba.S = Sb;
+  int64_t Lb = (V + Sb - 1) / Sb;
+  ba.seg_len = (Lb + 3) / 4 * 4;
+  ba.key0 = wa.key0;
+  ba.key1 = wa.key1;
+  ba.r0 = wa.r0;
+  ba.r1 = wa.r1;
+  ba.bonus = bonus;
+  verify_bonus_kernel<<<(unsigned)(h->B * Sb), kBonusThreads, 0, s>>>(ba);
+  return cudaGetLastError();
+}
+
+}  // namespace dt

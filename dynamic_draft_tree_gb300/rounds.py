@@ -1,0 +1,107 @@
+"""One draft-tree round as a sequence of libdt calls (orchestration only, no arithmetic).
+
+Call order (EAGLE-2 page §"一段更贴近实现的流程"; CAST page §关键设计 2-4; Graft page
+steps (1)-(3)):
+
+  reset -> [frontier -> draft rows -> expand -> prune]* -> (verify count) -> rerank
+  -> (retrieve) -> meta -> target rows -> verify -> (M refresh)
+
+The draft and target model forwards are outside the library: ``draft_rows(d,
+frontier_token)`` must return the logits tensor [B][F][V] of layer d (row f =
+the draft row of frontier slot f), and ``target_rows(meta)`` the tensor
+[B][P][V] (row i = the target's next-token row after position i). Every call
+is asynchronous on the current stream; no host synchronisation happens inside
+a round, so a round can be captured in a CUDA graph.
+"""
+import torch
+
+from . import (Handle, Meta, Template, make_prune_params, make_prune_out, dt_tree_reset, dt_select_frontier,
+               dt_expand_layer, dt_cast_prune, dt_rerank, dt_graft_retrieve, dt_build_tree_meta, dt_verify,
+               dt_adj_update, DT_GREEDY, DT_SAMPLE, DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY,
+               DT_POLICY_GRAFT_CHECKPOINT)
+
+
+class RoundRunner:
+    """Device buffers and call sequence of one round for a policy ('eagle' | 'cast' | 'graft')."""
+
+    def __init__(self, policy, B, V, K, k, D, P, D_path, m, dtype, T=0, cast=None, cast_tables=None,
+                 graft=None, template=None, flags=0, device="cuda"):
+        self.policy, self.B, self.V, self.K, self.k, self.D = policy, B, V, K, k, D
+        self.P, self.D_path, self.T = P, D_path, T
+        self.h = Handle(B, V, K, k, D, P, dtype, flags)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.frontier_token = torch.full((B, k), -1, **i32)
+        self.width = torch.full((1,), k, **i32)
+        self.stop = torch.zeros((B,), **i32)
+        self.stage = torch.full((B,), -1, **i32)
+        self.m_dev = torch.full((B if policy == "graft" else 1,), m, **i32)
+        self.m_cap = m
+        self.selected = torch.empty((B, m), **i32)
+        self.meta = Meta(B, P, D_path, device)
+        self.accept_len = torch.empty((B,), **i32)
+        self.accept_path = torch.empty((B, D_path), **i32)
+        self.bonus = torch.empty((B,), **i32)
+        self.pos_offset = torch.zeros((B,), **i32)
+        self.top8 = None
+        self.params = None
+        if policy == "cast":
+            S_T, S_D = cast_tables
+            self.S_T = torch.as_tensor(S_T, dtype=torch.float64, device=device).contiguous()
+            self.S_D = torch.as_tensor(S_D, dtype=torch.float64, device=device).contiguous()
+            self.cast = cast
+        if policy == "graft":
+            self.graft = graft
+            self.R_cap = graft["K_total"]
+            self.template = Template(*template)
+            self.ret_token = torch.empty((B, self.R_cap), **i32)
+            self.ret_parent = torch.empty((B, self.R_cap), **i32)
+            self.ret_count = torch.empty((B,), **i32)
+            self.top8 = torch.empty((B, P, 8), **i32)
+            self.params = make_prune_params(ckpt_layers=graft["ckpt_layers"], tau=graft["tau"],
+                                            k_draft=graft["k_draft"], K_total=graft["K_total"], D_max=D)
+            self.prune_out = make_prune_out(stop=self.stop, m=self.m_dev, stage=self.stage)
+
+    def set_n0(self, n0):
+        c = self.cast
+        self.params = make_prune_params(S_T=self.S_T, S_D=self.S_D, L=c["L"], n0=n0, C1=c["C1"], C2=c["C2"],
+                                        C3=c["C3"], R=c["R"], width_cap=c["width_cap"], m_cap=c["m_cap"],
+                                        D_max=self.D)
+        self.prune_out = make_prune_out(width=self.width, stop=self.stop)
+        self.verify_out = make_prune_out(m=self.m_dev)
+
+    def run(self, roots, draft_rows, target_rows, seed=0, rnd=0, M=None, n0=0):
+        """Launch one round; returns nothing (outputs live in this object's tensors)."""
+        h = self.h
+        pol = self.policy
+        if pol == "cast":
+            self.set_n0(n0)
+        self.stop.zero_()
+        dt_tree_reset(h, roots)
+        for d in range(1, self.D + 1):
+            if d > 1:
+                dt_select_frontier(h, self.width, self.stop, self.frontier_token)
+                F = self.k
+            else:
+                self.frontier_token.fill_(-1)
+                self.frontier_token[:, 0] = roots
+                F = 1
+            dt_expand_layer(h, draft_rows(d, self.frontier_token), F)
+            if pol == "cast":
+                dt_cast_prune(h, DT_POLICY_CAST_WIDTH_DEPTH, self.params, self.prune_out)
+            elif pol == "graft":
+                dt_cast_prune(h, DT_POLICY_GRAFT_CHECKPOINT, self.params, self.prune_out)
+        if pol == "cast":
+            dt_cast_prune(h, DT_POLICY_CAST_VERIFY, self.params, self.verify_out)
+        dt_rerank(h, self.m_dev, self.m_cap, self.selected)
+        if pol == "graft":
+            dt_graft_retrieve(h, M, self.m_dev, self.graft["K_total"], self.template, self.R_cap, self.ret_token,
+                              self.ret_parent, self.ret_count)
+            dt_build_tree_meta(h, self.selected, self.m_cap, self.meta, self.pos_offset, self.ret_token,
+                               self.ret_parent, self.ret_count, self.R_cap)
+        else:
+            dt_build_tree_meta(h, self.selected, self.m_cap, self.meta, self.pos_offset)
+        logits = target_rows(self.meta)
+        dt_verify(h, self.meta, logits, DT_SAMPLE if self.T == 1 else DT_GREEDY, seed, rnd, self.accept_len,
+                  self.accept_path, self.bonus, self.top8)
+        if pol == "graft":
+            dt_adj_update(h, M, self.meta, self.top8)

@@ -1,0 +1,254 @@
+/* dt.h - C ABI of the GB300 dynamic draft-tree library (libdt.so).
+ *
+ * The library runs the batched hot path of dynamic draft-tree speculative
+ * decoding between the draft and the target model forwards:
+ *
+ *   EAGLE-2 ("EAGLE-2 完全拆解：动态草稿树如何让投机解码上下文感知"):
+ *     vocab softmax + top-K per expanded node, path value as the product of
+ *     confidences (kept as a sum of logs), frontier top-k expansion
+ *     (§"扩展阶段"), global top-m rerank with shallow-first ties giving a
+ *     connected subtree, flattening with an ancestor-only mask (§"重排阶段"),
+ *     greedy and speculative-sampling acceptance along the tree with a bonus
+ *     token (§"先把投机解码的账本摆清楚", §"无损性为什么没有被动态树破坏").
+ *   CAST ("Inference-Cost-Aware Dynamic Tree Construction for Efficient
+ *     Inference in Large Language Models", §关键设计 1-4): cost-table driven
+ *     width, depth and verify-count pruning.
+ *   Graft ("Draft Less, Retrieve More: Hybrid Tree Construction for
+ *     Speculative Decoding", method steps (1)-(3)): confidence checkpoints,
+ *     retrieval graft from a GPU-resident adjacency matrix M[V][8], online
+ *     refresh of M from the target rows.
+ *
+ * Conventions (every entry point):
+ *   - Every array argument is a DEVICE pointer, allocated and owned by the
+ *     caller, unless the comment says "host". The library keeps no pointer
+ *     past the call.
+ *   - Calls are asynchronous on the caller's stream. A handle holds one draft
+ *     tree; using one handle from two streams at once is a race.
+ *   - Return value: DT_OK (0) or a negative DT_ERR_* code. DT_ERR_ARG means
+ *     the host-side argument check failed and nothing was launched;
+ *     dt_last_error_string() (thread-local) says why. DT_ERR_CUDA is a launch
+ *     or runtime error.
+ *   - Errors found on the device (bad logits, bad tokens, a bounded wait that
+ *     ran out) are OR-ed into the handle's sticky status word; read it with
+ *     dt_get_status(), which synchronises the given stream. Kernels never trap.
+ *   - Row-major contiguous layouts; logits rows are `ld` elements apart.
+ *   - Only dt_create allocates (device workspace sized from the config
+ *     maxima). Hot calls allocate nothing.
+ *
+ * Limits (checked, DT_ERR_ARG otherwise): 2 <= V < 2^31, 1 <= K <= 32,
+ * K <= V, 1 <= W <= 32, W*K <= 1024, 1 <= D_max <= 16, 1 <= P_max <= 512,
+ * 1 <= B_max <= 4096.
+ */
+#ifndef DT_H_
+#define DT_H_
+
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { DT_OK = 0, DT_ERR_ARG = -1, DT_ERR_CUDA = -2, DT_ERR_DEVICE = -3, DT_ERR_DEVICE_TIMEOUT = -4 };
+enum { DT_BF16 = 0, DT_F32 = 1 };
+enum { DT_GREEDY = 0, DT_SAMPLE = 1 };
+enum {
+  DT_POLICY_CAST_WIDTH_DEPTH = 0, /* CAST width n_d and grow/stop after layer d */
+  DT_POLICY_CAST_VERIFY = 1,      /* CAST batch-wide verify count m            */
+  DT_POLICY_GRAFT_CHECKPOINT = 2  /* Graft confidence checkpoint after layer d */
+};
+/* Bits of the device status word. */
+enum {
+  DT_DEV_BAD_LOGITS = 1,   /* a row read by a kernel holds NaN or +inf, or has no finite entry */
+  DT_DEV_BAD_TOKEN = 2,    /* a token id outside [0, V) where a token was required            */
+  DT_DEV_BAD_TREE = 4,     /* selection not parent-closed, or a tree deeper than D_path - 1    */
+  DT_DEV_TIMEOUT = 8,      /* a bounded wait on an asynchronous copy ran out                   */
+  DT_DEV_INTERNAL = 16     /* an internal iteration bound was hit                              */
+};
+/* dt_config.flags */
+enum { DT_FLAG_TEST_TIMEOUT = 1 }; /* test only: the first copy wait of each row kernel gives up at
+                                      once (it still drains its copies), exercising DT_DEV_TIMEOUT */
+
+typedef struct dt_handle dt_handle;
+
+typedef struct {
+  int32_t B_max;  /* largest batch                                                  */
+  int32_t V;      /* vocabulary size                                                */
+  int32_t K;      /* per-node top-K (children per expanded node)                    */
+  int32_t W;      /* largest frontier width k (nodes expanded per layer)            */
+  int32_t D_max;  /* largest number of draft layers (the root is depth 0)          */
+  int32_t P_max;  /* largest verify positions per request (root + nodes)            */
+  int32_t dtype;  /* DT_BF16 or DT_F32: element type of every logits buffer         */
+  int32_t flags;  /* DT_FLAG_*                                                      */
+} dt_config;
+
+/* Read-only view of the handle's draft tree (device pointers into the workspace).
+ * Node-id layout: root = 0; layer 1 = ids 1..K; layer d >= 2 = ids
+ * base(d) .. base(d)+W*K-1 with base(d) = 1 + K + (d-2)*W*K; the child of
+ * rank r of frontier slot f in layer d is base(d) + f*K + r. Frontier slots
+ * hold the selected frontier nodes in ascending id. Invalid slots have
+ * token -1, parent -1, logc = value = -inf. Values are log path values
+ * (sum of log confidences), fp32. */
+typedef struct {
+  int32_t B, K, W, D_max, N, LW; /* N = nodes per request, LW = W*K slots per layer (>= K)   */
+  int32_t depth;                 /* layers built so far                                        */
+  const int32_t* token;          /* [B_max][N]                                                 */
+  const int32_t* parent;         /* [B_max][N] node id of the parent, -1 for root/invalid     */
+  const int32_t* node_depth;     /* [B_max][N] layer of the slot                               */
+  const float* logc;             /* [B_max][N] log confidence                                  */
+  const float* value;            /* [B_max][N] log path value                                  */
+  const int32_t* layer_order;    /* [B_max][D_max+1][LW] layer d's valid ids by (value desc,
+                                    id asc), -1 padded                                         */
+  const int32_t* layer_count;    /* [B_max][D_max+1] valid nodes per layer                     */
+  const int32_t* frontier;       /* [B_max][W] ids of the current frontier, -1 padded          */
+  const int32_t* frontier_count; /* [B_max]                                                    */
+} dt_tree_view;
+
+/* CAST / Graft pruning parameters (host struct; the tables are device arrays). */
+typedef struct {
+  /* CAST (cost tables f(B, c, n) for the running batch size B) */
+  const double* S_T;  /* device [M_rows][N_cols]: target cost; column n-1 holds input length n */
+  const double* S_D;  /* device [M_rows][N_cols]: draft cost                                   */
+  int32_t M_rows, N_cols;
+  double L;           /* context grid step: row = min(floor(c / L), M_rows - 1)                */
+  int64_t n0;         /* prefix (context) length                                              */
+  double C1, C2, C3;  /* width, depth and verify-count thresholds                             */
+  int32_t R;          /* FIFO length of the depth ratio buffer, 1..16                         */
+  int32_t width_cap;  /* largest width n_d, <= min(W, N_cols)                                  */
+  int32_t m_cap;      /* largest verify count m, <= N_cols                                     */
+  int32_t D_max;      /* last layer: no growth after it                                        */
+  /* Graft */
+  int32_t n_ckpt;       /* number of checkpoints, 0..4                                         */
+  int32_t ckpt_layer[4];/* checkpoint layer indices (layer index 0 = draft layer 1)            */
+  double tau[4];        /* confidence thresholds: request continues iff exp(max value) > tau   */
+  int32_t k_draft[4];   /* draft nodes kept when stopped at checkpoint s                       */
+  int32_t K_total;      /* K_max: draft + retrieved nodes per request                         */
+} dt_prune_params;
+
+/* Outputs of dt_cast_prune (device pointers; NULL where a policy does not write). */
+typedef struct {
+  int32_t* width; /* [1]  CAST_WIDTH_DEPTH: n_d                                           */
+  int32_t* stop;  /* [B]  CAST_WIDTH_DEPTH: 1 = do not grow (batch-wide); GRAFT: per request,
+                          set once a request stops                                          */
+  int32_t* m;     /* [1]  CAST_VERIFY: m;  [B] GRAFT: K_draft of each request (set on stop) */
+  int32_t* stage; /* [B]  GRAFT: checkpoint index that stopped the request, n_ckpt if none  */
+} dt_prune_out;
+
+/* Retrieval template (host arrays), nodes in breadth-first order:
+ * parent[u] in [-1, u) (-1 = the root), rank[u] in [0, 8): x_u = M[x_parent][rank]. n <= 256. */
+typedef struct {
+  int32_t n;
+  const int32_t* parent;
+  const int32_t* rank;
+} dt_template;
+
+/* Flattened verify tree (device arrays, caller-owned), P positions per request. */
+typedef struct {
+  int32_t P;             /* positions per request = row stride of every [B][P] array     */
+  int32_t D_path;        /* width of a retrieve row (>= deepest position + 1)            */
+  int32_t* tokens;       /* [B][P] token, -1 for an invalid node or an unused position   */
+  int32_t* parents;      /* [B][P] parent position, -1 for the root / unused             */
+  int32_t* depth;        /* [B][P] depth (root 0), -1 unused                             */
+  int32_t* node_id;      /* [B][P] draft-tree node id, -1 for retrieved / unused          */
+  uint8_t* mask;         /* [B][P][P] 1 iff column is an ancestor-or-self of the row     */
+  int32_t* position_ids; /* [B][P] pos_offset + depth, -1 unused                        */
+  int32_t* retrieve;     /* [B][P][D_path] root-to-leaf positions, -1 padded              */
+  int32_t* n_leaves;     /* [B]                                                           */
+  int32_t* n_pos;        /* [B] positions in use                                          */
+} dt_tree_meta;
+
+const char* dt_last_error_string(void);
+
+/* Create a handle and its workspace (the only allocating call). */
+int dt_create(const dt_config* cfg, dt_handle** out);
+int dt_destroy(dt_handle* h);
+int dt_get_tree(const dt_handle* h, dt_tree_view* out);
+/* Synchronise `s`, then OR-ed DT_DEV_* bits since the last clear; returns DT_ERR_DEVICE or
+ * DT_ERR_DEVICE_TIMEOUT when bits are set, DT_OK otherwise. */
+int dt_get_status(dt_handle* h, cudaStream_t s, int32_t* device_bits);
+int dt_clear_status(dt_handle* h, cudaStream_t s);
+
+/* Start a round for B <= B_max requests: root node = root_token[b] (depth 0, value 0), every
+ * other slot invalid, the frontier = {root}, CAST state reset (FIFO = {1}). */
+int dt_tree_reset(dt_handle* h, int32_t B, const int32_t* root_token, cudaStream_t s);
+
+/* a2 (EAGLE-2 §扩展阶段): choose the frontier of the next layer: for request b, the first
+ * w_b nodes of the newest layer in (value desc, id asc) order, slotted in ascending id.
+ * w_b = min(width, W, nodes in the layer), 0 where stop[b] != 0. width: device [width_len]
+ * with width_len 1 (batch-wide) or B, or NULL for W. stop: device [B] or NULL.
+ * frontier_token: device [B][W] out (tokens of the slots, -1 padded) or NULL. */
+int dt_select_frontier(dt_handle* h, const int32_t* width, int32_t width_len, const int32_t* stop,
+                       int32_t* frontier_token, cudaStream_t s);
+
+/* a1 + a2 (EAGLE-2 §置信度…, §value 公式, §扩展阶段): expand the current frontier into the
+ * next layer. logits: device [B][F][V] of dtype, row (b, f) at element (b*F + f)*ld, the draft
+ * row of frontier slot f (F = 1 for layer 1, rows f >= frontier_count[b] are not read).
+ * Per row: m = max, S = sum exp(x - m), the K largest logits (ties: lower id) become children
+ * with log c = x - m - log S and value = value(parent) + log c; then the new layer is ordered
+ * by (value desc, id asc). A NaN/+inf row or a row without a finite entry sets
+ * DT_DEV_BAD_LOGITS. */
+int dt_expand_layer(dt_handle* h, const void* logits, int64_t ld, int32_t F, cudaStream_t s);
+
+/* a3/a4: CAST (width/depth after the newest layer, or verify count) or Graft checkpoint.
+ * CAST width (page 2 §关键设计 2): u_k = (1/B) sum_b sum_{s<=k} exp(value of the s-th node of
+ * b's newest layer), c_k = S_D[row][k-1] / S_T[row][0] with row from ctx = n0 + widths so far;
+ * k0 = 1, for k = 2..min(width_cap, candidates): k0 = k if c_k <= c_k0 or
+ * (u_k - u_k0)/(c_k - c_k0) >= C1; n_d = k0 -> out->width[0].
+ * CAST depth (§关键设计 3): after layer d >= 2 push u(d)/u(d-1) into a FIFO of length R
+ * (initial {1}); grow iff d < D_max and mean(FIFO) * u_{n_d} / c_{n_d} >= C2; out->stop[b] = !grow.
+ * CAST verify (§关键设计 4): same rule over all nodes of each request in the total order with
+ * c_k = S_T[row(n0)][k-1] / S_T[row(n0)][0], C3, cap m_cap -> out->m[0].
+ * Graft (page 3 step (1)): for every running request, if the newest layer index is checkpoint s
+ * and not exp(max value) > tau[s]: stop[b] = 1, stage[b] = s, m[b] = k_draft[s]; a request that
+ * reaches D_max gets stage n_ckpt and m = K_total. */
+int dt_cast_prune(dt_handle* h, int32_t policy, const dt_prune_params* p, const dt_prune_out* out,
+                  cudaStream_t s);
+
+/* a5 (EAGLE-2 §重排阶段): top-m_b valid non-root nodes in (value desc, depth asc, id asc) order,
+ * written in ascending id. m: device [m_len] (m_len 1 = batch-wide, or B), NULL = m_cap.
+ * selected: device [B][m_cap], -1 padded. */
+int dt_rerank(dt_handle* h, const int32_t* m, int32_t m_len, int32_t m_cap, int32_t* selected,
+              cudaStream_t s);
+
+/* a6 (Graft step (2)): gather k_ret_b = min(K_total - min(m_draft[b], tree nodes of b), tpl->n,
+ * R_cap) template nodes from M (device [B][V][8] int32, -1 = unset): token(u) =
+ * M[b][token(parent(u))][rank(u)], -1 when the parent is invalid or the entry unset.
+ * ret_token/ret_parent: device [B][R_cap] (parent = template parent index, -1 root, -2 unused),
+ * ret_count: device [B]. */
+int dt_graft_retrieve(dt_handle* h, const int32_t* M, const int32_t* m_draft, int32_t K_total,
+                      const dt_template* tpl, int32_t R_cap, int32_t* ret_token, int32_t* ret_parent,
+                      int32_t* ret_count, cudaStream_t s);
+
+/* a7 (EAGLE-2 §重排阶段; Graft step (3)): flatten and build the verify metadata. Position 0 is
+ * the root, then selected nodes (device [B][m_cap], ascending id, -1 padded), then retrieved
+ * nodes (ret_*: device, NULL when there is no graft) in template order. pos_offset: device [B]
+ * or NULL (0). Needs 1 + m_cap <= meta->P; a request whose root + selected + retrieved nodes
+ * exceed P sets DT_DEV_BAD_TREE and keeps the first P positions. */
+int dt_build_tree_meta(dt_handle* h, const int32_t* selected, int32_t m_cap, const int32_t* ret_token,
+                       const int32_t* ret_parent, const int32_t* ret_count, int32_t R_cap,
+                       const int32_t* pos_offset, const dt_tree_meta* meta, cudaStream_t s);
+
+/* a8 + a9 (EAGLE-2 §先把投机解码的账本摆清楚, §无损性…): verify against the target rows
+ * logits: device [B][P][V], row (b, i) at element (b*P + i)*ld, the target row after position i.
+ * DT_GREEDY: longest leaf path whose tokens equal the argmax (ties: lower id) of their parent's
+ * row (ties: first path), bonus = argmax of the last accepted position's row.
+ * DT_SAMPLE: from the root, children in position order are accepted with probability
+ * P_res(x) (point-mass proposals), P_res = softmax(row) with rejected tokens removed,
+ * u = Philox4x32-10(key seed; counter (round, 512*b + j, 0x80000000)) top 24 bits; the bonus is
+ * a Gumbel-max draw from the final residual (23-bit uniforms, counter (round, 512*b + i, v>>2),
+ * word v&3). accept_len: [B]; accept_path: [B][D_path] positions (root first, -1 padded);
+ * bonus: [B]; top8: [B][P][8] top-8 ids of each used row (NULL = skip). */
+int dt_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int32_t mode,
+              uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path, int32_t* bonus,
+              int32_t* top8, cudaStream_t s);
+
+/* a10 (Graft step (3)): M[b][token_i][0..7] = top8[b][i][0..7] for every used position i with a
+ * valid token; when a token repeats the highest position wins. M: device [B][V][8]. */
+int dt_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta, const int32_t* top8,
+                  cudaStream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DT_H_ */

@@ -24,7 +24,8 @@ Definition (all integer arithmetic mod 2^64):
   the peak and the height.
 * kind 1 (Zipf): rank(v) = (a*v + c) mod V with a coprime to V and c from the
   key; x_v = -s * ln_table[rank] + noise, ln_table[k] = fp32(ln(k + 1)) built
-  once on the host.
+  once on the host. kind 2: the Zipf row of kind 1 with the permutation shifted so that
+  the peak token of kind 0 has rank 0, plus that peak's height.
 * Every fp32 step rounds once (no fused multiply-add); bf16 output rounds to
   nearest even from the fp32 value.
 """
@@ -75,7 +76,7 @@ def _cpu_lib():
         lib = ctypes.CDLL(CPU_LIB)
         lib.synth_gen_rows.argtypes = [ctypes.POINTER(SpecC), ctypes.c_uint64, ctypes.c_uint64,
                                        ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
-                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                                        ctypes.c_int64, ctypes.c_int32]
         lib.synth_root_token.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int64,
                                          ctypes.c_int32]
@@ -126,7 +127,7 @@ class Spec:
         if hi.size == 1 and B > 1:
             hi = np.full(B, hi.item(), np.float32)
         self.peak_lo, self.peak_hi = lo, hi
-        self.ln_table = zipf_table(V) if kind == 1 else np.zeros(1, np.float32)
+        self.ln_table = zipf_table(V) if kind != 0 else np.zeros(1, np.float32)
         self._dev = None
 
     @property
@@ -147,10 +148,10 @@ class Spec:
                      self.zipf_s, lo.data_ptr(), hi.data_ptr(), ln.data_ptr())
 
 
-def gen_rows_cpu(spec, seed, salt, stream, ctx, depth=None, depth_add=0, rows_per_b=1):
+def gen_rows_cpu(spec, seed, salt, stream, ctx, depth=None, depth_add=0, rows_per_b=1, b0=0):
     """Rows for contexts ``ctx`` (int32 [R]); returns raw bits (uint16 for bf16) or fp32, [R][V].
 
-    Rows whose ctx is negative are returned as zeros.
+    Row rr belongs to request b0 + rr // rows_per_b. Rows whose ctx is negative are zeros.
     """
     ctx = np.ascontiguousarray(ctx, np.int32).ravel()
     R = ctx.size
@@ -161,7 +162,7 @@ def gen_rows_cpu(spec, seed, salt, stream, ctx, depth=None, depth_add=0, rows_pe
         dptr = depth.ctypes.data
     st = spec.c_struct_host()
     _cpu_lib().synth_gen_rows(ctypes.byref(st), seed, salt, stream, ctx.ctypes.data, dptr,
-                              depth_add, rows_per_b, out.ctypes.data, spec.V, R)
+                              depth_add, rows_per_b, b0, out.ctypes.data, spec.V, R)
     return out
 
 

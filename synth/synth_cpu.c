@@ -50,7 +50,8 @@ static uint16_t f32_to_bf16_rne(float x) {
 }
 
 typedef struct {
-  int32_t kind;        /* 0 = normal noise + one peak, 1 = Zipf over a permutation + noise */
+  int32_t kind;        /* 0 = normal noise + one peak, 1 = Zipf over a permutation + noise,
+                          2 = Zipf + noise + one peak */
   int32_t V;
   int32_t dtype;       /* 0 = bf16, 1 = fp32 */
   int32_t height_per_request;
@@ -93,7 +94,7 @@ static void gen_row(const synth_spec* sp, uint64_t seed, uint64_t salt, int stre
   int64_t peak = -1;
   float h = 0.0f;
   uint64_t za = 0, zc = 0;
-  if (sp->kind == 0) {
+  if (sp->kind != 1) {
     peak = (int64_t)(mix64(r ^ PEAK_SALT) % (uint64_t)V);
     uint64_t hsrc = sp->height_per_request ? hk(hk(seed, salt), (uint64_t)b) : r;
     uint32_t u24 = (uint32_t)(mix64(hsrc ^ HEIGHT_SALT) >> 40);
@@ -101,10 +102,13 @@ static void gen_row(const synth_spec* sp, uint64_t seed, uint64_t salt, int stre
     float lo = sp->peak_lo[b], range = sp->peak_hi[b] - sp->peak_lo[b];
     float t = range * uf;
     h = lo + t;
-  } else {
+  }
+  if (sp->kind != 0) {
     za = mix64(r ^ ZIPF_A_SALT) % (uint64_t)(V - 1) + 1;
     while (gcd64(za, (uint64_t)V) != 1) za = za % (uint64_t)(V - 1) + 1;
     zc = mix64(r ^ ZIPF_C_SALT) % (uint64_t)V;
+    /* kind 2: shift the permutation so that the peak token holds rank 0 (the Zipf mode) */
+    if (sp->kind == 2) zc = ((uint64_t)V - (za * (uint64_t)peak) % (uint64_t)V) % (uint64_t)V;
   }
   for (int32_t v = 0; v < V; ++v) {
     int32_t ia = ih12(r, (uint64_t)v, 0);
@@ -115,14 +119,13 @@ static void gen_row(const synth_spec* sp, uint64_t seed, uint64_t salt, int stre
       int32_t ib = ih12(r, (uint64_t)v, 1);
       noise = (float)(4 * ia + 3 * ib) * sT;
     }
-    float x;
-    if (sp->kind == 0) {
-      x = (v == peak) ? noise + h : noise;
-    } else {
+    float x = noise;
+    if (sp->kind != 0) {
       uint64_t rank = (za * (uint64_t)v + zc) % (uint64_t)V;
       float base = (-sp->zipf_s) * sp->ln_table[rank];
       x = base + noise;
     }
+    if (v == peak) x = x + h;
     if (sp->dtype == 0)
       ((uint16_t*)out)[v] = f32_to_bf16_rne(x);
     else
@@ -130,17 +133,17 @@ static void gen_row(const synth_spec* sp, uint64_t seed, uint64_t salt, int stre
   }
 }
 
-/* R rows. Row rr uses request b = rr / rows_per_b, context token ctx[rr]
+/* R rows. Row rr uses request b = b0 + rr / rows_per_b, context token ctx[rr]
  * (rows with ctx < 0 are left untouched) and depth key
  * (depth ? depth[rr] : 0) + depth_add. Row rr starts at element rr * ld. */
 void synth_gen_rows(const synth_spec* sp, uint64_t seed, uint64_t salt, int32_t stream,
                     const int32_t* ctx, const int32_t* depth, int32_t depth_add, int32_t rows_per_b,
-                    void* out, int64_t ld, int32_t R) {
+                    int32_t b0, void* out, int64_t ld, int32_t R) {
   const size_t esz = sp->dtype == 0 ? 2 : 4;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int32_t rr = 0; rr < R; ++rr) {
     if (ctx[rr] < 0) continue;
-    int64_t b = rr / rows_per_b;
+    int64_t b = b0 + rr / rows_per_b;
     int64_t dk = (int64_t)(depth ? depth[rr] : 0) + depth_add;
     gen_row(sp, seed, salt, stream, b, dk, ctx[rr], (char*)out + (size_t)rr * (size_t)ld * esz);
   }

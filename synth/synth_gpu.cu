@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) gen_rows_kernel(
       rp.peak = -1;
       rp.h = 0.0f;
       rp.za = rp.zc = 0;
-      if (sp.kind == 0) {
+      if (sp.kind != 1) {
         rp.peak = (int64_t)(mix64(r ^ PEAK_SALT) % (uint64_t)sp.V);
         uint64_t hsrc = sp.height_per_request ? hk(hk(seed, salt), (uint64_t)b) : r;
         uint32_t u24 = (uint32_t)(mix64(hsrc ^ HEIGHT_SALT) >> 40);
@@ -111,11 +111,14 @@ __global__ void __launch_bounds__(kThreads) gen_rows_kernel(
         float lo = sp.peak_lo[b];
         float range = __fsub_rn(sp.peak_hi[b], lo);
         rp.h = __fadd_rn(lo, __fmul_rn(range, uf));
-      } else {
+      }
+      if (sp.kind != 0) {
         uint64_t a = mix64(r ^ ZIPF_A_SALT) % (uint64_t)(sp.V - 1) + 1;
         while (gcd64(a, (uint64_t)sp.V) != 1) a = a % (uint64_t)(sp.V - 1) + 1;
         rp.za = a;
         rp.zc = mix64(r ^ ZIPF_C_SALT) % (uint64_t)sp.V;
+        // kind 2: shift the permutation so that the peak token holds rank 0 (the Zipf mode)
+        if (sp.kind == 2) rp.zc = ((uint64_t)sp.V - (a * (uint64_t)rp.peak) % (uint64_t)sp.V) % (uint64_t)sp.V;
       }
     }
   }
@@ -135,13 +138,12 @@ __global__ void __launch_bounds__(kThreads) gen_rows_kernel(
       const int32_t ib = ih12(rp.r, (uint64_t)v, 1);
       noise = __fmul_rn((float)(4 * ia + 3 * ib), sT);
     }
-    float x;
-    if (sp.kind == 0) {
-      x = (v == rp.peak) ? __fadd_rn(noise, rp.h) : noise;
-    } else {
+    float x = noise;
+    if (sp.kind != 0) {
       const uint64_t rank = (rp.za * (uint64_t)v + rp.zc) % (uint64_t)sp.V;
       x = __fadd_rn(__fmul_rn(-sp.zipf_s, sp.ln_table[rank]), noise);
     }
+    if (v == rp.peak) x = __fadd_rn(x, rp.h);
     if (sp.dtype == 0)
       reinterpret_cast<uint16_t*>(out)[(int64_t)rr * ld + v] = bf16_rne(x);
     else

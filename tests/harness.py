@@ -1,0 +1,188 @@
+"""Test harness: the same seeded rows fed to the oracle (host generator) and the GPU path
+(device generator), round drivers for both, and the comparison rules.
+
+Comparison rules (readings listed in the design doc):
+  * index outputs (tokens, parents, frontier sets, selections, masks, position ids, retrieve rows,
+    accepted lengths and paths, bonus tokens, M rows) must be equal;
+  * log confidences and log values: |gpu - oracle| <= 2e-6 * max(1, |oracle|);
+  * a round whose oracle decision gaps fall below 1e-5 relative is redrawn (attempt + 1) and counted.
+"""
+import functools
+
+import numpy as np
+
+import synth
+from synth.workloads import spec_for, geometry, cast_tables, chain_template
+from oracle.round import run_round
+from oracle.tree import Gaps
+
+TOL = 2e-6
+GAP = 1e-5
+
+
+def salt_of(w, rnd, attempt):
+    return attempt if w["policy"] == "graft" else (rnd << 8) | attempt
+
+
+def round_id(rnd, attempt):
+    return (rnd << 8) | attempt
+
+
+class HostRows:
+    """Row providers for the oracle, keyed like the device generator."""
+
+    def __init__(self, w, spec, salt):
+        self.w, self.spec, self.salt = w, spec, salt
+        self.depthkey = w["recipe"]["depthkey"]
+
+    @functools.lru_cache(maxsize=8192)
+    def _row(self, stream, b, dk, ctx):
+        r = synth.gen_rows_cpu(self.spec, self.w["seed"], self.salt, stream, [ctx], depth_add=dk, b0=b)
+        return synth.to_f64(r[0], self.spec.dtype)
+
+    def draft_row(self, b, d, ctx):
+        return self._row(synth.DRAFT, b, d if self.depthkey else 0, ctx)
+
+    def target_row(self, b, d, ctx):
+        return self._row(synth.TARGET, b, d if self.depthkey else 0, ctx)
+
+
+def oracle_cfg(w):
+    g = geometry(w)
+    c = dict(policy=w["policy"], B=w["B"], K=w["K"], W=g["W"], D=g["D_max"], k=w["k"], m=w["m"],
+             m_cap=g["m_cap"], P=g["P"], D_path=g["D_path"], T=w["T"], seed=w["seed"])
+    if w["policy"] == "cast":
+        cc = w["cast"]
+        S_T, S_D = cast_tables(w["B"], cc["M_rows"], cc["N_cols"], cc["L"])
+        c["cast"] = dict(S_T=S_T, S_D=S_D, L=cc["L"], n0=0, C1=cc["C1"], C2=cc["C2"], C3=cc["C3"], R=cc["R"],
+                         width_cap=cc["width_cap"], m_cap=cc["m_cap"], D_max=g["D_max"])
+    if w["policy"] == "graft":
+        c["graft"] = dict(w["graft"], template=chain_template(w["k"], w["D"]))
+    return c
+
+
+def cast_n0(rnd):
+    return 512 * (1 + rnd % 16)
+
+
+def oracle_round(w, rnd, roots=None, M=None, max_attempts=12):
+    """Oracle round with seed rejection; returns (ref, attempt, rejections)."""
+    spec = spec_for(w)
+    cfg = oracle_cfg(w)
+    for attempt in range(max_attempts):
+        salt = salt_of(w, rnd, attempt)
+        rows = HostRows(w, spec, salt)
+        r = roots if roots is not None else synth.root_tokens(w["seed"], salt, w["B"], w["V"])
+        if cfg["policy"] == "cast":
+            cfg["cast"]["n0"] = cast_n0(rnd)
+        gaps = Gaps()
+        M_try = None if M is None else M.copy()
+        ref = run_round(cfg, np.asarray(r), rows.draft_row, rows.target_row, rnd=round_id(rnd, attempt),
+                        M=M_try, gaps=gaps)
+        if not gaps.near_tie(GAP):
+            ref["M"] = M_try
+            ref["roots"] = np.asarray(r)
+            ref["salt"] = salt
+            return ref, attempt, attempt
+    raise AssertionError("no tie-free draw in %d attempts" % max_attempts)
+
+
+class GpuRound:
+    """GPU side of a workload: a RoundRunner plus device row generators."""
+
+    def __init__(self, w, flags=0):
+        import torch
+        from dynamic_draft_tree_gb300.rounds import RoundRunner
+
+        self.torch = torch
+        self.w = w
+        self.g = g = geometry(w)
+        self.spec = spec_for(w)
+        B, V, k = w["B"], w["V"], w["k"]
+        kw = {}
+        if w["policy"] == "cast":
+            cc = w["cast"]
+            kw = dict(cast=dict(cc), cast_tables=cast_tables(B, cc["M_rows"], cc["N_cols"], cc["L"]))
+        if w["policy"] == "graft":
+            kw = dict(graft=w["graft"], template=chain_template(k, w["D"]))
+        self.run = RoundRunner(w["policy"], B, V, w["K"], k, g["D_max"], g["P"], g["D_path"], g["m_cap"],
+                               self.spec.dtype, T=w["T"], flags=flags, **kw)
+        dt = torch.int16 if self.spec.dtype == synth.BF16 else torch.float32
+        self.dbuf = torch.zeros((B, k, V), dtype=dt, device="cuda")
+        self.tbuf = torch.zeros((B, g["P"], V), dtype=dt, device="cuda")
+        self.M = None
+        if w["policy"] == "graft":
+            self.M = torch.full((B, V, 8), -1, dtype=torch.int32, device="cuda")
+
+    def round(self, rnd, attempt, roots):
+        torch, w, g = self.torch, self.w, self.g
+        salt = salt_of(w, rnd, attempt)
+        dk = w["recipe"]["depthkey"]
+        V, k = w["V"], w["k"]
+
+        def draft_rows(d, ftok):
+            F = 1 if d == 1 else k
+            ctx = ftok[:, :F].contiguous().view(-1)
+            synth.gen_rows_gpu(torch, self.spec, w["seed"], salt, synth.DRAFT, ctx, self.dbuf, V,
+                               depth_add=d if dk else 0, rows_per_b=F)
+            return self.dbuf
+
+        def target_rows(meta):
+            synth.gen_rows_gpu(torch, self.spec, w["seed"], salt, synth.TARGET, meta.tokens.view(-1), self.tbuf,
+                               V, depth_dev=meta.depth.view(-1) if dk else None, depth_add=1 if dk else 0,
+                               rows_per_b=g["P"])
+            return self.tbuf
+
+        roots_dev = torch.as_tensor(np.asarray(roots, np.int32)).cuda()
+        self.run.run(roots_dev, draft_rows, target_rows, seed=w["seed"], rnd=round_id(rnd, attempt), M=self.M,
+                     n0=cast_n0(rnd))
+
+
+def tree_numpy(h):
+    from dynamic_draft_tree_gb300 import dt_get_tree
+
+    t = dt_get_tree(h)
+    B = t["B"]
+    return {k: (v[:B].cpu().numpy() if hasattr(v, "cpu") else v) for k, v in t.items()}
+
+
+def assert_close(gpu, ref, what):
+    ref = np.asarray(ref, np.float64)
+    gpu = np.asarray(gpu, np.float64)
+    both_inf = np.isinf(ref) & (gpu == ref)
+    err = np.abs(gpu - ref)
+    bound = TOL * np.maximum(1.0, np.abs(ref))
+    bad = ~both_inf & ~(err <= bound)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} values off; first at {tuple(i)}: gpu {gpu[tuple(i)]!r} "
+                             f"oracle {ref[tuple(i)]!r}")
+
+
+def compare_round(gr, ref, check_tree=True):
+    """Element-wise comparison of a GPU round against the oracle's."""
+    run = gr.run
+    w = gr.w
+    B = w["B"]
+    ot = ref["tree"]
+    if check_tree:
+        t = tree_numpy(run.h)
+        valid = ot.token >= 0
+        np.testing.assert_array_equal(t["token"], ot.token, err_msg="tree tokens")
+        np.testing.assert_array_equal(t["parent"][valid], ot.parent[valid], err_msg="tree parents")
+        assert_close(t["logc"][valid], ot.logc[valid], "log confidences")
+        assert_close(t["value"][valid], ot.value[valid], "log values")
+        assert t["depth"] == ot.cur_depth or w["policy"] != "eagle", "depth"
+    meta = run.meta.numpy()
+    om = ref["meta"]
+    for key in ("n_pos", "tokens", "parents", "depth", "node_id", "position_ids", "n_leaves", "mask", "retrieve"):
+        np.testing.assert_array_equal(meta[key], om[key], err_msg=f"meta {key}")
+    np.testing.assert_array_equal(run.accept_len.cpu().numpy(), ref["accept_len"], err_msg="accept_len")
+    np.testing.assert_array_equal(run.accept_path.cpu().numpy(), ref["accept_path"], err_msg="accept_path")
+    np.testing.assert_array_equal(run.bonus.cpu().numpy(), ref["bonus"], err_msg="bonus")
+    if w["policy"] == "cast":
+        assert int(run.m_dev.cpu()[0]) == ref["m"], "CAST verify count"
+    if w["policy"] == "graft":
+        np.testing.assert_array_equal(run.stage.cpu().numpy(), np.asarray(ref["stage"]), err_msg="graft stage")
+        np.testing.assert_array_equal(gr.M.cpu().numpy(), ref["M"], err_msg="M after refresh")
+    del B

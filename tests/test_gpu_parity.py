@@ -1,0 +1,184 @@
+"""GPU path vs the fp64 oracle, element by element, through the C ABI (needs a GB300)."""
+import numpy as np
+import pytest
+
+import synth
+from synth.workloads import with_sizes, spec_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    return t
+
+
+# ----------------------------------------------------------------- generator ----
+@pytest.mark.parametrize("name,over", [("pr1", dict(V=4099)), ("vicuna", dict(V=32000)),
+                                       ("cast", dict(V=128256)), ("stress", dict(V=5003, B=6))])
+def test_device_generator_matches_host_bitwise(torch, name, over):
+    w = with_sizes(name, **over)
+    spec = spec_for(w)
+    rng = np.random.default_rng(1)
+    B, F = w["B"], 3
+    ctx = rng.integers(-1, w["V"], B * F).astype(np.int32)
+    depth = rng.integers(0, 9, B * F).astype(np.int32)
+    for stream in (synth.DRAFT, synth.TARGET):
+        host = np.zeros((B * F, w["V"]), spec.np_dtype)
+        for b in range(B):
+            host[b * F:(b + 1) * F] = synth.gen_rows_cpu(spec, 7, 3, stream, ctx[b * F:(b + 1) * F],
+                                                         depth[b * F:(b + 1) * F], 1, F, b0=b)
+        dt = torch.int16 if spec.dtype == synth.BF16 else torch.float32
+        dev = torch.zeros((B * F, w["V"]), dtype=dt, device="cuda")
+        synth.gen_rows_gpu(torch, spec, 7, 3, stream, torch.from_numpy(ctx).cuda(), dev, w["V"],
+                           depth_dev=torch.from_numpy(depth).cuda(), depth_add=1, rows_per_b=F)
+        got = dev.cpu().numpy().view(spec.np_dtype)
+        assert np.array_equal(got, host)
+
+
+# ------------------------------------------------------------ single layer ----
+def _expand_case(torch, V, K, B, dtype, rows_fn, F=1, W=None):
+    import dynamic_draft_tree_gb300 as dt
+    from oracle.tree import OracleTree
+
+    W = W or max(F, 1)
+    h = dt.Handle(B, V, K, W, 2, 8, dtype)
+    roots = np.arange(B, dtype=np.int32) % V
+    dt.dt_tree_reset(h, torch.from_numpy(roots).cuda())
+    x = rows_fn(B, V)  # float64 [B][V], exactly representable in dtype
+    tdt = torch.bfloat16 if dtype == dt.DT_BF16 else torch.float32
+    logits = torch.from_numpy(x).to(tdt).cuda().reshape(B, 1, V).contiguous()
+    dt.dt_expand_layer(h, logits, 1)
+    assert dt.dt_get_status(h) == 0
+    ot = OracleTree(B, K, W, 2, roots)
+    ot.expand_layer(x.reshape(B, 1, V))
+    t = dt.dt_get_tree(h)
+    from harness import assert_close
+
+    tok = t["token"][:B].cpu().numpy()
+    np.testing.assert_array_equal(tok, ot.token)
+    valid = ot.token >= 0
+    np.testing.assert_array_equal(t["parent"][:B].cpu().numpy()[valid], ot.parent[valid])
+    assert_close(t["logc"][:B].cpu().numpy()[valid], ot.logc[valid], "logc")
+    assert_close(t["value"][:B].cpu().numpy()[valid], ot.value[valid], "value")
+    order = t["layer_order"][:B, 1, :K].cpu().numpy()
+    for b in range(B):
+        np.testing.assert_array_equal(order[b], ot.layer_sorted[b][1])
+    h.close()
+
+
+def _bf16_exact(x):
+    import torch as t
+
+    return t.from_numpy(x).to(t.bfloat16).to(t.float64).numpy()
+
+
+@pytest.mark.parametrize("V,K,B", [(1000, 10, 3), (1001, 4, 2), (4096 * 3 + 5, 32, 2), (32000, 1, 4),
+                                   (128256, 10, 8), (151936, 8, 3), (17, 17, 1)])
+def test_expand_layer_bf16(torch, V, K, B):
+    rng = np.random.default_rng(V + K)
+    _expand_case(torch, V, K, B, 0, lambda B, V: _bf16_exact(rng.normal(0, 2, (B, V))))
+
+
+@pytest.mark.parametrize("V,K,B", [(1000, 8, 2), (128256, 8, 4), (3, 2, 1)])
+def test_expand_layer_f32(torch, V, K, B):
+    rng = np.random.default_rng(V * 7 + K)
+    _expand_case(torch, V, K, B, 1, lambda B, V: rng.normal(0, 2, (B, V)).astype(np.float32).astype(np.float64))
+
+
+def test_expand_layer_all_equal_and_neg_inf(torch):
+    _expand_case(torch, 5000, 10, 2, 0, lambda B, V: np.zeros((B, V)))
+    def rows(B, V):
+        x = np.full((B, V), -np.inf)
+        x[:, ::97] = _bf16_exact(np.random.default_rng(3).normal(0, 1, (B, x[:, ::97].shape[1])))
+        return x
+    _expand_case(torch, 6000, 12, 2, 0, rows)
+
+
+def test_expand_layer_nan_sets_status(torch):
+    import dynamic_draft_tree_gb300 as dt
+
+    h = dt.Handle(1, 3000, 4, 1, 2, 8, dt.DT_F32)
+    dt.dt_tree_reset(h, torch.zeros(1, dtype=torch.int32, device="cuda"))
+    x = torch.zeros((1, 1, 3000), dtype=torch.float32, device="cuda")
+    x[0, 0, 1234] = float("nan")
+    dt.dt_expand_layer(h, x, 1)
+    assert dt.dt_get_status(h) & dt.DT_DEV_BAD_LOGITS
+    h.close()
+
+
+def test_timeout_path_reports_status(torch):
+    import dynamic_draft_tree_gb300 as dt
+
+    h = dt.Handle(1, 70000, 4, 1, 2, 8, dt.DT_BF16, flags=dt.DT_FLAG_TEST_TIMEOUT)
+    dt.dt_tree_reset(h, torch.zeros(1, dtype=torch.int32, device="cuda"))
+    x = torch.zeros((1, 1, 70000), dtype=torch.bfloat16, device="cuda")
+    dt.dt_expand_layer(h, x, 1)
+    assert dt.dt_get_status(h) & dt.DT_DEV_TIMEOUT
+    dt.dt_clear_status(h)
+    assert dt.dt_get_status(h) == 0
+    h.close()
+
+
+def test_host_argument_errors(torch):
+    import dynamic_draft_tree_gb300 as dt
+
+    h = dt.Handle(2, 1000, 4, 2, 3, 9, dt.DT_BF16)
+    x = torch.zeros((2, 2, 1000), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dt.DtError):
+        dt.dt_expand_layer(h, x, 1)                     # no tree yet
+    dt.dt_tree_reset(h, torch.zeros(2, dtype=torch.int32, device="cuda"))
+    with pytest.raises(dt.DtError):
+        dt.dt_expand_layer(h, x, 3)                     # F > W
+    with pytest.raises(dt.DtError):
+        dt.dt_select_frontier(h)                        # no layer built
+    with pytest.raises(dt.DtError):
+        dt.dt_expand_layer(h, x, 1, ld=999)             # ld < V
+    with pytest.raises(dt.DtError):
+        dt.dt_tree_reset(h, torch.zeros(3, dtype=torch.int32, device="cuda"))  # B > B_max
+    h.close()
+
+
+# --------------------------------------------------------------- full rounds ----
+SMALL = [("pr1", dict(V=4099)), ("pr1", dict(V=32000)), ("vicuna", dict(V=32000)),
+         ("cast", dict(V=20011)), ("graft", dict(V=9001, B=4)), ("stress", dict(V=7001, B=6, D=5)),
+         ("vicuna", dict(V=8192, T=1)), ("pr1", dict(V=3001, K=1, k=1, m=1)), ("pr1", dict(V=3001, m=60))]
+
+
+def _run_rounds(torch, w, rounds):
+    import harness
+
+    gr = harness.GpuRound(w)
+    M = None
+    if w["policy"] == "graft":
+        M = np.full((w["B"], w["V"], 8), -1, np.int64)
+    roots = None
+    rejections = 0
+    for rnd in range(rounds):
+        ref, attempt, rej = harness.oracle_round(w, rnd, roots=roots, M=M)
+        rejections += rej
+        gr.round(rnd, attempt, ref["roots"])
+        from dynamic_draft_tree_gb300 import dt_get_status
+
+        assert dt_get_status(gr.run.h) == 0
+        harness.compare_round(gr, ref)
+        if w["policy"] == "graft":
+            M = ref["M"]
+            roots = ref["bonus"].astype(np.int32)
+    gr.run.h.close()
+    return rejections
+
+
+@pytest.mark.parametrize("name,over", SMALL)
+def test_round_parity_small(torch, name, over):
+    w = with_sizes(name, **over)
+    if w["m"] > 1 and name == "pr1" and over.get("m") == 60:
+        w["D"] = 6
+    _run_rounds(torch, w, 3)
