@@ -1,0 +1,384 @@
+"""Benchmark of the draft-tree hot path on the CAST batch workload (B=8, V=128256, bf16).
+
+One step = one complete round of the path (EAGLE-2 expansion with CAST width/depth pruning for up
+to 8 layers, CAST verify count, rerank, flatten + metadata, greedy verify) over one batch of B=8
+requests, with its inputs already in HBM. The draft and target model forwards are not part of the
+path: their logits are produced by the seeded generator in an untimed recording pass (R rounds,
+each ~289 MB, so every timed step reads a different round: inputs larger than L2), and the timed
+steps replay the path on them. The replay must reproduce the recording pass's outputs bit for bit.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own independent batch (requests shard across GPUs with no
+exchange: weak scaling). The reference arm times the fp64 CPU oracle on a bounded sample.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft-tree rounds/s (expand+rerank+verify) at B=8,V=128256; logits HBM GB/s"
+UNIT = "rounds/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="cast")
+    ap.add_argument("--rec-rounds", type=int, default=16)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_config(w, g):
+    return {"workload": f"{w['policy']} tree round, B={w['B']}, V={w['V']}, bf16 logits, K={w['K']}, "
+                        f"k<={w['k']}, depth<={w['D']}, m<={g['m_cap']}, greedy verify",
+            "B": w["B"], "V": w["V"], "K": w["K"], "k_max": w["k"], "D_max": w["D"], "m_cap": g["m_cap"],
+            "global_batch": w["B"], "inputs": "recorded synthetic rounds replayed from HBM; every step reads a "
+                                              "different round (inputs larger than L2, no flush needed)"}
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6800.0), "measured"
+    return 6800.0, "fallback"
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as tdist
+
+    import synth
+    from synth.workloads import WORKLOADS, spec_for, geometry, cast_tables, chain_template
+    import __graft_entry__
+    from dynamic_draft_tree_gb300 import dt_get_status
+    from dynamic_draft_tree_gb300.rounds import RoundRunner
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if rank == 0 or world > 1:
+        __graft_entry__.build()
+
+    w = dict(WORKLOADS[args.workload])
+    w["seed"] = w["seed"] + 1000 * rank  # independent batch per rank
+    g = geometry(w)
+    spec = spec_for(w)
+    B, V, k, D, P = w["B"], w["V"], w["k"], g["D_max"], g["P"]
+    kw = {}
+    if w["policy"] == "cast":
+        cc = w["cast"]
+        kw = dict(cast=dict(cc), cast_tables=cast_tables(B, cc["M_rows"], cc["N_cols"], cc["L"]))
+    if w["policy"] == "graft":
+        kw = dict(graft=w["graft"], template=chain_template(k, w["D"]))
+    run = RoundRunner(w["policy"], B, V, w["K"], k, D, P, g["D_path"], g["m_cap"], spec.dtype, T=w["T"], **kw)
+    dt = torch.int16 if spec.dtype == synth.BF16 else torch.float32
+    esz = 2 if spec.dtype == synth.BF16 else 4
+    R = args.rec_rounds
+    rec_draft = torch.empty((R, D, B, k, V), dtype=dt, device="cuda")
+    rec_target = torch.empty((R, B, P, V), dtype=dt, device="cuda")
+    roots = torch.empty((R, B), dtype=torch.int32, device="cuda")
+    M = None
+    if w["policy"] == "graft":
+        M = torch.full((B, V, 8), -1, dtype=torch.int32, device="cuda")
+    dk = w["recipe"]["depthkey"]
+
+    # ---- recording pass (untimed): the model forwards are stood in for by the generator ----
+    rec_out, rows_expand, rows_verify = [], [], []
+    for r in range(R):
+        salt = (r << 8)
+        roots[r] = torch.from_numpy(synth.root_tokens(w["seed"], salt, B, V)).cuda()
+        widths = []
+
+        def draft_rows(d, ftok, r=r, salt=salt):
+            F = 1 if d == 1 else k
+            ctx = ftok[:, :F].contiguous().view(-1)
+            widths.append(int((ctx >= 0).sum()))
+            synth.gen_rows_gpu(torch, spec, w["seed"], salt, synth.DRAFT, ctx, rec_draft[r, d - 1], V,
+                               depth_add=d if dk else 0, rows_per_b=F)
+            return rec_draft[r, d - 1]
+
+        def target_rows(meta, r=r, salt=salt):
+            synth.gen_rows_gpu(torch, spec, w["seed"], salt, synth.TARGET, meta.tokens.view(-1), rec_target[r],
+                               V, depth_dev=meta.depth.view(-1) if dk else None, depth_add=1 if dk else 0,
+                               rows_per_b=P)
+            return rec_target[r]
+
+        run.run(roots[r], draft_rows, target_rows, seed=w["seed"], rnd=r, M=M, n0=512 * (1 + r % 16))
+        torch.cuda.synchronize()
+        rec_out.append((run.accept_len.clone(), run.bonus.clone(), run.m_dev.clone()))
+        # rows each kernel actually reads in this round
+        rows_verify.append(int((run.meta.tokens >= 0).sum()))
+        rows_expand.append(widths)
+    assert dt_get_status(run.h) == 0, "device status set during recording"
+
+    # ---- timed replay: the path only, on recorded inputs ----
+    ev_exp = []   # (start, end) events around each expand launch
+    ev_ver = []
+
+    def replay(r, timed):
+        def draft_rows(d, ftok):
+            if timed:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                ev_exp.append([e0, None])
+            return rec_draft[r, d - 1]
+
+        def target_rows(meta):
+            if timed:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                ev_ver.append([e0, None])
+            return rec_target[r]
+
+        run.run(roots[r], draft_rows, target_rows, seed=w["seed"], rnd=r, M=M, n0=512 * (1 + r % 16),
+                after_expand=(lambda: _close(ev_exp)) if timed else None,
+                after_verify=(lambda: _close(ev_ver)) if timed else None)
+
+    def _close(lst):
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record()
+        lst[-1][1] = e1
+
+    for i in range(args.warmup):
+        replay(i % R, False)
+    torch.cuda.synchronize()
+    # consistency: a replayed round equals its recording
+    replay(0, False)
+    torch.cuda.synchronize()
+    consistent = bool(torch.equal(run.accept_len, rec_out[0][0]) and torch.equal(run.bonus, rec_out[0][1]))
+
+    clocks = Clocks(local)
+    if world > 1:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for s in range(args.steps):
+        replay(s % R, True)
+    t1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        tdist.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = world * args.steps / (ms / 1e3)
+
+    # per-kernel figures from the live events
+    exp_ms = [a.elapsed_time(b) for a, b in ev_exp]
+    ver_ms = [a.elapsed_time(b) for a, b in ev_ver]
+    exp_bytes = sum(sum(rows_expand[s % R]) for s in range(args.steps)) * V * esz
+    ver_bytes = sum(rows_verify[s % R] for s in range(args.steps)) * V * esz
+    peak, peak_kind = measured_peaks()
+    ver_gbs = ver_bytes / (sum(ver_ms) / 1e3) / 1e9
+    exp_gbs = exp_bytes / (sum(exp_ms) / 1e3) / 1e9
+    launches_per_round = 1 + (D - 1) + D + (D if w["policy"] in ("cast", "graft") else 0) + \
+        (2 if w["policy"] == "cast" else 0) + 1 + 1 + (3 if w["T"] == 1 else 2) + \
+        (2 if w["policy"] == "graft" else 0)
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if args.e2e_steps > 0:
+        h_draft = torch.empty_like(rec_draft[0], device="cpu").pin_memory()
+        h_target = torch.empty_like(rec_target[0], device="cpu").pin_memory()
+        h_draft.copy_(rec_draft[0])
+        h_target.copy_(rec_target[0])
+        h_roots = roots[0].cpu().pin_memory()
+        out_len = torch.empty((B,), dtype=torch.int32).pin_memory()
+        out_bonus = torch.empty((B,), dtype=torch.int32).pin_memory()
+        out_path = torch.empty(tuple(run.accept_path.shape), dtype=torch.int32).pin_memory()
+        d_draft = torch.empty_like(rec_draft[0])
+        d_target = torch.empty_like(rec_target[0])
+        d_roots = torch.empty_like(roots[0])
+        bi = h_draft.numel() * esz + h_target.numel() * esz + h_roots.numel() * 4
+        bo = (out_len.numel() + out_bonus.numel() + out_path.numel()) * 4
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for s in range(args.e2e_steps):
+            d_roots.copy_(h_roots, non_blocking=True)
+            d_draft.copy_(h_draft, non_blocking=True)
+            d_target.copy_(h_target, non_blocking=True)
+            run.run(d_roots, lambda d, ftok: d_draft[d - 1], lambda meta: d_target, seed=w["seed"], rnd=0, M=M,
+                    n0=512)
+            out_len.copy_(run.accept_len, non_blocking=True)
+            out_bonus.copy_(run.bonus, non_blocking=True)
+            out_path.copy_(run.accept_path, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        e1.record()
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        e2e = {"value": world * args.e2e_steps / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(bi),
+               "d2h_bytes_per_step": int(bo)}
+        assert torch.equal(out_len.cuda(), rec_out[0][0]), "e2e result differs from the recording"
+
+    assert dt_get_status(run.h) == 0, "device status set during the timed region"
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if spec.dtype == synth.BF16 else "f32",
+        "data": "synthetic (seeded counter-hash logits standing in for the draft/target forwards)",
+        "config": dict(workload_config(w, g), parallelism=f"replicas x{world} (independent batches)"),
+        "roofline": {"bound": "hbm", "achieved": ver_gbs, "peak": peak, "unit": "GB/s", "frac": ver_gbs / peak,
+                     "traffic": None, "kernel": "dt_verify (row pass + acceptance walk)",
+                     "peak_source": peak_kind,
+                     "bytes_per_launch": ver_bytes / len(ver_ms), "avg_launch_us": 1e3 * sum(ver_ms) / len(ver_ms)},
+        "kernels": {"dt_verify": {"gbs": ver_gbs, "avg_us": 1e3 * float(np.mean(ver_ms)),
+                                  "avg_bytes": ver_bytes / len(ver_ms)},
+                    "dt_expand_layer": {"gbs": exp_gbs, "avg_us": 1e3 * float(np.mean(exp_ms)),
+                                        "avg_bytes": exp_bytes / len(exp_ms), "launches_per_round": D}},
+        "e2e": e2e,
+        "gpu_launches": launches_per_round * args.steps,
+        "replay_consistent": consistent,
+        "clocks": clk,
+    }
+    return line
+
+
+def run_reference(args):
+    """The fp64 CPU oracle as it stands, on a bounded sample of the same workload."""
+    rank, world, local = dist_env()
+    if rank != 0:
+        return None
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import harness
+    from synth.workloads import WORKLOADS, geometry
+
+    w = dict(WORKLOADS[args.workload])
+    g = geometry(w)
+    # the oracle's rows come from a warm cache so that only the oracle itself is timed
+    times = []
+    for s in range(args.warmup + args.steps):
+        rnd = s % 4
+        harness.oracle_round(w, rnd)  # warms the row cache of this round
+        t = time.perf_counter()
+        harness.oracle_round(w, rnd)
+        dtm = time.perf_counter() - t
+        if s >= args.warmup:
+            times.append(dtm)
+    sec = float(np.sum(times))
+    value = len(times) / sec
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": dict(workload_config(w, g), parallelism="1 host process"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{len(times)} full rounds of the workload (rows pre-generated)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def cpu_baseline_sample(seconds=12.0):
+    """Oracle rounds/s on the host, single process, rows pre-generated: bounded to ~seconds."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import harness
+    from synth.workloads import WORKLOADS
+
+    w = dict(WORKLOADS["cast"])
+    n, sec, rnd = 0, 0.0, 0
+    while sec < seconds and n < 50:
+        harness.oracle_round(w, rnd)
+        t = time.perf_counter()
+        harness.oracle_round(w, rnd)
+        sec += time.perf_counter() - t
+        n += 1
+        rnd += 1
+    return {"value": n / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} full rounds of the CAST workload, rows pre-generated (only the oracle timed)"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_ours(args)
+        if line is not None:
+            line["cpu_baseline"] = cpu_baseline_sample()
+    if line is not None:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -56,7 +56,7 @@ class _DevArray:
 
     def __init__(self, ptr, shape, typestr):
         self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
-                                         "data": (ptr, True), "version": 3, "strides": None}
+                                         "data": (ptr, False), "version": 3, "strides": None}
 
 
 def dt_create(B_max, V, K, W, D_max, P_max, dtype=DT_BF16, flags=0):

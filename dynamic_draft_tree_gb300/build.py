@@ -4,6 +4,7 @@ Each translation unit is compiled in parallel, then linked into one shared
 library next to this file. ``python -m dynamic_draft_tree_gb300.build``.
 """
 import os
+import platform
 import subprocess
 import sys
 
@@ -27,8 +28,24 @@ def nvcc_flags(verbose_ptxas=False):
     return f
 
 
+_ELF_MACHINE = {"x86_64": 62, "aarch64": 183, "arm64": 183}
+
+
+def elf_matches_host(path):
+    """True if the ELF file at path was built for this machine's architecture."""
+    want = _ELF_MACHINE.get(platform.machine())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    if len(head) < 20 or head[:4] != b"\x7fELF" or want is None:
+        return False
+    return int.from_bytes(head[18:20], "little") == want
+
+
 def _stale(out, deps):
-    if not os.path.exists(out):
+    if not os.path.exists(out) or not elf_matches_host(out):
         return True
     t = os.path.getmtime(out)
     return any(os.path.getmtime(d) > t for d in deps)

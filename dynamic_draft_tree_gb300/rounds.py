@@ -69,8 +69,13 @@ class RoundRunner:
         self.prune_out = make_prune_out(width=self.width, stop=self.stop)
         self.verify_out = make_prune_out(m=self.m_dev)
 
-    def run(self, roots, draft_rows, target_rows, seed=0, rnd=0, M=None, n0=0):
-        """Launch one round; returns nothing (outputs live in this object's tensors)."""
+    def run(self, roots, draft_rows, target_rows, seed=0, rnd=0, M=None, n0=0, after_expand=None,
+            after_verify=None):
+        """Launch one round; returns nothing (outputs live in this object's tensors).
+
+        ``after_expand`` / ``after_verify`` (optional) are called right after those launches are
+        enqueued, e.g. to record timing events on the stream.
+        """
         h = self.h
         pol = self.policy
         if pol == "cast":
@@ -86,6 +91,8 @@ class RoundRunner:
                 self.frontier_token[:, 0] = roots
                 F = 1
             dt_expand_layer(h, draft_rows(d, self.frontier_token), F)
+            if after_expand is not None:
+                after_expand()
             if pol == "cast":
                 dt_cast_prune(h, DT_POLICY_CAST_WIDTH_DEPTH, self.params, self.prune_out)
             elif pol == "graft":
@@ -103,5 +110,7 @@ class RoundRunner:
         logits = target_rows(self.meta)
         dt_verify(h, self.meta, logits, DT_SAMPLE if self.T == 1 else DT_GREEDY, seed, rnd, self.accept_len,
                   self.accept_path, self.bonus, self.top8)
+        if after_verify is not None:
+            after_verify()
         if pol == "graft":
             dt_adj_update(h, M, self.meta, self.top8)

@@ -51,16 +51,28 @@ class SpecC(ctypes.Structure):
                 ("peak_hi", ctypes.c_void_p), ("ln_table", ctypes.c_void_p)]
 
 
+def _fresh(lib, src):
+    """lib exists, is newer than src and is an ELF file for this machine."""
+    import platform
+
+    want = {"x86_64": 62, "aarch64": 183, "arm64": 183}.get(platform.machine())
+    if not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(src):
+        return False
+    with open(lib, "rb") as f:
+        head = f.read(20)
+    return head[:4] == b"\x7fELF" and int.from_bytes(head[18:20], "little") == want
+
+
 def build_cpu(force=False):
     src = os.path.join(HERE, "synth_cpu.c")
-    if force or not os.path.exists(CPU_LIB) or os.path.getmtime(CPU_LIB) < os.path.getmtime(src):
+    if force or not _fresh(CPU_LIB, src):
         subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
                                "-o", CPU_LIB, src, "-lm"])
 
 
 def build_gpu(force=False, arch="103a"):
     src = os.path.join(HERE, "synth_gpu.cu")
-    if force or not os.path.exists(GPU_LIB) or os.path.getmtime(GPU_LIB) < os.path.getmtime(src):
+    if force or not _fresh(GPU_LIB, src):
         subprocess.check_call(["nvcc", "-O3", f"-gencode=arch=compute_{arch},code=sm_{arch}",
                                "-lineinfo", "-Xcompiler", "-fPIC", "-shared", "-o", GPU_LIB, src])
 

@@ -12,9 +12,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def libdt():
-    from dynamic_draft_tree_gb300 import build
+    import __graft_entry__
 
-    build.build()
+    __graft_entry__._load_builder().build()
     from dynamic_draft_tree_gb300 import _lib
 
     return _lib
