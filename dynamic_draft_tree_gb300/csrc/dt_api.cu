@@ -74,6 +74,15 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
     return cuda_fail(e, "cudaDeviceGetAttribute");
   }
 
+  e = dt::init_tree_attributes();
+  if (e == cudaSuccess) e = dt::init_verify_attributes();
+  if (e == cudaSuccess) e = dt::init_select_attributes();
+  if (e == cudaSuccess) e = dt::init_meta_attributes();
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "cudaFuncSetAttribute");
+  }
+
   const size_t BN = (size_t)c.B_max * h->N;
   const size_t rows_max = (size_t)c.B_max * std::max(c.W, c.P_max);
   Carver cv;

@@ -115,6 +115,13 @@ cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* lo
 cudaError_t launch_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta, const int32_t* top8,
                               cudaStream_t s);
 
+// One-time kernel attributes (dynamic shared memory limits), set by dt_create so that no launch
+// path calls a non-stream API (launches stay capturable in CUDA graphs).
+cudaError_t init_tree_attributes();
+cudaError_t init_verify_attributes();
+cudaError_t init_select_attributes();
+cudaError_t init_meta_attributes();
+
 // Segments per row for a row-scan launch of `rows` rows of V elements.
 int choose_segments(const dt_handle* h, int64_t rows, int64_t V, int elt_bytes);
 

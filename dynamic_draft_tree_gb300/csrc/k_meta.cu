@@ -177,6 +177,11 @@ __global__ void __launch_bounds__(kMetaThreads) build_meta_kernel(MetaArgs a) {
 
 }  // namespace
 
+cudaError_t init_meta_attributes() {
+  // node -> position map of the largest tree: 16384 int16 entries
+  return cudaFuncSetAttribute(build_meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 2);
+}
+
 cudaError_t launch_build_meta(dt_handle* h, const int32_t* selected, int m_cap, const int32_t* ret_token,
                               const int32_t* ret_parent, const int32_t* ret_count, int R_cap,
                               const int32_t* pos_offset, const dt_tree_meta* meta, cudaStream_t s) {
@@ -192,8 +197,6 @@ cudaError_t launch_build_meta(dt_handle* h, const int32_t* selected, int m_cap, 
   a.pos_offset = pos_offset;
   a.meta = *meta;
   const size_t smem = ((size_t)h->N * sizeof(int16_t) + 15) / 16 * 16;
-  cudaError_t e = cudaFuncSetAttribute(build_meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   build_meta_kernel<<<h->B, kMetaThreads, smem, s>>>(a);
   return cudaGetLastError();
 }

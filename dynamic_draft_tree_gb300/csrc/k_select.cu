@@ -107,6 +107,21 @@ struct PruneArgs {
   int B, N, LW, D, d, policy;
 };
 
+// Batch-averaged utility items[s] = (1/B) sum_b v_b(s), s < cap, with v_b(s) given by `vb`.
+// One warp per item; lanes take requests b = lane, lane + 32, ... and reduce in a fixed order, so
+// the result is deterministic.
+template <typename F>
+__device__ __forceinline__ void batch_items(double* items, int cap, int B, F vb) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int s = warp; s < cap; s += nw) {
+    double acc = 0.0;
+    for (int b = lane; b < B; b += 32) acc += vb(b, s);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    if (lane == 0) items[s] = acc / (double)B;
+  }
+}
+
 // CAST width + depth after layer d (1 CTA).
 __global__ void cast_width_depth_kernel(PruneArgs a) {
   __shared__ double items[kMaxW * kMaxK + 1];
@@ -119,29 +134,25 @@ __global__ void cast_width_depth_kernel(PruneArgs a) {
   for (int b = tid; b < a.B; b += blockDim.x) atomicMax(&maxcand, ws.layer_count[(int64_t)b * (a.D + 1) + a.d]);
   __syncthreads();
   const int cap = min(a.p.width_cap, maxcand);
-  // items[s] = (1/B) sum_b exp(value of the s-th node of b's layer)
-  for (int s = tid; s < cap; s += blockDim.x) {
-    double acc = 0.0;
-    for (int b = 0; b < a.B; ++b) {
-      const int64_t lb = (int64_t)b * (a.D + 1) + a.d;
-      if (s < ws.layer_count[lb]) {
-        const int id = ws.layer_order[lb * a.LW + s];
-        acc += exp((double)ws.value[(int64_t)b * a.N + id]);
-      }
-    }
-    items[s] = acc / (double)a.B;
-  }
+  CastState* cs = ws.cast;
+  // normalised draft cost of k frontier nodes at the current context: c_k = S_D[row][k-1] / S_T[row][0]
+  const int row = table_row((double)(a.p.n0 + cs->ctx_sum), a.p.L, a.p.M_rows);
+  const double t1 = a.p.S_T[(int64_t)row * a.p.N_cols];
+  for (int k = 1 + tid; k <= cap; k += blockDim.x) cost[k] = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / t1;
+  // items[s] = (1/B) sum_b exp(value of the s-th node of b's layer), missing nodes count 0
+  batch_items(items, cap, a.B, [&](int b, int s) {
+    const int64_t lb = (int64_t)b * (a.D + 1) + a.d;
+    if (s >= ws.layer_count[lb]) return 0.0;
+    const int id = ws.layer_order[lb * a.LW + s];
+    return exp((double)ws.value[(int64_t)b * a.N + id]);
+  });
   __syncthreads();
   if (tid != 0) return;
-  CastState* cs = ws.cast;
   if (cap <= 0) {
     a.out.width[0] = 0;
     for (int b = 0; b < a.B; ++b) a.out.stop[b] = 1;
     return;
   }
-  const int row = table_row((double)(a.p.n0 + cs->ctx_sum), a.p.L, a.p.M_rows);
-  const double t1 = a.p.S_T[(int64_t)row * a.p.N_cols];
-  for (int k = 1; k <= cap; ++k) cost[k] = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / t1;
   const int n = selection_rule(items, cost, a.p.C1, cap);
   double u = 0.0;
   for (int s = 0; s < n; ++s) u += items[s];
@@ -179,21 +190,13 @@ __global__ void cast_verify_kernel(PruneArgs a) {
   __syncthreads();
   const int cap = min(a.p.m_cap, maxn);
   const double* lin = ws.sorted_lin;
-  for (int s = tid; s < cap; s += blockDim.x) {
-    double acc = 0.0;
-    for (int b = 0; b < a.B; ++b) acc += lin[(int64_t)b * a.p.m_cap + s];
-    items[s] = acc / (double)a.B;
-  }
-  __syncthreads();
-  if (tid != 0) return;
-  if (cap <= 0) {
-    a.out.m[0] = 0;
-    return;
-  }
   const int row = table_row((double)a.p.n0, a.p.L, a.p.M_rows);
   const double t1 = a.p.S_T[(int64_t)row * a.p.N_cols];
-  for (int k = 1; k <= cap; ++k) cost[k] = a.p.S_T[(int64_t)row * a.p.N_cols + (k - 1)] / t1;
-  a.out.m[0] = selection_rule(items, cost, a.p.C3, cap);
+  for (int k = 1 + tid; k <= cap; k += blockDim.x) cost[k] = a.p.S_T[(int64_t)row * a.p.N_cols + (k - 1)] / t1;
+  batch_items(items, cap, a.B, [&](int b, int s) { return lin[(int64_t)b * a.p.m_cap + s]; });
+  __syncthreads();
+  if (tid != 0) return;
+  a.out.m[0] = cap <= 0 ? 0 : selection_rule(items, cost, a.p.C3, cap);
 }
 
 // Graft checkpoint after layer d: one thread per request.
@@ -230,6 +233,11 @@ int next_pow2(int n) {
 
 }  // namespace
 
+cudaError_t init_select_attributes() {
+  // largest node count: 1 + 32 + 15 * 1024 slots -> 16384 keys of 8 bytes
+  return cudaFuncSetAttribute(sort_nodes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 8);
+}
+
 static cudaError_t launch_sort(dt_handle* h, int mode, const int32_t* m, int m_len, int m_cap, int32_t* selected,
                                cudaStream_t s) {
   SortArgs a;
@@ -243,8 +251,6 @@ static cudaError_t launch_sort(dt_handle* h, int mode, const int32_t* m, int m_l
   a.m_cap = m_cap;
   a.selected = selected;
   const size_t smem = (size_t)a.n_pad * sizeof(uint64_t);
-  cudaError_t e = cudaFuncSetAttribute(sort_nodes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   const int threads = std::min(1024, std::max(32, a.n_pad / 2));
   sort_nodes_kernel<<<h->B, threads, smem, s>>>(a);
   return cudaGetLastError();

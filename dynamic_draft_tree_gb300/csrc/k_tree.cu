@@ -150,25 +150,13 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
   __syncthreads();
   // empty keys are 0 and rank below every real key
   select_topk(sm, nk, a.K);
-  if (tid == 0) {
-    float M = -INFINITY;
-    for (int s = 0; s < a.S; ++s) M = fmaxf(M, __ldcg(&part[s].m));
-    double S = 0.0;
-    bool nan = false;
-    for (int s = 0; s < a.S; ++s) {
-      const float ms = __ldcg(&part[s].m);
-      const double ss = __ldcg(&part[s].s);
-      if (ss != ss) nan = true;
-      if (ms == -INFINITY) continue;
-      S += ss * (double)ex2((ms - M) * kLog2e);
-    }
-    if (nan || !(M > -INFINITY) || M == INFINITY || !(S > 0.0)) set_status(ws.status, DT_DEV_BAD_LOGITS);
-    sm.red_m[0] = M;
-    sm.red_s[0] = log(S);
-  }
-  __syncthreads();
-  const float M = sm.red_m[0];
-  const double logS = sm.red_s[0];
+  float M;
+  double Ssum;
+  bool nan;
+  merge_softmax(part, a.S, sm, M, Ssum, nan);
+  if (tid == 0 && (nan || !(M > -INFINITY) || M == INFINITY || !(Ssum > 0.0)))
+    set_status(ws.status, DT_DEV_BAD_LOGITS);
+  const double logS = log(Ssum);
   const int pid = ws.frontier[(int64_t)b * a.W + f];
   const float pval = ws.value[(int64_t)b * a.N + pid];
   if (tid < a.K) {
@@ -235,6 +223,14 @@ static int64_t seg_len_for(int64_t V, int S) {
 
 static size_t row_smem_bytes() { return (size_t)kStages * kTileBytes; }
 
+cudaError_t init_tree_attributes() {
+  const int smem = (int)row_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(expand_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(expand_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return e;
+}
+
 cudaError_t launch_tree_reset(dt_handle* h, const int32_t* root, cudaStream_t s) {
   const int64_t total = (int64_t)h->B * h->N;
   int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)h->num_sms * 4);
@@ -277,17 +273,11 @@ cudaError_t launch_expand(dt_handle* h, const void* logits, int64_t ld, int F, c
   a.first_wait_cap = (h->cfg.flags & DT_FLAG_TEST_TIMEOUT) ? 0u : kSpinCap;
   const unsigned grid = (unsigned)(rows * S);
   const size_t smem = row_smem_bytes();
-  cudaError_t e;
-  if (h->cfg.dtype == DT_BF16) {
-    e = cudaFuncSetAttribute(expand_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+  if (h->cfg.dtype == DT_BF16)
     expand_kernel<uint16_t><<<grid, kRowThreads, smem, s>>>(a);
-  } else {
-    e = cudaFuncSetAttribute(expand_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+  else
     expand_kernel<float><<<grid, kRowThreads, smem, s>>>(a);
-  }
-  e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) h->depth = d;
   return e;
 }

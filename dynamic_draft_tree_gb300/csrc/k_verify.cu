@@ -63,24 +63,17 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(RowPassArgs
   if (tid < kMaxK) sm.topk[tid] = 0ull;
   __syncthreads();
   select_topk(sm, nk, a.K);
+  float M = -INFINITY;
+  double Ssum = 0.0;
+  bool nan = false;
+  if (SOFTMAX) merge_softmax(part, a.S, sm, M, Ssum, nan);
   if (tid == 0) {
     RowStat st;
     st.amax = (int32_t)key_id(sm.topk[0]);
     if (SOFTMAX) {
-      float M = -INFINITY;
-      for (int s = 0; s < a.S; ++s) M = fmaxf(M, __ldcg(&part[s].m));
-      double S = 0.0;
-      bool nan = false;
-      for (int s = 0; s < a.S; ++s) {
-        const float ms = __ldcg(&part[s].m);
-        const double ss = __ldcg(&part[s].s);
-        if (ss != ss) nan = true;
-        if (ms == -INFINITY) continue;
-        S += ss * (double)ex2((ms - M) * kLog2e);
-      }
-      if (nan || !(M > -INFINITY) || M == INFINITY || !(S > 0.0)) set_status(ws.status, DT_DEV_BAD_LOGITS);
+      if (nan || !(M > -INFINITY) || M == INFINITY || !(Ssum > 0.0)) set_status(ws.status, DT_DEV_BAD_LOGITS);
       st.m = M;
-      st.s = S;
+      st.s = Ssum;
     } else {
       st.m = key_value(sm.topk[0]);
       st.s = 0.0;
@@ -142,6 +135,8 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
   __shared__ int32_t s_first_child[kMaxP], s_next_sib[kMaxP];
   __shared__ int32_t s_path[kMaxP];
   __shared__ int32_t s_rej[kMaxP];
+  __shared__ int32_t s_tok[kMaxP], s_par[kMaxP], s_amax[kMaxP], s_depth[kMaxP];
+  __shared__ uint8_t s_reach[kMaxP], s_haschild[kMaxP];
   __shared__ unsigned long long s_best;
   __shared__ int32_t s_cur, s_len, s_nrej, s_state;
   __shared__ double s_sres;
@@ -151,35 +146,61 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
   const int Dp = a.meta.D_path;
   const Workspace& ws = a.ws;
   const int64_t rb = (int64_t)b * P;
-  const int npos = a.meta.n_pos[b];
+  const int npos = min(a.meta.n_pos[b], P);
 
+  // stage the flattened tree (coalesced, independent loads)
+  for (int p = tid; p < P; p += blockDim.x) {
+    const bool used = p < npos;
+    s_tok[p] = used ? a.meta.tokens[rb + p] : -1;
+    s_par[p] = used ? a.meta.parents[rb + p] : -1;
+    s_depth[p] = used ? a.meta.depth[rb + p] : -1;
+    s_haschild[p] = 0;
+  }
+  __syncthreads();
   if (a.mode == DT_GREEDY) {
+    for (int p = tid; p < npos; p += blockDim.x) {
+      s_amax[p] = s_tok[p] >= 0 ? ws.row_stats[rb + p].amax : -1;
+      if (p > 0 && s_par[p] >= 0) s_haschild[s_par[p]] = 1;
+    }
     if (tid == 0) s_best = 0ull;
     __syncthreads();
-    const int nl = a.meta.n_leaves[b];
-    for (int l = tid; l < nl; l += blockDim.x) {
-      const int32_t* row = a.meta.retrieve + (rb + l) * Dp;
-      int cnt = 0;
-      for (int j = 1; j < Dp; ++j) {
-        const int p = row[j];
-        if (p < 0) break;
-        const int t = a.meta.tokens[rb + p];
-        if (t >= 0 && t == ws.row_stats[rb + row[j - 1]].amax) ++cnt;
-        else break;
+    // reach[p]: every position on the path root..p matches the argmax of its parent's row
+    for (int p = tid; p < npos; p += blockDim.x) {
+      bool ok = true;
+      for (int q = p, guard = 0; q > 0 && ok && guard < kMaxP; q = s_par[q], ++guard) {
+        const int pq = s_par[q];
+        ok = pq >= 0 && s_tok[q] >= 0 && s_tok[q] == s_amax[pq];
       }
-      // larger count wins, then the earlier row
-      const unsigned long long key = ((unsigned long long)(cnt + 1) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)l);
+      s_reach[p] = ok ? 1 : 0;
+    }
+    __syncthreads();
+    // every leaf: its accepted count is the depth of its deepest reachable ancestor; the largest
+    // count wins, ties go to the leaf of lowest position (retrieve rows are in leaf order)
+    for (int p = tid; p < npos; p += blockDim.x) {
+      if (s_haschild[p]) continue;
+      int q = p, guard = 0;
+      while (q > 0 && !s_reach[q] && guard++ < kMaxP) q = s_par[q];
+      if (q < 0) q = 0;
+      const int cnt = s_depth[q];
+      const unsigned long long key = ((unsigned long long)(cnt + 1) << 32) |
+                                     ((unsigned long long)(0xFFFFu - (uint32_t)p) << 16) | (uint32_t)q;
       atomicMax(&s_best, key);
     }
     __syncthreads();
     const int cnt = (int)(s_best >> 32) - 1;
-    const int l = (int)(0xFFFFFFFFu - (uint32_t)(s_best & 0xFFFFFFFFull));
-    const int32_t* row = a.meta.retrieve + (rb + l) * Dp;
-    for (int j = tid; j < Dp; j += blockDim.x) a.accept_path[(int64_t)b * Dp + j] = j <= cnt ? row[j] : -1;
+    const int last = (int)(s_best & 0xFFFFull);
     if (tid == 0) {
+      for (int j = 0; j < Dp; ++j) s_path[j] = -1;
+      int q = last;
+      for (int j = cnt; j >= 0 && j < Dp; --j) {
+        s_path[j] = q;
+        q = s_par[q];
+      }
       a.accept_len[b] = cnt;
-      a.bonus[b] = ws.row_stats[rb + row[cnt]].amax;
+      a.bonus[b] = s_amax[last];
     }
+    __syncthreads();
+    for (int j = tid; j < Dp; j += blockDim.x) a.accept_path[(int64_t)b * Dp + j] = s_path[j];
     return;
   }
 
@@ -190,7 +211,7 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
       s_next_sib[p] = -1;
     }
     for (int p = npos - 1; p >= 1; --p) {  // children in increasing position
-      const int q = a.meta.parents[rb + p];
+      const int q = s_par[p];
       if (q >= 0 && q < P) {
         s_next_sib[p] = s_first_child[q];
         s_first_child[q] = p;
@@ -216,7 +237,7 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
     while (child >= 0) {
       __syncthreads();  // every thread is done with the previous step's shared state
       if (tid == 0) {
-        const int t = a.meta.tokens[rb + child];
+        const int t = s_tok[child];
         bool skip = t < 0;
         if (t >= a.V) {
           set_status(ws.status, DT_DEV_BAD_TOKEN);
@@ -234,7 +255,7 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
       }
       __syncthreads();
       if (tid == 0 && st0 != 3) {
-        const int t = a.meta.tokens[rb + child];
+        const int t = s_tok[child];
         const float x = load_logit(a.logits, a.dtype, (rb + cur) * a.ld + t);
         const float e = ex2((x - st.m) * kLog2e);
         const double p = (double)e / s_sres;
@@ -348,6 +369,16 @@ __global__ void __launch_bounds__(kBonusThreads) verify_bonus_kernel(BonusArgs a
 
 }  // namespace
 
+cudaError_t init_verify_attributes() {
+  const int smem = kStages * kTileBytes;
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(verify_rows_kernel<uint16_t, false>, a, smem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<uint16_t, true>, a, smem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<float, false>, a, smem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<float, true>, a, smem);
+  return e;
+}
+
 cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int mode,
                           uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path,
                           int32_t* bonus, int32_t* top8, cudaStream_t s) {
@@ -373,13 +404,7 @@ cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* lo
   const unsigned grid = (unsigned)(rows * ra.S);
   const size_t smem = (size_t)kStages * kTileBytes;
   cudaError_t e;
-#define DT_LAUNCH_ROWS(T, SM)                                                                            \
-  do {                                                                                                   \
-    e = cudaFuncSetAttribute(verify_rows_kernel<T, SM>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
-                             (int)smem);                                                                 \
-    if (e != cudaSuccess) return e;                                                                      \
-    verify_rows_kernel<T, SM><<<grid, kRowThreads, smem, s>>>(ra);                                       \
-  } while (0)
+#define DT_LAUNCH_ROWS(T, SM) verify_rows_kernel<T, SM><<<grid, kRowThreads, smem, s>>>(ra)
   const bool sm_on = mode == DT_SAMPLE;
   if (h->cfg.dtype == DT_BF16) {
     if (sm_on) DT_LAUNCH_ROWS(uint16_t, true);

@@ -115,6 +115,39 @@ __device__ __forceinline__ int compact_topk(ScanSmem& sm, int cnt, int K) {
   return n;
 }
 
+// Merge of the S (<= blockDim) segment partials of a row by the whole CTA:
+// M = max_s m_s, S = sum_s s_s * exp(m_s - M). Every thread gets the results; `nan` reports a
+// poisoned (NaN) segment sum. All threads must call it.
+__device__ __forceinline__ void merge_softmax(const Partial* part, int S, ScanSmem& sm, float& M, double& Sum,
+                                              bool& nan) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float ms = -INFINITY;
+  double ss = 0.0;
+  if (tid < S) {
+    ms = __ldcg(&part[tid].m);
+    ss = __ldcg(&part[tid].s);
+  }
+  float bm = ms;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, o));
+  if (lane == 0) sm.red_m[warp] = bm;
+  __syncthreads();
+  M = -INFINITY;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) M = fmaxf(M, sm.red_m[w]);
+  double c = 0.0;
+  if (ss != ss) c = ss;
+  else if (ms != -INFINITY) c = ss * (double)ex2((ms - M) * kLog2e);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+  __syncthreads();  // red_m reads are done before red_s is written
+  if (lane == 0) sm.red_s[warp] = c;
+  __syncthreads();
+  Sum = 0.0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) Sum += sm.red_s[w];
+  nan = Sum != Sum;
+  __syncthreads();
+}
+
 struct SegOut {
   float m;        // thread 0 only (softmax scans); all threads: best key value otherwise
   double s;       // thread 0 only
