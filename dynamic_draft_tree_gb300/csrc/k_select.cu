@@ -59,7 +59,9 @@ __global__ void __launch_bounds__(1024) sort_nodes_kernel(SortArgs a) {
   }
   __syncthreads();
   const int n = cnt;
-  block_bitonic_desc(keys, a.n_pad);
+  int n_pad = 2;  // sort only the valid nodes (padded with empty keys to a power of two)
+  while (n_pad < n) n_pad <<= 1;
+  block_bitonic_desc(keys, n_pad);
   if (a.mode == 0) {
     int mb = a.m ? a.m[a.m_len == 1 ? 0 : b] : a.m_cap;
     mb = max(0, min(min(mb, a.m_cap), n));
@@ -87,15 +89,15 @@ __device__ __forceinline__ int table_row(double c, double L, int M_rows) {
 
 // Marginal-utility selection over k = 1..cap (thread-serial; cap <= 512).
 __device__ int selection_rule(const double* items, const double* cost, double thr, int cap) {
+  // du = items[k0] + ... + items[k-1], accumulated in that order as k advances
   int k0 = 1;
+  double du = 0.0;
   for (int k = 2; k <= cap; ++k) {
-    if (cost[k] <= cost[k0]) {
+    du += items[k - 1];
+    if (cost[k] <= cost[k0] || du / (cost[k] - cost[k0]) >= thr) {
       k0 = k;
-      continue;
+      du = 0.0;
     }
-    double du = 0.0;
-    for (int s = k0; s < k; ++s) du += items[s];
-    if (du / (cost[k] - cost[k0]) >= thr) k0 = k;
   }
   return k0;
 }

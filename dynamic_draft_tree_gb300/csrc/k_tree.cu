@@ -156,9 +156,13 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
   merge_softmax(part, a.S, sm, M, Ssum, nan);
   if (tid == 0 && (nan || !(M > -INFINITY) || M == INFINITY || !(Ssum > 0.0)))
     set_status(ws.status, DT_DEV_BAD_LOGITS);
-  const double logS = log(Ssum);
   const int pid = ws.frontier[(int64_t)b * a.W + f];
   const float pval = ws.value[(int64_t)b * a.N + pid];
+  double logS = 0.0;
+  if (tid < 32) {  // one fp64 log per row, broadcast over the first warp (K <= 32)
+    if (tid == 0) logS = log(Ssum);
+    logS = __shfl_sync(0xFFFFFFFFu, logS, 0);
+  }
   if (tid < a.K) {
     const uint64_t k = sm.topk[tid];
     const int id = a.base + f * a.K + tid;

@@ -120,30 +120,37 @@ __device__ __forceinline__ int compact_topk(ScanSmem& sm, int cnt, int K) {
 // poisoned (NaN) segment sum. All threads must call it.
 __device__ __forceinline__ void merge_softmax(const Partial* part, int S, ScanSmem& sm, float& M, double& Sum,
                                               bool& nan) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float ms = -INFINITY;
-  double ss = 0.0;
-  if (tid < S) {
-    ms = __ldcg(&part[tid].m);
-    ss = __ldcg(&part[tid].s);
+  // warp 0 merges (S <= 64: two segments per lane)
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float m0 = -INFINITY, m1 = -INFINITY;
+    double s0 = 0.0, s1 = 0.0;
+    if (lane < S) {
+      m0 = __ldcg(&part[lane].m);
+      s0 = __ldcg(&part[lane].s);
+    }
+    if (lane + 32 < S) {
+      m1 = __ldcg(&part[lane + 32].m);
+      s1 = __ldcg(&part[lane + 32].s);
+    }
+    float bm = fmaxf(m0, m1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, o));
+    double c = 0.0;
+    if (s0 != s0) c += s0;
+    else if (m0 != -INFINITY) c += s0 * (double)ex2((m0 - bm) * kLog2e);
+    if (s1 != s1) c += s1;
+    else if (m1 != -INFINITY) c += s1 * (double)ex2((m1 - bm) * kLog2e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+    if (lane == 0) {
+      sm.red_m[0] = bm;
+      sm.red_s[0] = c;
+    }
   }
-  float bm = ms;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, o));
-  if (lane == 0) sm.red_m[warp] = bm;
   __syncthreads();
-  M = -INFINITY;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) M = fmaxf(M, sm.red_m[w]);
-  double c = 0.0;
-  if (ss != ss) c = ss;
-  else if (ms != -INFINITY) c = ss * (double)ex2((ms - M) * kLog2e);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
-  __syncthreads();  // red_m reads are done before red_s is written
-  if (lane == 0) sm.red_s[warp] = c;
-  __syncthreads();
-  Sum = 0.0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) Sum += sm.red_s[w];
+  M = sm.red_m[0];
+  Sum = sm.red_s[0];
   nan = Sum != Sum;
   __syncthreads();
 }
@@ -416,15 +423,25 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
     __syncthreads();
     float M = -INFINITY;
     for (int w = 0; w < kRowThreads / 32; ++w) M = fmaxf(M, sm.red_m[w]);
-    // NaN in a thread's sum propagates; a thread with m_t = +inf makes M = +inf (caller flags it)
-    double c = 0.0;
+    // NaN in a thread's sum propagates; a thread with m_t = +inf makes M = +inf (caller flags it).
+    // Warp sums are double-float (hi, lo) pairs combined with TwoSum: no fp64 in the hot kernel.
+    float ch = 0.0f, cl = 0.0f;
     if (m_t != -INFINITY || s_hi != s_hi) {
       const float sc = (M == m_t) ? 1.0f : ex2((m_t - M) * kLog2e);
-      c = (double)s_hi * (double)sc + (double)s_lo * (double)sc;
+      ch = s_hi * sc;
+      cl = s_lo * sc;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
-    if (lane == 0) sm.red_s[warp] = c;
+    for (int o = 16; o > 0; o >>= 1) {
+      const float oh = __shfl_xor_sync(0xFFFFFFFFu, ch, o);
+      const float ol = __shfl_xor_sync(0xFFFFFFFFu, cl, o);
+      const float sum = ch + oh;
+      const float bp = sum - ch;
+      const float err = (ch - (sum - bp)) + (oh - bp);
+      ch = sum;
+      cl = cl + ol + err;
+    }
+    if (lane == 0) sm.red_s[warp] = (double)ch + (double)cl;
     __syncthreads();
     if (tid == 0) {
       double S = 0.0;
