@@ -13,10 +13,13 @@ constexpr int kMaxW = 32;
 constexpr int kMaxD = 16;
 constexpr int kMaxP = 512;
 constexpr int kMaxFifo = 16;
-constexpr int kRowThreads = 256;
-constexpr int kTileBytes = 16384;   // one TMA bulk tile
-constexpr int kStages = 4;          // tiles in flight per CTA
-constexpr int kCandCap = 1024;      // candidate keys buffered per CTA
+constexpr int kScanWarps = 4;        // warps of a row-scan CTA
+constexpr int kRowThreads = 32 * kScanWarps;
+constexpr int kStageBytes = 4096;   // one TMA bulk copy into a warp's ring
+constexpr int kWarpStages = 4;      // ring depth per warp
+constexpr int kWarpCand = 128;      // per-warp candidate buffer
+constexpr int kCandCap = 1024;      // CTA merge / sort buffer (keys)
+constexpr int kScanSmemBytes = kScanWarps * kWarpStages * kStageBytes;  // dynamic shared memory
 
 // Per-(row, segment) partial result of a row scan.
 struct Partial {

@@ -206,16 +206,18 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
 }  // namespace
 
 int choose_segments(const dt_handle* h, int64_t rows, int64_t V, int elt_bytes) {
-  const int64_t target = (int64_t)h->num_sms * 3;
-  int64_t S = (target + rows - 1) / rows;
-  const int64_t min_seg = 4096;  // elements
-  const int64_t max_by_len = (V + min_seg - 1) / min_seg;
+  // Enough CTAs for one full wave (3 resident per SM), segments of at most ~64 KB so that many
+  // small CTAs balance across SMs, and at least ~8 KB of work per CTA.
+  const int64_t row_bytes = V * elt_bytes;
+  const int64_t s_fill = ((int64_t)h->num_sms * 3 + rows - 1) / rows;
+  const int64_t s_size = (row_bytes + 65535) / 65536;
+  int64_t S = s_fill > s_size ? s_fill : s_size;
+  const int64_t max_by_len = (row_bytes + 8191) / 8192;
   if (S > max_by_len) S = max_by_len;
   const int64_t max_by_keys = kCandCap / h->cfg.K;
   if (S > max_by_keys) S = max_by_keys;
   if (S > 64) S = 64;
   if (S < 1) S = 1;
-  (void)elt_bytes;
   return (int)S;
 }
 
@@ -225,7 +227,7 @@ static int64_t seg_len_for(int64_t V, int S) {
   return L;
 }
 
-static size_t row_smem_bytes() { return (size_t)kStages * kTileBytes; }
+static size_t row_smem_bytes() { return (size_t)kScanSmemBytes; }
 
 cudaError_t init_tree_attributes() {
   const int smem = (int)row_smem_bytes();

@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kBonusThreads) verify_bonus_kernel(BonusArgs a
 }  // namespace
 
 cudaError_t init_verify_attributes() {
-  const int smem = kStages * kTileBytes;
+  const int smem = kScanSmemBytes;
   const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
   cudaError_t e = cudaFuncSetAttribute(verify_rows_kernel<uint16_t, false>, a, smem);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<uint16_t, true>, a, smem);
@@ -402,7 +402,7 @@ cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* lo
   ra.top8 = top8;
   ra.first_wait_cap = (h->cfg.flags & DT_FLAG_TEST_TIMEOUT) ? 0u : kSpinCap;
   const unsigned grid = (unsigned)(rows * ra.S);
-  const size_t smem = (size_t)kStages * kTileBytes;
+  const size_t smem = (size_t)kScanSmemBytes;
   cudaError_t e;
 #define DT_LAUNCH_ROWS(T, SM) verify_rows_kernel<T, SM><<<grid, kRowThreads, smem, s>>>(ra)
   const bool sm_on = mode == DT_SAMPLE;

@@ -1,18 +1,18 @@
 // Row-segment scan shared by the expand and verify row passes.
 //
-// One CTA streams a contiguous segment of one logits row through a ring of
-// shared-memory tiles filled by 1-D TMA bulk copies (cp.async.bulk, completion
-// counted on an mbarrier per stage), and reduces it to
-//   * the segment max m and s = sum exp(x - m) (online: per-thread running max,
-//     rescaled when it grows; per-tile sums added with a compensation term), and
-//   * the segment top-K under the total order (logit desc, token id asc),
-//     found by filtering against a running threshold key: the first tile sets
-//     it to the K-th largest per-thread maximum, later compactions raise it to
-//     the K-th best candidate so far; only elements at or above it are kept in
-//     a small shared-memory candidate buffer.
-// Unaligned row heads/tails (rows whose start is not 16-byte aligned, or
-// segments whose length is not a whole number of 16-byte vectors) are read
-// with plain loads and always kept as candidates.
+// A CTA of kScanWarps warps reduces one contiguous segment of one logits row to
+//   * the segment max m and s = sum exp(x - m), and
+//   * the segment top-K under the total order (logit desc, token id asc).
+// The segment's 16-byte-aligned middle is split into one contiguous chunk per warp. Each warp
+// streams its chunk through a private ring of shared-memory stages filled by 1-D TMA bulk copies
+// (cp.async.bulk, completion counted on one mbarrier per stage), so warps never wait on each
+// other while streaming; the CTA synchronises once, at the end of the segment.
+//   * softmax: every lane keeps a running max and a compensated sum, rescaled when its max grows;
+//   * top-K: every warp keeps a sorted list of its K best keys spread over its lanes (lane l holds
+//     the l-th best). The list starts as the K best per-lane maxima; afterwards only elements
+//     above the list's K-th key are candidates. Candidates go to a small per-warp buffer and are
+//     inserted into the list with warp shuffles.
+// Unaligned heads/tails (< 16 bytes at each end) are read with plain loads by warp 0.
 #pragma once
 
 #include "dt_internal.cuh"
@@ -80,25 +80,32 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 constexpr uint32_t kSpinCap = 1u << 22;
 
 // ---------------------------------------------------------------- shared state ----
-struct ScanSmem {
-  uint64_t bar[kStages];
-  uint64_t cand[kCandCap];
-  uint64_t topk[kMaxK];
-  unsigned long long tau;   // threshold key (CTA-uniform between syncs)
+struct WarpRing {
+  uint64_t bar[kWarpStages];
+  uint64_t cand[kWarpCand];
   int32_t cnt;
-  int32_t flag;
+  int32_t ovf;
+};
+
+struct ScanSmem {
+  WarpRing ring[kScanWarps];
+  uint64_t topk[kMaxK];
+  float red_m[kScanWarps];
+  double red_s[kScanWarps];
+  int32_t flags[kScanWarps];
   int32_t last;
-  int32_t pad;
-  float red_m[kRowThreads / 32];
-  double red_s[kRowThreads / 32];
+  // Merge / sort buffer of kCandCap keys. It aliases the dynamic stage memory, which is free once
+  // every warp has finished streaming (after the block barrier that ends the scan).
+  uint64_t* cand;
 };
 
 // Top-K (descending) of cand[0..cnt) into sm.topk[0..n), n = min(cnt, K); cand is not modified.
-// Keys are distinct (one per element). All threads must call it.
+// Real keys are distinct (one per element); empty (0) keys rank below them. All threads call it.
 __device__ __forceinline__ int select_topk(ScanSmem& sm, int cnt, int K) {
   const int tid = threadIdx.x;
   for (int i = tid; i < cnt; i += blockDim.x) {
     const uint64_t k = sm.cand[i];
+    if (k == 0ull) continue;
     int rank = 0;
     for (int j = 0; j < cnt; ++j) rank += (sm.cand[j] > k);
     if (rank < K) sm.topk[rank] = k;
@@ -107,20 +114,10 @@ __device__ __forceinline__ int select_topk(ScanSmem& sm, int cnt, int K) {
   return cnt < K ? cnt : K;
 }
 
-// Replaces cand[0..cnt) by its top-K; returns the new count.
-__device__ __forceinline__ int compact_topk(ScanSmem& sm, int cnt, int K) {
-  const int n = select_topk(sm, cnt, K);
-  for (int i = threadIdx.x; i < n; i += blockDim.x) sm.cand[i] = sm.topk[i];
-  __syncthreads();
-  return n;
-}
-
-// Merge of the S (<= blockDim) segment partials of a row by the whole CTA:
-// M = max_s m_s, S = sum_s s_s * exp(m_s - M). Every thread gets the results; `nan` reports a
-// poisoned (NaN) segment sum. All threads must call it.
+// Merge of the S (<= 64) segment partials of a row: M = max_s m_s, S = sum_s s_s * exp(m_s - M).
+// Every thread gets the results; `nan` reports a poisoned (NaN) sum. All threads call it.
 __device__ __forceinline__ void merge_softmax(const Partial* part, int S, ScanSmem& sm, float& M, double& Sum,
                                               bool& nan) {
-  // warp 0 merges (S <= 64: two segments per lane)
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     float m0 = -INFINITY, m1 = -INFINITY;
@@ -155,303 +152,366 @@ __device__ __forceinline__ void merge_softmax(const Partial* part, int S, ScanSm
   __syncthreads();
 }
 
+// ---------------------------------------------------------------- warp top-K list ----
+__device__ __forceinline__ uint64_t shfl_up_u64(uint64_t v, int d) {
+  uint32_t lo = __shfl_up_sync(0xFFFFFFFFu, (uint32_t)v, d);
+  uint32_t hi = __shfl_up_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), d);
+  return ((uint64_t)hi << 32) | lo;
+}
+
+// Inserts key k (same value in every lane) into the lane-distributed descending list L of K keys.
+__device__ __forceinline__ void wl_insert(uint64_t& L, uint64_t k, int K, int lane) {
+  const unsigned gt = __ballot_sync(0xFFFFFFFFu, lane < K && L > k);
+  const int p = __popc(gt);
+  if (p >= K) return;  // warp-uniform
+  const uint64_t up = shfl_up_u64(L, 1);
+  if (lane > p && lane < K) L = up;
+  if (lane == p) L = k;
+}
+
 struct SegOut {
-  float m;        // thread 0 only (softmax scans); all threads: best key value otherwise
-  double s;       // thread 0 only
-  int nkeys;      // all threads: keys in sm.cand[0..nkeys), descending
+  float m;        // thread 0 (softmax scans); every thread: best key value otherwise
+  double s;       // thread 0
+  int nkeys;      // every thread: keys in sm.cand[0..nkeys), descending
   bool timed_out; // a bounded copy wait ran out
   bool internal;  // the overflow refinement bound was hit
   bool bad;       // non-softmax scans: a NaN or +inf was seen
 };
 
-// Scans elements [s0, s1) of `row`. K <= kMaxK. `tiles` is kStages * kTileBytes of shared memory.
+// Per-lane softmax accumulation of one value (head/tail elements).
+__device__ __forceinline__ void lane_acc_one(float x, float& m_t, float& s_hi, float& s_lo) {
+  if (x != x) {
+    s_hi = x;  // NaN poisons the sum
+    return;
+  }
+  if (x == -INFINITY) return;
+  if (x > m_t) {
+    if (m_t != -INFINITY) {
+      const float sc = ex2((m_t - x) * kLog2e);
+      s_hi *= sc;
+      s_lo *= sc;
+    }
+    m_t = x;
+  }
+  const float y = ex2((x - m_t) * kLog2e) - s_lo;
+  const float t = s_hi + y;
+  s_lo = (t - s_hi) - y;
+  s_hi = t;
+}
+
+// Scans elements [s0, s1) of `row`. K <= kMaxK. `stages` is kScanWarps * kWarpStages * kStageBytes of
+// shared memory (dynamic). All threads of the CTA call it.
 template <typename T, bool SOFTMAX>
 __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1, int K, ScanSmem& sm,
-                               uint8_t* tiles, uint32_t first_wait_cap) {
+                               uint8_t* stages, uint32_t first_wait_cap) {
   constexpr int VEC = Elt<T>::kVec;
   constexpr int ESZ = (int)sizeof(T);
+  constexpr int HALF = 4;                                   // vectors per lane per processing step
+  constexpr int VPS = kStageBytes / 16;                     // vectors per stage (256)
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
+  WarpRing& rg = sm.ring[warp];
+  uint8_t* my_stages = stages + (size_t)warp * kWarpStages * kStageBytes;
 
-  // aligned middle [a0, a1) moved by bulk copies; head [s0, a0) and tail [a1, s1) by plain loads
+  // aligned middle [a0, a1) split into kScanWarps contiguous chunks of whole vectors
   const uintptr_t addr0 = reinterpret_cast<uintptr_t>(row + s0);
-  int64_t head = (int64_t)(((16u - (uint32_t)(addr0 & 15u)) & 15u) / ESZ);
-  int64_t a0 = s0 + head;
+  int64_t a0 = s0 + (int64_t)(((16u - (uint32_t)(addr0 & 15u)) & 15u) / ESZ);
   if (a0 > s1) a0 = s1;
   const int64_t nvec = ((s1 - a0) * ESZ) / 16;
   const int64_t a1 = a0 + nvec * (16 / ESZ);
-  const int64_t mid_bytes = nvec * 16;
-  const int n_tiles = (int)((mid_bytes + kTileBytes - 1) / kTileBytes);
+  const int64_t per = (nvec + kScanWarps - 1) / kScanWarps;
+  const int64_t wv0 = min(nvec, per * warp), wv1 = min(nvec, per * (warp + 1));
+  const int64_t wbytes = (wv1 - wv0) * 16;
+  const char* wsrc = reinterpret_cast<const char*>(row + a0) + wv0 * 16;
+  const int64_t we0 = a0 + wv0 * VEC;                       // first element of my chunk
+  const int n_st = (int)((wbytes + kStageBytes - 1) / kStageBytes);
 
-  if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(&sm.bar[st], 1);
+  if (tid == 0) sm.cand = reinterpret_cast<uint64_t*>(stages);  // used only after the closing barrier
+  if (lane == 0) {
+    for (int st = 0; st < kWarpStages; ++st) mbar_init(&rg.bar[st], 1);
     fence_mbar_init();
-    sm.cnt = 0;
-    sm.flag = 0;
-    sm.tau = 0ull;
-    const char* src = reinterpret_cast<const char*>(row + a0);
-    for (int t = 0; t < n_tiles && t < kStages; ++t) {
-      const int64_t off = (int64_t)t * kTileBytes;
-      const uint32_t bytes = (uint32_t)min((int64_t)kTileBytes, mid_bytes - off);
-      mbar_arrive_expect_tx(&sm.bar[t], bytes);
-      bulk_g2s(tiles + (size_t)t * kTileBytes, src + off, bytes, &sm.bar[t]);
+    rg.cnt = 0;
+    rg.ovf = 0;
+    sm.flags[warp] = 0;
+    for (int t = 0; t < n_st && t < kWarpStages; ++t) {
+      const int64_t off = (int64_t)t * kStageBytes;
+      const uint32_t bytes = (uint32_t)min((int64_t)kStageBytes, wbytes - off);
+      mbar_arrive_expect_tx(&rg.bar[t], bytes);
+      bulk_g2s(my_stages + (size_t)t * kStageBytes, wsrc + off, bytes, &rg.bar[t]);
     }
   }
-  __syncthreads();
+  __syncwarp();
 
-  float m_t = -INFINITY;
-  float s_hi = 0.0f, s_lo = 0.0f;
-
-  // head + tail elements: plain loads, always candidates
-  const int n_head = (int)(a0 - s0), n_tail = (int)(s1 - a1);
-  uint32_t bad_bits = 0u;  // non-softmax scans: largest |x| bit pattern (NaN above 0x7F800000)
+  float m_t = -INFINITY, s_hi = 0.0f, s_lo = 0.0f;
+  uint32_t bad_bits = 0u;
   float seen_max = -INFINITY;
-  if (tid < n_head + n_tail) {
-    const int64_t idx = tid < n_head ? s0 + tid : a1 + (tid - n_head);
+  uint64_t L = 0ull;            // my slot of the warp's top-K list
+  uint64_t tau_key = 0ull;      // K-th key of the list (0 while it has fewer than K keys)
+  float tau_val = -INFINITY;
+  bool inited = false;
+  bool timed_out = false;
+  int ovf_rounds = 0;
+
+  // head + tail elements (warp 0): softmax, and always candidates
+  const int n_head = (int)(a0 - s0), n_tail = (int)(s1 - a1);
+  if (warp == 0 && lane < n_head + n_tail) {
+    const int64_t idx = lane < n_head ? s0 + lane : a1 + (lane - n_head);
     const float x = Elt<T>::load(row + idx);
     if (SOFTMAX) {
-      // m = x, s = exp(0) = 1; a -inf element contributes nothing; NaN/+inf poison s
-      m_t = x;
-      s_hi = (x == -INFINITY) ? 0.0f : ex2((x - x) * kLog2e);
+      lane_acc_one(x, m_t, s_hi, s_lo);
     } else {
       bad_bits = __float_as_uint(x) & 0x7FFFFFFFu;
       seen_max = x;
     }
     if (!(x != x)) {
-      const int pos = atomicAdd(&sm.cnt, 1);
-      sm.cand[pos] = make_key(x, (uint32_t)idx);
+      const int pos = atomicAdd(&rg.cnt, 1);
+      rg.cand[pos] = make_key(x, (uint32_t)idx);
     }
   }
-  __syncthreads();
+  __syncwarp();
 
-  float tau_val = -INFINITY;
-  uint64_t tau_key = 0ull;
-  bool timed_out = false;
-  int overflow_rounds = 0;
+  // drains the warp's candidate buffer into the list; returns true if it had overflowed
+  auto drain = [&]() -> bool {
+    __syncwarp();
+    const int cnt = rg.cnt;
+    bool o = false;
+    if (cnt > 0) {
+      const int n = min(cnt, kWarpCand);
+      for (int c = 0; c < n; ++c) {
+        const uint64_t k = rg.cand[c];
+        if (k > tau_key) {
+          wl_insert(L, k, K, lane);
+          const uint64_t kth = shfl_u64(L, K - 1);
+          tau_key = kth;
+          tau_val = kth ? key_value(kth) : -INFINITY;
+        }
+      }
+      o = rg.ovf != 0;
+      __syncwarp();
+      if (lane == 0) {
+        rg.cnt = 0;
+        rg.ovf = 0;
+      }
+    }
+    __syncwarp();
+    return o;
+  };
 
-  for (int t = 0; t < n_tiles; ++t) {
-    const int st = t % kStages;
-    const uint32_t parity = (uint32_t)((t / kStages) & 1);
-    // every thread polls the barrier; a run-out is reported once per CTA
-    const uint32_t cap = (t == 0) ? first_wait_cap : kSpinCap;
-    bool ok = mbar_wait_bounded(&sm.bar[st], parity, cap);
-    if (__syncthreads_or(!ok)) {
+  for (int t = 0; t < n_st; ++t) {
+    const int st = t % kWarpStages;
+    const uint32_t parity = (uint32_t)((t / kWarpStages) & 1);
+    const bool ok = mbar_wait_bounded(&rg.bar[st], parity, t == 0 ? first_wait_cap : kSpinCap);
+    if (!__all_sync(0xFFFFFFFFu, ok)) {
       timed_out = true;
-      // drain: wait (bounded) for every copy that was issued, then leave
-      const int issued = min(n_tiles, t + kStages);
+      const int issued = min(n_st, t + kWarpStages);  // drain: wait (bounded) for every issued copy
       for (int u = t; u < issued; ++u)
-        mbar_wait_bounded(&sm.bar[u % kStages], (uint32_t)((u / kStages) & 1), kSpinCap);
-      __syncthreads();
+        mbar_wait_bounded(&rg.bar[u % kWarpStages], (uint32_t)((u / kWarpStages) & 1), kSpinCap);
       break;
     }
-    const int64_t tile_off = (int64_t)t * kTileBytes;
-    const int tile_bytes = (int)min((int64_t)kTileBytes, mid_bytes - tile_off);
-    const int64_t tile_e0 = a0 + tile_off / ESZ;
-    const uint8_t* tile = tiles + (size_t)st * kTileBytes;
+    const int64_t st_off = (int64_t)t * kStageBytes;
+    const int st_bytes = (int)min((int64_t)kStageBytes, wbytes - st_off);
+    const int64_t st_e0 = we0 + st_off / ESZ;
+    const uint8_t* sp = my_stages + (size_t)st * kStageBytes;
 
-    // my vectors: q*256 + tid, q = 0..3
-    constexpr int QV = kTileBytes / 16 / kRowThreads;  // vectors per thread per tile (4)
-    float x[QV * VEC];
-    bool have[QV];
+#pragma unroll 1
+    for (int h = 0; h < VPS / (32 * HALF); ++h) {
+      float x[HALF * VEC];
+      bool have[HALF];
 #pragma unroll
-    for (int q = 0; q < QV; ++q) {
-      const int vi = q * kRowThreads + tid;
-      have[q] = vi * 16 < tile_bytes;
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (have[q]) w = *reinterpret_cast<const uint4*>(tile + (size_t)vi * 16);
-      if (ESZ == 2) {
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+      for (int q = 0; q < HALF; ++q) {
+        const int vi = (h * HALF + q) * 32 + lane;
+        have[q] = vi * 16 < st_bytes;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (have[q]) w = *reinterpret_cast<const uint4*>(sp + (size_t)vi * 16);
+        if (ESZ == 2) {
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          x[q * VEC + 2 * e] = have[q] ? bf16_lo(ww[e]) : -INFINITY;
-          x[q * VEC + 2 * e + 1] = have[q] ? bf16_hi(ww[e]) : -INFINITY;
-        }
-      } else {
-        x[q * VEC + 0] = have[q] ? __uint_as_float(w.x) : -INFINITY;
-        x[q * VEC + 1] = have[q] ? __uint_as_float(w.y) : -INFINITY;
-        x[q * VEC + 2] = have[q] ? __uint_as_float(w.z) : -INFINITY;
-        x[q * VEC + 3] = have[q] ? __uint_as_float(w.w) : -INFINITY;
-      }
-    }
-
-    // ---- online softmax over my values ----
-    float lm = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < QV * VEC; ++j) lm = fmaxf(lm, x[j]);
-    if (!SOFTMAX) {
-#pragma unroll
-      for (int j = 0; j < QV * VEC; ++j) bad_bits = max(bad_bits, __float_as_uint(x[j]) & 0x7FFFFFFFu);
-      seen_max = fmaxf(seen_max, lm);
-    }
-    if (SOFTMAX) {
-      // NaN inputs are ignored by fmaxf but poison the sum below (detected by the caller)
-      if (lm > m_t) {
-        if (m_t != -INFINITY) {
-          const float sc = ex2((m_t - lm) * kLog2e);
-          s_hi *= sc;
-          s_lo *= sc;
-        }
-        m_t = lm;
-      }
-      if (m_t != -INFINITY) {
-        float e[QV * VEC];
-#pragma unroll
-        for (int j = 0; j < QV * VEC; ++j) e[j] = ex2((x[j] - m_t) * kLog2e);
-#pragma unroll
-        for (int w = 1; w < QV * VEC; w <<= 1)
-#pragma unroll
-          for (int j = 0; j + w < QV * VEC; j += 2 * w) e[j] += e[j + w];
-        const float part = e[0];
-        // compensated accumulation of the per-tile sums
-        const float y = part - s_lo;
-        const float tt = s_hi + y;
-        s_lo = (tt - s_hi) - y;
-        s_hi = tt;
-      } else {
-        // all my values so far are -inf (or NaN): a NaN must still poison the sum
-#pragma unroll
-        for (int j = 0; j < QV * VEC; ++j)
-          if (x[j] != x[j]) s_hi = x[j];
-      }
-    }
-
-    // ---- first tile: threshold from the K-th largest per-thread maximum key ----
-    if (tau_key == 0ull) {
-      uint64_t best = 0ull;
-#pragma unroll
-      for (int q = 0; q < QV; ++q)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          const float v = x[q * VEC + e];
-          if (have[q] && !(v != v)) {
-            const uint64_t k = make_key(v, (uint32_t)(tile_e0 + (int64_t)(q * kRowThreads + tid) * VEC + e));
-            best = k > best ? k : best;
+          for (int e = 0; e < 4; ++e) {
+            x[q * VEC + 2 * e] = have[q] ? bf16_lo(ww[e]) : -INFINITY;
+            x[q * VEC + 2 * e + 1] = have[q] ? bf16_hi(ww[e]) : -INFINITY;
           }
+        } else {
+          x[q * VEC + 0] = have[q] ? __uint_as_float(w.x) : -INFINITY;
+          x[q * VEC + 1] = have[q] ? __uint_as_float(w.y) : -INFINITY;
+          x[q * VEC + 2] = have[q] ? __uint_as_float(w.z) : -INFINITY;
+          x[q * VEC + 3] = have[q] ? __uint_as_float(w.w) : -INFINITY;
         }
-      const uint64_t srt = warp_sort_desc(best);
-      const uint64_t kth = shfl_u64(srt, K - 1);
-      if (lane == 0) atomicMax(&sm.tau, (unsigned long long)kth);
-      __syncthreads();
-      tau_key = sm.tau;
-      tau_val = tau_key ? key_value(tau_key) : -INFINITY;
-    }
-
-    // ---- filter into the candidate buffer (re-run with a higher threshold on overflow) ----
-    const int base_cnt = sm.cnt;  // entries of earlier tiles; at most kCandCap / 2
-    for (;;) {
-      if (lm >= tau_val) {
+      }
+      // element id of x[q*VEC + e]: st_e0 + ((h*HALF + q)*32 + lane)*VEC + e
+      float lm = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < QV; ++q)
+      for (int j = 0; j < HALF * VEC; ++j) lm = fmaxf(lm, x[j]);
+
+      if (SOFTMAX) {
+        if (lm > m_t) {
+          if (m_t != -INFINITY) {
+            const float sc = ex2((m_t - lm) * kLog2e);
+            s_hi *= sc;
+            s_lo *= sc;
+          }
+          m_t = lm;
+        }
+        if (m_t != -INFINITY) {
+          float e[HALF * VEC];
+#pragma unroll
+          for (int j = 0; j < HALF * VEC; ++j) e[j] = ex2((x[j] - m_t) * kLog2e);
+#pragma unroll
+          for (int w2 = 1; w2 < HALF * VEC; w2 <<= 1)
+#pragma unroll
+            for (int j = 0; j + w2 < HALF * VEC; j += 2 * w2) e[j] += e[j + w2];
+          const float y = e[0] - s_lo;
+          const float tt = s_hi + y;
+          s_lo = (tt - s_hi) - y;
+          s_hi = tt;
+        } else {
+#pragma unroll
+          for (int j = 0; j < HALF * VEC; ++j)
+            if (x[j] != x[j]) s_hi = x[j];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < HALF * VEC; ++j) bad_bits = max(bad_bits, __float_as_uint(x[j]) & 0x7FFFFFFFu);
+        seen_max = fmaxf(seen_max, lm);
+      }
+
+      // first step of the chunk: the list starts as the K best per-lane maxima
+      uint64_t excl = 0ull;
+      if (!inited) {
+        uint64_t best = 0ull;
+#pragma unroll
+        for (int q = 0; q < HALF; ++q)
 #pragma unroll
           for (int e = 0; e < VEC; ++e) {
             const float v = x[q * VEC + e];
-            if (have[q] && v >= tau_val) {
-              const uint64_t k =
-                  make_key(v, (uint32_t)(tile_e0 + (int64_t)(q * kRowThreads + tid) * VEC + e));
-              if (k >= tau_key) {
-                const int pos = atomicAdd(&sm.cnt, 1);
-                if (pos < kCandCap) sm.cand[pos] = k;
-              }
+            if (have[q] && !(v != v)) {
+              const uint64_t k = make_key(v, (uint32_t)(st_e0 + (int64_t)((h * HALF + q) * 32 + lane) * VEC + e));
+              best = k > best ? k : best;
             }
           }
+        excl = best;
+        const uint64_t srt = warp_sort_desc(best);
+        L = lane < K ? srt : 0ull;
+        tau_key = shfl_u64(L, K - 1);
+        tau_val = tau_key ? key_value(tau_key) : -INFINITY;
+        inited = true;
       }
-      __syncthreads();
-      if (sm.cnt <= kCandCap) break;
-      // Overflow: the K-th best of the full buffer is a valid, strictly higher threshold. Drop this
-      // tile's entries (earlier tiles' entries in [0, base_cnt) stay) and filter the tile again.
-      select_topk(sm, kCandCap, K);
-      if (tid == 0) {
-        sm.tau = sm.topk[K - 1];
-        sm.cnt = base_cnt;
-      }
-      __syncthreads();
-      tau_key = sm.tau;
-      tau_val = key_value(tau_key);
-      if (++overflow_rounds > 64) {
-        if (tid == 0) {
-          sm.flag |= 2;
-          sm.cnt = min(sm.cnt, kCandCap);
+
+      // filter against the list's K-th key; re-run with a higher threshold if the buffer overflowed
+      for (;;) {
+        if (lm >= tau_val) {
+#pragma unroll
+          for (int q = 0; q < HALF; ++q)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+              const float v = x[q * VEC + e];
+              if (have[q] && v >= tau_val) {
+                const uint64_t k =
+                    make_key(v, (uint32_t)(st_e0 + (int64_t)((h * HALF + q) * 32 + lane) * VEC + e));
+                if (k > tau_key && k != excl) {
+                  const int pos = atomicAdd(&rg.cnt, 1);
+                  if (pos < kWarpCand) rg.cand[pos] = k;
+                  else rg.ovf = 1;
+                }
+              }
+            }
         }
-        __syncthreads();
-        break;
+        if (!drain()) break;
+        // Overflow: the buffer's first kWarpCand entries are in the list now and tau rose; filter
+        // this step again for keys above tau that are not already in the list.
+        excl = 0ull;
+        if (++ovf_rounds > 64) {
+          if (lane == 0) sm.flags[warp] |= 2;
+          break;
+        }
+        // keys already in the list are excluded by a membership test in the re-run
+#pragma unroll
+        for (int q = 0; q < HALF; ++q)
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            const float v = x[q * VEC + e];
+            bool in_list = false;
+            const uint64_t k =
+                have[q] && !(v != v) ? make_key(v, (uint32_t)(st_e0 + (int64_t)((h * HALF + q) * 32 + lane) * VEC + e))
+                                     : 0ull;
+            for (int j = 0; j < K; ++j) in_list |= (shfl_u64(L, j) == k);
+            if (in_list) x[q * VEC + e] = -INFINITY;
+          }
+        lm = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < HALF * VEC; ++j) lm = fmaxf(lm, x[j]);
       }
     }
 
-    // ---- release the stage and refill it ----
-    if (tid == 0 && t + kStages < n_tiles) {
+    // release the stage and refill it
+    __syncwarp();
+    if (lane == 0 && t + kWarpStages < n_st) {
       fence_proxy_async_smem();
-      const int64_t off = (int64_t)(t + kStages) * kTileBytes;
-      const uint32_t bytes = (uint32_t)min((int64_t)kTileBytes, mid_bytes - off);
-      mbar_arrive_expect_tx(&sm.bar[st], bytes);
-      bulk_g2s(tiles + (size_t)st * kTileBytes, reinterpret_cast<const char*>(row + a0) + off, bytes,
-               &sm.bar[st]);
-    }
-
-    // ---- compaction: after the first tile, and whenever the buffer is half full ----
-    const int cnt = sm.cnt;
-    if (t == 0 || cnt > kCandCap / 2) {
-      const int n = compact_topk(sm, cnt, K);
-      if (tid == 0) {
-        sm.cnt = n;
-        if (n == K) sm.tau = sm.cand[K - 1];
-      }
-      __syncthreads();
-      tau_key = sm.tau;
-      tau_val = tau_key ? key_value(tau_key) : -INFINITY;
+      const int64_t off = (int64_t)(t + kWarpStages) * kStageBytes;
+      const uint32_t bytes = (uint32_t)min((int64_t)kStageBytes, wbytes - off);
+      mbar_arrive_expect_tx(&rg.bar[st], bytes);
+      bulk_g2s(my_stages + (size_t)st * kStageBytes, wsrc + off, bytes, &rg.bar[st]);
     }
   }
+  drain();  // head/tail entries of a chunk without stages
 
   SegOut out;
-  out.timed_out = timed_out;
-  out.internal = (sm.flag & 2) != 0;
+  out.timed_out = __syncthreads_or(timed_out) != 0;
+  // ---- warp results -> CTA ----
+  if (lane < K) sm.cand[warp * K + lane] = L;
+  float wm = m_t;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, o));
+  float ch = 0.0f, cl = 0.0f;
+  if (SOFTMAX && (m_t != -INFINITY || s_hi != s_hi)) {
+    const float sc = (wm == m_t) ? 1.0f : ex2((m_t - wm) * kLog2e);
+    ch = s_hi * sc;
+    cl = s_lo * sc;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {  // double-float warp sum (TwoSum)
+    const float oh = __shfl_xor_sync(0xFFFFFFFFu, ch, o);
+    const float ol = __shfl_xor_sync(0xFFFFFFFFu, cl, o);
+    const float sum = ch + oh;
+    const float bp = sum - ch;
+    const float err = (ch - (sum - bp)) + (oh - bp);
+    ch = sum;
+    cl = cl + ol + err;
+  }
+  if (lane == 0) {
+    sm.red_m[warp] = wm;
+    sm.red_s[warp] = (double)ch + (double)cl;
+  }
   out.bad = false;
   if (!SOFTMAX) out.bad = __syncthreads_or(bad_bits > 0x7F800000u || seen_max == INFINITY) != 0;
-  // ---- final top-K ----
-  {
-    __syncthreads();
-    const int cnt = min(sm.cnt, kCandCap);
-    out.nkeys = compact_topk(sm, cnt, K);
-  }
-  // ---- block reduction of (m, s) ----
+  if (tid < kMaxK) sm.topk[tid] = 0ull;
+  __syncthreads();
+  int internal = 0;
+  for (int w = 0; w < kScanWarps; ++w) internal |= sm.flags[w] & 2;
+  out.internal = internal != 0;
+  const int nk = kScanWarps * K;
+  select_topk(sm, nk, K);
+  int n = 0;
+  for (int i = 0; i < K; ++i) n += sm.topk[i] != 0ull;
+  out.nkeys = n;
+  for (int i = tid; i < K; i += blockDim.x) sm.cand[i] = sm.topk[i];
   out.m = -INFINITY;
   out.s = 0.0;
   if (SOFTMAX) {
-    float bm = m_t;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, o));
-    if (lane == 0) sm.red_m[warp] = bm;
-    __syncthreads();
-    float M = -INFINITY;
-    for (int w = 0; w < kRowThreads / 32; ++w) M = fmaxf(M, sm.red_m[w]);
-    // NaN in a thread's sum propagates; a thread with m_t = +inf makes M = +inf (caller flags it).
-    // Warp sums are double-float (hi, lo) pairs combined with TwoSum: no fp64 in the hot kernel.
-    float ch = 0.0f, cl = 0.0f;
-    if (m_t != -INFINITY || s_hi != s_hi) {
-      const float sc = (M == m_t) ? 1.0f : ex2((m_t - M) * kLog2e);
-      ch = s_hi * sc;
-      cl = s_lo * sc;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float oh = __shfl_xor_sync(0xFFFFFFFFu, ch, o);
-      const float ol = __shfl_xor_sync(0xFFFFFFFFu, cl, o);
-      const float sum = ch + oh;
-      const float bp = sum - ch;
-      const float err = (ch - (sum - bp)) + (oh - bp);
-      ch = sum;
-      cl = cl + ol + err;
-    }
-    if (lane == 0) sm.red_s[warp] = (double)ch + (double)cl;
-    __syncthreads();
     if (tid == 0) {
+      float M = -INFINITY;
+      for (int w = 0; w < kScanWarps; ++w) M = fmaxf(M, sm.red_m[w]);
       double S = 0.0;
-      for (int w = 0; w < kRowThreads / 32; ++w) S += sm.red_s[w];
+      for (int w = 0; w < kScanWarps; ++w) {
+        const double sw = sm.red_s[w];
+        if (sw != sw) S = sw;
+        else if (sm.red_m[w] != -INFINITY && S == S) S += sw * (double)ex2((sm.red_m[w] - M) * kLog2e);
+      }
       out.m = M;
       out.s = S;
     }
-  } else {
-    out.m = out.nkeys > 0 ? key_value(sm.cand[0]) : -INFINITY;
   }
+  __syncthreads();
+  if (!SOFTMAX) out.m = n > 0 ? key_value(sm.cand[0]) : -INFINITY;
   return out;
 }
 
