@@ -182,3 +182,22 @@ def test_round_parity_small(torch, name, over):
     if w["m"] > 1 and name == "pr1" and over.get("m") == 60:
         w["D"] = 6
     _run_rounds(torch, w, 3)
+
+
+def test_full_size_round_is_deterministic(torch):
+    """The same CAST round (B=8, V=128256) run twice gives bit-identical trees and outputs."""
+    import harness
+
+    w = with_sizes("cast")
+    gr = harness.GpuRound(w)
+    roots = synth.root_tokens(w["seed"], 0, w["B"], w["V"])
+    outs = []
+    for _ in range(3):
+        gr.round(0, 0, roots)
+        t = harness.tree_numpy(gr.run.h)
+        outs.append((t["token"].copy(), t["value"].copy(), gr.run.meta.numpy()["tokens"].copy(),
+                     gr.run.accept_len.cpu().numpy().copy(), gr.run.bonus.cpu().numpy().copy()))
+    for o in outs[1:]:
+        for a, b in zip(outs[0], o):
+            np.testing.assert_array_equal(a, b)
+    gr.run.h.close()
