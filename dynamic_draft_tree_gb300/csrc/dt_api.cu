@@ -92,7 +92,8 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   const size_t o_lcount = cv.take<int32_t>((size_t)c.B_max * (c.D_max + 1));
   const size_t o_front = cv.take<int32_t>((size_t)c.B_max * c.W);
   const size_t o_fcount = cv.take<int32_t>(c.B_max);
-  const size_t partial_cap = rows_max + (size_t)h->num_sms * 4 + 64;
+  // one partial per (row, segment) of a row-scan launch; launches clamp their segment count to it
+  const size_t partial_cap = rows_max * 8 + (size_t)h->num_sms * 64;
   const size_t o_part = cv.take<dt::Partial>(partial_cap);
   const size_t o_rowc = cv.take<int32_t>(rows_max);
   const size_t o_reqc = cv.take<int32_t>(c.B_max);

@@ -217,6 +217,8 @@ int choose_segments(const dt_handle* h, int64_t rows, int64_t V, int elt_bytes) 
   const int64_t max_by_keys = kCandCap / h->cfg.K;
   if (S > max_by_keys) S = max_by_keys;
   if (S > 64) S = 64;
+  const int64_t max_by_buf = h->ws.partial_cap / (rows > 0 ? rows : 1);  // partials buffer capacity
+  if (S > max_by_buf) S = max_by_buf;
   if (S < 1) S = 1;
   return (int)S;
 }

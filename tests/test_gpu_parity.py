@@ -201,3 +201,15 @@ def test_full_size_round_is_deterministic(torch):
         for a, b in zip(outs[0], o):
             np.testing.assert_array_equal(a, b)
     gr.run.h.close()
+
+
+# Full sizes of the five workloads, in the launch configuration the benchmark uses (several rounds
+# back to back on one handle, so that stale per-launch state would show up).
+FULL = [("pr1", {}, 3), ("vicuna", {}, 2), ("vicuna", dict(T=1), 2), ("cast", {}, 3), ("graft", {}, 3),
+        ("stress", {}, 1)]
+
+
+@pytest.mark.parametrize("name,over,rounds", FULL)
+def test_round_parity_full_size(torch, name, over, rounds):
+    w = with_sizes(name, **over)
+    _run_rounds(torch, w, rounds)
