@@ -48,7 +48,7 @@ def checkpoint(tree, d, p, stop, stage, m):
             ids = tree.layer_ids(b, d)
             c = float(np.exp(max(tree.value[b, i] for i in ids))) if ids else 0.0
             if p.get("gaps") is not None:
-                p["gaps"].add("tau", c - p["tau"][s], c)
+                p["gaps"].add("tau", c - p["tau"][s], c, b)
             if not (c > p["tau"][s]):
                 stop[b], stage[b], m[b] = True, s, p["k_draft"][s]
                 continue

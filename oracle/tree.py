@@ -49,8 +49,9 @@ class Gaps:
     def __init__(self):
         self.items = []
 
-    def add(self, kind, gap, key):
-        self.items.append((kind, float(gap), float(key)))
+    def add(self, kind, gap, key, b=None):
+        """Record a decision's distance from its boundary; ``b`` is the request (None: batch-wide)."""
+        self.items.append((kind, float(gap), float(key), b))
 
     def near_tie(self, tol=1e-5):
         return [it for it in self.items if abs(it[1]) < tol * max(1.0, abs(it[2]))]
@@ -188,7 +189,7 @@ class OracleTree:
         v_in, v_out = self.value[b, i_in], self.value[b, i_out]
         if v_in == v_out and self.parent[b, i_in] == self.parent[b, i_out]:
             return  # siblings with bitwise-equal logits: the id tie-break is exact
-        gaps.add(kind, v_in - v_out, v_in)
+        gaps.add(kind, v_in - v_out, v_in, b)
 
     # -- rerank (a5) -------------------------------------------------------------
     def rerank(self, m, m_cap, gaps=None):

@@ -107,7 +107,7 @@ def verify_sample(meta, rows, seed, rnd, gaps=None):
                     p_acc = resid[t] / resid.sum()
                 u = philox.accept_uniform(seed, rnd, b, j)
                 if gaps is not None and t >= 0 and resid[t] > 0:
-                    gaps.add("accept", u - p_acc, p_acc)
+                    gaps.add("accept", u - p_acc, p_acc, b)
                 if u < p_acc:
                     cur = j
                     chain.append(j)
@@ -124,7 +124,7 @@ def verify_sample(meta, rows, seed, rnd, gaps=None):
                 if gaps is not None:
                     y2 = y.copy()
                     y2[t] = -np.inf
-                    gaps.add("gumbel", y[t] - y2.max(), y[t])
+                    gaps.add("gumbel", y[t] - y2.max(), y[t], b)
                 bonus[b] = t
                 break
         acc[b] = len(chain) - 1

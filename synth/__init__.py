@@ -48,7 +48,8 @@ class SpecC(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("V", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("height_per_request", ctypes.c_int32), ("sigma", ctypes.c_float),
                 ("zipf_s", ctypes.c_float), ("peak_lo", ctypes.c_void_p),
-                ("peak_hi", ctypes.c_void_p), ("ln_table", ctypes.c_void_p)]
+                ("peak_hi", ctypes.c_void_p), ("ln_table", ctypes.c_void_p),
+                ("salts", ctypes.c_void_p)]
 
 
 def _fresh(lib, src):
@@ -146,24 +147,26 @@ class Spec:
     def np_dtype(self):
         return np.uint16 if self.dtype == BF16 else np.float32
 
-    def c_struct_host(self):
+    def c_struct_host(self, salts=None):
         return SpecC(self.kind, self.V, self.dtype, int(self.height_per_request), self.sigma,
                      self.zipf_s, self.peak_lo.ctypes.data, self.peak_hi.ctypes.data,
-                     self.ln_table.ctypes.data)
+                     self.ln_table.ctypes.data, None if salts is None else salts.ctypes.data)
 
-    def c_struct_device(self, torch):
+    def c_struct_device(self, torch, salts_dev=None):
         if self._dev is None:
             self._dev = [torch.from_numpy(self.peak_lo).cuda(), torch.from_numpy(self.peak_hi).cuda(),
                          torch.from_numpy(self.ln_table).cuda()]
         lo, hi, ln = self._dev
         return SpecC(self.kind, self.V, self.dtype, int(self.height_per_request), self.sigma,
-                     self.zipf_s, lo.data_ptr(), hi.data_ptr(), ln.data_ptr())
+                     self.zipf_s, lo.data_ptr(), hi.data_ptr(), ln.data_ptr(),
+                     None if salts_dev is None else salts_dev.data_ptr())
 
 
-def gen_rows_cpu(spec, seed, salt, stream, ctx, depth=None, depth_add=0, rows_per_b=1, b0=0):
+def gen_rows_cpu(spec, seed, salt, stream, ctx, depth=None, depth_add=0, rows_per_b=1, b0=0, salts=None):
     """Rows for contexts ``ctx`` (int32 [R]); returns raw bits (uint16 for bf16) or fp32, [R][V].
 
     Row rr belongs to request b0 + rr // rows_per_b. Rows whose ctx is negative are zeros.
+    ``salts`` (uint64 [B], optional) replaces ``salt`` per request.
     """
     ctx = np.ascontiguousarray(ctx, np.int32).ravel()
     R = ctx.size
@@ -172,16 +175,19 @@ def gen_rows_cpu(spec, seed, salt, stream, ctx, depth=None, depth_add=0, rows_pe
     if depth is not None:
         depth = np.ascontiguousarray(depth, np.int32).ravel()
         dptr = depth.ctypes.data
-    st = spec.c_struct_host()
+    if salts is not None:
+        salts = np.ascontiguousarray(salts, np.uint64)
+    st = spec.c_struct_host(salts)
     _cpu_lib().synth_gen_rows(ctypes.byref(st), seed, salt, stream, ctx.ctypes.data, dptr,
                               depth_add, rows_per_b, b0, out.ctypes.data, spec.V, R)
     return out
 
 
 def gen_rows_gpu(torch, spec, seed, salt, stream, ctx_dev, out_dev, ld, depth_dev=None, depth_add=0,
-                 rows_per_b=1, cuda_stream=None):
-    """Device rows into ``out_dev`` (row rr at element rr*ld); ctx/depth are device int32 tensors."""
-    st = spec.c_struct_device(torch)
+                 rows_per_b=1, cuda_stream=None, salts_dev=None):
+    """Device rows into ``out_dev`` (row rr at element rr*ld); ctx/depth are device int32 tensors;
+    ``salts_dev`` (device int64 [B], optional) replaces ``salt`` per request."""
+    st = spec.c_struct_device(torch, salts_dev)
     cs = (cuda_stream or torch.cuda.current_stream()).cuda_stream
     R = ctx_dev.numel()
     rc = _gpu_lib().synth_gen_rows_gpu(ctypes.byref(st), seed, salt, stream, ctx_dev.data_ptr(),

@@ -60,6 +60,7 @@ typedef struct {
   const float* peak_lo;  /* [B] */
   const float* peak_hi;  /* [B] */
   const float* ln_table; /* [V], kind 1: ln(rank + 1) rounded to fp32 */
+  const uint64_t* salts; /* [B] per-request salt, or NULL for the call's salt */
 } synth_spec;
 
 /* Integer Irwin-Hall sum of 12 16-bit uniforms, centred: in [-393210, 393210]. */
@@ -88,6 +89,7 @@ void synth_zipf_table(int32_t V, float* out) {
 static void gen_row(const synth_spec* sp, uint64_t seed, uint64_t salt, int stream, int64_t b,
                     int64_t depthkey, int64_t ctx, void* out) {
   const int32_t V = sp->V;
+  if (sp->salts) salt = sp->salts[b];
   const uint64_t r = synth_row_key(seed, salt, b, depthkey, ctx);
   const float sA = (float)((double)sp->sigma / 65536.0);
   const float sT = (float)((double)sp->sigma / (5.0 * 65536.0));

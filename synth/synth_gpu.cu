@@ -78,6 +78,7 @@ struct synth_spec {
   const float* peak_lo;   // [B] device
   const float* peak_hi;   // [B] device
   const float* ln_table;  // [V] device
+  const uint64_t* salts;  // [B] device per-request salt, or null for the call's salt
 };
 
 }
@@ -97,6 +98,7 @@ __global__ void __launch_bounds__(kThreads) gen_rows_kernel(
     rp.valid = c >= 0;
     if (rp.valid) {
       const int64_t b = rr / rows_per_b;
+      if (sp.salts) salt = sp.salts[b];
       const int64_t dk = (int64_t)(depth ? depth[rr] : 0) + depth_add;
       const uint64_t r = hk(hk(hk(hk(seed, salt), (uint64_t)b), (uint64_t)dk), (uint64_t)c);
       rp.r = r;

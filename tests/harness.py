@@ -5,10 +5,9 @@ Comparison rules (readings listed in the design doc):
   * index outputs (tokens, parents, frontier sets, selections, masks, position ids, retrieve rows,
     accepted lengths and paths, bonus tokens, M rows) must be equal;
   * log confidences and log values: |gpu - oracle| <= 2e-6 * max(1, |oracle|);
-  * a round whose oracle decision gaps fall below 1e-5 relative is redrawn (attempt + 1) and counted.
+  * a request whose oracle decision gaps fall below 1e-5 relative is redrawn (its attempt + 1, a new
+    generator salt) and counted; batch-coupled CAST decisions redraw the whole batch.
 """
-import functools
-
 import numpy as np
 
 import synth
@@ -20,25 +19,48 @@ TOL = 2e-6
 GAP = 1e-5
 
 
-def salt_of(w, rnd, attempt):
-    return attempt if w["policy"] == "graft" else (rnd << 8) | attempt
+def salts_of(w, rnd, attempts):
+    """Per-request generator salts. Graft rows are stationary across rounds (the salt is the
+    attempt only) so that M can learn successors; other workloads key rows by round."""
+    a = np.asarray(attempts, np.uint64)
+    if w["policy"] == "graft":
+        return a.copy()
+    return (np.uint64(rnd) << np.uint64(8)) | a
 
 
-def round_id(rnd, attempt):
-    return (rnd << 8) | attempt
+def round_id(rnd):
+    """Philox round of a round (the same for every redraw of its requests)."""
+    return rnd << 8
+
+
+_ROWS = {"owner": None, "rows": {}}
 
 
 class HostRows:
-    """Row providers for the oracle, keyed like the device generator."""
+    """Row providers for the oracle, keyed like the device generator.
 
-    def __init__(self, w, spec, salt):
-        self.w, self.spec, self.salt = w, spec, salt
+    Generated rows are cached (raw dtype) per (stream, request, depth key, context, salt), so a
+    redraw of some requests regenerates only theirs.
+    """
+
+    def __init__(self, w, spec, salts):
+        self.w, self.spec = w, spec
+        self.salts = np.ascontiguousarray(salts, np.uint64)
         self.depthkey = w["recipe"]["depthkey"]
+        owner = (w["seed"], w["V"], w["B"], w["dtype"], repr(w["recipe"]))
+        if _ROWS["owner"] != owner:
+            _ROWS["owner"] = owner
+            _ROWS["rows"] = {}
+        self._cache = _ROWS["rows"]
 
-    @functools.lru_cache(maxsize=8192)
     def _row(self, stream, b, dk, ctx):
-        r = synth.gen_rows_cpu(self.spec, self.w["seed"], self.salt, stream, [ctx], depth_add=dk, b0=b)
-        return synth.to_f64(r[0], self.spec.dtype)
+        key = (stream, b, dk, ctx, int(self.salts[b]))
+        raw = self._cache.get(key)
+        if raw is None:
+            raw = synth.gen_rows_cpu(self.spec, self.w["seed"], 0, stream, [ctx], depth_add=dk, b0=b,
+                                     salts=self.salts)[0]
+            self._cache[key] = raw
+        return synth.to_f64(raw, self.spec.dtype)
 
     def draft_row(self, b, d, ctx):
         return self._row(synth.DRAFT, b, d if self.depthkey else 0, ctx)
@@ -65,25 +87,45 @@ def cast_n0(rnd):
     return 512 * (1 + rnd % 16)
 
 
-def oracle_round(w, rnd, roots=None, M=None, max_attempts=12):
-    """Oracle round with seed rejection; returns (ref, attempt, rejections)."""
+def root_tokens(w, salts):
+    lib = synth._cpu_lib()
+    return np.array([lib.synth_root_token(w["seed"], int(salts[b]), b, w["V"]) for b in range(w["B"])], np.int32)
+
+
+def oracle_round(w, rnd, roots=None, M=None, max_attempts=16):
+    """Oracle round with seed rejection; returns (ref, attempts, redraws).
+
+    A request whose decision gaps fall below GAP relative is redrawn with its next attempt salt;
+    batch-coupled decisions (CAST) redraw the whole batch. ``redraws`` counts requests redrawn.
+    """
     spec = spec_for(w)
     cfg = oracle_cfg(w)
-    for attempt in range(max_attempts):
-        salt = salt_of(w, rnd, attempt)
-        rows = HostRows(w, spec, salt)
-        r = roots if roots is not None else synth.root_tokens(w["seed"], salt, w["B"], w["V"])
+    B = w["B"]
+    attempts = np.zeros(B, np.int64)
+    redraws = 0
+    for _ in range(max_attempts):
+        salts = salts_of(w, rnd, attempts)
+        rows = HostRows(w, spec, salts)
+        r = roots if roots is not None else root_tokens(w, salts)
         if cfg["policy"] == "cast":
             cfg["cast"]["n0"] = cast_n0(rnd)
         gaps = Gaps()
         M_try = None if M is None else M.copy()
-        ref = run_round(cfg, np.asarray(r), rows.draft_row, rows.target_row, rnd=round_id(rnd, attempt),
-                        M=M_try, gaps=gaps)
-        if not gaps.near_tie(GAP):
+        ref = run_round(cfg, np.asarray(r), rows.draft_row, rows.target_row, rnd=round_id(rnd), M=M_try, gaps=gaps)
+        near = gaps.near_tie(GAP)
+        if not near:
             ref["M"] = M_try
             ref["roots"] = np.asarray(r)
-            ref["salt"] = salt
-            return ref, attempt, attempt
+            ref["salts"] = salts
+            return ref, attempts, redraws
+        bs = {it[3] for it in near}
+        if None in bs or w["policy"] == "cast":
+            attempts += 1
+            redraws += B
+        else:
+            for b in bs:
+                attempts[b] += 1
+            redraws += len(bs)
     raise AssertionError("no tie-free draw in %d attempts" % max_attempts)
 
 
@@ -114,9 +156,10 @@ class GpuRound:
         if w["policy"] == "graft":
             self.M = torch.full((B, V, 8), -1, dtype=torch.int32, device="cuda")
 
-    def round(self, rnd, attempt, roots):
+    def round(self, rnd, attempts, roots):
         torch, w, g = self.torch, self.w, self.g
-        salt = salt_of(w, rnd, attempt)
+        salts_dev = torch.as_tensor(salts_of(w, rnd, attempts).astype(np.int64)).cuda()
+        salt = 0
         dk = w["recipe"]["depthkey"]
         V, k = w["V"], w["k"]
 
@@ -124,17 +167,17 @@ class GpuRound:
             F = 1 if d == 1 else k
             ctx = ftok[:, :F].contiguous().view(-1)
             synth.gen_rows_gpu(torch, self.spec, w["seed"], salt, synth.DRAFT, ctx, self.dbuf, V,
-                               depth_add=d if dk else 0, rows_per_b=F)
+                               depth_add=d if dk else 0, rows_per_b=F, salts_dev=salts_dev)
             return self.dbuf
 
         def target_rows(meta):
             synth.gen_rows_gpu(torch, self.spec, w["seed"], salt, synth.TARGET, meta.tokens.view(-1), self.tbuf,
                                V, depth_dev=meta.depth.view(-1) if dk else None, depth_add=1 if dk else 0,
-                               rows_per_b=g["P"])
+                               rows_per_b=g["P"], salts_dev=salts_dev)
             return self.tbuf
 
         roots_dev = torch.as_tensor(np.asarray(roots, np.int32)).cuda()
-        self.run.run(roots_dev, draft_rows, target_rows, seed=w["seed"], rnd=round_id(rnd, attempt), M=self.M,
+        self.run.run(roots_dev, draft_rows, target_rows, seed=w["seed"], rnd=round_id(rnd), M=self.M,
                      n0=cast_n0(rnd))
 
 

@@ -162,9 +162,9 @@ def _run_rounds(torch, w, rounds):
     roots = None
     rejections = 0
     for rnd in range(rounds):
-        ref, attempt, rej = harness.oracle_round(w, rnd, roots=roots, M=M)
+        ref, attempts, rej = harness.oracle_round(w, rnd, roots=roots, M=M)
         rejections += rej
-        gr.round(rnd, attempt, ref["roots"])
+        gr.round(rnd, attempts, ref["roots"])
         from dynamic_draft_tree_gb300 import dt_get_status
 
         assert dt_get_status(gr.run.h) == 0
@@ -190,10 +190,11 @@ def test_full_size_round_is_deterministic(torch):
 
     w = with_sizes("cast")
     gr = harness.GpuRound(w)
-    roots = synth.root_tokens(w["seed"], 0, w["B"], w["V"])
+    attempts = np.zeros(w["B"], np.int64)
+    roots = harness.root_tokens(w, harness.salts_of(w, 0, attempts))
     outs = []
     for _ in range(3):
-        gr.round(0, 0, roots)
+        gr.round(0, attempts, roots)
         t = harness.tree_numpy(gr.run.h)
         outs.append((t["token"].copy(), t["value"].copy(), gr.run.meta.numpy()["tokens"].copy(),
                      gr.run.accept_len.cpu().numpy().copy(), gr.run.bonus.cpu().numpy().copy()))
