@@ -146,8 +146,8 @@ __global__ void __launch_bounds__(kMetaThreads) build_meta_kernel(MetaArgs a) {
   // mask [P][P] bytes
   uint8_t* mask = a.meta.mask + rb * P;
   const int64_t mbytes = (int64_t)P * P;
-  for (int64_t e = tid; e < mbytes; e += blockDim.x) {
-    const int i = (int)(e / P), j = (int)(e % P);
+  for (int e = tid; e < (int)mbytes; e += blockDim.x) {  // P*P <= 2^18: 32-bit index arithmetic
+    const int i = e / P, j = e - i * P;
     mask[e] = (uint8_t)((anc[i][j >> 5] >> (j & 31)) & 1u);
   }
   // retrieve rows

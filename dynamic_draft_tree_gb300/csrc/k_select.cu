@@ -43,25 +43,30 @@ struct SortArgs {
 // One CTA per request: all valid non-root nodes in the total order.
 __global__ void __launch_bounds__(1024) sort_nodes_kernel(SortArgs a) {
   extern __shared__ __align__(16) uint64_t keys[];
-  __shared__ int cnt;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
-  if (tid == 0) cnt = 0;
-  for (int i = tid; i < a.n_pad; i += blockDim.x) keys[i] = 0ull;
-  __syncthreads();
   const Workspace& ws = a.ws;
-  for (int id = 1 + tid; id < a.N; id += blockDim.x) {
-    const int64_t gi = (int64_t)b * a.N + id;
-    if (ws.token[gi] >= 0) {
-      const int pos = atomicAdd(&cnt, 1);
-      keys[pos] = make_key(ws.value[gi], (uint32_t)id);
+  // slot i holds node i+1 (empty key 0 for invalid slots, which sort last)
+  int mine = 0;
+  for (int i = tid; i < a.n_pad; i += blockDim.x) {
+    uint64_t k = 0ull;
+    const int id = i + 1;
+    if (id < a.N) {
+      const int64_t gi = (int64_t)b * a.N + id;
+      if (ws.token[gi] >= 0) {
+        k = make_key(ws.value[gi], (uint32_t)id);
+        ++mine;
+      }
     }
+    keys[i] = k;
   }
+  __shared__ int s_n;
+  if (tid == 0) s_n = 0;
   __syncthreads();
-  const int n = cnt;
-  int n_pad = 2;  // sort only the valid nodes (padded with empty keys to a power of two)
-  while (n_pad < n) n_pad <<= 1;
-  block_bitonic_desc(keys, n_pad);
+  if (mine) atomicAdd(&s_n, mine);  // one atomic per thread
+  __syncthreads();
+  const int n = s_n;
+  block_bitonic_desc(keys, a.n_pad);
   if (a.mode == 0) {
     int mb = a.m ? a.m[a.m_len == 1 ? 0 : b] : a.m_cap;
     mb = max(0, min(min(mb, a.m_cap), n));
@@ -77,7 +82,7 @@ __global__ void __launch_bounds__(1024) sort_nodes_kernel(SortArgs a) {
   } else {
     double* lin = ws.sorted_lin + (int64_t)b * a.m_cap;
     for (int i = tid; i < a.m_cap; i += blockDim.x)
-      lin[i] = i < n ? exp((double)key_value(keys[i])) : 0.0;
+      lin[i] = i < n ? (double)expf(key_value(keys[i])) : 0.0;
     if (tid == 0) ws.sorted_cnt[b] = min(n, a.m_cap);
   }
 }
@@ -94,7 +99,8 @@ __device__ int selection_rule(const double* items, const double* cost, double th
   double du = 0.0;
   for (int k = 2; k <= cap; ++k) {
     du += items[k - 1];
-    if (cost[k] <= cost[k0] || du / (cost[k] - cost[k0]) >= thr) {
+    // marginal utility du / (c_k - c_k0) >= thr, written without the division (c_k > c_k0 here)
+    if (cost[k] <= cost[k0] || du >= thr * (cost[k] - cost[k0])) {
       k0 = k;
       du = 0.0;
     }
@@ -146,7 +152,7 @@ __global__ void cast_width_depth_kernel(PruneArgs a) {
     const int64_t lb = (int64_t)b * (a.D + 1) + a.d;
     if (s >= ws.layer_count[lb]) return 0.0;
     const int id = ws.layer_order[lb * a.LW + s];
-    return exp((double)ws.value[(int64_t)b * a.N + id]);
+    return (double)expf(ws.value[(int64_t)b * a.N + id]);
   });
   __syncthreads();
   if (tid != 0) return;
@@ -171,7 +177,7 @@ __global__ void cast_width_depth_kernel(PruneArgs a) {
   double alpha = 0.0;
   for (int j = 0; j < cs->fifo_len; ++j) alpha += cs->fifo[j];
   alpha /= (double)cs->fifo_len;
-  const bool grow = (a.d < a.p.D_max) && (alpha * u / cost[n] >= a.p.C2);
+  const bool grow = (a.d < a.p.D_max) && (alpha * u >= a.p.C2 * cost[n]);  // alpha * u / c_n >= C2
   cs->u_prev = u;
   cs->u_layer = u;
   cs->ctx_sum += n;
@@ -212,7 +218,7 @@ __global__ void graft_checkpoint_kernel(PruneArgs a) {
     if (a.p.ckpt_layer[s] != li) continue;
     const int64_t lb = (int64_t)b * (a.D + 1) + a.d;
     double c = 0.0;
-    if (ws.layer_count[lb] > 0) c = exp((double)ws.value[(int64_t)b * a.N + ws.layer_order[lb * a.LW]]);
+    if (ws.layer_count[lb] > 0) c = (double)expf(ws.value[(int64_t)b * a.N + ws.layer_order[lb * a.LW]]);
     if (!(c > a.p.tau[s])) {
       a.out.stop[b] = 1;
       if (a.out.stage) a.out.stage[b] = s;

@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
   if (tid < kMaxK) sm.topk[tid] = 0ull;
   __syncthreads();
   // empty keys are 0 and rank below every real key
-  select_topk(sm, nk, a.K);
+  merge_sorted_lists(sm, a.S, a.K);
   float M;
   double Ssum;
   bool nan;
@@ -158,10 +158,15 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
     set_status(ws.status, DT_DEV_BAD_LOGITS);
   const int pid = ws.frontier[(int64_t)b * a.W + f];
   const float pval = ws.value[(int64_t)b * a.N + pid];
-  double logS = 0.0;
-  if (tid < 32) {  // one fp64 log per row, broadcast over the first warp (K <= 32)
-    if (tid == 0) logS = log(Ssum);
-    logS = __shfl_sync(0xFFFFFFFFu, logS, 0);
+  // log S = e * ln 2 + log(mantissa), mantissa in [1, 2): the exponent split is exact and the fp32
+  // log of the mantissa is accurate to ~1e-7 absolute (no fp64 transcendental on the tail)
+  double logS;
+  {
+    const unsigned long long bits = (unsigned long long)__double_as_longlong(Ssum);
+    const int e = (int)((bits >> 52) & 0x7FF) - 1023;
+    const double mant = __longlong_as_double((long long)((bits & 0x000FFFFFFFFFFFFFull) | 0x3FF0000000000000ull));
+    logS = (double)e * 0.6931471805599453 + (double)logf((float)mant);
+    if (!(Ssum > 0.0) || Ssum != Ssum || e == 1024) logS = log(Ssum);  // zero, NaN, inf: let log decide
   }
   if (tid < a.K) {
     const uint64_t k = sm.topk[tid];

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(RowPassArgs
   for (int k = tid; k < nk; k += blockDim.x) sm.cand[k] = __ldcg(&part[k / a.K].keys[k % a.K]);
   if (tid < kMaxK) sm.topk[tid] = 0ull;
   __syncthreads();
-  select_topk(sm, nk, a.K);
+  merge_sorted_lists(sm, a.S, a.K);
   float M = -INFINITY;
   double Ssum = 0.0;
   bool nan = false;
@@ -258,10 +258,9 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
         const int t = s_tok[child];
         const float x = load_logit(a.logits, a.dtype, (rb + cur) * a.ld + t);
         const float e = ex2((x - st.m) * kLog2e);
-        const double p = (double)e / s_sres;
         const Philox4 w = philox4x32_10(a.r0, a.r1, (uint32_t)(512 * b + child), 0x80000000u, a.key0, a.key1);
         const double u = (double)(w.v[0] >> 8) * 5.9604644775390625e-08;  // 2^-24
-        if (u < p) {
+        if (u * s_sres < (double)e) {  // u < e / S_res = P_res(x), without the division
           s_state = 1;
         } else {
           s_rej[s_nrej] = t;

@@ -114,6 +114,30 @@ __device__ __forceinline__ int select_topk(ScanSmem& sm, int cnt, int K) {
   return cnt < K ? cnt : K;
 }
 
+// Top-K of S descending lists of K keys each, stored back to back in cand[0..S*K) (empty = 0), into
+// sm.topk[0..K). The rank of a key is the number of larger keys over all lists, found by binary
+// search in each list. All threads call it.
+__device__ __forceinline__ void merge_sorted_lists(ScanSmem& sm, int S, int K) {
+  const int n = S * K;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint64_t k = sm.cand[i];
+    if (k == 0ull) continue;
+    int rank = 0;
+    for (int s = 0; s < S && rank < K; ++s) {
+      const uint64_t* L = sm.cand + s * K;
+      int lo = 0, hi = K;  // first index whose key is <= k
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (L[mid] > k) lo = mid + 1;
+        else hi = mid;
+      }
+      rank += lo;
+    }
+    if (rank < K) sm.topk[rank] = k;
+  }
+  __syncthreads();
+}
+
 // Merge of the S (<= 64) segment partials of a row: M = max_s m_s, S = sum_s s_s * exp(m_s - M).
 // Every thread gets the results; `nan` reports a poisoned (NaN) sum. All threads call it.
 __device__ __forceinline__ void merge_softmax(const Partial* part, int S, ScanSmem& sm, float& M, double& Sum,
