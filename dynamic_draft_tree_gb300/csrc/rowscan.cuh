@@ -70,6 +70,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// NaN-propagating maxima (max.NaN): a NaN operand gives NaN.
+__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float max_nan_f32(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t max_nan_f32u(uint32_t a, uint32_t b) {
+  return __float_as_uint(max_nan_f32(__uint_as_float(a), __uint_as_float(b)));
+}
+
 // Waits at most `cap` polls; returns false when the bound ran out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t cap) {
   for (uint32_t it = 0; it < cap; ++it)
@@ -230,8 +245,6 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
                                uint8_t* stages, uint32_t first_wait_cap) {
   constexpr int VEC = Elt<T>::kVec;
   constexpr int ESZ = (int)sizeof(T);
-  constexpr int HALF = 4;                                   // vectors per lane per processing step
-  constexpr int VPS = kStageBytes / 16;                     // vectors per stage (256)
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   WarpRing& rg = sm.ring[warp];
@@ -267,14 +280,12 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
   __syncwarp();
 
   float m_t = -INFINITY, s_hi = 0.0f, s_lo = 0.0f;
-  uint32_t bad_bits = 0u;
   float seen_max = -INFINITY;
   uint64_t L = 0ull;            // my slot of the warp's top-K list
   uint64_t tau_key = 0ull;      // K-th key of the list (0 while it has fewer than K keys)
   float tau_val = -INFINITY;
   bool inited = false;
   bool timed_out = false;
-  int ovf_rounds = 0;
 
   // head + tail elements (warp 0): softmax, and always candidates
   const int n_head = (int)(a0 - s0), n_tail = (int)(s1 - a1);
@@ -284,7 +295,6 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
     if (SOFTMAX) {
       lane_acc_one(x, m_t, s_hi, s_lo);
     } else {
-      bad_bits = __float_as_uint(x) & 0x7FFFFFFFu;
       seen_max = x;
     }
     if (!(x != x)) {
@@ -321,6 +331,9 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
     return o;
   };
 
+  constexpr int QV = kStageBytes / 16 / 32;   // vectors per lane per stage (8)
+  constexpr int NV = QV * VEC;                 // values per lane per stage
+  const uint32_t neg_fill = ESZ == 2 ? 0xFF80FF80u : 0xFF800000u;  // -inf in every element
   for (int t = 0; t < n_st; ++t) {
     const int st = t % kWarpStages;
     const uint32_t parity = (uint32_t)((t / kWarpStages) & 1);
@@ -337,143 +350,132 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
     const int64_t st_e0 = we0 + st_off / ESZ;
     const uint8_t* sp = my_stages + (size_t)st * kStageBytes;
 
-#pragma unroll 1
-    for (int h = 0; h < VPS / (32 * HALF); ++h) {
-      float x[HALF * VEC];
-      bool have[HALF];
+    // the whole stage in registers: vector q of this lane is stage vector q*32 + lane
+    uint32_t wv[QV * 4];
 #pragma unroll
-      for (int q = 0; q < HALF; ++q) {
-        const int vi = (h * HALF + q) * 32 + lane;
-        have[q] = vi * 16 < st_bytes;
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (have[q]) w = *reinterpret_cast<const uint4*>(sp + (size_t)vi * 16);
-        if (ESZ == 2) {
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x[q * VEC + 2 * e] = have[q] ? bf16_lo(ww[e]) : -INFINITY;
-            x[q * VEC + 2 * e + 1] = have[q] ? bf16_hi(ww[e]) : -INFINITY;
-          }
-        } else {
-          x[q * VEC + 0] = have[q] ? __uint_as_float(w.x) : -INFINITY;
-          x[q * VEC + 1] = have[q] ? __uint_as_float(w.y) : -INFINITY;
-          x[q * VEC + 2] = have[q] ? __uint_as_float(w.z) : -INFINITY;
-          x[q * VEC + 3] = have[q] ? __uint_as_float(w.w) : -INFINITY;
-        }
-      }
-      // element id of x[q*VEC + e]: st_e0 + ((h*HALF + q)*32 + lane)*VEC + e
-      float lm = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < HALF * VEC; ++j) lm = fmaxf(lm, x[j]);
-
-      if (SOFTMAX) {
-        if (lm > m_t) {
-          if (m_t != -INFINITY) {
-            const float sc = ex2((m_t - lm) * kLog2e);
-            s_hi *= sc;
-            s_lo *= sc;
-          }
-          m_t = lm;
-        }
-        if (m_t != -INFINITY) {
-          float e[HALF * VEC];
-#pragma unroll
-          for (int j = 0; j < HALF * VEC; ++j) e[j] = ex2((x[j] - m_t) * kLog2e);
-#pragma unroll
-          for (int w2 = 1; w2 < HALF * VEC; w2 <<= 1)
-#pragma unroll
-            for (int j = 0; j + w2 < HALF * VEC; j += 2 * w2) e[j] += e[j + w2];
-          const float y = e[0] - s_lo;
-          const float tt = s_hi + y;
-          s_lo = (tt - s_hi) - y;
-          s_hi = tt;
-        } else {
-#pragma unroll
-          for (int j = 0; j < HALF * VEC; ++j)
-            if (x[j] != x[j]) s_hi = x[j];
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < HALF * VEC; ++j) bad_bits = max(bad_bits, __float_as_uint(x[j]) & 0x7FFFFFFFu);
-        seen_max = fmaxf(seen_max, lm);
-      }
-
-      // first step of the chunk: the list starts as the K best per-lane maxima
-      uint64_t excl = 0ull;
-      if (!inited) {
-        uint64_t best = 0ull;
-#pragma unroll
-        for (int q = 0; q < HALF; ++q)
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const float v = x[q * VEC + e];
-            if (have[q] && !(v != v)) {
-              const uint64_t k = make_key(v, (uint32_t)(st_e0 + (int64_t)((h * HALF + q) * 32 + lane) * VEC + e));
-              best = k > best ? k : best;
-            }
-          }
-        excl = best;
-        const uint64_t srt = warp_sort_desc(best);
-        L = lane < K ? srt : 0ull;
-        tau_key = shfl_u64(L, K - 1);
-        tau_val = tau_key ? key_value(tau_key) : -INFINITY;
-        inited = true;
-      }
-
-      // filter against the list's K-th key; re-run with a higher threshold if the buffer overflowed
-      for (;;) {
-        if (lm >= tau_val) {
-#pragma unroll
-          for (int q = 0; q < HALF; ++q)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              const float v = x[q * VEC + e];
-              if (have[q] && v >= tau_val) {
-                const uint64_t k =
-                    make_key(v, (uint32_t)(st_e0 + (int64_t)((h * HALF + q) * 32 + lane) * VEC + e));
-                if (k > tau_key && k != excl) {
-                  const int pos = atomicAdd(&rg.cnt, 1);
-                  if (pos < kWarpCand) rg.cand[pos] = k;
-                  else rg.ovf = 1;
-                }
-              }
-            }
-        }
-        if (!drain()) break;
-        // Overflow: the buffer's first kWarpCand entries are in the list now and tau rose; filter
-        // this step again for keys above tau that are not already in the list.
-        excl = 0ull;
-        if (++ovf_rounds > 64) {
-          if (lane == 0) sm.flags[warp] |= 2;
-          break;
-        }
-        // keys already in the list are excluded by a membership test in the re-run
-#pragma unroll
-        for (int q = 0; q < HALF; ++q)
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const float v = x[q * VEC + e];
-            bool in_list = false;
-            const uint64_t k =
-                have[q] && !(v != v) ? make_key(v, (uint32_t)(st_e0 + (int64_t)((h * HALF + q) * 32 + lane) * VEC + e))
-                                     : 0ull;
-            for (int j = 0; j < K; ++j) in_list |= (shfl_u64(L, j) == k);
-            if (in_list) x[q * VEC + e] = -INFINITY;
-          }
-        lm = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < HALF * VEC; ++j) lm = fmaxf(lm, x[j]);
-      }
+    for (int q = 0; q < QV; ++q) {
+      const int vi = q * 32 + lane;
+      uint4 w = make_uint4(neg_fill, neg_fill, neg_fill, neg_fill);
+      if (vi * 16 < st_bytes) w = *reinterpret_cast<const uint4*>(sp + (size_t)vi * 16);
+      wv[4 * q + 0] = w.x;
+      wv[4 * q + 1] = w.y;
+      wv[4 * q + 2] = w.z;
+      wv[4 * q + 3] = w.w;
     }
-
-    // release the stage and refill it
     __syncwarp();
+    // the stage's smem is free again: refill it with stage t + kWarpStages
     if (lane == 0 && t + kWarpStages < n_st) {
       fence_proxy_async_smem();
       const int64_t off = (int64_t)(t + kWarpStages) * kStageBytes;
       const uint32_t bytes = (uint32_t)min((int64_t)kStageBytes, wbytes - off);
       mbar_arrive_expect_tx(&rg.bar[st], bytes);
       bulk_g2s(my_stages + (size_t)st * kStageBytes, wsrc + off, bytes, &rg.bar[st]);
+    }
+
+    // lane max with NaN propagation (a NaN makes it NaN): packed bf16x2 or fp32 tree
+    float lm;
+    {
+      uint32_t r[QV * 4];
+#pragma unroll
+      for (int j = 0; j < QV * 4; ++j) r[j] = wv[j];
+#pragma unroll
+      for (int w2 = 1; w2 < QV * 4; w2 <<= 1)
+#pragma unroll
+        for (int j = 0; j + w2 < QV * 4; j += 2 * w2) r[j] = ESZ == 2 ? max_nan_bf16x2(r[j], r[j + w2])
+                                                                       : max_nan_f32u(r[j], r[j + w2]);
+      lm = ESZ == 2 ? max_nan_f32(bf16_lo(r[0]), bf16_hi(r[0])) : __uint_as_float(r[0]);
+    }
+    if (!SOFTMAX) seen_max = max_nan_f32(seen_max, lm);
+
+    if (SOFTMAX) {
+      if (lm > m_t) {
+        if (m_t != -INFINITY) {
+          const float sc = ex2((m_t - lm) * kLog2e);
+          s_hi *= sc;
+          s_lo *= sc;
+        }
+        m_t = lm;
+      }
+      if (lm != lm) {
+        s_hi = lm;  // NaN poisons the sum
+      } else if (m_t != -INFINITY) {
+        // sum of exp(x - m) over the stage: four 16-value trees (bf16) / 2 x 16 (fp32)
+        float part = 0.0f;
+#pragma unroll
+        for (int c = 0; c < NV / 16; ++c) {
+          float e[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int v = c * 16 + j;  // value index within the lane's stage values
+            float x;
+            if (ESZ == 2) x = (v & 1) ? bf16_hi(wv[v >> 1]) : bf16_lo(wv[v >> 1]);
+            else x = __uint_as_float(wv[v]);
+            e[j] = ex2((x - m_t) * kLog2e);
+          }
+#pragma unroll
+          for (int w2 = 1; w2 < 16; w2 <<= 1)
+#pragma unroll
+            for (int j = 0; j + w2 < 16; j += 2 * w2) e[j] += e[j + w2];
+          part += e[0];
+        }
+        const float y = part - s_lo;
+        const float tt = s_hi + y;
+        s_lo = (tt - s_hi) - y;
+        s_hi = tt;
+      }
+    }
+
+    // value v of this lane's stage values sits in vector q = v / VEC, element e = v % VEC, and has
+    // token id st_e0 + ((q * 32 + lane) * VEC + e)
+    auto value_at = [&](int v) -> float {
+      if (ESZ == 2) return (v & 1) ? bf16_hi(wv[v >> 1]) : bf16_lo(wv[v >> 1]);
+      return __uint_as_float(wv[v]);
+    };
+    auto id_at = [&](int v) -> uint32_t {
+      return (uint32_t)(st_e0 + (int64_t)(((v / VEC) * 32 + lane) * VEC + (v % VEC)));
+    };
+
+    // first stage of the chunk: the list starts as the K best per-lane maxima
+    uint64_t excl = 0ull;
+    if (!inited) {
+      uint64_t best = 0ull;
+      if (lm == lm && lm != -INFINITY) {
+        int vb = 0;
+#pragma unroll
+        for (int v = NV - 1; v >= 0; --v)
+          if (value_at(v) == lm) vb = v;  // lowest id among the maxima
+        best = make_key(lm, id_at(vb));
+      }
+      excl = best;
+      const uint64_t srt = warp_sort_desc(best);
+      L = lane < K ? srt : 0ull;
+      tau_key = shfl_u64(L, K - 1);
+      tau_val = tau_key ? key_value(tau_key) : -INFINITY;
+      inited = true;
+    }
+
+    // filter against the list's K-th key, only when some lane's maximum clears it: every value that
+    // beats the current K-th key is inserted at once (ballot + broadcast), which also raises the
+    // threshold for the values that follow
+    if (__any_sync(0xFFFFFFFFu, lm >= tau_val)) {
+      const bool lane_hot = lm >= tau_val;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const float x = value_at(v);
+        uint64_t k = 0ull;
+        if (lane_hot && x >= tau_val && x != -INFINITY) k = make_key(x, id_at(v));
+        unsigned want = __ballot_sync(0xFFFFFFFFu, k > tau_key && k != excl);
+        while (want) {  // warp-uniform
+          const int src = __ffs(want) - 1;
+          want &= want - 1;
+          const uint64_t kk = shfl_u64(k, src);
+          if (kk > tau_key) {
+            wl_insert(L, kk, K, lane);
+            tau_key = shfl_u64(L, K - 1);
+            tau_val = tau_key ? key_value(tau_key) : -INFINITY;
+          }
+        }
+      }
     }
   }
   drain();  // head/tail entries of a chunk without stages
@@ -506,7 +508,7 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
     sm.red_s[warp] = (double)ch + (double)cl;
   }
   out.bad = false;
-  if (!SOFTMAX) out.bad = __syncthreads_or(bad_bits > 0x7F800000u || seen_max == INFINITY) != 0;
+  if (!SOFTMAX) out.bad = __syncthreads_or(seen_max != seen_max || seen_max == INFINITY) != 0;
   if (tid < kMaxK) sm.topk[tid] = 0ull;
   __syncthreads();
   int internal = 0;
