@@ -124,15 +124,14 @@ def run_ours(args):
     import synth
     from synth.workloads import WORKLOADS, spec_for, geometry, cast_tables, chain_template
     import __graft_entry__
-    from dynamic_draft_tree_gb300 import dt_get_status
-    from dynamic_draft_tree_gb300.rounds import RoundRunner
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     if world > 1:
         tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    if rank == 0 or world > 1:
-        __graft_entry__.build()
+    __graft_entry__.build()  # every rank builds (or finds) the library before importing it
+    from dynamic_draft_tree_gb300 import dt_get_status
+    from dynamic_draft_tree_gb300.rounds import RoundRunner
 
     w = dict(WORKLOADS[args.workload])
     w["seed"] = w["seed"] + 1000 * rank  # independent batch per rank
