@@ -289,6 +289,7 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
 
   // head + tail elements (warp 0): softmax, and always candidates
   const int n_head = (int)(a0 - s0), n_tail = (int)(s1 - a1);
+  uint64_t ht_key = 0ull;
   if (warp == 0 && lane < n_head + n_tail) {
     const int64_t idx = lane < n_head ? s0 + lane : a1 + (lane - n_head);
     const float x = Elt<T>::load(row + idx);
@@ -297,10 +298,9 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
     } else {
       seen_max = x;
     }
-    if (!(x != x)) {
-      const int pos = atomicAdd(&rg.cnt, 1);
-      rg.cand[pos] = make_key(x, (uint32_t)idx);
-    }
+    // its key joins the warp list only after streaming: the strict tie test of later stages relies on
+    // the list holding earlier (smaller) ids of this warp's own chunk
+    if (!(x != x)) ht_key = make_key(x, (uint32_t)idx);
   }
   __syncwarp();
 
@@ -454,31 +454,59 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
       inited = true;
     }
 
-    // filter against the list's K-th key, only when some lane's maximum clears it: every value that
-    // beats the current K-th key is inserted at once (ballot + broadcast), which also raises the
-    // threshold for the values that follow
-    if (__any_sync(0xFFFFFFFFu, lm >= tau_val)) {
-      const bool lane_hot = lm >= tau_val;
+    // Filter against the list's K-th key. Within a warp's chunk token ids grow stage by stage, so
+    // after the first stage a value equal to the K-th key's value has a larger id and cannot beat it:
+    // the test is strict there. Lanes whose maximum clears the threshold push their candidates to
+    // the warp's buffer, which is then inserted into the list. If the buffer overflows, the stage is
+    // re-filtered with ballots (every candidate inserted directly; exact, slower, rare).
+    const bool hot = (t == 0) ? (lm >= tau_val) : (lm > tau_val);
+    if (__any_sync(0xFFFFFFFFu, hot)) {
+      if (hot) {
 #pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const float x = value_at(v);
-        uint64_t k = 0ull;
-        if (lane_hot && x >= tau_val && x != -INFINITY) k = make_key(x, id_at(v));
-        unsigned want = __ballot_sync(0xFFFFFFFFu, k > tau_key && k != excl);
-        while (want) {  // warp-uniform
-          const int src = __ffs(want) - 1;
-          want &= want - 1;
-          const uint64_t kk = shfl_u64(k, src);
-          if (kk > tau_key) {
-            wl_insert(L, kk, K, lane);
-            tau_key = shfl_u64(L, K - 1);
-            tau_val = tau_key ? key_value(tau_key) : -INFINITY;
+        for (int v = 0; v < NV; ++v) {
+          const float x = value_at(v);
+          if (x >= tau_val && x != -INFINITY) {
+            const uint64_t k = make_key(x, id_at(v));
+            if (k > tau_key && k != excl) {
+              const int pos = atomicAdd(&rg.cnt, 1);
+              if (pos < kWarpCand) rg.cand[pos] = k;
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (rg.cnt <= kWarpCand) {
+        drain();
+      } else {
+        __syncwarp();
+        if (lane == 0) rg.cnt = 0;
+        __syncwarp();
+        const bool lane_hot = lm >= tau_val;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          const float x = value_at(v);
+          uint64_t k = 0ull;
+          if (lane_hot && x >= tau_val && x != -INFINITY) k = make_key(x, id_at(v));
+          unsigned want = __ballot_sync(0xFFFFFFFFu, k > tau_key && k != excl);
+          while (want) {  // warp-uniform
+            const int src = __ffs(want) - 1;
+            want &= want - 1;
+            const uint64_t kk = shfl_u64(k, src);
+            if (kk > tau_key) {
+              wl_insert(L, kk, K, lane);
+              tau_key = shfl_u64(L, K - 1);
+              tau_val = tau_key ? key_value(tau_key) : -INFINITY;
+            }
           }
         }
       }
     }
   }
-  drain();  // head/tail entries of a chunk without stages
+  if (ht_key) {  // head/tail elements (warp 0)
+    const int pos = atomicAdd(&rg.cnt, 1);
+    rg.cand[pos] = ht_key;
+  }
+  drain();
 
   SegOut out;
   out.timed_out = __syncthreads_or(timed_out) != 0;
