@@ -211,12 +211,10 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
 }  // namespace
 
 int choose_segments(const dt_handle* h, int64_t rows, int64_t V, int elt_bytes) {
-  // Enough CTAs for one full wave (3 resident per SM), segments of at most ~64 KB so that many
-  // small CTAs balance across SMs, and at least ~8 KB of work per CTA.
+  // Enough CTAs for one full wave (3 resident per SM) with segments as long as possible, so that
+  // every warp streams through its ring for many stages; at least ~8 KB of work per CTA.
   const int64_t row_bytes = V * elt_bytes;
-  const int64_t s_fill = ((int64_t)h->num_sms * 3 + rows - 1) / rows;
-  const int64_t s_size = (row_bytes + 65535) / 65536;
-  int64_t S = s_fill > s_size ? s_fill : s_size;
+  int64_t S = ((int64_t)h->num_sms * 3 + rows - 1) / rows;
   const int64_t max_by_len = (row_bytes + 8191) / 8192;
   if (S > max_by_len) S = max_by_len;
   const int64_t max_by_keys = kCandCap / h->cfg.K;

@@ -214,3 +214,12 @@ FULL = [("pr1", {}, 3), ("vicuna", {}, 2), ("vicuna", dict(T=1), 2), ("cast", {}
 def test_round_parity_full_size(torch, name, over, rounds):
     w = with_sizes(name, **over)
     _run_rounds(torch, w, rounds)
+
+
+@pytest.mark.parametrize("V,K", [(128256, 32), (128256, 10), (70001, 8)])
+def test_expand_layer_ties_across_stages(torch, V, K):
+    """Exact ties everywhere (all-equal rows) and coarse values with many ties at the K-th boundary:
+    ties must go to the lower token id across stages, warps and segments (and the overflow path)."""
+    _expand_case(torch, V, K, 2, 0, lambda B, V: np.zeros((B, V)))
+    rng = np.random.default_rng(V + K)
+    _expand_case(torch, V, K, 3, 0, lambda B, V: rng.integers(0, 4, (B, V)).astype(np.float64))
