@@ -145,6 +145,21 @@ def dt_adj_update(h, M, meta, top8, stream=None):
     check(lib.dt_adj_update(h.h, _ptr(M), ctypes.byref(meta.c), _ptr(top8), _stream(stream)))
 
 
+def dt_row_topk_static(logits, K, logp, ids, V=None, status=None, stream=None):
+    """Row log-softmax top-K with no handle and no allocation: logits [rows][ld] (bf16 or fp32),
+    logp [rows][K] fp32 and ids [rows][K] int32 caller-owned; status an int32 device word or None."""
+    ld = logits.shape[-1]
+    rows = logits.numel() // ld
+    V = ld if V is None else V
+    if logits.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("logits must be bfloat16 or float32")
+    if logp.dtype != torch.float32 or ids.dtype != torch.int32 or logp.numel() < rows * K or ids.numel() < rows * K:
+        raise ValueError("logp must be float32 and ids int32, each with rows*K elements")
+    dtype = DT_BF16 if logits.dtype == torch.bfloat16 else DT_F32
+    check(lib.dt_row_topk_static(_ptr(logits), ld, rows, V, K, dtype, _ptr(logp), _ptr(ids), _ptr(status),
+                                 _stream(stream)))
+
+
 class Meta:
     """Caller-owned device arrays of a flattened verify tree (dt_tree_meta)."""
 

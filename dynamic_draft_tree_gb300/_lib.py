@@ -19,7 +19,8 @@ DT_FLAG_TEST_TIMEOUT = 1
 
 EXPORTS = ["dt_last_error_string", "dt_create", "dt_destroy", "dt_get_tree", "dt_get_status",
            "dt_clear_status", "dt_tree_reset", "dt_select_frontier", "dt_expand_layer", "dt_cast_prune",
-           "dt_rerank", "dt_graft_retrieve", "dt_build_tree_meta", "dt_verify", "dt_adj_update"]
+           "dt_rerank", "dt_graft_retrieve", "dt_build_tree_meta", "dt_verify", "dt_adj_update",
+           "dt_row_topk_static"]
 
 c_i32p = ctypes.c_void_p
 vp = ctypes.c_void_p
@@ -88,6 +89,8 @@ def _load():
         "dt_verify": ([vp, ctypes.POINTER(DtTreeMeta), vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64,
                        ctypes.c_uint64, vp, vp, vp, vp, vp], I),
         "dt_adj_update": ([vp, vp, ctypes.POINTER(DtTreeMeta), vp, vp], I),
+        "dt_row_topk_static": ([vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                vp, vp, vp, vp], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)

@@ -16,7 +16,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libdt.so")
 ARCH = "103a"
 
-SOURCES = ["dt_api.cu", "k_tree.cu", "k_select.cu", "k_meta.cu", "k_verify.cu", "k_graft.cu"]
+SOURCES = ["dt_api.cu", "k_tree.cu", "k_select.cu", "k_meta.cu", "k_verify.cu", "k_graft.cu",
+           "k_rowtopk_static.cu"]
 HEADERS = ["dt_internal.cuh", "rowscan.cuh"]
 
 

@@ -343,4 +343,22 @@ int dt_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta, const int3
   return DT_OK;
 }
 
+int dt_row_topk_static(const void* logits, int64_t ld, int32_t rows, int32_t V, int32_t K, int32_t dtype,
+                       float* logp, int32_t* ids, int32_t* status, cudaStream_t s) {
+  if (!logits || !logp || !ids) return fail(DT_ERR_ARG, "dt_row_topk_static: null argument");
+  if (rows < 1 || rows > dt::kStaticRows)
+    return fail(DT_ERR_ARG, "rows=%d outside [1, %d] (size of the static scratch)", rows, dt::kStaticRows);
+  if (V < 2) return fail(DT_ERR_ARG, "V must be >= 2");
+  if (K < 1 || K > dt::kMaxK || K > V) return fail(DT_ERR_ARG, "K must be in [1, min(32, V)]");
+  if (dtype != DT_BF16 && dtype != DT_F32) return fail(DT_ERR_ARG, "dtype must be DT_BF16 or DT_F32");
+  if (ld < V) return fail(DT_ERR_ARG, "ld=%lld < V", (long long)ld);
+  const size_t esz = dtype == DT_BF16 ? 2 : 4;
+  if (!aligned(logits, esz)) return fail(DT_ERR_ARG, "logits not aligned to its element size");
+  if (!aligned(logp, 4) || !aligned(ids, 4) || !aligned(status, 4))
+    return fail(DT_ERR_ARG, "logp, ids and status must be 4-byte aligned");
+  cudaError_t e = dt::launch_row_topk_static(logits, ld, rows, V, K, dtype, logp, ids, status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dt_row_topk_static");
+  return DT_OK;
+}
+
 }  // extern "C"

@@ -20,6 +20,8 @@ constexpr int kWarpStages = 4;      // ring depth per warp
 constexpr int kWarpCand = 128;      // per-warp candidate buffer
 constexpr int kCandCap = 1024;      // CTA merge / sort buffer (keys)
 constexpr int kScanSmemBytes = kScanWarps * kWarpStages * kStageBytes;  // dynamic shared memory
+constexpr int kStaticRows = 1024;      // rows per call of the static-scratch row top-K
+constexpr int kStaticPartials = 4096;  // row segments per call of the static-scratch row top-K
 
 // Per-(row, segment) partial result of a row scan.
 struct Partial {
@@ -117,6 +119,8 @@ cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* lo
                           int32_t* bonus, int32_t* top8, cudaStream_t s);
 cudaError_t launch_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta, const int32_t* top8,
                               cudaStream_t s);
+cudaError_t launch_row_topk_static(const void* logits, int64_t ld, int rows, int V, int K, int dtype, float* logp,
+                                   int32_t* ids, int32_t* status, cudaStream_t s);
 
 // One-time kernel attributes (dynamic shared memory limits), set by dt_create so that no launch
 // path calls a non-stream API (launches stay capturable in CUDA graphs).

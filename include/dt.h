@@ -247,6 +247,28 @@ int dt_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_
 int dt_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta, const int32_t* top8,
                   cudaStream_t s);
 
+/* Standalone row log-softmax top-K that allocates nothing. This entry point has no counterpart in
+ * the method's pages: it is the expansion's row pass (EAGLE-2 §扩展阶段: the children of a node
+ * are the top-K tokens of softmax(row), c = draft probability) offered without a handle, for
+ * callers that cannot allocate device memory at the point of the call: dt_create's workspace
+ * comes from cudaMalloc, which synchronises the device and fails once the process has handed all
+ * of its memory to other pools (a serving engine that reserves HBM for its KV cache at start-up).
+ *   logits: device [rows][ld] (DT_BF16 or DT_F32 per dtype), element-aligned; V <= ld.
+ *   logp:   device [rows][K] fp32, log softmax(row)[ids], descending.
+ *   ids:    device [rows][K] int32 token ids; equal logits go to the lower id.
+ *   status: device int32 or NULL; DT_DEV_* bits are OR-ed into it (never cleared here).
+ * Scratch: file-scope device arrays of fixed size, about 1.1 MB per device: 4096 row-segment
+ * partial results and 1024 per-row arrival counters. Hence rows <= 1024 (DT_ERR_ARG beyond).
+ * The counters must be zero when a call starts: they are zero when the library is loaded and each
+ * call leaves them zero. The partials need no initial value.
+ * The first call on each device does a one-time set-up (cudaGetSymbolAddress of the scratch,
+ * the SM count, the kernels' shared-memory limit); make that first call outside any stream
+ * capture. Every call on a device shares the one scratch: two calls that may overlap in time
+ * (different streams with no ordering between them) race and corrupt each other's results;
+ * issue them on one stream or order them with events. */
+int dt_row_topk_static(const void* logits, int64_t ld, int32_t rows, int32_t V, int32_t K, int32_t dtype,
+                       float* logp, int32_t* ids, int32_t* status, cudaStream_t s);
+
 #ifdef __cplusplus
 }
 #endif

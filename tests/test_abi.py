@@ -75,3 +75,15 @@ def test_python_binding_names_match_abi(libdt):
         if name == "dt_last_error_string":
             continue
         assert hasattr(pkg, name), name
+
+
+def test_static_topk_arguments_rejected_on_host(libdt):
+    """dt_row_topk_static checks its sizes before any CUDA call; the pointers are never touched."""
+    lib = libdt.lib
+    fake = 256  # 256-byte aligned, never dereferenced: every call below fails the host check
+    assert lib.dt_row_topk_static(None, 1000, 4, 1000, 4, 0, fake, fake, None, None) == libdt.DT_ERR_ARG
+    assert lib.dt_row_topk_static(fake, 1000, 1025, 1000, 4, 0, fake, fake, None, None) == libdt.DT_ERR_ARG
+    assert "static scratch" in lib.dt_last_error_string().decode()
+    for rows, V, K, dtype, ld in [(0, 1000, 4, 0, 1000), (4, 1, 1, 0, 1000), (4, 1000, 33, 0, 1000),
+                                  (4, 10, 11, 0, 10), (4, 1000, 4, 5, 1000), (4, 1000, 4, 0, 999)]:
+        assert lib.dt_row_topk_static(fake, ld, rows, V, K, dtype, fake, fake, None, None) == libdt.DT_ERR_ARG
