@@ -326,9 +326,10 @@ def run_ours(args):
                      "peak_source": peak_kind,
                      "bytes_per_launch": ver_bytes / len(ver_ms), "avg_launch_us": 1e3 * sum(ver_ms) / len(ver_ms)},
         "kernels": {"dt_verify": {"gbs": ver_gbs, "avg_us": 1e3 * float(np.mean(ver_ms)),
-                                  "avg_bytes": ver_bytes / len(ver_ms)},
+                                  "avg_bytes": ver_bytes / len(ver_ms), "rows_per_round": rows_verify},
                     "dt_expand_layer": {"gbs": exp_gbs, "avg_us": 1e3 * float(np.mean(exp_ms)),
-                                        "avg_bytes": exp_bytes / len(exp_ms), "launches_per_round": D}},
+                                        "avg_bytes": exp_bytes / len(exp_ms), "launches_per_round": D,
+                                        "rows_per_round": rows_expand}},
         "e2e": e2e,
         "gpu_launches": launches_per_round * args.steps,
         "replay_consistent": consistent,
