@@ -130,7 +130,10 @@ cudaError_t init_select_attributes();
 cudaError_t init_meta_attributes();
 
 // Segments per row for a row-scan launch of `rows` rows of V elements.
-int choose_segments(const dt_handle* h, int64_t rows, int64_t V, int elt_bytes);
+// Balanced row pass: CTAs per launch (one wave) and the most pieces a row may be cut into when
+// its partial lists hold K keys.
+int row_pass_grid(const dt_handle* h);
+int row_pass_smax(int K);
 
 }  // namespace dt
 

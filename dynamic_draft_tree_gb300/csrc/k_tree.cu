@@ -97,140 +97,110 @@ struct ExpandArgs {
   Workspace ws;
   const void* logits;
   int64_t ld;
-  int F, S, B, N, K, W, LW, D, d, V;
-  int64_t seg_len;
+  int F, B, N, K, W, LW, D, d, V;
+  int Smax;      // pieces per row at most
   int32_t base;  // first id of layer d
   uint32_t first_wait_cap;
 };
 
+// Balanced over the active rows (request b expands min(frontier_count[b], F) nodes); see the
+// balanced row pass in rowscan.cuh.
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
   extern __shared__ __align__(128) uint8_t dyn_smem[];
   __shared__ ScanSmem sm;
-  const int r = blockIdx.x / a.S;
-  const int seg = blockIdx.x % a.S;
-  const int b = r / a.F, f = r % a.F;
+  __shared__ RowPlan plan;
   const int tid = threadIdx.x;
   Workspace& ws = a.ws;
-  const int fc = ws.frontier_count[b];
-  const int active = min(fc, a.F);
-  if (f >= active) {  // no node in this slot: the row is not read
-    if (f == 0 && seg == 0 && tid == 0 && fc > a.F) set_status(ws.status, DT_DEV_BAD_TREE);
-    return;
+  auto cnt = [&](int b) -> int { return min(max(ws.frontier_count[b], 0), a.F); };
+  if (tid < 32) {
+    RowPlan p;
+    plan_rows(p, a.B, a.V, a.Smax, (int)sizeof(T), cnt);
+    if (tid == 0) plan = p;
+    if (blockIdx.x == 0)  // a frontier wider than the launch's F is a caller error
+      for (int b = tid; b < a.B; b += 32)
+        if (ws.frontier_count[b] > a.F) set_status(ws.status, DT_DEV_BAD_TREE);
   }
+  __syncthreads();
+  const RowPlan p = plan;
+  if ((int)blockIdx.x >= p.G) return;
 
-  const T* row = reinterpret_cast<const T*>(a.logits) + (int64_t)r * a.ld;
-  const int64_t s0 = (int64_t)seg * a.seg_len;
-  const int64_t s1 = min((int64_t)a.V, s0 + a.seg_len);
-  SegOut so = scan_segment<T, true>(row, s0, s1, a.K, sm, dyn_smem, a.first_wait_cap);
-
-  Partial* part = ws.partials + (int64_t)r * a.S;
-  for (int i = tid; i < a.K; i += blockDim.x) part[seg].keys[i] = i < so.nkeys ? sm.cand[i] : 0ull;
-  if (tid == 0) {
-    part[seg].m = so.m;
-    part[seg].s = so.s;
-    if (so.timed_out) set_status(ws.status, DT_DEV_TIMEOUT);
-    if (so.internal) set_status(ws.status, DT_DEV_INTERNAL);
+  auto row_of = [&](int b, int f) -> const T* {
+    return reinterpret_cast<const T*>(a.logits) + ((int64_t)b * a.F + f) * a.ld;
+  };
+  // last piece of row (b, f): write the K children of frontier slot f
+  auto finish = [&](int b, int f, const Partial* rp, int S) {
+    float M;
+    double Ssum;
+    bool nan;
+    merge_softmax(rp, S, sm, M, Ssum, nan);
+    if (tid == 0 && (nan || !(M > -INFINITY) || M == INFINITY || !(Ssum > 0.0)))
+      set_status(ws.status, DT_DEV_BAD_LOGITS);
+    const int pid = ws.frontier[(int64_t)b * a.W + f];
+    const float pval = ws.value[(int64_t)b * a.N + pid];
+    // log S = e * ln 2 + log(mantissa), mantissa in [1, 2): the exponent split is exact and the fp32
+    // log of the mantissa is accurate to ~1e-7 absolute (no fp64 transcendental on the tail)
+    double logS;
+    {
+      const unsigned long long bits = (unsigned long long)__double_as_longlong(Ssum);
+      const int e = (int)((bits >> 52) & 0x7FF) - 1023;
+      const double mant =
+          __longlong_as_double((long long)((bits & 0x000FFFFFFFFFFFFFull) | 0x3FF0000000000000ull));
+      logS = (double)e * 0.6931471805599453 + (double)logf((float)mant);
+      if (!(Ssum > 0.0) || Ssum != Ssum || e == 1024) logS = log(Ssum);  // zero, NaN, inf: let log decide
+    }
+    if (tid < a.K) {
+      const uint64_t k = sm.topk[tid];
+      const int id = a.base + f * a.K + tid;
+      const int64_t gi = (int64_t)b * a.N + id;
+      const float x = key_value(k);
+      const double lc = ((double)x - (double)M) - logS;
+      ws.token[gi] = (int32_t)key_id(k);
+      ws.parent[gi] = pid;
+      ws.logc[gi] = (float)lc;
+      ws.value[gi] = (float)((double)pval + lc);
+    }
     __threadfence();
-    const int prev = atomicAdd(&ws.row_counter[r], 1);
-    sm.last = (prev == a.S - 1);
-  }
-  __syncthreads();
-  if (!sm.last) return;
-
-  // ---- last segment of the row: merge the partials and write the K children ----
-  __threadfence();
-  if (tid == 0) ws.row_counter[r] = 0;
-  const int nk = a.S * a.K;
-  for (int i = tid; i < nk; i += blockDim.x) {
-    const uint64_t k = __ldcg(&part[i / a.K].keys[i % a.K]);
-    sm.cand[i] = k;
-  }
-  if (tid < kMaxK) sm.topk[tid] = 0ull;
-  __syncthreads();
-  // empty keys are 0 and rank below every real key
-  merge_sorted_lists(sm, a.S, a.K);
-  float M;
-  double Ssum;
-  bool nan;
-  merge_softmax(part, a.S, sm, M, Ssum, nan);
-  if (tid == 0 && (nan || !(M > -INFINITY) || M == INFINITY || !(Ssum > 0.0)))
-    set_status(ws.status, DT_DEV_BAD_LOGITS);
-  const int pid = ws.frontier[(int64_t)b * a.W + f];
-  const float pval = ws.value[(int64_t)b * a.N + pid];
-  // log S = e * ln 2 + log(mantissa), mantissa in [1, 2): the exponent split is exact and the fp32
-  // log of the mantissa is accurate to ~1e-7 absolute (no fp64 transcendental on the tail)
-  double logS;
-  {
-    const unsigned long long bits = (unsigned long long)__double_as_longlong(Ssum);
-    const int e = (int)((bits >> 52) & 0x7FF) - 1023;
-    const double mant = __longlong_as_double((long long)((bits & 0x000FFFFFFFFFFFFFull) | 0x3FF0000000000000ull));
-    logS = (double)e * 0.6931471805599453 + (double)logf((float)mant);
-    if (!(Ssum > 0.0) || Ssum != Ssum || e == 1024) logS = log(Ssum);  // zero, NaN, inf: let log decide
-  }
-  if (tid < a.K) {
-    const uint64_t k = sm.topk[tid];
-    const int id = a.base + f * a.K + tid;
-    const int64_t gi = (int64_t)b * a.N + id;
-    const float x = key_value(k);
-    const double lc = ((double)x - (double)M) - logS;
-    ws.token[gi] = (int32_t)key_id(k);
-    ws.parent[gi] = pid;
-    ws.logc[gi] = (float)lc;
-    ws.value[gi] = (float)((double)pval + lc);
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(&ws.req_counter[b], 1);
-    sm.last = (prev == active - 1);
-  }
-  __syncthreads();
-  if (!sm.last) return;
-
-  // ---- last row of the request: order the new layer by (value desc, id asc) ----
-  __threadfence();
-  if (tid == 0) ws.req_counter[b] = 0;
-  const int n = active * a.K;
-  int32_t* order = ws.layer_order + ((int64_t)b * (a.D + 1) + a.d) * a.LW;
-  // keys staged in the candidate buffer (n <= W*K <= 1024 = kCandCap)
-  for (int i = tid; i < n; i += blockDim.x) {
-    const int id = a.base + i;
-    sm.cand[i] = make_key(__ldcg(&ws.value[(int64_t)b * a.N + id]), (uint32_t)id);
-  }
-  __syncthreads();
-  for (int i = tid; i < n; i += blockDim.x) {
-    const uint64_t k = sm.cand[i];
-    int rank = 0;
-    for (int j = 0; j < n; ++j) rank += (sm.cand[j] > k);
-    order[rank] = (int32_t)key_id(k);
-  }
-  if (tid == 0) ws.layer_count[(int64_t)b * (a.D + 1) + a.d] = n;
+    __syncthreads();
+    const int active = cnt(b);
+    if (tid == 0) {
+      const int prev = atomicAdd(&ws.req_counter[b], 1);
+      sm.last = (prev == active - 1);
+    }
+    __syncthreads();
+    if (sm.last) {  // last row of the request: order the new layer by (value desc, id asc)
+      __threadfence();
+      if (tid == 0) ws.req_counter[b] = 0;
+      const int n = active * a.K;
+      int32_t* order = ws.layer_order + ((int64_t)b * (a.D + 1) + a.d) * a.LW;
+      // keys staged in the candidate buffer (n <= W*K <= 1024 = kCandCap)
+      for (int i = tid; i < n; i += blockDim.x) {
+        const int id = a.base + i;
+        sm.cand[i] = make_key(__ldcg(&ws.value[(int64_t)b * a.N + id]), (uint32_t)id);
+      }
+      __syncthreads();
+      for (int i = tid; i < n; i += blockDim.x) {
+        const uint64_t k = sm.cand[i];
+        int rank = 0;
+        for (int j = 0; j < n; ++j) rank += (sm.cand[j] > k);
+        order[rank] = (int32_t)key_id(k);
+      }
+      if (tid == 0) ws.layer_count[(int64_t)b * (a.D + 1) + a.d] = n;
+    }
+  };
+  scan_pieces<T, true>(p, a.V, a.K, a.B, ws.partials, ws.row_counter, sm, dyn_smem, a.first_wait_cap, ws.status,
+                       row_of, cnt, finish);
 }
 
 }  // namespace
 
-int choose_segments(const dt_handle* h, int64_t rows, int64_t V, int elt_bytes) {
-  // Enough CTAs for one full wave (3 resident per SM) with segments as long as possible, so that
-  // every warp streams through its ring for many stages; at least ~8 KB of work per CTA.
-  const int64_t row_bytes = V * elt_bytes;
-  int64_t S = ((int64_t)h->num_sms * 3 + rows - 1) / rows;
-  const int64_t max_by_len = (row_bytes + 8191) / 8192;
-  if (S > max_by_len) S = max_by_len;
-  const int64_t max_by_keys = kCandCap / h->cfg.K;
-  if (S > max_by_keys) S = max_by_keys;
-  if (S > 64) S = 64;
-  const int64_t max_by_buf = h->ws.partial_cap / (rows > 0 ? rows : 1);  // partials buffer capacity
-  if (S > max_by_buf) S = max_by_buf;
-  if (S < 1) S = 1;
-  return (int)S;
+int row_pass_grid(const dt_handle* h) {
+  // one wave: 3 CTAs per SM (registers and shared memory allow 3), within the piece-slot capacity
+  const int64_t g = std::min<int64_t>((int64_t)h->num_sms * 3, 4096);
+  return (int)std::max<int64_t>(1, g);
 }
 
-static int64_t seg_len_for(int64_t V, int S) {
-  int64_t L = (V + S - 1) / S;
-  L = (L + 7) / 8 * 8;
-  return L;
-}
+int row_pass_smax(int K) { return std::min(64, kCandCap / K); }
 
 static size_t row_smem_bytes() { return (size_t)kScanSmemBytes; }
 
@@ -262,15 +232,11 @@ cudaError_t launch_select_frontier(dt_handle* h, const int32_t* width, int width
 
 cudaError_t launch_expand(dt_handle* h, const void* logits, int64_t ld, int F, cudaStream_t s) {
   const int d = h->depth + 1;
-  const int esz = h->cfg.dtype == DT_BF16 ? 2 : 4;
-  const int64_t rows = (int64_t)h->B * F;
-  const int S = choose_segments(h, rows, h->cfg.V, esz);
   ExpandArgs a;
   a.ws = h->ws;
   a.logits = logits;
   a.ld = ld;
   a.F = F;
-  a.S = S;
   a.B = h->B;
   a.N = h->N;
   a.K = h->cfg.K;
@@ -279,10 +245,10 @@ cudaError_t launch_expand(dt_handle* h, const void* logits, int64_t ld, int F, c
   a.D = h->cfg.D_max;
   a.d = d;
   a.V = h->cfg.V;
-  a.seg_len = seg_len_for(h->cfg.V, S);
+  a.Smax = row_pass_smax(h->cfg.K);
   a.base = d == 1 ? 1 : 1 + h->cfg.K + (d - 2) * h->LW;
   a.first_wait_cap = (h->cfg.flags & DT_FLAG_TEST_TIMEOUT) ? 0u : kSpinCap;
-  const unsigned grid = (unsigned)(rows * S);
+  const unsigned grid = (unsigned)row_pass_grid(h);
   const size_t smem = row_smem_bytes();
   if (h->cfg.dtype == DT_BF16)
     expand_kernel<uint16_t><<<grid, kRowThreads, smem, s>>>(a);

@@ -17,74 +17,65 @@ struct RowPassArgs {
   Workspace ws;
   const void* logits;
   int64_t ld;
-  int P, S, V, K;
-  int64_t seg_len;
+  int B, P, V, K, Smax;
   const int32_t* tokens;  // meta [B][P]
   const int32_t* n_pos;   // meta [B]
   int32_t* top8;          // [B][P][8] or null
   uint32_t first_wait_cap;
 };
 
+// Balanced over the used positions (request b reads rows i < n_pos[b]; a position without a valid
+// token is counted but not read); see the balanced row pass in rowscan.cuh.
 template <typename T, bool SOFTMAX>
 __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(RowPassArgs a) {
   extern __shared__ __align__(128) uint8_t dyn_smem[];
   __shared__ ScanSmem sm;
-  const int r = blockIdx.x / a.S;
-  const int seg = blockIdx.x % a.S;
-  const int b = r / a.P, i = r % a.P;
+  __shared__ RowPlan plan;
   const int tid = threadIdx.x;
   Workspace& ws = a.ws;
-  if (i >= a.n_pos[b] || a.tokens[r] < 0) return;  // unused position or invalid token: row not needed
-
-  const T* row = reinterpret_cast<const T*>(a.logits) + (int64_t)r * a.ld;
-  const int64_t s0 = (int64_t)seg * a.seg_len;
-  const int64_t s1 = min((int64_t)a.V, s0 + a.seg_len);
-  SegOut so = scan_segment<T, SOFTMAX>(row, s0, s1, a.K, sm, dyn_smem, a.first_wait_cap);
-
-  Partial* part = ws.partials + (int64_t)r * a.S;
-  for (int k = tid; k < a.K; k += blockDim.x) part[seg].keys[k] = k < so.nkeys ? sm.cand[k] : 0ull;
-  if (tid == 0) {
-    part[seg].m = so.m;
-    part[seg].s = so.s;
-    if (so.timed_out) set_status(ws.status, DT_DEV_TIMEOUT);
-    if (so.internal) set_status(ws.status, DT_DEV_INTERNAL);
-    if (so.bad) set_status(ws.status, DT_DEV_BAD_LOGITS);
-    __threadfence();
-    const int prev = atomicAdd(&ws.row_counter[r], 1);
-    sm.last = (prev == a.S - 1);
+  auto cnt = [&](int b) -> int { return min(max(a.n_pos[b], 0), a.P); };
+  if (tid < 32) {
+    RowPlan p;
+    plan_rows(p, a.B, a.V, a.Smax, (int)sizeof(T), cnt);
+    if (tid == 0) plan = p;
   }
   __syncthreads();
-  if (!sm.last) return;
+  const RowPlan p = plan;
+  if ((int)blockIdx.x >= p.G) return;
 
-  __threadfence();
-  if (tid == 0) ws.row_counter[r] = 0;
-  const int nk = a.S * a.K;
-  for (int k = tid; k < nk; k += blockDim.x) sm.cand[k] = __ldcg(&part[k / a.K].keys[k % a.K]);
-  if (tid < kMaxK) sm.topk[tid] = 0ull;
-  __syncthreads();
-  merge_sorted_lists(sm, a.S, a.K);
-  float M = -INFINITY;
-  double Ssum = 0.0;
-  bool nan = false;
-  if (SOFTMAX) merge_softmax(part, a.S, sm, M, Ssum, nan);
-  if (tid == 0) {
-    RowStat st;
-    st.amax = (int32_t)key_id(sm.topk[0]);
-    if (SOFTMAX) {
-      if (nan || !(M > -INFINITY) || M == INFINITY || !(Ssum > 0.0)) set_status(ws.status, DT_DEV_BAD_LOGITS);
-      st.m = M;
-      st.s = Ssum;
-    } else {
-      st.m = key_value(sm.topk[0]);
-      st.s = 0.0;
-      if (sm.topk[0] == 0ull || !(st.m > -INFINITY)) set_status(ws.status, DT_DEV_BAD_LOGITS);
+  auto row_of = [&](int b, int i) -> const T* {
+    const int64_t r = (int64_t)b * a.P + i;
+    if (a.tokens[r] < 0) return nullptr;  // invalid token: row not needed
+    return reinterpret_cast<const T*>(a.logits) + r * a.ld;
+  };
+  auto finish = [&](int b, int i, const Partial* rp, int S) {
+    const int64_t r = (int64_t)b * a.P + i;
+    if (a.tokens[r] < 0) return;  // block-uniform
+    float M = -INFINITY;
+    double Ssum = 0.0;
+    bool nan = false;
+    if (SOFTMAX) merge_softmax(rp, S, sm, M, Ssum, nan);
+    if (tid == 0) {
+      RowStat st;
+      st.amax = (int32_t)key_id(sm.topk[0]);
+      if (SOFTMAX) {
+        if (nan || !(M > -INFINITY) || M == INFINITY || !(Ssum > 0.0)) set_status(ws.status, DT_DEV_BAD_LOGITS);
+        st.m = M;
+        st.s = Ssum;
+      } else {
+        st.m = key_value(sm.topk[0]);
+        st.s = 0.0;
+        if (sm.topk[0] == 0ull || !(st.m > -INFINITY)) set_status(ws.status, DT_DEV_BAD_LOGITS);
+      }
+      ws.row_stats[r] = st;
     }
-    ws.row_stats[r] = st;
-  }
-  if (a.top8 && tid < 8) {
-    const uint64_t k = sm.topk[tid];
-    a.top8[(int64_t)r * 8 + tid] = (tid < a.K && k != 0ull) ? (int32_t)key_id(k) : -1;
-  }
+    if (a.top8 && tid < 8) {
+      const uint64_t k = sm.topk[tid];
+      a.top8[r * 8 + tid] = (tid < a.K && k != 0ull) ? (int32_t)key_id(k) : -1;
+    }
+  };
+  scan_pieces<T, SOFTMAX>(p, a.V, a.K, a.B, ws.partials, ws.row_counter, sm, dyn_smem, a.first_wait_cap,
+                          ws.status, row_of, cnt, finish);
 }
 
 struct WalkArgs {
@@ -383,24 +374,20 @@ cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* lo
                           int32_t* bonus, int32_t* top8, cudaStream_t s) {
   const int P = meta->P;
   const int V = h->cfg.V;
-  const int esz = h->cfg.dtype == DT_BF16 ? 2 : 4;
-  const int64_t rows = (int64_t)h->B * P;
   RowPassArgs ra;
   ra.ws = h->ws;
   ra.logits = logits;
   ra.ld = ld;
+  ra.B = h->B;
   ra.P = P;
   ra.V = V;
   ra.K = top8 ? 8 : 1;
-  ra.S = choose_segments(h, rows, V, esz);
-  if (ra.S * ra.K > kCandCap) ra.S = kCandCap / ra.K;
-  int64_t L = (V + ra.S - 1) / ra.S;
-  ra.seg_len = (L + 7) / 8 * 8;
+  ra.Smax = row_pass_smax(ra.K);
   ra.tokens = meta->tokens;
   ra.n_pos = meta->n_pos;
   ra.top8 = top8;
   ra.first_wait_cap = (h->cfg.flags & DT_FLAG_TEST_TIMEOUT) ? 0u : kSpinCap;
-  const unsigned grid = (unsigned)(rows * ra.S);
+  const unsigned grid = (unsigned)row_pass_grid(h);
   const size_t smem = (size_t)kScanSmemBytes;
   cudaError_t e;
 #define DT_LAUNCH_ROWS(T, SM) verify_rows_kernel<T, SM><<<grid, kRowThreads, smem, s>>>(ra)

@@ -41,6 +41,9 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -98,6 +101,7 @@ constexpr uint32_t kSpinCap = 1u << 22;
 struct WarpRing {
   uint64_t bar[kWarpStages];
   uint64_t cand[kWarpCand];
+  uint64_t list[2][kMaxK];  // the warp's top-K list (descending), double-buffered for merges
   int32_t cnt;
   int32_t ovf;
 };
@@ -281,7 +285,7 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
 
   float m_t = -INFINITY, s_hi = 0.0f, s_lo = 0.0f;
   float seen_max = -INFINITY;
-  uint64_t L = 0ull;            // my slot of the warp's top-K list
+  int lb = 0, nl = 0;           // current list buffer, keys in the list
   uint64_t tau_key = 0ull;      // K-th key of the list (0 while it has fewer than K keys)
   float tau_val = -INFINITY;
   bool inited = false;
@@ -304,31 +308,65 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
   }
   __syncwarp();
 
-  // drains the warp's candidate buffer into the list; returns true if it had overflowed
-  auto drain = [&]() -> bool {
+  // Merges the candidate buffer rg.cand[0..min(cnt, kWarpCand)) into the list. Keys are distinct
+  // elements, so a key's place in the merged list is its rank among list + candidates; with `dedup` a
+  // candidate already in the list is dropped first. Returns true if the buffer had overflowed (the
+  // candidates beyond its capacity were not stored).
+  auto merge = [&](bool dedup) -> bool {
     __syncwarp();
     const int cnt = rg.cnt;
-    bool o = false;
-    if (cnt > 0) {
-      const int n = min(cnt, kWarpCand);
-      for (int c = 0; c < n; ++c) {
-        const uint64_t k = rg.cand[c];
-        if (k > tau_key) {
-          wl_insert(L, k, K, lane);
-          const uint64_t kth = shfl_u64(L, K - 1);
-          tau_key = kth;
-          tau_val = kth ? key_value(kth) : -INFINITY;
-        }
+    if (cnt == 0) return false;
+    const int n = min(cnt, kWarpCand);
+    const uint64_t* cur = rg.list[lb];
+    uint64_t* nxt = rg.list[lb ^ 1];
+    if (dedup) {
+      for (int q = lane; q < n; q += 32) {
+        const uint64_t k = rg.cand[q];
+        bool dup = false;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) dup |= (j < nl) && (cur[j] == k);
+        if (dup) rg.cand[q] = 0ull;
       }
-      o = rg.ovf != 0;
       __syncwarp();
-      if (lane == 0) {
-        rg.cnt = 0;
-        rg.ovf = 0;
-      }
     }
+    int valid = 0;
+    for (int q = lane; q < n; q += 32) {
+      const uint64_t k = rg.cand[q];
+      if (k == 0ull) continue;
+      ++valid;
+      int r = 0;
+      for (int j0 = 0; j0 < nl; j0 += 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) r += (j0 + u < nl) && (cur[j0 + u] > k);
+      }
+      for (int j0 = 0; j0 < n; j0 += 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) r += (j0 + u < n) && (rg.cand[j0 + u] > k);
+      }
+      if (r < K) nxt[r] = k;
+    }
+    if (lane < nl) {
+      const uint64_t l = cur[lane];
+      int r = lane;
+      for (int j0 = 0; j0 < n; j0 += 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) r += (j0 + u < n) && (rg.cand[j0 + u] > l);
+      }
+      if (r < K) nxt[r] = l;
+    }
+    valid = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)valid);
     __syncwarp();
-    return o;
+    nl = min(K, nl + valid);
+    lb ^= 1;
+    tau_key = nl == K ? rg.list[lb][K - 1] : 0ull;
+    tau_val = tau_key ? key_value(tau_key) : -INFINITY;
+    if (lane == 0) rg.cnt = 0;
+    __syncwarp();
+    return cnt > kWarpCand;
+  };
+  auto push = [&](uint64_t k) {
+    const int pos = atomicAdd(&rg.cnt, 1);
+    if (pos < kWarpCand) rg.cand[pos] = k;
   };
 
   constexpr int QV = kStageBytes / 16 / 32;   // vectors per lane per stage (8)
@@ -362,27 +400,26 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
       wv[4 * q + 2] = w.z;
       wv[4 * q + 3] = w.w;
     }
-    __syncwarp();
-    // the stage's smem is free again: refill it with stage t + kWarpStages
-    if (lane == 0 && t + kWarpStages < n_st) {
-      fence_proxy_async_smem();
-      const int64_t off = (int64_t)(t + kWarpStages) * kStageBytes;
-      const uint32_t bytes = (uint32_t)min((int64_t)kStageBytes, wbytes - off);
-      mbar_arrive_expect_tx(&rg.bar[st], bytes);
-      bulk_g2s(my_stages + (size_t)st * kStageBytes, wsrc + off, bytes, &rg.bar[st]);
-    }
 
-    // lane max with NaN propagation (a NaN makes it NaN): packed bf16x2 or fp32 tree
+    // lane max with NaN propagation (a NaN makes it NaN): packed bf16x2 or fp32 tree. Its first two
+    // levels give the maximum of each of the lane's vectors (vmax), kept for the rare paths below.
     float lm;
+    float vmax[QV];
     {
       uint32_t r[QV * 4];
 #pragma unroll
       for (int j = 0; j < QV * 4; ++j) r[j] = wv[j];
 #pragma unroll
-      for (int w2 = 1; w2 < QV * 4; w2 <<= 1)
+      for (int w2 = 1; w2 < QV * 4; w2 <<= 1) {
 #pragma unroll
         for (int j = 0; j + w2 < QV * 4; j += 2 * w2) r[j] = ESZ == 2 ? max_nan_bf16x2(r[j], r[j + w2])
                                                                        : max_nan_f32u(r[j], r[j + w2]);
+        if (w2 == 2) {
+#pragma unroll
+          for (int q = 0; q < QV; ++q)
+            vmax[q] = ESZ == 2 ? max_nan_f32(bf16_lo(r[4 * q]), bf16_hi(r[4 * q])) : __uint_as_float(r[4 * q]);
+        }
+      }
       lm = ESZ == 2 ? max_nan_f32(bf16_lo(r[0]), bf16_hi(r[0])) : __uint_as_float(r[0]);
     }
     if (!SOFTMAX) seen_max = max_nan_f32(seen_max, lm);
@@ -425,93 +462,110 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
       }
     }
 
-    // value v of this lane's stage values sits in vector q = v / VEC, element e = v % VEC, and has
-    // token id st_e0 + ((q * 32 + lane) * VEC + e)
-    auto value_at = [&](int v) -> float {
-      if (ESZ == 2) return (v & 1) ? bf16_hi(wv[v >> 1]) : bf16_lo(wv[v >> 1]);
-      return __uint_as_float(wv[v]);
+    // The rarely taken paths below (list start, candidates) read the stage from shared memory with
+    // rolled loops: straight-line code over all NV register values would be large and, being rarely
+    // executed, always cold in the instruction cache. Vector q of this lane is stage vector
+    // q * 32 + lane; its element e has token id st_e0 + (q * 32 + lane) * VEC + e.
+    auto vec_at = [&](int q, uint4& w) -> bool {
+      const int vi = q * 32 + lane;
+      if (vi * 16 >= st_bytes) return false;
+      w = *reinterpret_cast<const uint4*>(sp + (size_t)vi * 16);
+      return true;
     };
-    auto id_at = [&](int v) -> uint32_t {
-      return (uint32_t)(st_e0 + (int64_t)(((v / VEC) * 32 + lane) * VEC + (v % VEC)));
+    auto elt = [&](const uint4& w, int e) -> float {
+      uint32_t word;
+      if (ESZ == 2) {
+        const int wi = e >> 1;
+        word = wi == 0 ? w.x : wi == 1 ? w.y : wi == 2 ? w.z : w.w;
+        return (e & 1) ? bf16_hi(word) : bf16_lo(word);
+      }
+      word = e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w;
+      return __uint_as_float(word);
+    };
+    auto id_of = [&](int q, int e) -> uint32_t {
+      return (uint32_t)(st_e0 + (int64_t)((q * 32 + lane) * VEC + e));
     };
 
     // first stage of the chunk: the list starts as the K best per-lane maxima
     uint64_t excl = 0ull;
     if (!inited) {
-      uint64_t best = 0ull;
       if (lm == lm && lm != -INFINITY) {
-        int vb = 0;
+        // lowest id among the maxima: the first element equal to lm of the first vector holding it
+        int qf = QV - 1;
 #pragma unroll
-        for (int v = NV - 1; v >= 0; --v)
-          if (value_at(v) == lm) vb = v;  // lowest id among the maxima
-        best = make_key(lm, id_at(vb));
+        for (int q = QV - 1; q >= 0; --q)
+          if (vmax[q] == lm) qf = q;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        vec_at(qf, w);
+        uint32_t id = id_of(qf, 0);
+#pragma unroll
+        for (int e = VEC - 1; e >= 0; --e)
+          if (elt(w, e) == lm) id = id_of(qf, e);
+        excl = make_key(lm, id);
+        push(excl);
       }
-      excl = best;
-      const uint64_t srt = warp_sort_desc(best);
-      L = lane < K ? srt : 0ull;
-      tau_key = shfl_u64(L, K - 1);
-      tau_val = tau_key ? key_value(tau_key) : -INFINITY;
+      merge(false);
       inited = true;
     }
 
     // Filter against the list's K-th key. Within a warp's chunk token ids grow stage by stage, so
     // after the first stage a value equal to the K-th key's value has a larger id and cannot beat it:
-    // the test is strict there. Lanes whose maximum clears the threshold push their candidates to
-    // the warp's buffer, which is then inserted into the list. If the buffer overflows, the stage is
-    // re-filtered with ballots (every candidate inserted directly; exact, slower, rare).
-    const bool hot = (t == 0) ? (lm >= tau_val) : (lm > tau_val);
-    if (__any_sync(0xFFFFFFFFu, hot)) {
+    // the test is strict there. Lanes whose maximum clears the threshold push their candidates, which
+    // are then merged into the list. If the buffer overflowed, the merge still raised the threshold:
+    // the stage is filtered again against it (keys already in the list are dropped by the merge).
+    bool again = __any_sync(0xFFFFFFFFu, (t == 0) ? (lm >= tau_val) : (lm > tau_val));
+    bool dedup = false;
+    for (int round = 0; again; ++round) {
+      const bool hot = (t == 0) ? (lm >= tau_val) : (lm > tau_val);
       if (hot) {
+        unsigned vm = 0u;  // vectors that may hold candidates
 #pragma unroll
-        for (int v = 0; v < NV; ++v) {
-          const float x = value_at(v);
-          if (x >= tau_val && x != -INFINITY) {
-            const uint64_t k = make_key(x, id_at(v));
-            if (k > tau_key && k != excl) {
-              const int pos = atomicAdd(&rg.cnt, 1);
-              if (pos < kWarpCand) rg.cand[pos] = k;
+        for (int q = 0; q < QV; ++q)
+          if ((t == 0) ? (vmax[q] >= tau_val) : (vmax[q] > tau_val)) vm |= 1u << q;
+        while (vm) {
+          const int q = __ffs(vm) - 1;
+          vm &= vm - 1;
+          uint4 w;
+          if (!vec_at(q, w)) break;
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            const float x = elt(w, e);
+            if (x >= tau_val && x != -INFINITY) {
+              const uint64_t k = make_key(x, id_of(q, e));
+              if (k > tau_key && k != excl) push(k);
             }
           }
         }
       }
-      __syncwarp();
-      if (rg.cnt <= kWarpCand) {
-        drain();
-      } else {
-        __syncwarp();
-        if (lane == 0) rg.cnt = 0;
-        __syncwarp();
-        const bool lane_hot = lm >= tau_val;
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-          const float x = value_at(v);
-          uint64_t k = 0ull;
-          if (lane_hot && x >= tau_val && x != -INFINITY) k = make_key(x, id_at(v));
-          unsigned want = __ballot_sync(0xFFFFFFFFu, k > tau_key && k != excl);
-          while (want) {  // warp-uniform
-            const int src = __ffs(want) - 1;
-            want &= want - 1;
-            const uint64_t kk = shfl_u64(k, src);
-            if (kk > tau_key) {
-              wl_insert(L, kk, K, lane);
-              tau_key = shfl_u64(L, K - 1);
-              tau_val = tau_key ? key_value(tau_key) : -INFINITY;
-            }
-          }
-        }
+      again = merge(dedup);
+      dedup = true;
+      if (round >= NV * 32 / (kWarpCand - kMaxK) + 1) {  // the threshold rises every round: never hit
+        if (lane == 0) sm.flags[warp] |= 2;
+        break;
       }
     }
+
+    // the stage has been read for the last time: refill its buffer with stage t + kWarpStages
+    __syncwarp();
+    if (lane == 0 && t + kWarpStages < n_st) {
+      fence_proxy_async_smem();
+      const int64_t off = (int64_t)(t + kWarpStages) * kStageBytes;
+      const uint32_t bytes = (uint32_t)min((int64_t)kStageBytes, wbytes - off);
+      mbar_arrive_expect_tx(&rg.bar[st], bytes);
+      bulk_g2s(my_stages + (size_t)st * kStageBytes, wsrc + off, bytes, &rg.bar[st]);
+    }
   }
-  if (ht_key) {  // head/tail elements (warp 0)
-    const int pos = atomicAdd(&rg.cnt, 1);
-    rg.cand[pos] = ht_key;
-  }
-  drain();
+  if (ht_key) push(ht_key);  // head/tail elements (warp 0)
+  merge(false);
+  // every copy has landed: retire the barriers so that a later scan in this CTA can initialise them
+  // again (after a timeout a copy may still be in flight, and the barriers are left alone)
+  if (lane == 0 && !timed_out)
+    for (int st = 0; st < kWarpStages; ++st) mbar_inval(&rg.bar[st]);
 
   SegOut out;
   out.timed_out = __syncthreads_or(timed_out) != 0;
   // ---- warp results -> CTA ----
-  if (lane < K) sm.cand[warp * K + lane] = L;
+  if (lane < K) sm.cand[warp * K + lane] = lane < nl ? rg.list[lb][lane] : 0ull;
   float wm = m_t;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, o));
@@ -567,6 +621,183 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
   __syncthreads();
   if (!SOFTMAX) out.m = n > 0 ? key_value(sm.cand[0]) : -INFINITY;
   return out;
+}
+
+// ---------------------------------------------------------------- balanced row pass ----
+// The rows a launch reads ("active rows") are numbered j = 0..A-1 in request order: request b owns
+// cnt(b) consecutive numbers, its rows i = 0..cnt(b)-1. The work is laid out in one of two ways:
+//  * few rows (2 A <= gridDim): every row is cut into S_row equal segments, one per CTA (CTA c takes
+//    segment c % S_row of row c / S_row); a row's pieces are CTAs j S_row .. j S_row + S_row - 1 and
+//    piece c leaves its partial at slot c;
+//  * many rows: the rows' E = A * V elements, concatenated, are cut into G equal ranges, one per CTA
+//    (CTA c takes [floor(c E / G), floor((c + 1) E / G))), so that every SM gets the same bytes. The
+//    part of row j inside CTA c's range is the piece (j, c), with its partial at slot j + c (distinct
+//    for distinct pieces, since j and c both grow along the concatenation); a row's pieces are CTAs
+//    cta_of(j V) .. cta_of(j V + V - 1).
+// The CTA whose arrival completes a row's count merges the row's partials.
+struct RowPlan {
+  int64_t A, E;    // active rows, A * V
+  int G;           // CTAs with work (the others exit)
+  int S_row;       // segments per row (few-rows layout), 0 for the concatenated layout
+  int64_t j0;      // first row of this CTA
+  int64_t x0, x1;  // this CTA's element range in the concatenation (x0 == x1: an empty segment)
+  int b, i;        // request and row of active row j0
+};
+
+__device__ __forceinline__ int64_t range_start(int64_t c, int64_t E, int64_t G) {
+  return (E / G) * c + ((E % G) * c) / G;  // floor(c E / G) without overflow
+}
+// CTA whose range holds element x (E * G < 2^63: E <= 2^52, G <= 4096)
+__device__ __forceinline__ int cta_of(int64_t x, int64_t E, int64_t G) {
+  return (int)(((uint64_t)(x + 1) * (uint64_t)G - 1ull) / (uint64_t)E);
+}
+
+// Warp 0 of every CTA: the layout, this CTA's range and the (b, i) of its first row. A piece holds at
+// least r_min elements: two stages per warp (so that every lane of a warp sees data and the top-K list
+// starts full), and r_min >= (V - 1) / (Smax - 2), so that a row has at most Smax pieces. The first 32
+// counts are read once and kept in a register.
+template <class Cnt>
+__device__ void plan_rows(RowPlan& p, int B, int64_t V, int Smax, int esz, Cnt cnt) {
+  const int lane = threadIdx.x & 31;
+  const int head = lane < B ? cnt(lane) : 0;
+  int64_t A = 0;
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    int c = b0 == 0 ? head : ((b0 + lane < B) ? cnt(b0 + lane) : 0);
+    A += __reduce_add_sync(0xFFFFFFFFu, (unsigned)c);
+  }
+  p.A = A;
+  p.E = A * V;
+  p.G = 0;
+  p.S_row = 0;
+  p.j0 = p.x0 = p.x1 = 0;
+  p.b = p.i = 0;
+  if (p.E == 0) return;
+  const int64_t r_min = max((int64_t)kScanWarps * 2 * kStageBytes / esz, (V - 1 + (Smax - 3)) / (Smax - 2));
+  const int64_t c = blockIdx.x;
+  if (2 * A <= (int64_t)gridDim.x) {
+    int64_t S = min((int64_t)gridDim.x / A, (V + r_min - 1) / r_min);
+    S = max((int64_t)1, min(S, (int64_t)Smax));
+    p.S_row = (int)S;
+    p.G = (int)(A * S);
+    if (c >= p.G) return;
+    p.j0 = c / S;
+    int64_t L = (V + S - 1) / S;
+    L = (L + 7) / 8 * 8;
+    const int64_t e0 = min(V, (c % S) * L), e1 = min(V, e0 + L);
+    p.x0 = p.j0 * V + e0;
+    p.x1 = p.j0 * V + e1;
+  } else {
+    int64_t G = p.E / r_min;
+    G = max(G, (int64_t)1);
+    G = min(G, (int64_t)gridDim.x);
+    p.G = (int)G;
+    if (c >= G) return;
+    p.x0 = range_start(c, p.E, G);
+    p.x1 = range_start(c + 1, p.E, G);
+    p.j0 = p.x0 / V;
+  }
+  const int64_t j = p.j0;
+  int64_t base = 0;
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const int n = b0 == 0 ? head : ((b0 + lane < B) ? cnt(b0 + lane) : 0);
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int64_t lo = base + incl - n;
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, n > 0 && lo <= j && j < base + incl);
+    const int off = (int)(j - lo);
+    if (hit) {  // warp-uniform
+      const int src = __ffs(hit) - 1;
+      p.b = b0 + src;
+      p.i = __shfl_sync(0xFFFFFFFFu, off, src);
+      break;
+    }
+    base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+  }
+}
+
+// Scans this CTA's pieces in order (all threads). row_of(b, i) gives row i of request b, or nullptr
+// when that row is not to be read (its pieces leave empty partials). When a piece completes its
+// row, finish(b, i, part, S) runs on all threads with the row's merged top-K in sm.topk and its S
+// partials at part. After a timed-out copy wait the CTA reads nothing more (empty partials), so
+// that every row still completes its count.
+template <typename T, bool SOFTMAX, class RowOf, class Cnt, class Finish>
+__device__ void scan_pieces(const RowPlan& p, int64_t V, int K, int B, Partial* partials, int32_t* counter,
+                            ScanSmem& sm, uint8_t* stages, uint32_t first_wait_cap, int32_t* status, RowOf row_of,
+                            Cnt cnt, Finish finish) {
+  const int tid = threadIdx.x;
+  const int64_t c = blockIdx.x;
+  if (tid == 0) sm.cand = reinterpret_cast<uint64_t*>(stages);
+  __syncthreads();
+  int64_t x = p.x0, j = p.j0;
+  int b = p.b, i = p.i;
+  bool halted = false;
+  while (true) {
+    const int64_t e0 = x - j * V;
+    const int64_t e1 = min(V, p.x1 - j * V);
+    int c_first, c_last;
+    int64_t slot, row_slot0;
+    if (p.S_row > 0) {
+      c_first = (int)(j * p.S_row);
+      c_last = c_first + p.S_row - 1;
+      slot = c;
+      row_slot0 = c_first;
+    } else {
+      c_first = cta_of(j * V, p.E, p.G);
+      c_last = cta_of(j * V + V - 1, p.E, p.G);
+      slot = j + c;
+      row_slot0 = j + c_first;
+    }
+    Partial* part = partials + slot;
+    const T* row = row_of(b, i);
+    SegOut so;
+    if (row != nullptr && !halted && e1 > e0) {
+      so = scan_segment<T, SOFTMAX>(row, e0, e1, K, sm, stages, first_wait_cap);
+    } else {
+      so.m = -INFINITY;
+      so.s = 0.0;
+      so.nkeys = 0;
+      so.timed_out = so.internal = so.bad = false;
+    }
+    for (int k = tid; k < K; k += blockDim.x) part->keys[k] = k < so.nkeys ? sm.cand[k] : 0ull;
+    if (tid == 0) {
+      part->m = so.m;
+      part->s = so.s;
+      if (so.timed_out) set_status(status, DT_DEV_TIMEOUT);
+      if (so.internal) set_status(status, DT_DEV_INTERNAL);
+      if (so.bad) set_status(status, DT_DEV_BAD_LOGITS);
+      __threadfence();
+      const int prev = atomicAdd(&counter[j], 1);
+      sm.last = (prev == c_last - c_first);
+    }
+    halted = halted || so.timed_out;
+    __syncthreads();
+    if (sm.last) {  // block-uniform
+      __threadfence();
+      if (tid == 0) counter[j] = 0;
+      const int S = c_last - c_first + 1;
+      const Partial* rp = partials + row_slot0;
+      for (int k = tid; k < S * K; k += blockDim.x) sm.cand[k] = __ldcg(&rp[k / K].keys[k % K]);
+      if (tid < kMaxK) sm.topk[tid] = 0ull;
+      __syncthreads();
+      merge_sorted_lists(sm, S, K);
+      finish(b, i, rp, S);
+    }
+    x = (j + 1) * V;
+    ++j;
+    if (x >= p.x1) break;
+    // next row; the stage memory is handed back to the async proxy
+    ++i;
+    while (b < B && i >= cnt(b)) {
+      ++b;
+      i = 0;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+  }
 }
 
 }  // namespace dt
