@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(kMetaThreads) build_meta_kernel(MetaArgs a) {
   __shared__ uint32_t anc[kMaxP][kWords];
   __shared__ int32_t has_child[kMaxP];
   __shared__ int32_t leaf_idx[kMaxP];
-  __shared__ int32_t s_nsel, s_npos, s_bad;
+  __shared__ int32_t s_nsel, s_npos, s_bad, s_rc;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const Workspace& ws = a.ws;
@@ -41,15 +41,25 @@ __global__ void __launch_bounds__(kMetaThreads) build_meta_kernel(MetaArgs a) {
 
   for (int i = tid; i < a.N; i += blockDim.x) pos_of[i] = -1;
   if (tid == 0) {
-    int n = 0;
-    while (n < a.m_cap && a.selected[(int64_t)b * a.m_cap + n] >= 0) ++n;
-    s_nsel = n;
-    int rc = a.ret_count ? a.ret_count[b] : 0;
-    rc = max(0, min(rc, a.R_cap));
-    s_npos = min(P, 1 + n + rc);
-    s_bad = (1 + n + rc > P) ? 1 : 0;  // positions would not fit: flagged, the extra ones dropped
+    s_nsel = a.m_cap;
+    s_bad = 0;
+  }
+  if (tid == 32) {
+    const int rc = a.ret_count ? a.ret_count[b] : 0;
+    s_rc = max(0, min(rc, a.R_cap));
   }
   for (int i = tid; i < P; i += blockDim.x) has_child[i] = 0;
+  __syncthreads();
+  // selected nodes: the entries before the first -1 (all loaded at once, the first -1 found by a min)
+  for (int j = tid; j < a.m_cap; j += blockDim.x)
+    if (a.selected[(int64_t)b * a.m_cap + j] < 0) atomicMin(&s_nsel, j);
+  __syncthreads();
+  if (tid == 0) {
+    const int n = s_nsel;
+    const int rc = s_rc;
+    s_npos = min(P, 1 + n + rc);
+    if (1 + n + rc > P) s_bad = 1;  // positions would not fit: flagged, the extra ones dropped
+  }
   __syncthreads();
   const int nsel = s_nsel, npos = s_npos;
   if (tid == 0) pos_of[0] = 0;

@@ -12,78 +12,102 @@
 namespace dt {
 namespace {
 
-// Descending bitonic sort of n_pad (power of two) 64-bit keys in shared memory.
-__device__ void block_bitonic_desc(uint64_t* keys, int n_pad) {
-  for (int size = 2; size <= n_pad; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      __syncthreads();
-      for (int i = threadIdx.x; i < n_pad / 2; i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const uint64_t a = keys[lo], b = keys[hi];
-        if ((a < b) == desc) {
-          keys[lo] = b;
-          keys[hi] = a;
-        }
-      }
-    }
-  }
-  __syncthreads();
-}
-
 struct SortArgs {
   Workspace ws;
-  int N, depth, n_pad, mode;  // mode 0: rerank -> selected; 1: linear values of the top m_cap
+  int N, LW, D, depth, mode;  // mode 0: rerank -> selected; 1: linear values of the top m_cap
   const int32_t* m;
   int m_len, m_cap;
   int32_t* selected;
 };
 
-// One CTA per request: all valid non-root nodes in the total order.
-__global__ void __launch_bounds__(1024) sort_nodes_kernel(SortArgs a) {
-  extern __shared__ __align__(16) uint64_t keys[];
+constexpr int kSortThreads = 512;
+
+// One CTA per request: the valid non-root nodes in the total order (value desc, id asc), which puts
+// shallower nodes first on equal values since ids grow with depth. Every layer is already sorted by
+// the expansion (layer_order), so a node's rank is its place in its own layer plus, for every other
+// layer, the number of keys above it there (binary search): no full sort is needed.
+__global__ void __launch_bounds__(kSortThreads) sort_nodes_kernel(SortArgs a) {
+  extern __shared__ __align__(16) uint64_t keys[];  // [depth][LW]: layer d's valid keys at (d-1)*LW
+  __shared__ int cnt[kMaxD + 1];
+  __shared__ int32_t sel[kMaxP];
   const int b = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const Workspace& ws = a.ws;
-  // slot i holds node i+1 (empty key 0 for invalid slots, which sort last)
-  int mine = 0;
-  for (int i = tid; i < a.n_pad; i += blockDim.x) {
+  // every node's key in one round of loads (slot (d-1)*LW + p holds layer d's p-th node, 0 if none or
+  // invalid); then warp d-1 compacts layer d's valid keys in place, order preserved
+  for (int f = tid; f < a.depth * a.LW; f += blockDim.x) {
+    const int d = 1 + f / a.LW, p = f % a.LW;
+    const int64_t lb = (int64_t)b * (a.D + 1) + d;
     uint64_t k = 0ull;
-    const int id = i + 1;
-    if (id < a.N) {
-      const int64_t gi = (int64_t)b * a.N + id;
-      if (ws.token[gi] >= 0) {
-        k = make_key(ws.value[gi], (uint32_t)id);
-        ++mine;
+    if (p < ws.layer_count[lb]) {
+      const int id = ws.layer_order[lb * a.LW + p];
+      if (id > 0 && id < a.N) {
+        const int64_t gi = (int64_t)b * a.N + id;
+        const int tok = ws.token[gi];
+        const float v = ws.value[gi];
+        if (tok >= 0) k = make_key(v, (uint32_t)id);
       }
     }
-    keys[i] = k;
+    keys[f] = k;
   }
-  __shared__ int s_n;
-  if (tid == 0) s_n = 0;
   __syncthreads();
-  if (mine) atomicAdd(&s_n, mine);  // one atomic per thread
+  for (int d = 1 + warp; d <= a.depth; d += kSortThreads / 32) {
+    uint64_t* g = keys + (int64_t)(d - 1) * a.LW;
+    int c = 0;
+    for (int p0 = 0; p0 < a.LW; p0 += 32) {
+      const uint64_t k = p0 + lane < a.LW ? g[p0 + lane] : 0ull;
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, k != 0ull);
+      __syncwarp();
+      if (k != 0ull) g[c + __popc(m & ((1u << lane) - 1u))] = k;  // c + rank <= p0 + lane: no overtaking
+      c += __popc(m);
+    }
+    if (lane == 0) cnt[d] = c;
+  }
   __syncthreads();
-  const int n = s_n;
-  block_bitonic_desc(keys, a.n_pad);
+  int n = 0;
+  for (int d = 1; d <= a.depth; ++d) n += cnt[d];
+  int limit;
   if (a.mode == 0) {
     int mb = a.m ? a.m[a.m_len == 1 ? 0 : b] : a.m_cap;
-    mb = max(0, min(min(mb, a.m_cap), n));
-    // selected ids, ascending: rank each of the first mb ids among themselves
-    int32_t* out = a.selected + (int64_t)b * a.m_cap;
-    for (int i = tid; i < mb; i += blockDim.x) {
-      const uint32_t id = key_id(keys[i]);
-      int rank = 0;
-      for (int j = 0; j < mb; ++j) rank += key_id(keys[j]) < id;
-      out[rank] = (int32_t)id;
-    }
-    for (int i = mb + tid; i < a.m_cap; i += blockDim.x) out[i] = -1;
+    limit = max(0, min(min(mb, a.m_cap), n));
   } else {
-    double* lin = ws.sorted_lin + (int64_t)b * a.m_cap;
-    for (int i = tid; i < a.m_cap; i += blockDim.x)
-      lin[i] = i < n ? (double)expf(key_value(keys[i])) : 0.0;
-    if (tid == 0) ws.sorted_cnt[b] = min(n, a.m_cap);
+    limit = min(n, a.m_cap);
+  }
+  double* lin = ws.sorted_lin + (int64_t)b * a.m_cap;
+  for (int f = tid; f < a.depth * a.LW; f += blockDim.x) {
+    const int d = 1 + f / a.LW, p = f % a.LW;
+    if (p >= cnt[d]) continue;
+    const uint64_t k = keys[f];
+    int rank = p;
+    for (int e = 1; e <= a.depth && rank < limit; ++e) {
+      if (e == d) continue;
+      const uint64_t* g = keys + (int64_t)(e - 1) * a.LW;
+      int lo = 0, hi = cnt[e];  // keys above k in layer e
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (g[mid] > k) lo = mid + 1;
+        else hi = mid;
+      }
+      rank += lo;
+    }
+    if (rank >= limit) continue;
+    if (a.mode == 0) sel[rank] = (int32_t)key_id(k);
+    else lin[rank] = (double)expf(key_value(k));
+  }
+  if (a.mode == 0) {
+    __syncthreads();
+    // selected ids, ascending: rank each of the first `limit` ids among themselves
+    int32_t* out = a.selected + (int64_t)b * a.m_cap;
+    for (int i = tid; i < limit; i += blockDim.x) {
+      const int32_t id = sel[i];
+      int r = 0;
+      for (int j = 0; j < limit; ++j) r += sel[j] < id;
+      out[r] = id;
+    }
+    for (int i = limit + tid; i < a.m_cap; i += blockDim.x) out[i] = -1;
+  } else {
+    for (int i = limit + tid; i < a.m_cap; i += blockDim.x) lin[i] = 0.0;
+    if (tid == 0) ws.sorted_cnt[b] = limit;
   }
 }
 
@@ -92,20 +116,97 @@ __device__ __forceinline__ int table_row(double c, double L, int M_rows) {
   return q >= (double)(M_rows - 1) ? M_rows - 1 : (int)q;
 }
 
-// Marginal-utility selection over k = 1..cap (thread-serial; cap <= 512).
-__device__ int selection_rule(const double* items, const double* cost, double thr, int cap) {
-  // du = items[k0] + ... + items[k-1], accumulated in that order as k advances
-  int k0 = 1;
-  double du = 0.0;
-  for (int k = 2; k <= cap; ++k) {
-    du += items[k - 1];
-    // marginal utility du / (c_k - c_k0) >= thr, written without the division (c_k > c_k0 here)
-    if (cost[k] <= cost[k0] || du >= thr * (cost[k] - cost[k0])) {
-      k0 = k;
-      du = 0.0;
+// GB300 runs fp64 at a small fraction of its fp32 rate, so a dependent chain of fp64 operations is
+// slow. The CAST kernels below keep fp64 for every sum and product, but lay the work out so that each
+// fp64 instruction serves a whole warp of items, and turn the sequential selection into integer
+// comparisons of precomputed fp64 values.
+
+// Ordered 64-bit image of a double: unsigned comparison of images follows the fp64 order (-0 == +0).
+__device__ __forceinline__ uint64_t d2ord(double x) {
+  uint64_t u = (uint64_t)__double_as_longlong(x == 0.0 ? 0.0 : x);
+  return (u & 0x8000000000000000ull) ? ~u : (u | 0x8000000000000000ull);
+}
+
+constexpr int kPruneThreads = 1024;  // 32 warps
+constexpr int kItemChunk = 64;       // items per pass (two per lane)
+
+// items[s] = (1/B) sum_b vb(b, s) for s < cap, in fp64. Warp w sums requests b = w, w + 32, ... for
+// every item (lanes over items), then warps 0 and 1 add the 32 warp partials in warp order.
+// `part` is shared scratch of 32 * kItemChunk doubles. All threads call it.
+template <typename F>
+__device__ void batch_items(double* items, double* part, int cap, int B, F vb) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = min(32, B);
+  for (int s0 = 0; s0 < cap; s0 += kItemChunk) {
+    if (warp < nw) {
+      double a0 = 0.0, a1 = 0.0;
+      const int sa = s0 + lane, sb = s0 + 32 + lane;
+      for (int b = warp; b < B; b += 32) {
+        if (sa < cap) a0 += vb(b, sa);
+        if (sb < cap) a1 += vb(b, sb);
+      }
+      part[warp * kItemChunk + lane] = a0;
+      part[warp * kItemChunk + 32 + lane] = a1;
+    }
+    __syncthreads();
+    if (warp < 2) {
+      const int j = warp * 32 + lane, s2 = s0 + j;
+      if (s2 < cap) {
+        double acc = 0.0;
+        for (int w = 0; w < nw; ++w) acc += part[w * kItemChunk + j];
+        items[s2] = acc / (double)B;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Marginal-utility selection over k = 1..cap (CAST): k0 = 1; for k = 2..cap, k0 = k when
+// c_k <= c_k0 or (u_k - u_k0) / (c_k - c_k0) >= thr, with u_k = items[0] + ... + items[k-1]. For
+// c_k > c_k0 the second test is u_k - thr c_k >= u_k0 - thr c_k0, so with q_k = u_k - thr c_k both
+// tests compare precomputed values. Warp 0 builds u (prefix sums, u[0] = 0), q and the ordered
+// images of c and q; thread 0 then walks k. `u`, `cq` ([2][cap+1] images) are shared scratch.
+// All threads call it; every thread gets k0.
+__device__ int selection_rule(const double* items, const double* cost, double thr, int cap, double* u,
+                              uint64_t* cimg, uint64_t* qimg, int* result) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid < 32) {
+    double carry = 0.0;
+    if (lane == 0) u[0] = 0.0;
+    for (int c0 = 0; c0 < cap; c0 += 32) {
+      const int k = c0 + lane + 1;  // u[k] = carry + inclusive prefix of items[c0..k-1]
+      double x = k <= cap ? items[k - 1] : 0.0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      x += carry;
+      if (k <= cap) {
+        u[k] = x;
+        const double q = x - thr * cost[k];
+        cimg[k] = d2ord(cost[k]);
+        qimg[k] = d2ord(q);
+      }
+      carry = __shfl_sync(0xFFFFFFFFu, x, 31);
     }
   }
-  return k0;
+  __syncthreads();
+  if (tid == 0) {
+    int k0 = 1;
+    uint64_t c0 = cimg[1], q0 = qimg[1];
+    for (int k = 2; k <= cap; ++k) {
+      const uint64_t ck = cimg[k], qk = qimg[k];
+      if (ck <= c0 || qk >= q0) {
+        k0 = k;
+        c0 = ck;
+        q0 = qk;
+      }
+    }
+    *result = k0;
+  }
+  __syncthreads();
+  return *result;
 }
 
 struct PruneArgs {
@@ -115,96 +216,95 @@ struct PruneArgs {
   int B, N, LW, D, d, policy;
 };
 
-// Batch-averaged utility items[s] = (1/B) sum_b v_b(s), s < cap, with v_b(s) given by `vb`.
-// One warp per item; lanes take requests b = lane, lane + 32, ... and reduce in a fixed order, so
-// the result is deterministic.
-template <typename F>
-__device__ __forceinline__ void batch_items(double* items, int cap, int B, F vb) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int s = warp; s < cap; s += nw) {
-    double acc = 0.0;
-    for (int b = lane; b < B; b += 32) acc += vb(b, s);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-    if (lane == 0) items[s] = acc / (double)B;
-  }
-}
-
-// CAST width + depth after layer d (1 CTA).
-__global__ void cast_width_depth_kernel(PruneArgs a) {
+// CAST width + depth after layer d (1 CTA). The CAST state is copied to shared memory; every global
+// input is read in one round of independent loads.
+__global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneArgs a) {
   __shared__ double items[kMaxW * kMaxK + 1];
   __shared__ double cost[kMaxW * kMaxK + 2];
-  __shared__ int maxcand;
+  __shared__ double part[32 * kItemChunk];
+  __shared__ double u[kMaxW + 2];
+  __shared__ uint64_t cimg[kMaxW + 2], qimg[kMaxW + 2];
+  __shared__ CastState cs;
+  __shared__ int maxcand, s_grow, s_k0;
   const Workspace& ws = a.ws;
   const int tid = threadIdx.x;
-  if (tid == 0) maxcand = 0;
+  if (tid == 0) {
+    maxcand = 0;
+    cs = *ws.cast;
+  }
   __syncthreads();
   for (int b = tid; b < a.B; b += blockDim.x) atomicMax(&maxcand, ws.layer_count[(int64_t)b * (a.D + 1) + a.d]);
+  // normalised draft cost of k frontier nodes at the current context: c_k = S_D[row][k-1] / S_T[row][0]
+  const int row = table_row((double)(a.p.n0 + cs.ctx_sum), a.p.L, a.p.M_rows);
+  const int wcap = min(a.p.width_cap, a.LW);
+  for (int k = 1 + tid; k <= wcap; k += blockDim.x)
+    cost[k] = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
   __syncthreads();
   const int cap = min(a.p.width_cap, maxcand);
-  CastState* cs = ws.cast;
-  // normalised draft cost of k frontier nodes at the current context: c_k = S_D[row][k-1] / S_T[row][0]
-  const int row = table_row((double)(a.p.n0 + cs->ctx_sum), a.p.L, a.p.M_rows);
-  const double t1 = a.p.S_T[(int64_t)row * a.p.N_cols];
-  for (int k = 1 + tid; k <= cap; k += blockDim.x) cost[k] = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / t1;
   // items[s] = (1/B) sum_b exp(value of the s-th node of b's layer), missing nodes count 0
-  batch_items(items, cap, a.B, [&](int b, int s) {
+  batch_items(items, part, cap, a.B, [&](int b, int s) {
     const int64_t lb = (int64_t)b * (a.D + 1) + a.d;
-    if (s >= ws.layer_count[lb]) return 0.0;
-    const int id = ws.layer_order[lb * a.LW + s];
+    const int cnt = ws.layer_count[lb];
+    const int id = ws.layer_order[lb * a.LW + s];  // read with the count: -1 past it
+    if (s >= cnt || id < 0) return 0.0;
     return (double)expf(ws.value[(int64_t)b * a.N + id]);
   });
-  __syncthreads();
-  if (tid != 0) return;
-  if (cap <= 0) {
-    a.out.width[0] = 0;
-    for (int b = 0; b < a.B; ++b) a.out.stop[b] = 1;
-    return;
-  }
-  const int n = selection_rule(items, cost, a.p.C1, cap);
-  double u = 0.0;
-  for (int s = 0; s < n; ++s) u += items[s];
-  if (cs->u_prev >= 0.0) {
-    int len = cs->fifo_len;
-    if (len < a.p.R) {
-      cs->fifo[len++] = u / cs->u_prev;
-    } else {
-      for (int j = 1; j < len; ++j) cs->fifo[j - 1] = cs->fifo[j];
-      cs->fifo[len - 1] = u / cs->u_prev;
+  int n = 0;
+  if (cap > 0) n = selection_rule(items, cost, a.p.C1, cap, u, cimg, qimg, &s_k0);
+  if (tid == 0) {
+    bool grow = false;
+    if (cap > 0) {
+      const double un = u[n];
+      if (cs.u_prev >= 0.0) {
+        int len = cs.fifo_len;
+        if (len < a.p.R) {
+          cs.fifo[len++] = un / cs.u_prev;
+        } else {
+          for (int j = 1; j < len; ++j) cs.fifo[j - 1] = cs.fifo[j];
+          cs.fifo[len - 1] = un / cs.u_prev;
+        }
+        cs.fifo_len = len;
+      }
+      double alpha = 0.0;
+      for (int j = 0; j < cs.fifo_len; ++j) alpha += cs.fifo[j];
+      alpha /= (double)cs.fifo_len;
+      grow = (a.d < a.p.D_max) && (alpha * un >= a.p.C2 * cost[n]);  // alpha * u / c_n >= C2
+      cs.u_prev = un;
+      cs.u_layer = un;
+      cs.ctx_sum += n;
+      *ws.cast = cs;
     }
-    cs->fifo_len = len;
+    a.out.width[0] = n;
+    s_grow = grow ? 1 : 0;
   }
-  double alpha = 0.0;
-  for (int j = 0; j < cs->fifo_len; ++j) alpha += cs->fifo[j];
-  alpha /= (double)cs->fifo_len;
-  const bool grow = (a.d < a.p.D_max) && (alpha * u >= a.p.C2 * cost[n]);  // alpha * u / c_n >= C2
-  cs->u_prev = u;
-  cs->u_layer = u;
-  cs->ctx_sum += n;
-  a.out.width[0] = n;
-  for (int b = 0; b < a.B; ++b) a.out.stop[b] = grow ? 0 : 1;
+  __syncthreads();
+  for (int b = tid; b < a.B; b += blockDim.x) a.out.stop[b] = s_grow ? 0 : 1;
 }
 
 // CAST verify count from the per-request sorted linear values (1 CTA).
-__global__ void cast_verify_kernel(PruneArgs a) {
+__global__ void __launch_bounds__(kPruneThreads) cast_verify_kernel(PruneArgs a) {
   __shared__ double items[kMaxP + 1];
   __shared__ double cost[kMaxP + 2];
-  __shared__ int maxn;
+  __shared__ double part[32 * kItemChunk];
+  __shared__ double u[kMaxP + 2];
+  __shared__ uint64_t cimg[kMaxP + 2], qimg[kMaxP + 2];
+  __shared__ int maxn, s_k0;
   const Workspace& ws = a.ws;
   const int tid = threadIdx.x;
   if (tid == 0) maxn = 0;
   __syncthreads();
   for (int b = tid; b < a.B; b += blockDim.x) atomicMax(&maxn, ws.sorted_cnt[b]);
-  __syncthreads();
-  const int cap = min(a.p.m_cap, maxn);
   const double* lin = ws.sorted_lin;
   const int row = table_row((double)a.p.n0, a.p.L, a.p.M_rows);
-  const double t1 = a.p.S_T[(int64_t)row * a.p.N_cols];
-  for (int k = 1 + tid; k <= cap; k += blockDim.x) cost[k] = a.p.S_T[(int64_t)row * a.p.N_cols + (k - 1)] / t1;
-  batch_items(items, cap, a.B, [&](int b, int s) { return lin[(int64_t)b * a.p.m_cap + s]; });
+  const int mcap = a.p.m_cap;
+  for (int k = 1 + tid; k <= mcap; k += blockDim.x)
+    cost[k] = a.p.S_T[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
   __syncthreads();
-  if (tid != 0) return;
-  a.out.m[0] = cap <= 0 ? 0 : selection_rule(items, cost, a.p.C3, cap);
+  const int cap = min(a.p.m_cap, maxn);
+  batch_items(items, part, cap, a.B, [&](int b, int s) { return lin[(int64_t)b * a.p.m_cap + s]; });
+  int m = 0;
+  if (cap > 0) m = selection_rule(items, cost, a.p.C3, cap, u, cimg, qimg, &s_k0);
+  if (tid == 0) a.out.m[0] = m;
 }
 
 // Graft checkpoint after layer d: one thread per request.
@@ -233,17 +333,11 @@ __global__ void graft_checkpoint_kernel(PruneArgs a) {
   }
 }
 
-int next_pow2(int n) {
-  int p = 1;
-  while (p < n) p <<= 1;
-  return p;
-}
-
 }  // namespace
 
 cudaError_t init_select_attributes() {
-  // largest node count: 1 + 32 + 15 * 1024 slots -> 16384 keys of 8 bytes
-  return cudaFuncSetAttribute(sort_nodes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 8);
+  // the largest tree: 16 layers of W*K <= 1024 keys of 8 bytes
+  return cudaFuncSetAttribute(sort_nodes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxD * kCandCap * 8);
 }
 
 static cudaError_t launch_sort(dt_handle* h, int mode, const int32_t* m, int m_len, int m_cap, int32_t* selected,
@@ -251,16 +345,16 @@ static cudaError_t launch_sort(dt_handle* h, int mode, const int32_t* m, int m_l
   SortArgs a;
   a.ws = h->ws;
   a.N = h->N;
+  a.LW = h->LW;
+  a.D = h->cfg.D_max;
   a.depth = h->depth;
-  a.n_pad = next_pow2(std::max(2, h->N - 1));
   a.mode = mode;
   a.m = m;
   a.m_len = m_len;
   a.m_cap = m_cap;
   a.selected = selected;
-  const size_t smem = (size_t)a.n_pad * sizeof(uint64_t);
-  const int threads = std::min(1024, std::max(32, a.n_pad / 2));
-  sort_nodes_kernel<<<h->B, threads, smem, s>>>(a);
+  const size_t smem = (size_t)std::max(1, h->depth) * h->LW * sizeof(uint64_t);
+  sort_nodes_kernel<<<h->B, kSortThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -282,13 +376,13 @@ cudaError_t launch_cast_prune(dt_handle* h, int policy, const dt_prune_params* p
   a.d = h->depth;
   a.policy = policy;
   if (policy == DT_POLICY_CAST_WIDTH_DEPTH) {
-    cast_width_depth_kernel<<<1, 256, 0, s>>>(a);
+    cast_width_depth_kernel<<<1, kPruneThreads, 0, s>>>(a);
     return cudaGetLastError();
   }
   if (policy == DT_POLICY_CAST_VERIFY) {
     cudaError_t e = launch_sort(h, 1, nullptr, 1, p->m_cap, nullptr, s);
     if (e != cudaSuccess) return e;
-    cast_verify_kernel<<<1, 256, 0, s>>>(a);
+    cast_verify_kernel<<<1, kPruneThreads, 0, s>>>(a);
     return cudaGetLastError();
   }
   graft_checkpoint_kernel<<<(h->B + 127) / 128, 128, 0, s>>>(a);

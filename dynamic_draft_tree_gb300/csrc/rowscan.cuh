@@ -118,21 +118,6 @@ struct ScanSmem {
   uint64_t* cand;
 };
 
-// Top-K (descending) of cand[0..cnt) into sm.topk[0..n), n = min(cnt, K); cand is not modified.
-// Real keys are distinct (one per element); empty (0) keys rank below them. All threads call it.
-__device__ __forceinline__ int select_topk(ScanSmem& sm, int cnt, int K) {
-  const int tid = threadIdx.x;
-  for (int i = tid; i < cnt; i += blockDim.x) {
-    const uint64_t k = sm.cand[i];
-    if (k == 0ull) continue;
-    int rank = 0;
-    for (int j = 0; j < cnt; ++j) rank += (sm.cand[j] > k);
-    if (rank < K) sm.topk[rank] = k;
-  }
-  __syncthreads();
-  return cnt < K ? cnt : K;
-}
-
 // Top-K of S descending lists of K keys each, stored back to back in cand[0..S*K) (empty = 0), into
 // sm.topk[0..K). The rank of a key is the number of larger keys over all lists, found by binary
 // search in each list. All threads call it.
@@ -596,8 +581,7 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
   int internal = 0;
   for (int w = 0; w < kScanWarps; ++w) internal |= sm.flags[w] & 2;
   out.internal = internal != 0;
-  const int nk = kScanWarps * K;
-  select_topk(sm, nk, K);
+  merge_sorted_lists(sm, kScanWarps, K);
   int n = 0;
   for (int i = 0; i < K; ++i) n += sm.topk[i] != 0ull;
   out.nkeys = n;
