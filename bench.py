@@ -227,16 +227,24 @@ def run_ours(args):
     torch.cuda.synchronize()
     consistent = bool(torch.equal(run.accept_len, rec_out[0][0]) and torch.equal(run.bonus, rec_out[0][1]))
 
-    graph = torch.cuda.CUDAGraph()
-    cap_stream = torch.cuda.Stream()
-    cap_stream.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(cap_stream):
-        with torch.cuda.graph(graph, stream=cap_stream):
-            for s in range(args.steps):
-                replay(s % R, True)
-    torch.cuda.current_stream().wait_stream(cap_stream)
-    graph.replay()  # untimed: uploads the graph
-    torch.cuda.synchronize()
+    # two graphs of the same K steps: the timed one holds the path only; the other adds event records
+    # around each expansion and verify launch for the per-kernel figures (events between launches
+    # would also split the programmatic launch overlap of the kernels they separate)
+    def capture(with_events):
+        g = torch.cuda.CUDAGraph()
+        cap_stream = torch.cuda.Stream()
+        cap_stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(g, stream=cap_stream):
+                for s in range(args.steps):
+                    replay(s % R, with_events)
+        torch.cuda.current_stream().wait_stream(cap_stream)
+        g.replay()  # untimed: uploads the graph
+        torch.cuda.synchronize()
+        return g
+
+    graph = capture(False)
+    graph_ev = capture(True)
 
     clocks = Clocks(local)
     if world > 1:
@@ -253,6 +261,8 @@ def run_ours(args):
         tdist.barrier()
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
+    graph_ev.replay()  # per-kernel events (not part of the timed region)
+    torch.cuda.synchronize()
     if world > 1:
         tt = torch.tensor([ms], device="cuda")
         tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)

@@ -99,6 +99,22 @@ struct dt_handle {
 
 namespace dt {
 
+// Launches `kernel` on `s` with programmatic stream serialization allowed (see pdl_begin).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---- launchers implemented in the kernel translation units (host functions) ----
 cudaError_t launch_tree_reset(dt_handle* h, const int32_t* root, cudaStream_t s);
 cudaError_t launch_select_frontier(dt_handle* h, const int32_t* width, int width_len, const int32_t* stop,
@@ -129,7 +145,6 @@ cudaError_t init_verify_attributes();
 cudaError_t init_select_attributes();
 cudaError_t init_meta_attributes();
 
-// Segments per row for a row-scan launch of `rows` rows of V elements.
 // Balanced row pass: CTAs per launch (one wave) and the most pieces a row may be cut into when
 // its partial lists hold K keys.
 int row_pass_grid(const dt_handle* h);
@@ -169,6 +184,16 @@ __device__ __forceinline__ float ex2(float x) {
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void set_status(int32_t* status, int32_t bits) { atomicOr(status, bits); }
+
+// Programmatic dependent launch. Every kernel of the path starts with pdl_begin(): it waits until the
+// previous kernel in the stream has completed and its writes are visible (a no-op when the kernel was
+// launched without the attribute), then lets the next kernel's CTAs be scheduled, so that the next
+// launch overlaps this kernel instead of following it. Nothing is read or written before the wait.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 
 __device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
   uint32_t lo = __shfl_sync(0xFFFFFFFFu, (uint32_t)v, src);

@@ -33,6 +33,7 @@ struct RetrieveArgs {
 
 // One CTA per request; template levels are resolved in order (a node's parent is one level up).
 __global__ void __launch_bounds__(kMaxTpl) graft_retrieve_kernel(RetrieveArgs a) {
+  pdl_begin();
   __shared__ int32_t tok[kMaxTpl];
   __shared__ int32_t s_kret;
   const int b = blockIdx.x;
@@ -77,6 +78,7 @@ struct AdjArgs {
 
 // One CTA per request: the highest position of each distinct valid token writes its row.
 __global__ void __launch_bounds__(kMaxP) adj_update_kernel(AdjArgs a) {
+  pdl_begin();
   __shared__ int32_t tok[kMaxP];
   const int b = blockIdx.x;
   const int i = threadIdx.x;
@@ -125,7 +127,7 @@ cudaError_t launch_graft_retrieve(dt_handle* h, const int32_t* M, const int32_t*
   a.ret_token = ret_token;
   a.ret_parent = ret_parent;
   a.ret_count = ret_count;
-  graft_retrieve_kernel<<<h->B, kMaxTpl, 0, s>>>(a);
+  launch_k(graft_retrieve_kernel, dim3(h->B), dim3(kMaxTpl), 0, s, a);
   return cudaGetLastError();
 }
 
@@ -139,7 +141,7 @@ cudaError_t launch_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta
   a.n_pos = meta->n_pos;
   a.P = meta->P;
   a.V = h->cfg.V;
-  adj_update_kernel<<<h->B, kMaxP, 0, s>>>(a);
+  launch_k(adj_update_kernel, dim3(h->B), dim3(kMaxP), 0, s, a);
   return cudaGetLastError();
 }
 

@@ -27,6 +27,7 @@ constexpr int kWords = kMaxP / 32;
 
 // One CTA per request.
 __global__ void __launch_bounds__(kMetaThreads) build_meta_kernel(MetaArgs a) {
+  pdl_begin();
   extern __shared__ __align__(16) int16_t pos_of[];  // [N] node id -> position, -1 if not placed
   __shared__ int32_t tok[kMaxP], par[kMaxP], dep[kMaxP], nid[kMaxP];
   __shared__ uint32_t anc[kMaxP][kWords];
@@ -207,7 +208,7 @@ cudaError_t launch_build_meta(dt_handle* h, const int32_t* selected, int m_cap, 
   a.pos_offset = pos_offset;
   a.meta = *meta;
   const size_t smem = ((size_t)h->N * sizeof(int16_t) + 15) / 16 * 16;
-  build_meta_kernel<<<h->B, kMetaThreads, smem, s>>>(a);
+  launch_k(build_meta_kernel, dim3(h->B), dim3(kMetaThreads), smem, s, a);
   return cudaGetLastError();
 }
 

@@ -27,6 +27,7 @@ constexpr int kSortThreads = 512;
 // the expansion (layer_order), so a node's rank is its place in its own layer plus, for every other
 // layer, the number of keys above it there (binary search): no full sort is needed.
 __global__ void __launch_bounds__(kSortThreads) sort_nodes_kernel(SortArgs a) {
+  pdl_begin();
   extern __shared__ __align__(16) uint64_t keys[];  // [depth][LW]: layer d's valid keys at (d-1)*LW
   __shared__ int cnt[kMaxD + 1];
   __shared__ int32_t sel[kMaxP];
@@ -219,6 +220,7 @@ struct PruneArgs {
 // CAST width + depth after layer d (1 CTA). The CAST state is copied to shared memory; every global
 // input is read in one round of independent loads.
 __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneArgs a) {
+  pdl_begin();
   __shared__ double items[kMaxW * kMaxK + 1];
   __shared__ double cost[kMaxW * kMaxK + 2];
   __shared__ double part[32 * kItemChunk];
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
 
 // CAST verify count from the per-request sorted linear values (1 CTA).
 __global__ void __launch_bounds__(kPruneThreads) cast_verify_kernel(PruneArgs a) {
+  pdl_begin();
   __shared__ double items[kMaxP + 1];
   __shared__ double cost[kMaxP + 2];
   __shared__ double part[32 * kItemChunk];
@@ -309,6 +312,7 @@ __global__ void __launch_bounds__(kPruneThreads) cast_verify_kernel(PruneArgs a)
 
 // Graft checkpoint after layer d: one thread per request.
 __global__ void graft_checkpoint_kernel(PruneArgs a) {
+  pdl_begin();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= a.B) return;
   if (a.out.stop[b]) return;
@@ -354,7 +358,7 @@ static cudaError_t launch_sort(dt_handle* h, int mode, const int32_t* m, int m_l
   a.m_cap = m_cap;
   a.selected = selected;
   const size_t smem = (size_t)std::max(1, h->depth) * h->LW * sizeof(uint64_t);
-  sort_nodes_kernel<<<h->B, kSortThreads, smem, s>>>(a);
+  launch_k(sort_nodes_kernel, dim3(h->B), dim3(kSortThreads), smem, s, a);
   return cudaGetLastError();
 }
 
@@ -376,16 +380,16 @@ cudaError_t launch_cast_prune(dt_handle* h, int policy, const dt_prune_params* p
   a.d = h->depth;
   a.policy = policy;
   if (policy == DT_POLICY_CAST_WIDTH_DEPTH) {
-    cast_width_depth_kernel<<<1, kPruneThreads, 0, s>>>(a);
+    launch_k(cast_width_depth_kernel, dim3(1), dim3(kPruneThreads), 0, s, a);
     return cudaGetLastError();
   }
   if (policy == DT_POLICY_CAST_VERIFY) {
     cudaError_t e = launch_sort(h, 1, nullptr, 1, p->m_cap, nullptr, s);
     if (e != cudaSuccess) return e;
-    cast_verify_kernel<<<1, kPruneThreads, 0, s>>>(a);
+    launch_k(cast_verify_kernel, dim3(1), dim3(kPruneThreads), 0, s, a);
     return cudaGetLastError();
   }
-  graft_checkpoint_kernel<<<(h->B + 127) / 128, 128, 0, s>>>(a);
+  launch_k(graft_checkpoint_kernel, dim3((h->B + 127) / 128), dim3(128), 0, s, a);
   return cudaGetLastError();
 }
 

@@ -19,6 +19,7 @@ __device__ __forceinline__ int layer_of(int id, int K, int LW) {
 
 __global__ void tree_reset_kernel(Workspace ws, const int32_t* __restrict__ root, int B, int N, int K, int LW,
                                   int D, int V) {
+  pdl_begin();
   const int64_t total = (int64_t)B * N;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -65,6 +66,7 @@ __global__ void tree_reset_kernel(Workspace ws, const int32_t* __restrict__ root
 __global__ void select_frontier_kernel(Workspace ws, int B, int N, int K, int W, int LW, int D, int d,
                                        const int32_t* __restrict__ width, int width_len,
                                        const int32_t* __restrict__ stop, int32_t* __restrict__ ftok) {
+  pdl_begin();
   const int warps = blockDim.x >> 5;
   const int b = blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -107,6 +109,7 @@ struct ExpandArgs {
 // balanced row pass in rowscan.cuh.
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
+  pdl_begin();
   extern __shared__ __align__(128) uint8_t dyn_smem[];
   __shared__ ScanSmem sm;
   __shared__ RowPlan plan;
@@ -216,7 +219,7 @@ cudaError_t launch_tree_reset(dt_handle* h, const int32_t* root, cudaStream_t s)
   const int64_t total = (int64_t)h->B * h->N;
   int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)h->num_sms * 4);
   if (blocks < 1) blocks = 1;
-  tree_reset_kernel<<<blocks, 256, 0, s>>>(h->ws, root, h->B, h->N, h->cfg.K, h->LW, h->cfg.D_max, h->cfg.V);
+  launch_k(tree_reset_kernel, dim3(blocks), dim3(256), 0, s, h->ws, root, h->B, h->N, h->cfg.K, h->LW, h->cfg.D_max, h->cfg.V);
   return cudaGetLastError();
 }
 
@@ -224,7 +227,7 @@ cudaError_t launch_select_frontier(dt_handle* h, const int32_t* width, int width
                                    int32_t* frontier_token, cudaStream_t s) {
   const int warps = 8;
   const int blocks = (h->B + warps - 1) / warps;
-  select_frontier_kernel<<<blocks, warps * 32, 0, s>>>(h->ws, h->B, h->N, h->cfg.K, h->cfg.W, h->LW,
+  launch_k(select_frontier_kernel, dim3(blocks), dim3(warps * 32), 0, s, h->ws, h->B, h->N, h->cfg.K, h->cfg.W, h->LW,
                                                         h->cfg.D_max, h->depth, width, width_len, stop,
                                                         frontier_token);
   return cudaGetLastError();
@@ -251,9 +254,9 @@ cudaError_t launch_expand(dt_handle* h, const void* logits, int64_t ld, int F, c
   const unsigned grid = (unsigned)row_pass_grid(h);
   const size_t smem = row_smem_bytes();
   if (h->cfg.dtype == DT_BF16)
-    expand_kernel<uint16_t><<<grid, kRowThreads, smem, s>>>(a);
+    launch_k(expand_kernel<uint16_t>, dim3(grid), dim3(kRowThreads), smem, s, a);
   else
-    expand_kernel<float><<<grid, kRowThreads, smem, s>>>(a);
+    launch_k(expand_kernel<float>, dim3(grid), dim3(kRowThreads), smem, s, a);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) h->depth = d;
   return e;

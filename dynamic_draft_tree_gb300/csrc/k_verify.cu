@@ -28,6 +28,7 @@ struct RowPassArgs {
 // token is counted but not read); see the balanced row pass in rowscan.cuh.
 template <typename T, bool SOFTMAX>
 __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(RowPassArgs a) {
+  pdl_begin();
   extern __shared__ __align__(128) uint8_t dyn_smem[];
   __shared__ ScanSmem sm;
   __shared__ RowPlan plan;
@@ -123,6 +124,7 @@ __device__ double residual_rescan(const WalkArgs& a, int64_t r, float M, const i
 
 // One CTA per request.
 __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
+  pdl_begin();
   __shared__ int32_t s_first_child[kMaxP], s_next_sib[kMaxP];
   __shared__ int32_t s_path[kMaxP];
   __shared__ int32_t s_rej[kMaxP];
@@ -306,6 +308,7 @@ constexpr int kBonusThreads = 256;
 // Gumbel-max draw from the final residual: argmax over tokens not rejected at that position of
 // x_v - log(-log(u_v)). Grid: B * S CTAs, each a segment of the row.
 __global__ void __launch_bounds__(kBonusThreads) verify_bonus_kernel(BonusArgs a) {
+  pdl_begin();
   __shared__ unsigned long long s_best;
   __shared__ int32_t s_rej[kMaxP];
   __shared__ int32_t s_last;
@@ -390,7 +393,7 @@ cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* lo
   const unsigned grid = (unsigned)row_pass_grid(h);
   const size_t smem = (size_t)kScanSmemBytes;
   cudaError_t e;
-#define DT_LAUNCH_ROWS(T, SM) verify_rows_kernel<T, SM><<<grid, kRowThreads, smem, s>>>(ra)
+#define DT_LAUNCH_ROWS(T, SM) e = launch_k(verify_rows_kernel<T, SM>, dim3(grid), dim3(kRowThreads), smem, s, ra)
   const bool sm_on = mode == DT_SAMPLE;
   if (h->cfg.dtype == DT_BF16) {
     if (sm_on) DT_LAUNCH_ROWS(uint16_t, true);
@@ -419,7 +422,7 @@ cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* lo
   wa.accept_len = accept_len;
   wa.accept_path = accept_path;
   wa.bonus = bonus;
-  verify_walk_kernel<<<h->B, kWalkThreads, 0, s>>>(wa);
+  launch_k(verify_walk_kernel, dim3(h->B), dim3(kWalkThreads), 0, s, wa);
   e = cudaGetLastError();
   if (e != cudaSuccess || mode != DT_SAMPLE) return e;
 
@@ -440,7 +443,7 @@ cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* lo
   ba.r0 = wa.r0;
   ba.r1 = wa.r1;
   ba.bonus = bonus;
-  verify_bonus_kernel<<<(unsigned)(h->B * Sb), kBonusThreads, 0, s>>>(ba);
+  launch_k(verify_bonus_kernel, dim3((unsigned)(h->B * Sb)), dim3(kBonusThreads), 0, s, ba);
   return cudaGetLastError();
 }
 
