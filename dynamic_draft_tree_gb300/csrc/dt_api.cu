@@ -96,6 +96,7 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   const size_t partial_cap = rows_max * 8 + (size_t)h->num_sms * 64;
   const size_t o_part = cv.take<dt::Partial>(partial_cap);
   const size_t o_rowc = cv.take<int32_t>(rows_max);
+  const size_t o_rtau = cv.take<unsigned long long>(rows_max);
   const size_t o_reqc = cv.take<int32_t>(c.B_max);
   const size_t o_rstat = cv.take<dt::RowStat>((size_t)c.B_max * c.P_max);
   const size_t o_slin = cv.take<double>((size_t)c.B_max * c.P_max);
@@ -133,6 +134,7 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   w.partials = reinterpret_cast<dt::Partial*>(bp + o_part);
   w.partial_cap = (int64_t)partial_cap;
   w.row_counter = reinterpret_cast<int32_t*>(bp + o_rowc);
+  w.row_tau = reinterpret_cast<unsigned long long*>(bp + o_rtau);
   w.row_counter_cap = (int64_t)rows_max;
   w.req_counter = reinterpret_cast<int32_t*>(bp + o_reqc);
   w.row_stats = reinterpret_cast<dt::RowStat*>(bp + o_rstat);

@@ -71,6 +71,7 @@ struct Workspace {
   int64_t partial_cap;
   int32_t* row_counter;
   int64_t row_counter_cap;
+  unsigned long long* row_tau;  // [row_counter_cap] best K-th key published by a row's pieces (0 = none)
   int32_t* req_counter;
   RowStat* row_stats;
   // selection scratch

@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) row_topk_static_kernel(StaticA
   const T* row = reinterpret_cast<const T*>(a.logits) + (int64_t)r * a.ld;
   const int64_t s0 = (int64_t)seg * a.seg_len;
   const int64_t s1 = min((int64_t)a.V, s0 + a.seg_len);
-  SegOut so = scan_segment<T, true>(row, s0, s1, a.K, sm, dyn_smem, kSpinCap);
+  SegOut so = scan_segment<T, true>(row, s0, s1, a.K, sm, dyn_smem, kSpinCap, nullptr);
 
   Partial* part = a.partials + (int64_t)r * a.S;
   for (int i = tid; i < a.K; i += blockDim.x) part[seg].keys[i] = i < so.nkeys ? sm.cand[i] : 0ull;

@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
       if (tid == 0) ws.layer_count[(int64_t)b * (a.D + 1) + a.d] = n;
     }
   };
-  scan_pieces<T, true>(p, a.V, a.K, a.B, ws.partials, ws.row_counter, sm, dyn_smem, a.first_wait_cap, ws.status,
+  scan_pieces<T, true>(p, a.V, a.K, a.B, ws.partials, ws.row_counter, ws.row_tau, sm, dyn_smem, a.first_wait_cap, ws.status,
                        row_of, cnt, finish);
 }
 

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(RowPassArgs
       a.top8[r * 8 + tid] = (tid < a.K && k != 0ull) ? (int32_t)key_id(k) : -1;
     }
   };
-  scan_pieces<T, SOFTMAX>(p, a.V, a.K, a.B, ws.partials, ws.row_counter, sm, dyn_smem, a.first_wait_cap,
+  scan_pieces<T, SOFTMAX>(p, a.V, a.K, a.B, ws.partials, ws.row_counter, ws.row_tau, sm, dyn_smem, a.first_wait_cap,
                           ws.status, row_of, cnt, finish);
 }
 

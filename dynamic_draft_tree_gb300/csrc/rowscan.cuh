@@ -231,7 +231,7 @@ __device__ __forceinline__ void lane_acc_one(float x, float& m_t, float& s_hi, f
 // shared memory (dynamic). All threads of the CTA call it.
 template <typename T, bool SOFTMAX>
 __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1, int K, ScanSmem& sm,
-                               uint8_t* stages, uint32_t first_wait_cap) {
+                               uint8_t* stages, uint32_t first_wait_cap, unsigned long long* gtau) {
   constexpr int VEC = Elt<T>::kVec;
   constexpr int ESZ = (int)sizeof(T);
   const int tid = threadIdx.x;
@@ -360,6 +360,8 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
   for (int t = 0; t < n_st; ++t) {
     const int st = t % kWarpStages;
     const uint32_t parity = (uint32_t)((t / kWarpStages) & 1);
+    // the row's shared threshold (read early; used by the filter below)
+    const uint64_t gt = gtau ? (uint64_t)__ldcg(gtau) : 0ull;
     const bool ok = mbar_wait_bounded(&rg.bar[st], parity, t == 0 ? first_wait_cap : kSpinCap);
     if (!__all_sync(0xFFFFFFFFu, ok)) {
       timed_out = true;
@@ -493,20 +495,31 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
       inited = true;
     }
 
-    // Filter against the list's K-th key. Within a warp's chunk token ids grow stage by stage, so
-    // after the first stage a value equal to the K-th key's value has a larger id and cannot beat it:
-    // the test is strict there. Lanes whose maximum clears the threshold push their candidates, which
-    // are then merged into the list. If the buffer overflowed, the merge still raised the threshold:
-    // the stage is filtered again against it (keys already in the list are dropped by the merge).
-    bool again = __any_sync(0xFFFFFFFFu, (t == 0) ? (lm >= tau_val) : (lm > tau_val));
+    // Filter against the larger of the list's K-th key and the row's shared threshold (the best K-th
+    // key any warp of any piece of the row has published: that warp holds K keys at or above it, so
+    // no element below it can be in the row's top-K). Within a warp's chunk token ids grow stage by
+    // stage, so after the first stage a value equal to the warp's own K-th key's value has a larger
+    // id and cannot beat it: the test is strict there (not against another warp's key). Lanes whose
+    // maximum clears the threshold push their candidates, which are then merged into the list. If the
+    // buffer overflowed, the merge still raised the threshold: the stage is filtered again against it
+    // (keys already in the list are dropped by the merge).
     bool dedup = false;
-    for (int round = 0; again; ++round) {
-      const bool hot = (t == 0) ? (lm >= tau_val) : (lm > tau_val);
+    for (int round = 0;; ++round) {
+      uint64_t tk = tau_key;
+      bool own = true;
+      if (gt > tk) {
+        tk = gt;
+        own = false;
+      }
+      const float tv = tk ? key_value(tk) : -INFINITY;
+      const bool strict = t > 0 && own;
+      const bool hot = strict ? (lm > tv) : (lm >= tv);
+      if (!__any_sync(0xFFFFFFFFu, hot)) break;
       if (hot) {
         unsigned vm = 0u;  // vectors that may hold candidates
 #pragma unroll
         for (int q = 0; q < QV; ++q)
-          if ((t == 0) ? (vmax[q] >= tau_val) : (vmax[q] > tau_val)) vm |= 1u << q;
+          if (strict ? (vmax[q] > tv) : (vmax[q] >= tv)) vm |= 1u << q;
         while (vm) {
           const int q = __ffs(vm) - 1;
           vm &= vm - 1;
@@ -515,15 +528,17 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
 #pragma unroll
           for (int e = 0; e < VEC; ++e) {
             const float x = elt(w, e);
-            if (x >= tau_val && x != -INFINITY) {
+            if (x >= tv && x != -INFINITY) {
               const uint64_t k = make_key(x, id_of(q, e));
-              if (k > tau_key && k != excl) push(k);
+              if (k > tk && k != excl) push(k);
             }
           }
         }
       }
-      again = merge(dedup);
+      const bool overflow = merge(dedup);
       dedup = true;
+      if (gtau && lane == 0 && nl == K) atomicMax(gtau, (unsigned long long)tau_key);
+      if (!overflow) break;
       if (round >= NV * 32 / (kWarpCand - kMaxK) + 1) {  // the threshold rises every round: never hit
         if (lane == 0) sm.flags[warp] |= 2;
         break;
@@ -710,8 +725,8 @@ __device__ void plan_rows(RowPlan& p, int B, int64_t V, int Smax, int esz, Cnt c
 // that every row still completes its count.
 template <typename T, bool SOFTMAX, class RowOf, class Cnt, class Finish>
 __device__ void scan_pieces(const RowPlan& p, int64_t V, int K, int B, Partial* partials, int32_t* counter,
-                            ScanSmem& sm, uint8_t* stages, uint32_t first_wait_cap, int32_t* status, RowOf row_of,
-                            Cnt cnt, Finish finish) {
+                            unsigned long long* row_tau, ScanSmem& sm, uint8_t* stages, uint32_t first_wait_cap,
+                            int32_t* status, RowOf row_of, Cnt cnt, Finish finish) {
   const int tid = threadIdx.x;
   const int64_t c = blockIdx.x;
   if (tid == 0) sm.cand = reinterpret_cast<uint64_t*>(stages);
@@ -739,7 +754,7 @@ __device__ void scan_pieces(const RowPlan& p, int64_t V, int K, int B, Partial* 
     const T* row = row_of(b, i);
     SegOut so;
     if (row != nullptr && !halted && e1 > e0) {
-      so = scan_segment<T, SOFTMAX>(row, e0, e1, K, sm, stages, first_wait_cap);
+      so = scan_segment<T, SOFTMAX>(row, e0, e1, K, sm, stages, first_wait_cap, row_tau ? row_tau + j : nullptr);
     } else {
       so.m = -INFINITY;
       so.s = 0.0;
@@ -761,7 +776,10 @@ __device__ void scan_pieces(const RowPlan& p, int64_t V, int K, int B, Partial* 
     __syncthreads();
     if (sm.last) {  // block-uniform
       __threadfence();
-      if (tid == 0) counter[j] = 0;
+      if (tid == 0) {
+        counter[j] = 0;
+        if (row_tau) row_tau[j] = 0ull;  // every piece of the row has finished with it
+      }
       const int S = c_last - c_first + 1;
       const Partial* rp = partials + row_slot0;
       for (int k = tid; k < S * K; k += blockDim.x) sm.cand[k] = __ldcg(&rp[k / K].keys[k % K]);
