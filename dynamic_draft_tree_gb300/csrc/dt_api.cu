@@ -91,6 +91,7 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   const size_t o_lorder = cv.take<int32_t>((size_t)c.B_max * (c.D_max + 1) * h->LW);
   const size_t o_lcount = cv.take<int32_t>((size_t)c.B_max * (c.D_max + 1));
   const size_t o_front = cv.take<int32_t>((size_t)c.B_max * c.W);
+  const size_t o_fval = cv.take<float>((size_t)c.B_max * c.W);
   const size_t o_fcount = cv.take<int32_t>(c.B_max);
   // one partial per (row, segment) of a row-scan launch; launches clamp their segment count to it
   const size_t partial_cap = rows_max * 8 + (size_t)h->num_sms * 64;
@@ -130,6 +131,7 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   w.layer_order = reinterpret_cast<int32_t*>(bp + o_lorder);
   w.layer_count = reinterpret_cast<int32_t*>(bp + o_lcount);
   w.frontier = reinterpret_cast<int32_t*>(bp + o_front);
+  w.frontier_val = reinterpret_cast<float*>(bp + o_fval);
   w.frontier_count = reinterpret_cast<int32_t*>(bp + o_fcount);
   w.partials = reinterpret_cast<dt::Partial*>(bp + o_part);
   w.partial_cap = (int64_t)partial_cap;

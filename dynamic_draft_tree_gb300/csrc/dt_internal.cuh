@@ -26,8 +26,8 @@ constexpr int kStaticPartials = 4096;  // row segments per call of the static-sc
 // Per-(row, segment) partial result of a row scan.
 struct Partial {
   float m;           // segment max (or -inf)
+  float s_hi, s_lo;  // sum exp(x - m) over the segment as an unevaluated sum of two floats
   int32_t pad;
-  double s;          // sum exp(x - m) over the segment
   uint64_t keys[kMaxK];  // segment top-K keys, descending; 0 = empty
 };
 
@@ -65,6 +65,7 @@ struct Workspace {
   int32_t* layer_order;
   int32_t* layer_count;
   int32_t* frontier;
+  float* frontier_val;   // [B_max][W] value of each frontier node (read with the frontier)
   int32_t* frontier_count;
   // row scans
   Partial* partials;
@@ -185,6 +186,22 @@ __device__ __forceinline__ float ex2(float x) {
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void set_status(int32_t* status, int32_t bits) { atomicOr(status, bits); }
+
+// Unevaluated sums of two floats (hi + lo, |lo| <= ulp(hi) / 2): exact error-free transformations
+// (Knuth's TwoSum, Dekker's FastTwoSum) give about 48 bits of precision with fp32 operations only.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+// (h, l) += (h2, l2)
+__device__ __forceinline__ void ff_add(float& h, float& l, float h2, float l2) {
+  float s, e;
+  two_sum(h, h2, s, e);
+  e = __fadd_rn(e, __fadd_rn(l, l2));
+  h = __fadd_rn(s, e);
+  l = __fsub_rn(e, __fsub_rn(h, s));
+}
 
 // Programmatic dependent launch. Every kernel of the path starts with pdl_begin(): it waits until the
 // previous kernel in the stream has completed and its writes are visible (a no-op when the kernel was

@@ -53,15 +53,21 @@ __global__ void __launch_bounds__(kRowThreads, 3) row_topk_static_kernel(StaticA
   SegOut so = scan_segment<T, true>(row, s0, s1, a.K, sm, dyn_smem, kSpinCap, nullptr);
 
   Partial* part = a.partials + (int64_t)r * a.S;
-  for (int i = tid; i < a.K; i += blockDim.x) part[seg].keys[i] = i < so.nkeys ? sm.cand[i] : 0ull;
-  if (tid == 0) {
-    part[seg].m = so.m;
-    part[seg].s = so.s;
-    if (so.timed_out) or_status(a.status, DT_DEV_TIMEOUT);
-    if (so.internal) or_status(a.status, DT_DEV_INTERNAL);
+  if (tid < 32) {  // warp 0 publishes the segment, then (after a fence) its arrival
+    if (tid < a.K) part[seg].keys[tid] = sm.topk[tid];
+    if (tid == 0) {
+      part[seg].m = so.m;
+      part[seg].s_hi = so.s_hi;
+      part[seg].s_lo = so.s_lo;
+      if (so.timed_out) or_status(a.status, DT_DEV_TIMEOUT);
+      if (so.internal) or_status(a.status, DT_DEV_INTERNAL);
+    }
     __threadfence();
-    const int prev = atomicAdd(&a.counter[r], 1);
-    sm.last = (prev == a.S - 1);
+    __syncwarp();
+    if (tid == 0) {
+      const int prev = atomicAdd(&a.counter[r], 1);
+      sm.last = (prev == a.S - 1);
+    }
   }
   __syncthreads();
   if (!sm.last) return;
@@ -71,13 +77,26 @@ __global__ void __launch_bounds__(kRowThreads, 3) row_topk_static_kernel(StaticA
   if (tid == 0) a.counter[r] = 0;  // back to zero for the next call
   const int nk = a.S * a.K;
   for (int i = tid; i < nk; i += blockDim.x) sm.cand[i] = __ldcg(&part[i / a.K].keys[i % a.K]);
+  float m0 = -INFINITY, h0 = 0.0f, l0 = 0.0f, m1 = -INFINITY, h1 = 0.0f, l1 = 0.0f;
+  if (tid < 32) {
+    if (tid < a.S) {
+      m0 = __ldcg(&part[tid].m);
+      h0 = __ldcg(&part[tid].s_hi);
+      l0 = __ldcg(&part[tid].s_lo);
+    }
+    if (tid + 32 < a.S) {
+      m1 = __ldcg(&part[tid + 32].m);
+      h1 = __ldcg(&part[tid + 32].s_hi);
+      l1 = __ldcg(&part[tid + 32].s_lo);
+    }
+  }
   if (tid < kMaxK) sm.topk[tid] = 0ull;
   __syncthreads();
-  merge_sorted_lists(sm, a.S, a.K);
-  float M;
-  double Ssum;
-  bool nan;
-  merge_softmax(part, a.S, sm, M, Ssum, nan);
+  if (tid < 32) combine_partial_sums(sm, m0, h0, l0, m1, h1, l1);
+  merge_sorted_lists(sm, sm.cand, a.S, a.K, a.K);
+  const float M = sm.red_m[0];
+  const double Ssum = (double)sm.red_sh[0] + (double)sm.red_sl[0];
+  const bool nan = Ssum != Ssum;
   if (tid == 0 && (nan || !(M > -INFINITY) || M == INFINITY || !(Ssum > 0.0)))
     or_status(a.status, DT_DEV_BAD_LOGITS);
   // log S from the exponent (exact) plus the fp32 log of the mantissa in [1, 2)

@@ -47,8 +47,10 @@ __global__ void tree_reset_kernel(Workspace ws, const int32_t* __restrict__ root
     ws.layer_count[i] = (i % (D + 1)) == 0 ? 1 : 0;
   const int W = LW / K;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)B * W;
-       i += (int64_t)gridDim.x * blockDim.x)
+       i += (int64_t)gridDim.x * blockDim.x) {
     ws.frontier[i] = (i % W) == 0 ? 0 : -1;
+    ws.frontier_val[i] = (i % W) == 0 ? 0.0f : -INFINITY;
+  }
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < B; i += (int64_t)gridDim.x * blockDim.x)
     ws.frontier_count[i] = 1;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -85,12 +87,15 @@ __global__ void select_frontier_kernel(Workspace ws, int B, int N, int K, int W,
   }
   if (lane < W) {
     ws.frontier[(int64_t)b * W + lane] = -1;
+    ws.frontier_val[(int64_t)b * W + lane] = -INFINITY;
     if (ftok) ftok[(int64_t)b * W + lane] = -1;
   }
   __syncwarp();
   if (lane < w) {
+    const int64_t gi = (int64_t)b * N + id;
     ws.frontier[(int64_t)b * W + slot] = id;
-    if (ftok) ftok[(int64_t)b * W + slot] = ws.token[(int64_t)b * N + id];
+    ws.frontier_val[(int64_t)b * W + slot] = ws.value[gi];
+    if (ftok) ftok[(int64_t)b * W + slot] = ws.token[gi];
   }
   if (lane == 0) ws.frontier_count[b] = w;
 }
@@ -128,40 +133,51 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
   const RowPlan p = plan;
   if ((int)blockIdx.x >= p.G) return;
 
+  // the parent's id and value are loaded when a piece starts (no dependent load in the finish)
+  int pid = -1;
+  float pval = 0.0f;
   auto row_of = [&](int b, int f) -> const T* {
+    pid = ws.frontier[(int64_t)b * a.W + f];
+    pval = ws.frontier_val[(int64_t)b * a.W + f];
     return reinterpret_cast<const T*>(a.logits) + ((int64_t)b * a.F + f) * a.ld;
   };
   // last piece of row (b, f): write the K children of frontier slot f
-  auto finish = [&](int b, int f, const Partial* rp, int S) {
-    float M;
-    double Ssum;
-    bool nan;
-    merge_softmax(rp, S, sm, M, Ssum, nan);
-    if (tid == 0 && (nan || !(M > -INFINITY) || M == INFINITY || !(Ssum > 0.0)))
+  auto finish = [&](int b, int f, const SoftmaxStat& st) {
+    const float M = st.m;
+    if (tid == 0 && (st.nan || !(M > -INFINITY) || M == INFINITY || !(st.s_hi > 0.0f) || st.s_hi == INFINITY))
       set_status(ws.status, DT_DEV_BAD_LOGITS);
-    const int pid = ws.frontier[(int64_t)b * a.W + f];
-    const float pval = ws.value[(int64_t)b * a.N + pid];
-    // log S = e * ln 2 + log(mantissa), mantissa in [1, 2): the exponent split is exact and the fp32
-    // log of the mantissa is accurate to ~1e-7 absolute (no fp64 transcendental on the tail)
-    double logS;
-    {
-      const unsigned long long bits = (unsigned long long)__double_as_longlong(Ssum);
-      const int e = (int)((bits >> 52) & 0x7FF) - 1023;
-      const double mant =
-          __longlong_as_double((long long)((bits & 0x000FFFFFFFFFFFFFull) | 0x3FF0000000000000ull));
-      logS = (double)e * 0.6931471805599453 + (double)logf((float)mant);
-      if (!(Ssum > 0.0) || Ssum != Ssum || e == 1024) logS = log(Ssum);  // zero, NaN, inf: let log decide
-    }
     if (tid < a.K) {
+      // log S as a double-float: S = mant * 2^e with mant in [1, 2) (exact scaling), log S =
+      // e * ln2 (Cody-Waite split: e * LN2_HI is exact for |e| < 2^9) + log(mant_hi) + mant_lo / mant_hi
+      constexpr float LN2_HI = 0.693145751953125f, LN2_LO = 1.4286068203094173e-06f;
+      float lh, ll;
+      const float sh = st.s_hi, sl = st.s_lo;
+      if (sh > 0.0f && sh < INFINITY) {
+        const int e = (int)((__float_as_uint(sh) >> 23) & 0xFF) - 127;
+        const float scale = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+        const float mh = __fmul_rn(sh, scale), ml = __fmul_rn(sl, scale);
+        const float lm = __fadd_rn(logf(mh), __fdiv_rn(ml, mh));
+        two_sum(__fmul_rn((float)e, LN2_HI), fmaf((float)e, LN2_LO, lm), lh, ll);
+      } else {
+        lh = logf(sh);
+        ll = 0.0f;
+      }
       const uint64_t k = sm.topk[tid];
       const int id = a.base + f * a.K + tid;
       const int64_t gi = (int64_t)b * a.N + id;
       const float x = key_value(k);
-      const double lc = ((double)x - (double)M) - logS;
+      // log c = (x - M) - log S and value = value(parent) + log c, each kept as a double-float until
+      // the final rounding
+      float dh, dl;
+      two_sum(x, -M, dh, dl);
+      ff_add(dh, dl, -lh, -ll);
+      const float lc = __fadd_rn(dh, dl);
+      float vh = pval, vl = 0.0f;
+      ff_add(vh, vl, dh, dl);
       ws.token[gi] = (int32_t)key_id(k);
       ws.parent[gi] = pid;
-      ws.logc[gi] = (float)lc;
-      ws.value[gi] = (float)((double)pval + lc);
+      ws.logc[gi] = lc;
+      ws.value[gi] = __fadd_rn(vh, vl);
     }
     __threadfence();
     __syncthreads();

@@ -49,22 +49,18 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(RowPassArgs
     if (a.tokens[r] < 0) return nullptr;  // invalid token: row not needed
     return reinterpret_cast<const T*>(a.logits) + r * a.ld;
   };
-  auto finish = [&](int b, int i, const Partial* rp, int S) {
+  auto finish = [&](int b, int i, const SoftmaxStat& stt) {
     const int64_t r = (int64_t)b * a.P + i;
     if (a.tokens[r] < 0) return;  // block-uniform
-    float M = -INFINITY;
-    double Ssum = 0.0;
-    bool nan = false;
-    if (SOFTMAX) merge_softmax(rp, S, sm, M, Ssum, nan);
     if (tid == 0) {
       RowStat st;
       st.amax = (int32_t)key_id(sm.topk[0]);
+      st.m = stt.m;
       if (SOFTMAX) {
-        if (nan || !(M > -INFINITY) || M == INFINITY || !(Ssum > 0.0)) set_status(ws.status, DT_DEV_BAD_LOGITS);
-        st.m = M;
-        st.s = Ssum;
+        if (stt.nan || !(stt.m > -INFINITY) || stt.m == INFINITY || !(stt.s_hi > 0.0f) || stt.s_hi == INFINITY)
+          set_status(ws.status, DT_DEV_BAD_LOGITS);
+        st.s = (double)stt.s_hi + (double)stt.s_lo;
       } else {
-        st.m = key_value(sm.topk[0]);
         st.s = 0.0;
         if (sm.topk[0] == 0ull || !(st.m > -INFINITY)) set_status(ws.status, DT_DEV_BAD_LOGITS);
       }

@@ -109,8 +109,9 @@ struct WarpRing {
 struct ScanSmem {
   WarpRing ring[kScanWarps];
   uint64_t topk[kMaxK];
+  uint64_t wl[kScanWarps][kMaxK];  // the warps' final lists (not aliased with the stages)
   float red_m[kScanWarps];
-  double red_s[kScanWarps];
+  float red_sh[kScanWarps], red_sl[kScanWarps];
   int32_t flags[kScanWarps];
   int32_t last;
   // Merge / sort buffer of kCandCap keys. It aliases the dynamic stage memory, which is free once
@@ -118,17 +119,17 @@ struct ScanSmem {
   uint64_t* cand;
 };
 
-// Top-K of S descending lists of K keys each, stored back to back in cand[0..S*K) (empty = 0), into
+// Top-K of S descending lists of K keys each, list s at src[s * stride ..] (empty = 0), into
 // sm.topk[0..K). The rank of a key is the number of larger keys over all lists, found by binary
 // search in each list. All threads call it.
-__device__ __forceinline__ void merge_sorted_lists(ScanSmem& sm, int S, int K) {
+__device__ __forceinline__ void merge_sorted_lists(ScanSmem& sm, const uint64_t* src, int S, int K, int stride) {
   const int n = S * K;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint64_t k = sm.cand[i];
+    const uint64_t k = src[(i / K) * stride + i % K];
     if (k == 0ull) continue;
     int rank = 0;
     for (int s = 0; s < S && rank < K; ++s) {
-      const uint64_t* L = sm.cand + s * K;
+      const uint64_t* L = src + s * stride;
       int lo = 0, hi = K;  // first index whose key is <= k
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
@@ -142,42 +143,53 @@ __device__ __forceinline__ void merge_sorted_lists(ScanSmem& sm, int S, int K) {
   __syncthreads();
 }
 
-// Merge of the S (<= 64) segment partials of a row: M = max_s m_s, S = sum_s s_s * exp(m_s - M).
-// Every thread gets the results; `nan` reports a poisoned (NaN) sum. All threads call it.
-__device__ __forceinline__ void merge_softmax(const Partial* part, int S, ScanSmem& sm, float& M, double& Sum,
-                                              bool& nan) {
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    float m0 = -INFINITY, m1 = -INFINITY;
-    double s0 = 0.0, s1 = 0.0;
-    if (lane < S) {
-      m0 = __ldcg(&part[lane].m);
-      s0 = __ldcg(&part[lane].s);
-    }
-    if (lane + 32 < S) {
-      m1 = __ldcg(&part[lane + 32].m);
-      s1 = __ldcg(&part[lane + 32].s);
-    }
-    float bm = fmaxf(m0, m1);
+// Softmax statistics of a row or segment: max m and S = sum exp(x - m) = s_hi + s_lo.
+struct SoftmaxStat {
+  float m, s_hi, s_lo;
+  bool nan;  // the sum was poisoned by a NaN
+};
+
+// (h, l) * f for a float factor f, renormalised (the product's rounding error is kept by an fma).
+__device__ __forceinline__ void ff_scale(float& h, float& l, float f) {
+  const float p = __fmul_rn(h, f);
+  const float pe = fmaf(h, f, -p);
+  const float t = fmaf(l, f, pe);
+  h = __fadd_rn(p, t);
+  l = __fsub_rn(t, __fsub_rn(h, p));
+}
+
+// Warp 0: combines up to 64 (m, s_hi, s_lo) partials held two per lane into M = max m and
+// S = sum s * exp(m - M) (double-float); lane 0 leaves the result in sm.red_*[0]. A NaN sum poisons
+// the result.
+__device__ __forceinline__ void combine_partial_sums(ScanSmem& sm, float m0, float h0, float l0, float m1, float h1,
+                                                     float l1) {
+  float bm = fmaxf(m0, m1);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, o));
-    double c = 0.0;
-    if (s0 != s0) c += s0;
-    else if (m0 != -INFINITY) c += s0 * (double)ex2((m0 - bm) * kLog2e);
-    if (s1 != s1) c += s1;
-    else if (m1 != -INFINITY) c += s1 * (double)ex2((m1 - bm) * kLog2e);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
-    if (lane == 0) {
-      sm.red_m[0] = bm;
-      sm.red_s[0] = c;
+  for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, o));
+  bool nan = (h0 != h0) || (h1 != h1);
+  float h = 0.0f, l = 0.0f;
+  if (!nan) {
+    if (m0 != -INFINITY) {
+      ff_scale(h0, l0, ex2((m0 - bm) * kLog2e));
+      ff_add(h, l, h0, l0);
+    }
+    if (m1 != -INFINITY) {
+      ff_scale(h1, l1, ex2((m1 - bm) * kLog2e));
+      ff_add(h, l, h1, l1);
     }
   }
-  __syncthreads();
-  M = sm.red_m[0];
-  Sum = sm.red_s[0];
-  nan = Sum != Sum;
-  __syncthreads();
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xFFFFFFFFu, h, o);
+    const float ol = __shfl_xor_sync(0xFFFFFFFFu, l, o);
+    ff_add(h, l, oh, ol);
+  }
+  nan = __any_sync(0xFFFFFFFFu, nan);
+  if ((threadIdx.x & 31) == 0) {
+    sm.red_m[0] = bm;
+    sm.red_sh[0] = nan ? __int_as_float(0x7FC00000) : h;
+    sm.red_sl[0] = nan ? 0.0f : l;
+  }
 }
 
 // ---------------------------------------------------------------- warp top-K list ----
@@ -197,13 +209,13 @@ __device__ __forceinline__ void wl_insert(uint64_t& L, uint64_t k, int K, int la
   if (lane == p) L = k;
 }
 
+// Result of a segment scan; the segment's top-K keys are left in sm.topk (descending, 0-padded).
 struct SegOut {
-  float m;        // thread 0 (softmax scans); every thread: best key value otherwise
-  double s;       // thread 0
-  int nkeys;      // every thread: keys in sm.cand[0..nkeys), descending
-  bool timed_out; // a bounded copy wait ran out
-  bool internal;  // the overflow refinement bound was hit
-  bool bad;       // non-softmax scans: a NaN or +inf was seen
+  float m;            // softmax scans: thread 0 holds the max; otherwise every thread: the best key's value
+  float s_hi, s_lo;   // softmax scans, thread 0: sum exp(x - m)
+  bool timed_out;     // a bounded copy wait ran out
+  bool internal;      // the overflow refinement bound was hit
+  bool bad;           // non-softmax scans: a NaN or +inf was seen
 };
 
 // Per-lane softmax accumulation of one value (head/tail elements).
@@ -253,6 +265,7 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
   const int n_st = (int)((wbytes + kStageBytes - 1) / kStageBytes);
 
   if (tid == 0) sm.cand = reinterpret_cast<uint64_t*>(stages);  // used only after the closing barrier
+  if (tid < kMaxK) sm.topk[tid] = 0ull;                          // filled by the closing merge
   if (lane == 0) {
     for (int st = 0; st < kWarpStages; ++st) mbar_init(&rg.bar[st], 1);
     fence_mbar_init();
@@ -562,63 +575,68 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
   if (lane == 0 && !timed_out)
     for (int st = 0; st < kWarpStages; ++st) mbar_inval(&rg.bar[st]);
 
-  SegOut out;
-  out.timed_out = __syncthreads_or(timed_out) != 0;
-  // ---- warp results -> CTA ----
-  if (lane < K) sm.cand[warp * K + lane] = lane < nl ? rg.list[lb][lane] : 0ull;
+  // ---- warp results -> CTA: one barrier, then the merge of the warp lists ----
+  // (the stage memory, which sm.cand aliases, may still be in use by other warps here)
+  if (lane < K) sm.wl[warp][lane] = lane < nl ? rg.list[lb][lane] : 0ull;
   float wm = m_t;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, o));
   float ch = 0.0f, cl = 0.0f;
-  if (SOFTMAX && (m_t != -INFINITY || s_hi != s_hi)) {
-    const float sc = (wm == m_t) ? 1.0f : ex2((m_t - wm) * kLog2e);
-    ch = s_hi * sc;
-    cl = s_lo * sc;
-  }
+  bool wnan = false;
+  if (SOFTMAX) {
+    wnan = __any_sync(0xFFFFFFFFu, s_hi != s_hi);
+    if (m_t != -INFINITY && !(s_hi != s_hi)) {
+      ch = s_hi;
+      cl = s_lo;
+      if (wm != m_t) ff_scale(ch, cl, ex2((m_t - wm) * kLog2e));
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {  // double-float warp sum (TwoSum)
-    const float oh = __shfl_xor_sync(0xFFFFFFFFu, ch, o);
-    const float ol = __shfl_xor_sync(0xFFFFFFFFu, cl, o);
-    const float sum = ch + oh;
-    const float bp = sum - ch;
-    const float err = (ch - (sum - bp)) + (oh - bp);
-    ch = sum;
-    cl = cl + ol + err;
+    for (int o = 16; o > 0; o >>= 1) {  // double-float warp sum
+      const float oh = __shfl_xor_sync(0xFFFFFFFFu, ch, o);
+      const float ol = __shfl_xor_sync(0xFFFFFFFFu, cl, o);
+      ff_add(ch, cl, oh, ol);
+    }
   }
+  const bool wbad = !SOFTMAX && __any_sync(0xFFFFFFFFu, seen_max != seen_max || seen_max == INFINITY);
   if (lane == 0) {
     sm.red_m[warp] = wm;
-    sm.red_s[warp] = (double)ch + (double)cl;
+    sm.red_sh[warp] = wnan ? __int_as_float(0x7FC00000) : ch;
+    sm.red_sl[warp] = wnan ? 0.0f : cl;
+    sm.flags[warp] |= (timed_out ? 4 : 0) | (wbad ? 8 : 0);
   }
-  out.bad = false;
-  if (!SOFTMAX) out.bad = __syncthreads_or(seen_max != seen_max || seen_max == INFINITY) != 0;
-  if (tid < kMaxK) sm.topk[tid] = 0ull;
   __syncthreads();
-  int internal = 0;
-  for (int w = 0; w < kScanWarps; ++w) internal |= sm.flags[w] & 2;
-  out.internal = internal != 0;
-  merge_sorted_lists(sm, kScanWarps, K);
-  int n = 0;
-  for (int i = 0; i < K; ++i) n += sm.topk[i] != 0ull;
-  out.nkeys = n;
-  for (int i = tid; i < K; i += blockDim.x) sm.cand[i] = sm.topk[i];
+  int fl = 0;
+#pragma unroll
+  for (int w = 0; w < kScanWarps; ++w) fl |= sm.flags[w];
+  SegOut out;
+  out.timed_out = (fl & 4) != 0;
+  out.bad = (fl & 8) != 0;
+  out.internal = (fl & 2) != 0;
+  merge_sorted_lists(sm, &sm.wl[0][0], kScanWarps, K, kMaxK);  // sm.topk was cleared at the start
   out.m = -INFINITY;
-  out.s = 0.0;
+  out.s_hi = 0.0f;
+  out.s_lo = 0.0f;
   if (SOFTMAX) {
     if (tid == 0) {
       float M = -INFINITY;
       for (int w = 0; w < kScanWarps; ++w) M = fmaxf(M, sm.red_m[w]);
-      double S = 0.0;
+      float h = 0.0f, l = 0.0f;
+      bool nan = false;
       for (int w = 0; w < kScanWarps; ++w) {
-        const double sw = sm.red_s[w];
-        if (sw != sw) S = sw;
-        else if (sm.red_m[w] != -INFINITY && S == S) S += sw * (double)ex2((sm.red_m[w] - M) * kLog2e);
+        float hh = sm.red_sh[w], ll = sm.red_sl[w];
+        if (hh != hh) nan = true;
+        else if (sm.red_m[w] != -INFINITY) {
+          ff_scale(hh, ll, ex2((sm.red_m[w] - M) * kLog2e));
+          ff_add(h, l, hh, ll);
+        }
       }
       out.m = M;
-      out.s = S;
+      out.s_hi = nan ? __int_as_float(0x7FC00000) : h;
+      out.s_lo = nan ? 0.0f : l;
     }
+  } else {
+    out.m = sm.topk[0] ? key_value(sm.topk[0]) : -INFINITY;
   }
-  __syncthreads();
-  if (!SOFTMAX) out.m = n > 0 ? key_value(sm.cand[0]) : -INFINITY;
   return out;
 }
 
@@ -719,9 +737,10 @@ __device__ void plan_rows(RowPlan& p, int B, int64_t V, int Smax, int esz, Cnt c
 }
 
 // Scans this CTA's pieces in order (all threads). row_of(b, i) gives row i of request b, or nullptr
-// when that row is not to be read (its pieces leave empty partials). When a piece completes its
-// row, finish(b, i, part, S) runs on all threads with the row's merged top-K in sm.topk and its S
-// partials at part. After a timed-out copy wait the CTA reads nothing more (empty partials), so
+// when that row is not to be read (its pieces leave empty partials); it is called when a piece
+// starts, so it may also start loads the row's finish will need. When a piece completes its row,
+// finish(b, i, st) runs on all threads with the row's merged top-K in sm.topk and its softmax
+// statistics st (max and sum for softmax passes; the best key's value otherwise). After a timed-out copy wait the CTA reads nothing more (empty partials), so
 // that every row still completes its count.
 template <typename T, bool SOFTMAX, class RowOf, class Cnt, class Finish>
 __device__ void scan_pieces(const RowPlan& p, int64_t V, int K, int B, Partial* partials, int32_t* counter,
@@ -752,29 +771,36 @@ __device__ void scan_pieces(const RowPlan& p, int64_t V, int K, int B, Partial* 
     }
     Partial* part = partials + slot;
     const T* row = row_of(b, i);
+    const bool scan = row != nullptr && !halted && e1 > e0;
     SegOut so;
-    if (row != nullptr && !halted && e1 > e0) {
+    if (scan) {
       so = scan_segment<T, SOFTMAX>(row, e0, e1, K, sm, stages, first_wait_cap, row_tau ? row_tau + j : nullptr);
     } else {
       so.m = -INFINITY;
-      so.s = 0.0;
-      so.nkeys = 0;
+      so.s_hi = so.s_lo = 0.0f;
       so.timed_out = so.internal = so.bad = false;
     }
-    for (int k = tid; k < K; k += blockDim.x) part->keys[k] = k < so.nkeys ? sm.cand[k] : 0ull;
-    if (tid == 0) {
-      part->m = so.m;
-      part->s = so.s;
-      if (so.timed_out) set_status(status, DT_DEV_TIMEOUT);
-      if (so.internal) set_status(status, DT_DEV_INTERNAL);
-      if (so.bad) set_status(status, DT_DEV_BAD_LOGITS);
+    // warp 0 publishes the piece: its keys and sums, then (after a fence) its arrival
+    if (tid < 32) {
+      if (tid < K) part->keys[tid] = scan ? sm.topk[tid] : 0ull;
+      if (tid == 0) {
+        part->m = so.m;
+        part->s_hi = so.s_hi;
+        part->s_lo = so.s_lo;
+        if (so.timed_out) set_status(status, DT_DEV_TIMEOUT);
+        if (so.internal) set_status(status, DT_DEV_INTERNAL);
+        if (so.bad) set_status(status, DT_DEV_BAD_LOGITS);
+      }
       __threadfence();
-      const int prev = atomicAdd(&counter[j], 1);
-      sm.last = (prev == c_last - c_first);
+      __syncwarp();
+      if (tid == 0) {
+        const int prev = atomicAdd(&counter[j], 1);
+        sm.last = (prev == c_last - c_first);
+      }
     }
     halted = halted || so.timed_out;
     __syncthreads();
-    if (sm.last) {  // block-uniform
+    if (sm.last) {  // block-uniform: merge the row's partials
       __threadfence();
       if (tid == 0) {
         counter[j] = 0;
@@ -783,10 +809,30 @@ __device__ void scan_pieces(const RowPlan& p, int64_t V, int K, int B, Partial* 
       const int S = c_last - c_first + 1;
       const Partial* rp = partials + row_slot0;
       for (int k = tid; k < S * K; k += blockDim.x) sm.cand[k] = __ldcg(&rp[k / K].keys[k % K]);
+      // warp 0 loads the partial sums alongside (two per lane, S <= 64)
+      float m0 = -INFINITY, h0 = 0.0f, l0 = 0.0f, m1 = -INFINITY, h1 = 0.0f, l1 = 0.0f;
+      if (SOFTMAX && tid < 32) {
+        if (tid < S) {
+          m0 = __ldcg(&rp[tid].m);
+          h0 = __ldcg(&rp[tid].s_hi);
+          l0 = __ldcg(&rp[tid].s_lo);
+        }
+        if (tid + 32 < S) {
+          m1 = __ldcg(&rp[tid + 32].m);
+          h1 = __ldcg(&rp[tid + 32].s_hi);
+          l1 = __ldcg(&rp[tid + 32].s_lo);
+        }
+      }
       if (tid < kMaxK) sm.topk[tid] = 0ull;
       __syncthreads();
-      merge_sorted_lists(sm, S, K);
-      finish(b, i, rp, S);
+      if (SOFTMAX && tid < 32) combine_partial_sums(sm, m0, h0, l0, m1, h1, l1);
+      merge_sorted_lists(sm, sm.cand, S, K, K);  // ends with a barrier, after which sm.red_*[0] is visible
+      SoftmaxStat st;
+      st.m = SOFTMAX ? sm.red_m[0] : (sm.topk[0] ? key_value(sm.topk[0]) : -INFINITY);
+      st.s_hi = SOFTMAX ? sm.red_sh[0] : 0.0f;
+      st.s_lo = SOFTMAX ? sm.red_sl[0] : 0.0f;
+      st.nan = st.s_hi != st.s_hi;
+      finish(b, i, st);
     }
     x = (j + 1) * V;
     ++j;
