@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
       ws.parent[gi] = pid;
       ws.logc[gi] = lc;
       ws.value[gi] = __fadd_rn(vh, vl);
+      __threadfence();  // the children reach L2 before this row's arrival below
     }
-    __threadfence();
     __syncthreads();
     const int active = cnt(b);
     if (tid == 0) {
@@ -188,7 +188,6 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
     }
     __syncthreads();
     if (sm.last) {  // last row of the request: order the new layer by (value desc, id asc)
-      __threadfence();
       if (tid == 0) ws.req_counter[b] = 0;
       const int n = active * a.K;
       int32_t* order = ws.layer_order + ((int64_t)b * (a.D + 1) + a.d) * a.LW;

@@ -322,7 +322,10 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
         const uint64_t k = rg.cand[q];
         bool dup = false;
 #pragma unroll
-        for (int j = 0; j < kMaxK; ++j) dup |= (j < nl) && (cur[j] == k);
+        for (int j = 0; j < kMaxK; ++j) {
+          const uint64_t v = cur[j];  // read unconditionally (in bounds), masked after
+          dup |= (j < nl) & (v == k);
+        }
         if (dup) rg.cand[q] = 0ull;
       }
       __syncwarp();
@@ -333,13 +336,21 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
       if (k == 0ull) continue;
       ++valid;
       int r = 0;
+      // loads are unconditional (every index is inside the arrays) and masked after, so that the
+      // eight of a group issue back to back
       for (int j0 = 0; j0 < nl; j0 += 8) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) r += (j0 + u < nl) && (cur[j0 + u] > k);
+        for (int u = 0; u < 8; ++u) {
+          const uint64_t v = cur[j0 + u];
+          r += (j0 + u < nl) & (v > k);
+        }
       }
       for (int j0 = 0; j0 < n; j0 += 8) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) r += (j0 + u < n) && (rg.cand[j0 + u] > k);
+        for (int u = 0; u < 8; ++u) {
+          const uint64_t v = rg.cand[j0 + u];
+          r += (j0 + u < n) & (v > k);
+        }
       }
       if (r < K) nxt[r] = k;
     }
@@ -348,7 +359,10 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
       int r = lane;
       for (int j0 = 0; j0 < n; j0 += 8) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) r += (j0 + u < n) && (rg.cand[j0 + u] > l);
+        for (int u = 0; u < 8; ++u) {
+          const uint64_t v = rg.cand[j0 + u];
+          r += (j0 + u < n) & (v > l);
+        }
       }
       if (r < K) nxt[r] = l;
     }
@@ -800,8 +814,8 @@ __device__ void scan_pieces(const RowPlan& p, int64_t V, int K, int B, Partial* 
     }
     halted = halted || so.timed_out;
     __syncthreads();
-    if (sm.last) {  // block-uniform: merge the row's partials
-      __threadfence();
+    if (sm.last) {  // block-uniform: merge the row's partials (read from L2, which the fenced
+                    // publications of every piece reached before their arrivals)
       if (tid == 0) {
         counter[j] = 0;
         if (row_tau) row_tau[j] = 0ull;  // every piece of the row has finished with it
