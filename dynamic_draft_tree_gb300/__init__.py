@@ -117,6 +117,12 @@ def dt_cast_prune(h, policy, params, out, stream=None):
     check(lib.dt_cast_prune(h.h, policy, ctypes.byref(params), ctypes.byref(out), _stream(stream)))
 
 
+def dt_cast_prune_select(h, params, out, frontier_token=None, stream=None):
+    """CAST width/depth pruning of the newest layer, then the next layer's frontier, in one launch."""
+    check(lib.dt_cast_prune_select(h.h, ctypes.byref(params), ctypes.byref(out), _ptr(frontier_token),
+                                   _stream(stream)))
+
+
 def dt_rerank(h, m, m_cap, selected, stream=None):
     ml = 0 if m is None else m.numel()
     check(lib.dt_rerank(h.h, _ptr(m), ml, m_cap, _ptr(selected), _stream(stream)))

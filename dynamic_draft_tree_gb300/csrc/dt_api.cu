@@ -269,6 +269,24 @@ int dt_cast_prune(dt_handle* h, int32_t policy, const dt_prune_params* p, const 
   return DT_OK;
 }
 
+int dt_cast_prune_select(dt_handle* h, const dt_prune_params* p, const dt_prune_out* out, int32_t* frontier_token,
+                         cudaStream_t s) {
+  if (!h || !p || !out) return fail(DT_ERR_ARG, "dt_cast_prune_select: null argument");
+  if (h->B < 1) return fail(DT_ERR_ARG, "dt_cast_prune_select: no tree (call dt_tree_reset)");
+  if (!p->S_T || !p->S_D) return fail(DT_ERR_ARG, "cost tables missing");
+  if (p->M_rows < 1 || p->N_cols < 1) return fail(DT_ERR_ARG, "table shape must be positive");
+  if (!(p->L > 0.0)) return fail(DT_ERR_ARG, "L must be > 0");
+  if (p->n0 < 0) return fail(DT_ERR_ARG, "n0 must be >= 0");
+  if (h->depth < 1) return fail(DT_ERR_ARG, "no layer to prune");
+  if (p->width_cap < 1 || p->width_cap > h->cfg.W || p->width_cap > p->N_cols)
+    return fail(DT_ERR_ARG, "width_cap must be in [1, min(W, N_cols)]");
+  if (p->R < 1 || p->R > dt::kMaxFifo) return fail(DT_ERR_ARG, "R must be in [1, 16]");
+  if (!out->width || !out->stop) return fail(DT_ERR_ARG, "width and stop outputs required");
+  cudaError_t e = dt::launch_cast_prune_select(h, p, out, frontier_token, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dt_cast_prune_select");
+  return DT_OK;
+}
+
 int dt_rerank(dt_handle* h, const int32_t* m, int32_t m_len, int32_t m_cap, int32_t* selected, cudaStream_t s) {
   if (!h || !selected) return fail(DT_ERR_ARG, "dt_rerank: null argument");
   if (h->B < 1) return fail(DT_ERR_ARG, "dt_rerank: no tree (call dt_tree_reset)");

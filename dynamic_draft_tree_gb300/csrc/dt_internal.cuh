@@ -126,6 +126,8 @@ cudaError_t launch_cast_prune(dt_handle* h, int policy, const dt_prune_params* p
                               cudaStream_t s);
 cudaError_t launch_rerank(dt_handle* h, const int32_t* m, int m_len, int m_cap, int32_t* selected,
                           cudaStream_t s);
+cudaError_t launch_cast_prune_select(dt_handle* h, const dt_prune_params* p, const dt_prune_out* out,
+                                     int32_t* frontier_token, cudaStream_t s);
 cudaError_t launch_graft_retrieve(dt_handle* h, const int32_t* M, const int32_t* m_draft, int K_total,
                                   const dt_template* tpl, int R_cap, int32_t* ret_token,
                                   int32_t* ret_parent, int32_t* ret_count, cudaStream_t s);
@@ -201,6 +203,35 @@ __device__ __forceinline__ void ff_add(float& h, float& l, float h2, float l2) {
   e = __fadd_rn(e, __fadd_rn(l, l2));
   h = __fadd_rn(s, e);
   l = __fsub_rn(e, __fsub_rn(h, s));
+}
+
+// Frontier of the next layer for request b (one warp): the first w nodes of layer d in (value desc,
+// id asc) order (layer_order), slotted in ascending id; w = min(w_req, W, nodes in the layer).
+__device__ __forceinline__ void select_frontier_warp(const Workspace& ws, int b, int N, int W, int LW, int D, int d,
+                                                     int w_req, int32_t* __restrict__ ftok) {
+  const int lane = threadIdx.x & 31;
+  const int avail = ws.layer_count[(int64_t)b * (D + 1) + d];
+  const int w = max(0, min(min(w_req, W), avail));
+  int id = -1;
+  if (lane < w) id = ws.layer_order[((int64_t)b * (D + 1) + d) * LW + lane];
+  int slot = 0;  // rank of my id among the chosen ids
+  for (int j = 0; j < w; ++j) {
+    const int o = __shfl_sync(0xFFFFFFFFu, id, j);
+    slot += (o < id);
+  }
+  if (lane < W) {
+    ws.frontier[(int64_t)b * W + lane] = -1;
+    ws.frontier_val[(int64_t)b * W + lane] = -INFINITY;
+    if (ftok) ftok[(int64_t)b * W + lane] = -1;
+  }
+  __syncwarp();
+  if (lane < w) {
+    const int64_t gi = (int64_t)b * N + id;
+    ws.frontier[(int64_t)b * W + slot] = id;
+    ws.frontier_val[(int64_t)b * W + slot] = ws.value[gi];
+    if (ftok) ftok[(int64_t)b * W + slot] = ws.token[gi];
+  }
+  if (lane == 0) ws.frontier_count[b] = w;
 }
 
 // Programmatic dependent launch. Every kernel of the path starts with pdl_begin(): it waits until the

@@ -215,6 +215,9 @@ struct PruneArgs {
   dt_prune_params p;
   dt_prune_out out;
   int B, N, LW, D, d, policy;
+  int W;          // frontier width limit
+  int select;     // width/depth only: also select the next layer's frontier
+  int32_t* ftok;  // frontier tokens [B][W] of that selection, or null
 };
 
 // CAST width + depth after layer d (1 CTA). The CAST state is copied to shared memory; every global
@@ -227,7 +230,7 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
   __shared__ double u[kMaxW + 2];
   __shared__ uint64_t cimg[kMaxW + 2], qimg[kMaxW + 2];
   __shared__ CastState cs;
-  __shared__ int maxcand, s_grow, s_k0;
+  __shared__ int maxcand, s_grow, s_k0, s_width;
   const Workspace& ws = a.ws;
   const int tid = threadIdx.x;
   if (tid == 0) {
@@ -278,9 +281,15 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
     }
     a.out.width[0] = n;
     s_grow = grow ? 1 : 0;
+    s_width = n;
   }
   __syncthreads();
   for (int b = tid; b < a.B; b += blockDim.x) a.out.stop[b] = s_grow ? 0 : 1;
+  if (a.select) {  // the next layer's frontier, as dt_select_frontier(width, stop) would choose it
+    const int w_req = s_grow ? s_width : 0;
+    for (int b = tid >> 5; b < a.B; b += blockDim.x >> 5)
+      select_frontier_warp(ws, b, a.N, a.W, a.LW, a.D, a.d, w_req, a.ftok);
+  }
 }
 
 // CAST verify count from the per-request sorted linear values (1 CTA).
@@ -379,6 +388,9 @@ cudaError_t launch_cast_prune(dt_handle* h, int policy, const dt_prune_params* p
   a.D = h->cfg.D_max;
   a.d = h->depth;
   a.policy = policy;
+  a.W = h->cfg.W;
+  a.select = 0;
+  a.ftok = nullptr;
   if (policy == DT_POLICY_CAST_WIDTH_DEPTH) {
     launch_k(cast_width_depth_kernel, dim3(1), dim3(kPruneThreads), 0, s, a);
     return cudaGetLastError();
@@ -390,6 +402,25 @@ cudaError_t launch_cast_prune(dt_handle* h, int policy, const dt_prune_params* p
     return cudaGetLastError();
   }
   launch_k(graft_checkpoint_kernel, dim3((h->B + 127) / 128), dim3(128), 0, s, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast_prune_select(dt_handle* h, const dt_prune_params* p, const dt_prune_out* out,
+                                     int32_t* frontier_token, cudaStream_t s) {
+  PruneArgs a;
+  a.ws = h->ws;
+  a.p = *p;
+  a.out = *out;
+  a.B = h->B;
+  a.N = h->N;
+  a.LW = h->LW;
+  a.D = h->cfg.D_max;
+  a.d = h->depth;
+  a.policy = DT_POLICY_CAST_WIDTH_DEPTH;
+  a.W = h->cfg.W;
+  a.select = 1;
+  a.ftok = frontier_token;
+  launch_k(cast_width_depth_kernel, dim3(1), dim3(kPruneThreads), 0, s, a);
   return cudaGetLastError();
 }
 

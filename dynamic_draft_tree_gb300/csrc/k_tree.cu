@@ -71,33 +71,10 @@ __global__ void select_frontier_kernel(Workspace ws, int B, int N, int K, int W,
   pdl_begin();
   const int warps = blockDim.x >> 5;
   const int b = blockIdx.x * warps + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
   if (b >= B) return;
   int w = width ? width[width_len == 1 ? 0 : b] : W;
   if (stop && stop[b]) w = 0;
-  const int avail = ws.layer_count[(int64_t)b * (D + 1) + d];
-  w = max(0, min(min(w, W), avail));
-  int id = -1;
-  if (lane < w) id = ws.layer_order[((int64_t)b * (D + 1) + d) * LW + lane];
-  // slot = rank of my id among the chosen ids
-  int slot = 0;
-  for (int j = 0; j < w; ++j) {
-    const int o = __shfl_sync(0xFFFFFFFFu, id, j);
-    slot += (o < id);
-  }
-  if (lane < W) {
-    ws.frontier[(int64_t)b * W + lane] = -1;
-    ws.frontier_val[(int64_t)b * W + lane] = -INFINITY;
-    if (ftok) ftok[(int64_t)b * W + lane] = -1;
-  }
-  __syncwarp();
-  if (lane < w) {
-    const int64_t gi = (int64_t)b * N + id;
-    ws.frontier[(int64_t)b * W + slot] = id;
-    ws.frontier_val[(int64_t)b * W + slot] = ws.value[gi];
-    if (ftok) ftok[(int64_t)b * W + slot] = ws.token[gi];
-  }
-  if (lane == 0) ws.frontier_count[b] = w;
+  select_frontier_warp(ws, b, N, W, LW, D, d, w, ftok);
 }
 
 struct ExpandArgs {

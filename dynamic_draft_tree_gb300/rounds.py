@@ -4,6 +4,7 @@ Call order (EAGLE-2 page Â§"ä¸€æ®µæ›´è´´è¿‘å®žçŽ°çš„æµç¨‹"; CAST page Â§å…³é”®è
 steps (1)-(3)):
 
   reset -> [frontier -> draft rows -> expand -> prune]* -> (verify count) -> rerank
+  (CAST prunes a layer and chooses the next frontier in one call)
   -> (retrieve) -> meta -> target rows -> verify -> (M refresh)
 
 The draft and target model forwards are outside the library: ``draft_rows(d,
@@ -16,7 +17,7 @@ a round, so a round can be captured in a CUDA graph.
 import torch
 
 from . import (Handle, Meta, Template, make_prune_params, make_prune_out, dt_tree_reset, dt_select_frontier,
-               dt_expand_layer, dt_cast_prune, dt_rerank, dt_graft_retrieve, dt_build_tree_meta, dt_verify,
+               dt_expand_layer, dt_cast_prune, dt_cast_prune_select, dt_rerank, dt_graft_retrieve, dt_build_tree_meta, dt_verify,
                dt_adj_update, DT_GREEDY, DT_SAMPLE, DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY,
                DT_POLICY_GRAFT_CHECKPOINT)
 
@@ -84,7 +85,8 @@ class RoundRunner:
         dt_tree_reset(h, roots)
         for d in range(1, self.D + 1):
             if d > 1:
-                dt_select_frontier(h, self.width, self.stop, self.frontier_token)
+                if pol != "cast":  # CAST selected it together with the pruning of layer d - 1
+                    dt_select_frontier(h, self.width, self.stop, self.frontier_token)
                 F = self.k
             else:
                 self.frontier_token.fill_(-1)
@@ -94,7 +96,10 @@ class RoundRunner:
             if after_expand is not None:
                 after_expand()
             if pol == "cast":
-                dt_cast_prune(h, DT_POLICY_CAST_WIDTH_DEPTH, self.params, self.prune_out)
+                if d < self.D:  # prune layer d and choose the frontier of layer d + 1 in one launch
+                    dt_cast_prune_select(h, self.params, self.prune_out, self.frontier_token)
+                else:
+                    dt_cast_prune(h, DT_POLICY_CAST_WIDTH_DEPTH, self.params, self.prune_out)
             elif pol == "graft":
                 dt_cast_prune(h, DT_POLICY_GRAFT_CHECKPOINT, self.params, self.prune_out)
         if pol == "cast":

@@ -204,6 +204,13 @@ int dt_expand_layer(dt_handle* h, const void* logits, int64_t ld, int32_t F, cud
 int dt_cast_prune(dt_handle* h, int32_t policy, const dt_prune_params* p, const dt_prune_out* out,
                   cudaStream_t s);
 
+/* a3 + a2 in one launch: exactly dt_cast_prune(h, DT_POLICY_CAST_WIDTH_DEPTH, p, out, s) followed by
+ * dt_select_frontier(h, out->width, 1, out->stop, frontier_token, s): CAST width and grow/stop after
+ * the newest layer, then the next layer's frontier (none for stopped requests). One kernel instead of
+ * two dependent ones between the draft forwards. */
+int dt_cast_prune_select(dt_handle* h, const dt_prune_params* p, const dt_prune_out* out, int32_t* frontier_token,
+                         cudaStream_t s);
+
 /* a5 (EAGLE-2 §重排阶段): top-m_b valid non-root nodes in (value desc, depth asc, id asc) order,
  * written in ascending id. m: device [m_len] (m_len 1 = batch-wide, or B), NULL = m_cap.
  * selected: device [B][m_cap], -1 padded. */
