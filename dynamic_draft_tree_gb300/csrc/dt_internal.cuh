@@ -206,14 +206,11 @@ __device__ __forceinline__ void ff_add(float& h, float& l, float h2, float l2) {
 }
 
 // Frontier of the next layer for request b (one warp): the first w nodes of layer d in (value desc,
-// id asc) order (layer_order), slotted in ascending id; w = min(w_req, W, nodes in the layer).
-__device__ __forceinline__ void select_frontier_warp(const Workspace& ws, int b, int N, int W, int LW, int D, int d,
-                                                     int w_req, int32_t* __restrict__ ftok) {
+// id asc) order (layer_order), slotted in ascending id. Lane l < w holds the l-th node (id, token,
+// value); select_frontier_write slots and stores them.
+__device__ __forceinline__ void select_frontier_write(const Workspace& ws, int b, int W, int w, int id, int tok,
+                                                      float val, int32_t* __restrict__ ftok) {
   const int lane = threadIdx.x & 31;
-  const int avail = ws.layer_count[(int64_t)b * (D + 1) + d];
-  const int w = max(0, min(min(w_req, W), avail));
-  int id = -1;
-  if (lane < w) id = ws.layer_order[((int64_t)b * (D + 1) + d) * LW + lane];
   int slot = 0;  // rank of my id among the chosen ids
   for (int j = 0; j < w; ++j) {
     const int o = __shfl_sync(0xFFFFFFFFu, id, j);
@@ -226,12 +223,34 @@ __device__ __forceinline__ void select_frontier_warp(const Workspace& ws, int b,
   }
   __syncwarp();
   if (lane < w) {
-    const int64_t gi = (int64_t)b * N + id;
     ws.frontier[(int64_t)b * W + slot] = id;
-    ws.frontier_val[(int64_t)b * W + slot] = ws.value[gi];
-    if (ftok) ftok[(int64_t)b * W + slot] = ws.token[gi];
+    ws.frontier_val[(int64_t)b * W + slot] = val;
+    if (ftok) ftok[(int64_t)b * W + slot] = tok;
   }
   if (lane == 0) ws.frontier_count[b] = w;
+}
+// Loads the candidates of request b's frontier (the first min(W, nodes) nodes of layer d) into lanes.
+__device__ __forceinline__ int frontier_candidates(const Workspace& ws, int b, int N, int W, int LW, int D, int d,
+                                                   int& id, int& tok, float& val) {
+  const int lane = threadIdx.x & 31;
+  const int64_t lb = (int64_t)b * (D + 1) + d;
+  const int avail = ws.layer_count[lb];
+  id = lane < W ? ws.layer_order[lb * LW + lane] : -1;  // read with the count: -1 past it
+  tok = -1;
+  val = -INFINITY;
+  if (lane < min(avail, W) && id >= 0) {
+    const int64_t gi = (int64_t)b * N + id;
+    tok = ws.token[gi];
+    val = ws.value[gi];
+  }
+  return avail;
+}
+__device__ __forceinline__ void select_frontier_warp(const Workspace& ws, int b, int N, int W, int LW, int D, int d,
+                                                     int w_req, int32_t* __restrict__ ftok) {
+  int id, tok;
+  float val;
+  const int avail = frontier_candidates(ws, b, N, W, LW, D, d, id, tok, val);
+  select_frontier_write(ws, b, W, max(0, min(min(w_req, W), avail)), id, tok, val, ftok);
 }
 
 // Programmatic dependent launch. Every kernel of the path starts with pdl_begin(): it waits until the

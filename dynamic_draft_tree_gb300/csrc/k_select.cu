@@ -232,28 +232,34 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
   __shared__ CastState cs;
   __shared__ int maxcand, s_grow, s_k0, s_width;
   const Workspace& ws = a.ws;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  // one round of independent loads: the CAST state, the layer sizes, the layer's values (inside
+  // batch_items) and, for the frontier that follows, each request's candidate nodes
   if (tid == 0) {
     maxcand = 0;
     cs = *ws.cast;
   }
+  int f_id = -1, f_tok = -1, f_avail = 0;
+  float f_val = -INFINITY;
+  const bool f_pref = a.select && a.B <= (int)(blockDim.x >> 5);
+  if (f_pref && warp < a.B) f_avail = frontier_candidates(ws, warp, a.N, a.W, a.LW, a.D, a.d, f_id, f_tok, f_val);
   __syncthreads();
   for (int b = tid; b < a.B; b += blockDim.x) atomicMax(&maxcand, ws.layer_count[(int64_t)b * (a.D + 1) + a.d]);
-  // normalised draft cost of k frontier nodes at the current context: c_k = S_D[row][k-1] / S_T[row][0]
-  const int row = table_row((double)(a.p.n0 + cs.ctx_sum), a.p.L, a.p.M_rows);
   const int wcap = min(a.p.width_cap, a.LW);
-  for (int k = 1 + tid; k <= wcap; k += blockDim.x)
-    cost[k] = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
-  __syncthreads();
-  const int cap = min(a.p.width_cap, maxcand);
   // items[s] = (1/B) sum_b exp(value of the s-th node of b's layer), missing nodes count 0
-  batch_items(items, part, cap, a.B, [&](int b, int s) {
+  batch_items(items, part, wcap, a.B, [&](int b, int s) {
     const int64_t lb = (int64_t)b * (a.D + 1) + a.d;
     const int cnt = ws.layer_count[lb];
     const int id = ws.layer_order[lb * a.LW + s];  // read with the count: -1 past it
     if (s >= cnt || id < 0) return 0.0;
     return (double)expf(ws.value[(int64_t)b * a.N + id]);
   });
+  // normalised draft cost of k frontier nodes at the current context: c_k = S_D[row][k-1] / S_T[row][0]
+  const int row = table_row((double)(a.p.n0 + cs.ctx_sum), a.p.L, a.p.M_rows);
+  for (int k = 1 + tid; k <= wcap; k += blockDim.x)
+    cost[k] = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
+  __syncthreads();
+  const int cap = min(a.p.width_cap, maxcand);
   int n = 0;
   if (cap > 0) n = selection_rule(items, cost, a.p.C1, cap, u, cimg, qimg, &s_k0);
   if (tid == 0) {
@@ -287,8 +293,13 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
   for (int b = tid; b < a.B; b += blockDim.x) a.out.stop[b] = s_grow ? 0 : 1;
   if (a.select) {  // the next layer's frontier, as dt_select_frontier(width, stop) would choose it
     const int w_req = s_grow ? s_width : 0;
-    for (int b = tid >> 5; b < a.B; b += blockDim.x >> 5)
-      select_frontier_warp(ws, b, a.N, a.W, a.LW, a.D, a.d, w_req, a.ftok);
+    if (f_pref) {
+      if (warp < a.B)
+        select_frontier_write(ws, warp, a.W, max(0, min(min(w_req, a.W), f_avail)), f_id, f_tok, f_val, a.ftok);
+    } else {
+      for (int b = warp; b < a.B; b += blockDim.x >> 5)
+        select_frontier_warp(ws, b, a.N, a.W, a.LW, a.D, a.d, w_req, a.ftok);
+    }
   }
 }
 
