@@ -296,7 +296,7 @@ def run_ours(args):
                 "bytes_per_launch": bpl, "avg_launch_us": us}
     launches_per_round = 1 + (D - 1 if w["policy"] != "cast" else 0) + D + \
         (D if w["policy"] in ("cast", "graft") else 0) + \
-        (2 if w["policy"] == "cast" else 0) + 1 + 1 + (3 if w["T"] == 1 else 2) + \
+        (2 if w["policy"] == "cast" else 1) + 1 + (3 if w["T"] == 1 else 2) + \
         (2 if w["policy"] == "graft" else 0)
 
     # ---- end to end through the public API with host buffers ----

@@ -123,6 +123,12 @@ def dt_cast_prune_select(h, params, out, frontier_token=None, stream=None):
                                    _stream(stream)))
 
 
+def dt_cast_verify_rerank(h, params, out, selected, stream=None):
+    """CAST verify count, then the rerank to that count (selected [B][m_cap]), in two launches."""
+    check(lib.dt_cast_verify_rerank(h.h, ctypes.byref(params), ctypes.byref(out), _ptr(selected),
+                                    _stream(stream)))
+
+
 def dt_rerank(h, m, m_cap, selected, stream=None):
     ml = 0 if m is None else m.numel()
     check(lib.dt_rerank(h.h, _ptr(m), ml, m_cap, _ptr(selected), _stream(stream)))

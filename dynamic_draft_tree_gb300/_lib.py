@@ -20,7 +20,8 @@ DT_FLAG_TEST_TIMEOUT = 1
 EXPORTS = ["dt_last_error_string", "dt_create", "dt_destroy", "dt_get_tree", "dt_get_status",
            "dt_clear_status", "dt_tree_reset", "dt_select_frontier", "dt_expand_layer", "dt_cast_prune",
            "dt_rerank", "dt_graft_retrieve", "dt_build_tree_meta", "dt_verify", "dt_adj_update",
-           "dt_row_topk_static", "dt_cast_prune_select"]
+           "dt_row_topk_static", "dt_cast_prune_select",
+           "dt_cast_verify_rerank"]
 
 c_i32p = ctypes.c_void_p
 vp = ctypes.c_void_p
@@ -90,6 +91,7 @@ def _load():
                        ctypes.c_uint64, vp, vp, vp, vp, vp], I),
         "dt_adj_update": ([vp, vp, ctypes.POINTER(DtTreeMeta), vp, vp], I),
         "dt_cast_prune_select": ([vp, ctypes.POINTER(DtPruneParams), ctypes.POINTER(DtPruneOut), vp, vp], I),
+        "dt_cast_verify_rerank": ([vp, ctypes.POINTER(DtPruneParams), ctypes.POINTER(DtPruneOut), vp, vp], I),
         "dt_row_topk_static": ([vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                 vp, vp, vp, vp], I),
     }

@@ -102,6 +102,7 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   const size_t o_rstat = cv.take<dt::RowStat>((size_t)c.B_max * c.P_max);
   const size_t o_slin = cv.take<double>((size_t)c.B_max * c.P_max);
   const size_t o_scnt = cv.take<int32_t>(c.B_max);
+  const size_t o_sids = cv.take<int32_t>((size_t)c.B_max * c.P_max);
   const size_t o_cast = cv.take<dt::CastState>(1);
   const size_t o_walk = cv.take<dt::WalkState>(c.B_max);
   const size_t o_bkey = cv.take<unsigned long long>(c.B_max);
@@ -142,6 +143,7 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   w.row_stats = reinterpret_cast<dt::RowStat*>(bp + o_rstat);
   w.sorted_lin = reinterpret_cast<double*>(bp + o_slin);
   w.sorted_cnt = reinterpret_cast<int32_t*>(bp + o_scnt);
+  w.sorted_ids = reinterpret_cast<int32_t*>(bp + o_sids);
   w.cast = reinterpret_cast<dt::CastState*>(bp + o_cast);
   w.walk = reinterpret_cast<dt::WalkState*>(bp + o_walk);
   w.bonus_key = reinterpret_cast<unsigned long long*>(bp + o_bkey);
@@ -266,6 +268,22 @@ int dt_cast_prune(dt_handle* h, int32_t policy, const dt_prune_params* p, const 
   }
   cudaError_t e = dt::launch_cast_prune(h, policy, p, out, s);
   if (e != cudaSuccess) return cuda_fail(e, "dt_cast_prune");
+  return DT_OK;
+}
+
+int dt_cast_verify_rerank(dt_handle* h, const dt_prune_params* p, const dt_prune_out* out, int32_t* selected,
+                          cudaStream_t s) {
+  if (!h || !p || !out || !selected) return fail(DT_ERR_ARG, "dt_cast_verify_rerank: null argument");
+  if (h->B < 1) return fail(DT_ERR_ARG, "dt_cast_verify_rerank: no tree (call dt_tree_reset)");
+  if (!p->S_T) return fail(DT_ERR_ARG, "cost tables missing");
+  if (p->M_rows < 1 || p->N_cols < 1) return fail(DT_ERR_ARG, "table shape must be positive");
+  if (!(p->L > 0.0)) return fail(DT_ERR_ARG, "L must be > 0");
+  if (p->n0 < 0) return fail(DT_ERR_ARG, "n0 must be >= 0");
+  if (p->m_cap < 1 || p->m_cap > p->N_cols || p->m_cap > h->cfg.P_max - 1)
+    return fail(DT_ERR_ARG, "m_cap must be in [1, min(N_cols, P_max-1)]");
+  if (!out->m) return fail(DT_ERR_ARG, "m output required");
+  cudaError_t e = dt::launch_cast_verify_rerank(h, p, out, selected, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dt_cast_verify_rerank");
   return DT_OK;
 }
 

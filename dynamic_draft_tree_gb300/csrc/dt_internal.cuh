@@ -78,6 +78,7 @@ struct Workspace {
   // selection scratch
   double* sorted_lin;    // [B_max][P_max] linear values of each request's top nodes
   int32_t* sorted_cnt;   // [B_max]
+  int32_t* sorted_ids;   // [B_max][P_max] ids of each request's top nodes in rank order
   CastState* cast;
   WalkState* walk;
   unsigned long long* bonus_key;  // [B_max]
@@ -126,6 +127,8 @@ cudaError_t launch_cast_prune(dt_handle* h, int policy, const dt_prune_params* p
                               cudaStream_t s);
 cudaError_t launch_rerank(dt_handle* h, const int32_t* m, int m_len, int m_cap, int32_t* selected,
                           cudaStream_t s);
+cudaError_t launch_cast_verify_rerank(dt_handle* h, const dt_prune_params* p, const dt_prune_out* out,
+                                     int32_t* selected, cudaStream_t s);
 cudaError_t launch_cast_prune_select(dt_handle* h, const dt_prune_params* p, const dt_prune_out* out,
                                      int32_t* frontier_token, cudaStream_t s);
 cudaError_t launch_graft_retrieve(dt_handle* h, const int32_t* M, const int32_t* m_draft, int K_total,

@@ -92,8 +92,12 @@ __global__ void __launch_bounds__(kSortThreads) sort_nodes_kernel(SortArgs a) {
       rank += lo;
     }
     if (rank >= limit) continue;
-    if (a.mode == 0) sel[rank] = (int32_t)key_id(k);
-    else lin[rank] = (double)expf(key_value(k));
+    if (a.mode == 0) {
+      sel[rank] = (int32_t)key_id(k);
+    } else {
+      lin[rank] = (double)expf(key_value(k));
+      ws.sorted_ids[(int64_t)b * a.m_cap + rank] = (int32_t)key_id(k);
+    }
   }
   if (a.mode == 0) {
     __syncthreads();
@@ -218,6 +222,7 @@ struct PruneArgs {
   int W;          // frontier width limit
   int select;     // width/depth only: also select the next layer's frontier
   int32_t* ftok;  // frontier tokens [B][W] of that selection, or null
+  int32_t* sel;   // verify count only: also write the rerank [B][m_cap], or null
 };
 
 // CAST width + depth after layer d (1 CTA). The CAST state is copied to shared memory; every global
@@ -328,6 +333,24 @@ __global__ void __launch_bounds__(kPruneThreads) cast_verify_kernel(PruneArgs a)
   int m = 0;
   if (cap > 0) m = selection_rule(items, cost, a.p.C3, cap, u, cimg, qimg, &s_k0);
   if (tid == 0) a.out.m[0] = m;
+  if (a.sel) {  // the rerank, as dt_rerank(m) would write it: each request's top-m ids, ascending
+    const int lane = tid & 31;
+    for (int b = tid >> 5; b < a.B; b += blockDim.x >> 5) {
+      const int mb = max(0, min(min(m, a.p.m_cap), ws.sorted_cnt[b]));
+      const int32_t* ids = ws.sorted_ids + (int64_t)b * a.p.m_cap;
+      int32_t* out = a.sel + (int64_t)b * a.p.m_cap;
+      for (int i = lane; i < a.p.m_cap; i += 32) {
+        if (i < mb) {
+          const int32_t id = ids[i];
+          int r = 0;
+          for (int j = 0; j < mb; ++j) r += ids[j] < id;
+          out[r] = id;
+        } else {
+          out[i] = -1;
+        }
+      }
+    }
+  }
 }
 
 // Graft checkpoint after layer d: one thread per request.
@@ -402,6 +425,7 @@ cudaError_t launch_cast_prune(dt_handle* h, int policy, const dt_prune_params* p
   a.W = h->cfg.W;
   a.select = 0;
   a.ftok = nullptr;
+  a.sel = nullptr;
   if (policy == DT_POLICY_CAST_WIDTH_DEPTH) {
     launch_k(cast_width_depth_kernel, dim3(1), dim3(kPruneThreads), 0, s, a);
     return cudaGetLastError();
@@ -431,7 +455,30 @@ cudaError_t launch_cast_prune_select(dt_handle* h, const dt_prune_params* p, con
   a.W = h->cfg.W;
   a.select = 1;
   a.ftok = frontier_token;
+  a.sel = nullptr;
   launch_k(cast_width_depth_kernel, dim3(1), dim3(kPruneThreads), 0, s, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast_verify_rerank(dt_handle* h, const dt_prune_params* p, const dt_prune_out* out,
+                                     int32_t* selected, cudaStream_t s) {
+  cudaError_t e = launch_sort(h, 1, nullptr, 1, p->m_cap, nullptr, s);
+  if (e != cudaSuccess) return e;
+  PruneArgs a;
+  a.ws = h->ws;
+  a.p = *p;
+  a.out = *out;
+  a.B = h->B;
+  a.N = h->N;
+  a.LW = h->LW;
+  a.D = h->cfg.D_max;
+  a.d = h->depth;
+  a.policy = DT_POLICY_CAST_VERIFY;
+  a.W = h->cfg.W;
+  a.select = 0;
+  a.ftok = nullptr;
+  a.sel = selected;
+  launch_k(cast_verify_kernel, dim3(1), dim3(kPruneThreads), 0, s, a);
   return cudaGetLastError();
 }
 

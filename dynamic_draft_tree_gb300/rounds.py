@@ -4,7 +4,7 @@ Call order (EAGLE-2 page Â§"ä¸€æ®µæ›´è´´è¿‘å®žçŽ°çš„æµç¨‹"; CAST page Â§å…³é”®è
 steps (1)-(3)):
 
   reset -> [frontier -> draft rows -> expand -> prune]* -> (verify count) -> rerank
-  (CAST prunes a layer and chooses the next frontier in one call)
+  (CAST prunes a layer and chooses the next frontier in one call, and reranks with the verify count)
   -> (retrieve) -> meta -> target rows -> verify -> (M refresh)
 
 The draft and target model forwards are outside the library: ``draft_rows(d,
@@ -17,7 +17,7 @@ a round, so a round can be captured in a CUDA graph.
 import torch
 
 from . import (Handle, Meta, Template, make_prune_params, make_prune_out, dt_tree_reset, dt_select_frontier,
-               dt_expand_layer, dt_cast_prune, dt_cast_prune_select, dt_rerank, dt_graft_retrieve, dt_build_tree_meta, dt_verify,
+               dt_expand_layer, dt_cast_prune, dt_cast_prune_select, dt_cast_verify_rerank, dt_rerank, dt_graft_retrieve, dt_build_tree_meta, dt_verify,
                dt_adj_update, DT_GREEDY, DT_SAMPLE, DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY,
                DT_POLICY_GRAFT_CHECKPOINT)
 
@@ -102,9 +102,10 @@ class RoundRunner:
                     dt_cast_prune(h, DT_POLICY_CAST_WIDTH_DEPTH, self.params, self.prune_out)
             elif pol == "graft":
                 dt_cast_prune(h, DT_POLICY_GRAFT_CHECKPOINT, self.params, self.prune_out)
-        if pol == "cast":
-            dt_cast_prune(h, DT_POLICY_CAST_VERIFY, self.params, self.verify_out)
-        dt_rerank(h, self.m_dev, self.m_cap, self.selected)
+        if pol == "cast":  # verify count and the rerank to it
+            dt_cast_verify_rerank(h, self.params, self.verify_out, self.selected)
+        else:
+            dt_rerank(h, self.m_dev, self.m_cap, self.selected)
         if pol == "graft":
             dt_graft_retrieve(h, M, self.m_dev, self.graft["K_total"], self.template, self.R_cap, self.ret_token,
                               self.ret_parent, self.ret_count)

@@ -211,6 +211,12 @@ int dt_cast_prune(dt_handle* h, int32_t policy, const dt_prune_params* p, const 
 int dt_cast_prune_select(dt_handle* h, const dt_prune_params* p, const dt_prune_out* out, int32_t* frontier_token,
                          cudaStream_t s);
 
+/* a3 (verify count) + a5 in two launches instead of three: exactly
+ * dt_cast_prune(h, DT_POLICY_CAST_VERIFY, p, out, s) followed by
+ * dt_rerank(h, out->m, 1, p->m_cap, selected, s). selected: device [B][p->m_cap]. */
+int dt_cast_verify_rerank(dt_handle* h, const dt_prune_params* p, const dt_prune_out* out, int32_t* selected,
+                          cudaStream_t s);
+
 /* a5 (EAGLE-2 §重排阶段): top-m_b valid non-root nodes in (value desc, depth asc, id asc) order,
  * written in ascending id. m: device [m_len] (m_len 1 = batch-wide, or B), NULL = m_cap.
  * selected: device [B][m_cap], -1 padded. */
