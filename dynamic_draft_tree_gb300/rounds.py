@@ -26,7 +26,10 @@ class RoundRunner:
     """Device buffers and call sequence of one round for a policy ('eagle' | 'cast' | 'graft')."""
 
     def __init__(self, policy, B, V, K, k, D, P, D_path, m, dtype, T=0, cast=None, cast_tables=None,
-                 graft=None, template=None, flags=0, device="cuda"):
+                 graft=None, template=None, flags=0, device="cuda", fused=True):
+        """``fused`` (CAST): prune + frontier and verify count + rerank as single calls
+        (dt_cast_prune_select, dt_cast_verify_rerank) instead of the separate calls."""
+        self.fused = fused
         self.policy, self.B, self.V, self.K, self.k, self.D = policy, B, V, K, k, D
         self.P, self.D_path, self.T = P, D_path, T
         self.h = Handle(B, V, K, k, D, P, dtype, flags)
@@ -85,7 +88,7 @@ class RoundRunner:
         dt_tree_reset(h, roots)
         for d in range(1, self.D + 1):
             if d > 1:
-                if pol != "cast":  # CAST selected it together with the pruning of layer d - 1
+                if pol != "cast" or not self.fused:  # fused CAST chose it when pruning layer d - 1
                     dt_select_frontier(h, self.width, self.stop, self.frontier_token)
                 F = self.k
             else:
@@ -96,15 +99,17 @@ class RoundRunner:
             if after_expand is not None:
                 after_expand()
             if pol == "cast":
-                if d < self.D:  # prune layer d and choose the frontier of layer d + 1 in one launch
+                if d < self.D and self.fused:  # prune layer d and choose the frontier of layer d + 1
                     dt_cast_prune_select(h, self.params, self.prune_out, self.frontier_token)
                 else:
                     dt_cast_prune(h, DT_POLICY_CAST_WIDTH_DEPTH, self.params, self.prune_out)
             elif pol == "graft":
                 dt_cast_prune(h, DT_POLICY_GRAFT_CHECKPOINT, self.params, self.prune_out)
-        if pol == "cast":  # verify count and the rerank to it
+        if pol == "cast" and self.fused:  # verify count and the rerank to it
             dt_cast_verify_rerank(h, self.params, self.verify_out, self.selected)
         else:
+            if pol == "cast":
+                dt_cast_prune(h, DT_POLICY_CAST_VERIFY, self.params, self.verify_out)
             dt_rerank(h, self.m_dev, self.m_cap, self.selected)
         if pol == "graft":
             dt_graft_retrieve(h, M, self.m_dev, self.graft["K_total"], self.template, self.R_cap, self.ret_token,

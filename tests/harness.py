@@ -132,7 +132,7 @@ def oracle_round(w, rnd, roots=None, M=None, max_attempts=16):
 class GpuRound:
     """GPU side of a workload: a RoundRunner plus device row generators."""
 
-    def __init__(self, w, flags=0):
+    def __init__(self, w, flags=0, fused=True):
         import torch
         from dynamic_draft_tree_gb300.rounds import RoundRunner
 
@@ -148,7 +148,7 @@ class GpuRound:
         if w["policy"] == "graft":
             kw = dict(graft=w["graft"], template=chain_template(k, w["D"]))
         self.run = RoundRunner(w["policy"], B, V, w["K"], k, g["D_max"], g["P"], g["D_path"], g["m_cap"],
-                               self.spec.dtype, T=w["T"], flags=flags, **kw)
+                               self.spec.dtype, T=w["T"], flags=flags, fused=fused, **kw)
         dt = torch.int16 if self.spec.dtype == synth.BF16 else torch.float32
         self.dbuf = torch.zeros((B, k, V), dtype=dt, device="cuda")
         self.tbuf = torch.zeros((B, g["P"], V), dtype=dt, device="cuda")

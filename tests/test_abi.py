@@ -87,3 +87,11 @@ def test_static_topk_arguments_rejected_on_host(libdt):
     for rows, V, K, dtype, ld in [(0, 1000, 4, 0, 1000), (4, 1, 1, 0, 1000), (4, 1000, 33, 0, 1000),
                                   (4, 10, 11, 0, 10), (4, 1000, 4, 5, 1000), (4, 1000, 4, 0, 999)]:
         assert lib.dt_row_topk_static(fake, ld, rows, V, K, dtype, fake, fake, None, None) == libdt.DT_ERR_ARG
+
+
+def test_fused_cast_calls_reject_bad_arguments(libdt):
+    """The fused CAST entry points check their arguments on the host (no GPU needed)."""
+    lib = libdt.lib
+    assert lib.dt_cast_prune_select(None, None, None, None, None) == libdt.DT_ERR_ARG
+    assert lib.dt_cast_verify_rerank(None, None, None, None, None) == libdt.DT_ERR_ARG
+    assert "null" in lib.dt_last_error_string().decode()

@@ -204,6 +204,30 @@ def test_full_size_round_is_deterministic(torch):
     gr.run.h.close()
 
 
+def test_cast_fused_calls_equal_separate_calls(torch):
+    """dt_cast_prune_select and dt_cast_verify_rerank give exactly what the separate calls give."""
+    import harness
+
+    w = with_sizes("cast", V=32000)
+    outs = []
+    for fused in (True, False):
+        gr = harness.GpuRound(w, fused=fused)
+        res = []
+        for rnd in range(3):
+            attempts = np.zeros(w["B"], np.int64)
+            roots = harness.root_tokens(w, harness.salts_of(w, rnd, attempts))
+            gr.round(rnd, attempts, roots)
+            t = harness.tree_numpy(gr.run.h)
+            res.append((t["token"].copy(), t["value"].copy(), gr.run.selected.cpu().numpy().copy(),
+                        gr.run.m_dev.cpu().numpy().copy(), gr.run.accept_len.cpu().numpy().copy(),
+                        gr.run.bonus.cpu().numpy().copy(), gr.run.frontier_token.cpu().numpy().copy()))
+        outs.append(res)
+        gr.run.h.close()
+    for ra, rb in zip(*outs):
+        for a, b in zip(ra, rb):
+            np.testing.assert_array_equal(a, b)
+
+
 # Full sizes of the five workloads, in the launch configuration the benchmark uses (several rounds
 # back to back on one handle, so that stale per-launch state would show up).
 FULL = [("pr1", {}, 3), ("vicuna", {}, 2), ("vicuna", dict(T=1), 2), ("cast", {}, 3), ("graft", {}, 3),
