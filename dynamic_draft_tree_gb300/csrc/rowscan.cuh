@@ -239,6 +239,91 @@ __device__ __forceinline__ void lane_acc_one(float x, float& m_t, float& s_hi, f
   s_hi = t;
 }
 
+// The warp's list after a merge.
+struct ListState {
+  int nl, lb;        // keys in the list, current list buffer
+  uint64_t tau_key;  // K-th key of the list (0 while it has fewer than K keys)
+  int overflow;      // the candidate buffer had overflowed (candidates beyond it were not stored)
+};
+
+// Merges the warp's candidate buffer rg.cand[0..min(cnt, kWarpCand)) into its top-K list. Keys are
+// distinct elements, so a key's place in the merged list is its rank among list + candidates; with
+// `dedup` a candidate already in the list is dropped first. Out of line: one copy serves every call
+// site, which keeps the scan's code small enough for the instruction cache.
+static __device__ __noinline__ ListState warp_list_merge(WarpRing& rg, int K, int nl, int lb, bool dedup) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  const int cnt = rg.cnt;
+  ListState out;
+  out.overflow = cnt > kWarpCand;
+  if (cnt == 0) {
+    out.nl = nl;
+    out.lb = lb;
+    out.tau_key = nl == K ? rg.list[lb][K - 1] : 0ull;
+    return out;
+  }
+  const int n = min(cnt, kWarpCand);
+  const uint64_t* cur = rg.list[lb];
+  uint64_t* nxt = rg.list[lb ^ 1];
+  if (dedup) {
+    for (int q = lane; q < n; q += 32) {
+      const uint64_t k = rg.cand[q];
+      bool dup = false;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        const uint64_t v = cur[j];  // read unconditionally (in bounds), masked after
+        dup |= (j < nl) & (v == k);
+      }
+      if (dup) rg.cand[q] = 0ull;
+    }
+    __syncwarp();
+  }
+  int valid = 0;
+  for (int q = lane; q < n; q += 32) {
+    const uint64_t k = rg.cand[q];
+    if (k == 0ull) continue;
+    ++valid;
+    int r = 0;
+    // loads are unconditional (every index is inside the arrays) and masked after, so that the eight
+    // of a group issue back to back
+    for (int j0 = 0; j0 < nl; j0 += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint64_t v = cur[j0 + u];
+        r += (j0 + u < nl) & (v > k);
+      }
+    }
+    for (int j0 = 0; j0 < n; j0 += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint64_t v = rg.cand[j0 + u];
+        r += (j0 + u < n) & (v > k);
+      }
+    }
+    if (r < K) nxt[r] = k;
+  }
+  if (lane < nl) {
+    const uint64_t l = cur[lane];
+    int r = lane;
+    for (int j0 = 0; j0 < n; j0 += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint64_t v = rg.cand[j0 + u];
+        r += (j0 + u < n) & (v > l);
+      }
+    }
+    if (r < K) nxt[r] = l;
+  }
+  valid = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)valid);
+  __syncwarp();
+  out.nl = min(K, nl + valid);
+  out.lb = lb ^ 1;
+  out.tau_key = out.nl == K ? rg.list[out.lb][K - 1] : 0ull;
+  if (lane == 0) rg.cnt = 0;
+  __syncwarp();
+  return out;
+}
+
 // Scans elements [s0, s1) of `row`. K <= kMaxK. `stages` is kScanWarps * kWarpStages * kStageBytes of
 // shared memory (dynamic). All threads of the CTA call it.
 template <typename T, bool SOFTMAX>
@@ -311,70 +396,12 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
   // candidate already in the list is dropped first. Returns true if the buffer had overflowed (the
   // candidates beyond its capacity were not stored).
   auto merge = [&](bool dedup) -> bool {
-    __syncwarp();
-    const int cnt = rg.cnt;
-    if (cnt == 0) return false;
-    const int n = min(cnt, kWarpCand);
-    const uint64_t* cur = rg.list[lb];
-    uint64_t* nxt = rg.list[lb ^ 1];
-    if (dedup) {
-      for (int q = lane; q < n; q += 32) {
-        const uint64_t k = rg.cand[q];
-        bool dup = false;
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-          const uint64_t v = cur[j];  // read unconditionally (in bounds), masked after
-          dup |= (j < nl) & (v == k);
-        }
-        if (dup) rg.cand[q] = 0ull;
-      }
-      __syncwarp();
-    }
-    int valid = 0;
-    for (int q = lane; q < n; q += 32) {
-      const uint64_t k = rg.cand[q];
-      if (k == 0ull) continue;
-      ++valid;
-      int r = 0;
-      // loads are unconditional (every index is inside the arrays) and masked after, so that the
-      // eight of a group issue back to back
-      for (int j0 = 0; j0 < nl; j0 += 8) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint64_t v = cur[j0 + u];
-          r += (j0 + u < nl) & (v > k);
-        }
-      }
-      for (int j0 = 0; j0 < n; j0 += 8) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint64_t v = rg.cand[j0 + u];
-          r += (j0 + u < n) & (v > k);
-        }
-      }
-      if (r < K) nxt[r] = k;
-    }
-    if (lane < nl) {
-      const uint64_t l = cur[lane];
-      int r = lane;
-      for (int j0 = 0; j0 < n; j0 += 8) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint64_t v = rg.cand[j0 + u];
-          r += (j0 + u < n) & (v > l);
-        }
-      }
-      if (r < K) nxt[r] = l;
-    }
-    valid = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)valid);
-    __syncwarp();
-    nl = min(K, nl + valid);
-    lb ^= 1;
-    tau_key = nl == K ? rg.list[lb][K - 1] : 0ull;
+    const ListState o = warp_list_merge(rg, K, nl, lb, dedup);
+    nl = o.nl;
+    lb = o.lb;
+    tau_key = o.tau_key;
     tau_val = tau_key ? key_value(tau_key) : -INFINITY;
-    if (lane == 0) rg.cnt = 0;
-    __syncwarp();
-    return cnt > kWarpCand;
+    return o.overflow != 0;
   };
   auto push = [&](uint64_t k) {
     const int pos = atomicAdd(&rg.cnt, 1);
@@ -657,7 +684,7 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
 // ---------------------------------------------------------------- balanced row pass ----
 // The rows a launch reads ("active rows") are numbered j = 0..A-1 in request order: request b owns
 // cnt(b) consecutive numbers, its rows i = 0..cnt(b)-1. The work is laid out in one of two ways:
-//  * few rows (2 A <= gridDim): every row is cut into S_row equal segments, one per CTA (CTA c takes
+//  * few rows (A <= gridDim): every row is cut into S_row equal segments, one per CTA (CTA c takes
 //    segment c % S_row of row c / S_row); a row's pieces are CTAs j S_row .. j S_row + S_row - 1 and
 //    piece c leaves its partial at slot c;
 //  * many rows: the rows' E = A * V elements, concatenated, are cut into G equal ranges, one per CTA
@@ -705,7 +732,7 @@ __device__ void plan_rows(RowPlan& p, int B, int64_t V, int Smax, int esz, Cnt c
   if (p.E == 0) return;
   const int64_t r_min = max((int64_t)kScanWarps * 2 * kStageBytes / esz, (V - 1 + (Smax - 3)) / (Smax - 2));
   const int64_t c = blockIdx.x;
-  if (2 * A <= (int64_t)gridDim.x) {
+  if (A <= (int64_t)gridDim.x) {
     int64_t S = min((int64_t)gridDim.x / A, (V + r_min - 1) / r_min);
     S = max((int64_t)1, min(S, (int64_t)Smax));
     p.S_row = (int)S;
