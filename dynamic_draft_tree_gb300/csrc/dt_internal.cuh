@@ -16,7 +16,7 @@ constexpr int kMaxFifo = 16;
 constexpr int kScanWarps = 4;        // warps of a row-scan CTA
 constexpr int kRowThreads = 32 * kScanWarps;
 constexpr int kStageBytes = 4096;   // one TMA bulk copy into a warp's ring
-constexpr int kWarpStages = 4;      // ring depth per warp
+constexpr int kWarpStages = 3;      // ring depth per warp
 constexpr int kWarpCand = 128;      // per-warp candidate buffer
 constexpr int kCandCap = 1024;      // CTA merge / sort buffer (keys)
 constexpr int kScanSmemBytes = kScanWarps * kWarpStages * kStageBytes;  // dynamic shared memory

@@ -90,7 +90,7 @@ struct ExpandArgs {
 // Balanced over the active rows (request b expands min(frontier_count[b], F) nodes); see the
 // balanced row pass in rowscan.cuh.
 template <typename T>
-__global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
+__global__ void __launch_bounds__(kRowThreads, 4) expand_kernel(ExpandArgs a) {
   pdl_begin();
   extern __shared__ __align__(128) uint8_t dyn_smem[];
   __shared__ ScanSmem sm;
@@ -190,8 +190,8 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(ExpandArgs a) {
 }  // namespace
 
 int row_pass_grid(const dt_handle* h) {
-  // one wave: 3 CTAs per SM (registers and shared memory allow 3), within the piece-slot capacity
-  const int64_t g = std::min<int64_t>((int64_t)h->num_sms * 3, 4096);
+  // one wave: 4 CTAs per SM (128 registers and 56 KB of shared memory each), within the piece-slot capacity
+  const int64_t g = std::min<int64_t>((int64_t)h->num_sms * 4, 4096);
   return (int)std::max<int64_t>(1, g);
 }
 
@@ -204,6 +204,13 @@ cudaError_t init_tree_attributes() {
   cudaError_t e = cudaFuncSetAttribute(expand_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(expand_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // all of the unified L1 as shared memory, so that 4 CTAs fit on an SM
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(expand_kernel<uint16_t>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(expand_kernel<float>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
   return e;
 }
 

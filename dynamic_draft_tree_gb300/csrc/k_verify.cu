@@ -27,7 +27,7 @@ struct RowPassArgs {
 // Balanced over the used positions (request b reads rows i < n_pos[b]; a position without a valid
 // token is counted but not read); see the balanced row pass in rowscan.cuh.
 template <typename T, bool SOFTMAX>
-__global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(RowPassArgs a) {
+__global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(RowPassArgs a) {
   pdl_begin();
   extern __shared__ __align__(128) uint8_t dyn_smem[];
   __shared__ ScanSmem sm;
@@ -365,6 +365,13 @@ cudaError_t init_verify_attributes() {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<uint16_t, true>, a, smem);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<float, false>, a, smem);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<float, true>, a, smem);
+  // all of the unified L1 as shared memory, so that 4 CTAs fit on an SM
+  const cudaFuncAttribute c = cudaFuncAttributePreferredSharedMemoryCarveout;
+  const int mx = cudaSharedmemCarveoutMaxShared;
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<uint16_t, false>, c, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<uint16_t, true>, c, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<float, false>, c, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<float, true>, c, mx);
   return e;
 }
 
