@@ -251,6 +251,11 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
   __syncthreads();
   for (int b = tid; b < a.B; b += blockDim.x) atomicMax(&maxcand, ws.layer_count[(int64_t)b * (a.D + 1) + a.d]);
   const int wcap = min(a.p.width_cap, a.LW);
+  // normalised draft cost of k frontier nodes at the current context: c_k = S_D[row][k-1] / S_T[row][0]
+  // (issued before the utilities, whose loads then overlap these)
+  const int row = table_row((double)(a.p.n0 + cs.ctx_sum), a.p.L, a.p.M_rows);
+  for (int k = 1 + tid; k <= wcap; k += blockDim.x)
+    cost[k] = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
   // items[s] = (1/B) sum_b exp(value of the s-th node of b's layer), missing nodes count 0
   batch_items(items, part, wcap, a.B, [&](int b, int s) {
     const int64_t lb = (int64_t)b * (a.D + 1) + a.d;
@@ -259,10 +264,6 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
     if (s >= cnt || id < 0) return 0.0;
     return (double)expf(ws.value[(int64_t)b * a.N + id]);
   });
-  // normalised draft cost of k frontier nodes at the current context: c_k = S_D[row][k-1] / S_T[row][0]
-  const int row = table_row((double)(a.p.n0 + cs.ctx_sum), a.p.L, a.p.M_rows);
-  for (int k = 1 + tid; k <= wcap; k += blockDim.x)
-    cost[k] = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
   __syncthreads();
   const int cap = min(a.p.width_cap, maxcand);
   int n = 0;

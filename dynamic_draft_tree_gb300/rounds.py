@@ -84,7 +84,8 @@ class RoundRunner:
         pol = self.policy
         if pol == "cast":
             self.set_n0(n0)
-        self.stop.zero_()
+        if pol == "graft":  # the checkpoints only ever set stop; CAST writes every entry, EAGLE none
+            self.stop.zero_()
         dt_tree_reset(h, roots)
         for d in range(1, self.D + 1):
             if d > 1:
