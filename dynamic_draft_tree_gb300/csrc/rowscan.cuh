@@ -8,10 +8,11 @@
 // (cp.async.bulk, completion counted on one mbarrier per stage), so warps never wait on each
 // other while streaming; the CTA synchronises once, at the end of the segment.
 //   * softmax: every lane keeps a running max and a compensated sum, rescaled when its max grows;
-//   * top-K: every warp keeps a sorted list of its K best keys spread over its lanes (lane l holds
-//     the l-th best). The list starts as the K best per-lane maxima; afterwards only elements
-//     above the list's K-th key are candidates. Candidates go to a small per-warp buffer and are
-//     inserted into the list with warp shuffles.
+//   * top-K: every warp keeps a sorted list of its K best keys in shared memory. A chunk that fits
+//     the warp's ring is filtered in one pass once all of it has arrived, against the K-th largest
+//     lane maximum; a longer chunk filters its first stage that way and every later stage against
+//     the list's K-th key. Candidates go to a small per-warp buffer and are merged into the list by
+//     rank counting.
 // Unaligned heads/tails (< 16 bytes at each end) are read with plain loads by warp 0.
 #pragma once
 
@@ -120,23 +121,40 @@ struct ScanSmem {
 };
 
 // Top-K of S descending lists of K keys each, list s at src[s * stride ..] (empty = 0), into
-// sm.topk[0..K). The rank of a key is the number of larger keys over all lists, found by binary
-// search in each list. All threads call it.
+// sm.topk[0..K). Keys are distinct, so the place of a key is the number of larger keys over all
+// lists. Up to kLinearMerge keys that number is counted directly (independent loads, issued in
+// groups of eight); above it by a binary search in each list. All threads call it. The reads of a
+// group may run up to 7 keys past a list's end; the callers' buffers extend past it.
+constexpr int kLinearMerge = 256;
 __device__ __forceinline__ void merge_sorted_lists(ScanSmem& sm, const uint64_t* src, int S, int K, int stride) {
   const int n = S * K;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint64_t k = src[(i / K) * stride + i % K];
+    const int s0 = i / K;
+    const uint64_t k = src[s0 * stride + (i - s0 * K)];
     if (k == 0ull) continue;
     int rank = 0;
-    for (int s = 0; s < S && rank < K; ++s) {
-      const uint64_t* L = src + s * stride;
-      int lo = 0, hi = K;  // first index whose key is <= k
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (L[mid] > k) lo = mid + 1;
-        else hi = mid;
+    if (n <= kLinearMerge) {
+      for (int s = 0; s < S; ++s) {
+        const uint64_t* L = src + s * stride;
+        for (int j0 = 0; j0 < K; j0 += 8) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint64_t v = L[j0 + u];
+            rank += (j0 + u < K) & (v > k);
+          }
+        }
       }
-      rank += lo;
+    } else {
+      for (int s = 0; s < S && rank < K; ++s) {
+        const uint64_t* L = src + s * stride;
+        int lo = 0, hi = K;  // first index whose key is <= k
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (L[mid] > k) lo = mid + 1;
+          else hi = mid;
+        }
+        rank += lo;
+      }
     }
     if (rank < K) sm.topk[rank] = k;
   }
@@ -324,6 +342,71 @@ static __device__ __noinline__ ListState warp_list_merge(WarpRing& rg, int K, in
   return out;
 }
 
+// Element e of a 16-byte vector of T.
+template <typename T>
+__device__ __forceinline__ float vec_elt(const uint4& w, int e) {
+  if (sizeof(T) == 2) {
+    const int wi = e >> 1;
+    const uint32_t word = wi == 0 ? w.x : wi == 1 ? w.y : wi == 2 ? w.z : w.w;
+    return (e & 1) ? bf16_hi(word) : bf16_lo(word);
+  }
+  const uint32_t word = e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w;
+  return __uint_as_float(word);
+}
+
+// The K-th largest (K <= 32) of the 32 lane values v, -inf standing for NaN; every lane gets it.
+// A lane's rank is the number of lanes with a larger value, or an equal one at a lower lane, so the
+// ranks are 0..31 and exactly one lane has rank K - 1.
+__device__ __forceinline__ float warp_kth_largest(float v, int K) {
+  const int lane = threadIdx.x & 31;
+  if (!(v > -INFINITY)) v = -INFINITY;
+  int rank = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float o = __shfl_sync(0xFFFFFFFFu, v, j);
+    rank += (o > v) | ((o == v) & (j < lane));
+  }
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, rank == K - 1);
+  return __shfl_sync(0xFFFFFFFFu, v, __ffs(hit) - 1);
+}
+
+// Pushes into the warp's candidate buffer the elements of the warp's first nb chunk stages (resident
+// in its ring, stage u in buffer u) whose value is >= tv and not -inf and whose key exceeds tk.
+// Lanes without `scan` push nothing. Out of line: one copy serves every call site.
+template <typename T>
+static __device__ __noinline__ void push_batch_candidates(WarpRing& rg, const uint8_t* my_stages, int nb,
+                                                          int64_t wbytes, int64_t we0, float tv, uint64_t tk,
+                                                          bool scan) {
+  constexpr int VEC = Elt<T>::kVec;
+  constexpr int ESZ = (int)sizeof(T);
+  constexpr int QV = kStageBytes / 16 / 32;
+  const int lane = threadIdx.x & 31;
+  if (scan) {
+    for (int u = 0; u < nb; ++u) {
+      const uint8_t* sp = my_stages + (size_t)u * kStageBytes;
+      const int st_bytes = (int)min((int64_t)kStageBytes, wbytes - (int64_t)u * kStageBytes);
+      const int64_t st_e0 = we0 + (int64_t)u * (kStageBytes / ESZ);
+      for (int q = 0; q < QV; ++q) {
+        const int vi = q * 32 + lane;
+        if (vi * 16 >= st_bytes) break;
+        const uint4 w = *reinterpret_cast<const uint4*>(sp + (size_t)vi * 16);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const float x = vec_elt<T>(w, e);
+          if (x >= tv && x != -INFINITY) {
+            const uint64_t k = make_key(x, (uint32_t)(st_e0 + (int64_t)(vi * VEC + e)));
+            if (k > tk) {
+              const int pos = atomicAdd(&rg.cnt, 1);
+              if (pos < kWarpCand) rg.cand[pos] = k;
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
 // Scans elements [s0, s1) of `row`. K <= kMaxK. `stages` is kScanWarps * kWarpStages * kStageBytes of
 // shared memory (dynamic). All threads of the CTA call it.
 template <typename T, bool SOFTMAX>
@@ -371,7 +454,6 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
   int lb = 0, nl = 0;           // current list buffer, keys in the list
   uint64_t tau_key = 0ull;      // K-th key of the list (0 while it has fewer than K keys)
   float tau_val = -INFINITY;
-  bool inited = false;
   bool timed_out = false;
 
   // head + tail elements (warp 0): softmax, and always candidates
@@ -411,11 +493,17 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
   constexpr int QV = kStageBytes / 16 / 32;   // vectors per lane per stage (8)
   constexpr int NV = QV * VEC;                 // values per lane per stage
   const uint32_t neg_fill = ESZ == 2 ? 0xFF80FF80u : 0xFF800000u;  // -inf in every element
+  // The first nb stages are filtered together once all of them are in (the whole chunk, when it
+  // fits the ring; else the first stage): against the K-th largest lane maximum over them, with one
+  // merge. Later stages stream against the list's K-th key.
+  const int nb = n_st <= kWarpStages ? n_st : 1;
+  float bmax = -INFINITY;  // lane maximum over the batch stages (a stage's NaN maximum is skipped)
+  // the row's shared threshold (read early: used after the stage's data has arrived)
+  uint64_t gt = gtau ? (uint64_t)__ldcg(gtau) : 0ull;
   for (int t = 0; t < n_st; ++t) {
     const int st = t % kWarpStages;
     const uint32_t parity = (uint32_t)((t / kWarpStages) & 1);
-    // the row's shared threshold (read early; used by the filter below)
-    const uint64_t gt = gtau ? (uint64_t)__ldcg(gtau) : 0ull;
+    if (t >= nb && gtau) gt = (uint64_t)__ldcg(gtau);
     const bool ok = mbar_wait_bounded(&rg.bar[st], parity, t == 0 ? first_wait_cap : kSpinCap);
     if (!__all_sync(0xFFFFFFFFu, ok)) {
       timed_out = true;
@@ -503,99 +591,94 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
       }
     }
 
-    // The rarely taken paths below (list start, candidates) read the stage from shared memory with
-    // rolled loops: straight-line code over all NV register values would be large and, being rarely
-    // executed, always cold in the instruction cache. Vector q of this lane is stage vector
-    // q * 32 + lane; its element e has token id st_e0 + (q * 32 + lane) * VEC + e.
+    // The rarely taken candidate paths below read the stage from shared memory with rolled loops:
+    // straight-line code over all NV register values would be large and, being rarely executed,
+    // always cold in the instruction cache. Vector q of this lane is stage vector q * 32 + lane; its
+    // element e has token id st_e0 + (q * 32 + lane) * VEC + e.
     auto vec_at = [&](int q, uint4& w) -> bool {
       const int vi = q * 32 + lane;
       if (vi * 16 >= st_bytes) return false;
       w = *reinterpret_cast<const uint4*>(sp + (size_t)vi * 16);
       return true;
     };
-    auto elt = [&](const uint4& w, int e) -> float {
-      uint32_t word;
-      if (ESZ == 2) {
-        const int wi = e >> 1;
-        word = wi == 0 ? w.x : wi == 1 ? w.y : wi == 2 ? w.z : w.w;
-        return (e & 1) ? bf16_hi(word) : bf16_lo(word);
-      }
-      word = e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w;
-      return __uint_as_float(word);
-    };
     auto id_of = [&](int q, int e) -> uint32_t {
       return (uint32_t)(st_e0 + (int64_t)((q * 32 + lane) * VEC + e));
     };
 
-    // first stage of the chunk: the list starts as the K best per-lane maxima
-    uint64_t excl = 0ull;
-    if (!inited) {
-      if (lm == lm && lm != -INFINITY) {
-        // lowest id among the maxima: the first element equal to lm of the first vector holding it
-        int qf = QV - 1;
-#pragma unroll
-        for (int q = QV - 1; q >= 0; --q)
-          if (vmax[q] == lm) qf = q;
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        vec_at(qf, w);
-        uint32_t id = id_of(qf, 0);
-#pragma unroll
-        for (int e = VEC - 1; e >= 0; --e)
-          if (elt(w, e) == lm) id = id_of(qf, e);
-        excl = make_key(lm, id);
-        push(excl);
+    if (t < nb) {
+      bmax = fmaxf(bmax, lm);
+      if (t + 1 < nb) continue;  // the next batch stage
+      // Threshold: the K-th largest lane maximum (K lanes hold an element at or above it, so no
+      // element below it is in the top-K), or the row's shared threshold if larger. The warp has
+      // published nothing to the shared threshold yet, so a key equal to it is not in this chunk.
+      uint64_t tk = gt;
+      float tv = fmaxf(warp_kth_largest(bmax, K), gt ? key_value(gt) : -INFINITY);
+      if (__any_sync(0xFFFFFFFFu, bmax >= tv)) {
+        push_batch_candidates<T>(rg, my_stages, nb, wbytes, we0, tv, tk, bmax >= tv);
+        bool overflow = merge(false);
+        // An overflowed buffer still raised the list's K-th key: filter again above it (keys already
+        // in the list are dropped by the merge). The key rises every round.
+        for (int round = 1; overflow; ++round) {
+          if (round > nb * NV * 32 / (kWarpCand - kMaxK) + 1) {  // never hit
+            if (lane == 0) sm.flags[warp] |= 2;
+            break;
+          }
+          tk = tau_key;
+          tv = tau_val;
+          push_batch_candidates<T>(rg, my_stages, nb, wbytes, we0, tv, tk, bmax >= tv);
+          overflow = merge(true);
+        }
+        if (gtau && lane == 0 && nl == K) atomicMax(gtau, (unsigned long long)tau_key);
       }
-      merge(false);
-      inited = true;
-    }
-
-    // Filter against the larger of the list's K-th key and the row's shared threshold (the best K-th
-    // key any warp of any piece of the row has published: that warp holds K keys at or above it, so
-    // no element below it can be in the row's top-K). Within a warp's chunk token ids grow stage by
-    // stage, so after the first stage a value equal to the warp's own K-th key's value has a larger
-    // id and cannot beat it: the test is strict there (not against another warp's key). Lanes whose
-    // maximum clears the threshold push their candidates, which are then merged into the list. If the
-    // buffer overflowed, the merge still raised the threshold: the stage is filtered again against it
-    // (keys already in the list are dropped by the merge).
-    bool dedup = false;
-    for (int round = 0;; ++round) {
-      uint64_t tk = tau_key;
-      bool own = true;
-      if (gt > tk) {
-        tk = gt;
-        own = false;
-      }
-      const float tv = tk ? key_value(tk) : -INFINITY;
-      const bool strict = t > 0 && own;
-      const bool hot = strict ? (lm > tv) : (lm >= tv);
-      if (!__any_sync(0xFFFFFFFFu, hot)) break;
-      if (hot) {
-        unsigned vm = 0u;  // vectors that may hold candidates
+    } else {
+      // Filter against the larger of the list's K-th key and the row's shared threshold (the best K-th
+      // key any warp of any piece of the row has published: that warp holds K keys at or above it, so
+      // no element below it can be in the row's top-K). Within a warp's chunk token ids grow stage by
+      // stage, so after the first stage a value equal to the warp's own K-th key's value has a larger
+      // id and cannot beat it: the test is strict there (not against another warp's key). Lanes whose
+      // maximum clears the threshold push their candidates, which are then merged into the list. If the
+      // buffer overflowed, the merge still raised the threshold: the stage is filtered again against it
+      // (keys already in the list are dropped by the merge).
+      bool dedup = false;
+      for (int round = 0;; ++round) {
+        uint64_t tk = tau_key;
+        bool own = true;
+        if (gt > tk) {
+          tk = gt;
+          own = false;
+        }
+        const float tv = tk ? key_value(tk) : -INFINITY;
+        const bool strict = t > 0 && own;
+        const bool hot = strict ? (lm > tv) : (lm >= tv);
+        if (!__any_sync(0xFFFFFFFFu, hot)) break;
+        if (hot) {
+          unsigned vm = 0u;  // vectors that may hold candidates
 #pragma unroll
-        for (int q = 0; q < QV; ++q)
-          if (strict ? (vmax[q] > tv) : (vmax[q] >= tv)) vm |= 1u << q;
-        while (vm) {
-          const int q = __ffs(vm) - 1;
-          vm &= vm - 1;
-          uint4 w;
-          if (!vec_at(q, w)) break;
+          for (int q = 0; q < QV; ++q)
+            if (strict ? (vmax[q] > tv) : (vmax[q] >= tv)) vm |= 1u << q;
+          while (vm) {
+            const int q = __ffs(vm) - 1;
+            vm &= vm - 1;
+            uint4 w;
+            if (!vec_at(q, w)) break;
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const float x = elt(w, e);
-            if (x >= tv && x != -INFINITY) {
-              const uint64_t k = make_key(x, id_of(q, e));
-              if (k > tk && k != excl) push(k);
+            for (int e = 0; e < VEC; ++e) {
+              const float x = vec_elt<T>(w, e);
+              if (x >= tv && x != -INFINITY) {
+                const uint64_t k = make_key(x, id_of(q, e));
+                if (k > tk) push(k);
+              }
             }
           }
         }
-      }
-      const bool overflow = merge(dedup);
-      dedup = true;
-      if (gtau && lane == 0 && nl == K) atomicMax(gtau, (unsigned long long)tau_key);
-      if (!overflow) break;
-      if (round >= NV * 32 / (kWarpCand - kMaxK) + 1) {  // the threshold rises every round: never hit
-        if (lane == 0) sm.flags[warp] |= 2;
-        break;
+        const bool overflow = merge(dedup);
+        dedup = true;
+        if (gtau && lane == 0 && nl == K) atomicMax(gtau, (unsigned long long)tau_key);
+        if (!overflow) break;
+        if (round >= NV * 32 / (kWarpCand - kMaxK) + 1) {  // the threshold rises every round: never hit
+          if (lane == 0) sm.flags[warp] |= 2;
+          break;
+        }
       }
     }
 
@@ -609,8 +692,10 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
       bulk_g2s(my_stages + (size_t)st * kStageBytes, wsrc + off, bytes, &rg.bar[st]);
     }
   }
-  if (ht_key) push(ht_key);  // head/tail elements (warp 0)
-  merge(false);
+  if (__any_sync(0xFFFFFFFFu, ht_key != 0ull)) {  // head/tail elements (warp 0)
+    if (ht_key) push(ht_key);
+    merge(false);
+  }
   // every copy has landed: retire the barriers so that a later scan in this CTA can initialise them
   // again (after a timeout a copy may still be in flight, and the barriers are left alone)
   if (lane == 0 && !timed_out)
@@ -730,22 +815,27 @@ __device__ void plan_rows(RowPlan& p, int B, int64_t V, int Smax, int esz, Cnt c
   p.j0 = p.x0 = p.x1 = 0;
   p.b = p.i = 0;
   if (p.E == 0) return;
-  const int64_t r_min = max((int64_t)kScanWarps * 2 * kStageBytes / esz, (V - 1 + (Smax - 3)) / (Smax - 2));
+  // 32-bit unsigned arithmetic where it suffices (V < 2^31, A and the grid <= 4096): the divisions
+  // here are on the launch's critical path
+  const uint32_t Vu = (uint32_t)V;
+  const uint32_t r_min = max((uint32_t)(kScanWarps * 2 * kStageBytes / esz), (Vu - 1u + (uint32_t)(Smax - 3)) / (uint32_t)(Smax - 2));
   const int64_t c = blockIdx.x;
   if (A <= (int64_t)gridDim.x) {
-    int64_t S = min((int64_t)gridDim.x / A, (V + r_min - 1) / r_min);
-    S = max((int64_t)1, min(S, (int64_t)Smax));
+    const uint32_t Au = (uint32_t)A, cu = (uint32_t)c;
+    uint32_t S = min(gridDim.x / Au, (Vu - 1u) / r_min + 1u);  // ceil(V / r_min) for V >= 1
+    S = max(1u, min(S, (uint32_t)Smax));
     p.S_row = (int)S;
-    p.G = (int)(A * S);
+    p.G = (int)(Au * S);
     if (c >= p.G) return;
-    p.j0 = c / S;
-    int64_t L = (V + S - 1) / S;
-    L = (L + 7) / 8 * 8;
-    const int64_t e0 = min(V, (c % S) * L), e1 = min(V, e0 + L);
+    const uint32_t j0 = cu / S, seg = cu - j0 * S;
+    uint32_t L = (Vu - 1u) / S + 1u;  // ceil(V / S)
+    L = (L + 7u) / 8u * 8u;
+    p.j0 = j0;
+    const int64_t e0 = min(V, (int64_t)seg * L), e1 = min(V, e0 + L);
     p.x0 = p.j0 * V + e0;
     p.x1 = p.j0 * V + e1;
   } else {
-    int64_t G = p.E / r_min;
+    int64_t G = p.E / (int64_t)r_min;
     G = max(G, (int64_t)1);
     G = min(G, (int64_t)gridDim.x);
     p.G = (int)G;
