@@ -170,10 +170,12 @@ __device__ void batch_items(double* items, double* part, int cap, int B, F vb) {
 // c_k <= c_k0 or (u_k - u_k0) / (c_k - c_k0) >= thr, with u_k = items[0] + ... + items[k-1]. For
 // c_k > c_k0 the second test is u_k - thr c_k >= u_k0 - thr c_k0, so with q_k = u_k - thr c_k both
 // tests compare precomputed values. Warp 0 builds u (prefix sums, u[0] = 0), q and the ordered
-// images of c and q; thread 0 then walks k. `u`, `cq` ([2][cap+1] images) are shared scratch.
-// All threads call it; every thread gets k0.
+// images of c and q; thread 0 then walks k while warp 1 runs `during_walk` (work that needs u and
+// may overlap the walk). `u`, `cimg`, `qimg` ([cap+1] each) are shared scratch. All threads call
+// it; every thread gets k0.
+template <class DuringWalk>
 __device__ int selection_rule(const double* items, const double* cost, double thr, int cap, double* u,
-                              uint64_t* cimg, uint64_t* qimg, int* result) {
+                              uint64_t* cimg, uint64_t* qimg, int* result, DuringWalk during_walk) {
   const int tid = threadIdx.x, lane = tid & 31;
   if (tid < 32) {
     double carry = 0.0;
@@ -209,6 +211,8 @@ __device__ int selection_rule(const double* items, const double* cost, double th
       }
     }
     *result = k0;
+  } else if ((tid >> 5) == 1) {
+    during_walk();
   }
   __syncthreads();
   return *result;
@@ -234,29 +238,38 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
   __shared__ double part[32 * kItemChunk];
   __shared__ double u[kMaxW + 2];
   __shared__ uint64_t cimg[kMaxW + 2], qimg[kMaxW + 2];
+  __shared__ double ratio_k[kMaxW + 2];
+  __shared__ uint8_t grow_k[kMaxW + 2];
   __shared__ CastState cs;
-  __shared__ int maxcand, s_grow, s_k0, s_width;
+  __shared__ int s_maxcand, s_grow, s_k0, s_width;
   const Workspace& ws = a.ws;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  // one round of independent loads: the CAST state, the layer sizes, the layer's values (inside
-  // batch_items) and, for the frontier that follows, each request's candidate nodes
-  if (tid == 0) {
-    maxcand = 0;
-    cs = *ws.cast;
-  }
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nwarps = (int)(blockDim.x >> 5);
+  // One round of independent loads, no barrier before them: the CAST state (thread 0), each
+  // request's candidate nodes for the frontier that follows (warp b), the layer's values (inside
+  // batch_items), the layer sizes (warp nwarps - 2) and the cost vector (warp nwarps - 1, which reads
+  // the context sum itself rather than waiting for the state).
+  if (tid == 0) cs = *ws.cast;
   int f_id = -1, f_tok = -1, f_avail = 0;
   float f_val = -INFINITY;
-  const bool f_pref = a.select && a.B <= (int)(blockDim.x >> 5);
+  const bool f_pref = a.select && a.B <= nwarps;
   if (f_pref && warp < a.B) f_avail = frontier_candidates(ws, warp, a.N, a.W, a.LW, a.D, a.d, f_id, f_tok, f_val);
-  __syncthreads();
-  for (int b = tid; b < a.B; b += blockDim.x) atomicMax(&maxcand, ws.layer_count[(int64_t)b * (a.D + 1) + a.d]);
   const int wcap = min(a.p.width_cap, a.LW);
-  // normalised draft cost of k frontier nodes at the current context: c_k = S_D[row][k-1] / S_T[row][0]
-  // (issued before the utilities, whose loads then overlap these)
-  const int row = table_row((double)(a.p.n0 + cs.ctx_sum), a.p.L, a.p.M_rows);
-  for (int k = 1 + tid; k <= wcap; k += blockDim.x)
-    cost[k] = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
-  // items[s] = (1/B) sum_b exp(value of the s-th node of b's layer), missing nodes count 0
+  if (warp == nwarps - 1) {
+    // normalised draft cost of k frontier nodes at the current context: c_k = S_D[row][k-1] / S_T[row][0]
+    const int64_t ctx = ws.cast->ctx_sum;
+    const int row = table_row((double)(a.p.n0 + ctx), a.p.L, a.p.M_rows);
+    for (int k = 1 + lane; k <= wcap; k += 32)
+      cost[k] = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
+  }
+  if (warp == nwarps - 2) {
+    int mc = 0;
+    for (int b = lane; b < a.B; b += 32) mc = max(mc, ws.layer_count[(int64_t)b * (a.D + 1) + a.d]);
+    mc = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)max(mc, 0));
+    if (lane == 0) s_maxcand = mc;
+  }
+  // items[s] = (1/B) sum_b exp(value of the s-th node of b's layer), missing nodes count 0 (its first
+  // barrier publishes everything above)
   batch_items(items, part, wcap, a.B, [&](int b, int s) {
     const int64_t lb = (int64_t)b * (a.D + 1) + a.d;
     const int cnt = ws.layer_count[lb];
@@ -265,29 +278,47 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
     return (double)expf(ws.value[(int64_t)b * a.N + id]);
   });
   __syncthreads();
-  const int cap = min(a.p.width_cap, maxcand);
+  const int cap = min(a.p.width_cap, s_maxcand);
+  // While thread 0 walks the selection, warp 1 evaluates the grow test for every width k the walk
+  // may choose (the FIFO as it would be after appending u_k / u_prev), so that no fp64 division is
+  // left for after the walk. Same operations, in the same order, as the update below.
+  auto grow_for_all_widths = [&]() {
+    const int len = cs.fifo_len;
+    for (int k = 1 + lane; k <= cap; k += 32) {
+      const double uk = u[k];
+      double sum = 0.0;
+      int nlen = len;
+      if (cs.u_prev >= 0.0) {
+        const double r = uk / cs.u_prev;
+        ratio_k[k] = r;
+        for (int j = len < a.p.R ? 0 : 1; j < len; ++j) sum += cs.fifo[j];
+        sum += r;
+        nlen = len < a.p.R ? len + 1 : len;
+      } else {
+        for (int j = 0; j < len; ++j) sum += cs.fifo[j];
+      }
+      const double alpha = sum / (double)nlen;
+      grow_k[k] = (a.d < a.p.D_max) && (alpha * uk >= a.p.C2 * cost[k]);  // alpha * u / c_k >= C2
+    }
+  };
   int n = 0;
-  if (cap > 0) n = selection_rule(items, cost, a.p.C1, cap, u, cimg, qimg, &s_k0);
+  if (cap > 0) n = selection_rule(items, cost, a.p.C1, cap, u, cimg, qimg, &s_k0, grow_for_all_widths);
   if (tid == 0) {
     bool grow = false;
     if (cap > 0) {
-      const double un = u[n];
       if (cs.u_prev >= 0.0) {
         int len = cs.fifo_len;
         if (len < a.p.R) {
-          cs.fifo[len++] = un / cs.u_prev;
+          cs.fifo[len++] = ratio_k[n];
         } else {
           for (int j = 1; j < len; ++j) cs.fifo[j - 1] = cs.fifo[j];
-          cs.fifo[len - 1] = un / cs.u_prev;
+          cs.fifo[len - 1] = ratio_k[n];
         }
         cs.fifo_len = len;
       }
-      double alpha = 0.0;
-      for (int j = 0; j < cs.fifo_len; ++j) alpha += cs.fifo[j];
-      alpha /= (double)cs.fifo_len;
-      grow = (a.d < a.p.D_max) && (alpha * un >= a.p.C2 * cost[n]);  // alpha * u / c_n >= C2
-      cs.u_prev = un;
-      cs.u_layer = un;
+      grow = grow_k[n] != 0;
+      cs.u_prev = u[n];
+      cs.u_layer = u[n];
       cs.ctx_sum += n;
       *ws.cast = cs;
     }
@@ -332,7 +363,7 @@ __global__ void __launch_bounds__(kPruneThreads) cast_verify_kernel(PruneArgs a)
   const int cap = min(a.p.m_cap, maxn);
   batch_items(items, part, cap, a.B, [&](int b, int s) { return lin[(int64_t)b * a.p.m_cap + s]; });
   int m = 0;
-  if (cap > 0) m = selection_rule(items, cost, a.p.C3, cap, u, cimg, qimg, &s_k0);
+  if (cap > 0) m = selection_rule(items, cost, a.p.C3, cap, u, cimg, qimg, &s_k0, [] {});
   if (tid == 0) a.out.m[0] = m;
   if (a.sel) {  // the rerank, as dt_rerank(m) would write it: each request's top-m ids, ascending
     const int lane = tid & 31;
