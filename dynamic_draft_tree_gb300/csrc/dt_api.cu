@@ -89,6 +89,8 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   const size_t o_token = cv.take<int32_t>(BN), o_parent = cv.take<int32_t>(BN), o_depth = cv.take<int32_t>(BN);
   const size_t o_logc = cv.take<float>(BN), o_value = cv.take<float>(BN);
   const size_t o_lorder = cv.take<int32_t>((size_t)c.B_max * (c.D_max + 1) * h->LW);
+  const size_t o_lval = cv.take<float>((size_t)c.B_max * (c.D_max + 1) * h->LW);
+  const size_t o_ltok = cv.take<int32_t>((size_t)c.B_max * (c.D_max + 1) * h->LW);
   const size_t o_lcount = cv.take<int32_t>((size_t)c.B_max * (c.D_max + 1));
   const size_t o_front = cv.take<int32_t>((size_t)c.B_max * c.W);
   const size_t o_fval = cv.take<float>((size_t)c.B_max * c.W);
@@ -130,6 +132,8 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   w.logc = reinterpret_cast<float*>(bp + o_logc);
   w.value = reinterpret_cast<float*>(bp + o_value);
   w.layer_order = reinterpret_cast<int32_t*>(bp + o_lorder);
+  w.layer_val = reinterpret_cast<float*>(bp + o_lval);
+  w.layer_tok = reinterpret_cast<int32_t*>(bp + o_ltok);
   w.layer_count = reinterpret_cast<int32_t*>(bp + o_lcount);
   w.frontier = reinterpret_cast<int32_t*>(bp + o_front);
   w.frontier_val = reinterpret_cast<float*>(bp + o_fval);

@@ -20,6 +20,7 @@ constexpr int kWarpStages = 3;      // ring depth per warp
 constexpr int kWarpCand = 128;      // per-warp candidate buffer
 constexpr int kCandCap = 1024;      // CTA merge / sort buffer (keys)
 constexpr int kScanSmemBytes = kScanWarps * kWarpStages * kStageBytes;  // dynamic shared memory
+static_assert(kCandCap * (8 + 4) <= kScanSmemBytes, "layer sort keys + tokens must fit the stage memory");
 constexpr int kStaticRows = 1024;      // rows per call of the static-scratch row top-K
 constexpr int kStaticPartials = 4096;  // row segments per call of the static-scratch row top-K
 
@@ -63,6 +64,8 @@ struct Workspace {
   float* logc;
   float* value;
   int32_t* layer_order;
+  float* layer_val;      // [B_max][D_max+1][LW] value of layer_order's node at the same place
+  int32_t* layer_tok;    // [B_max][D_max+1][LW] token of layer_order's node at the same place
   int32_t* layer_count;
   int32_t* frontier;
   float* frontier_val;   // [B_max][W] value of each frontier node (read with the frontier)
@@ -232,19 +235,25 @@ __device__ __forceinline__ void select_frontier_write(const Workspace& ws, int b
   }
   if (lane == 0) ws.frontier_count[b] = w;
 }
-// Loads the candidates of request b's frontier (the first min(W, nodes) nodes of layer d) into lanes.
+// Loads the candidates of request b's frontier (the first min(W, nodes) nodes of layer d) into lanes:
+// id, token and value come from the layer's sorted arrays in one round of loads.
 __device__ __forceinline__ int frontier_candidates(const Workspace& ws, int b, int N, int W, int LW, int D, int d,
                                                    int& id, int& tok, float& val) {
   const int lane = threadIdx.x & 31;
   const int64_t lb = (int64_t)b * (D + 1) + d;
   const int avail = ws.layer_count[lb];
-  id = lane < W ? ws.layer_order[lb * LW + lane] : -1;  // read with the count: -1 past it
+  id = -1;
   tok = -1;
   val = -INFINITY;
-  if (lane < min(avail, W) && id >= 0) {
-    const int64_t gi = (int64_t)b * N + id;
-    tok = ws.token[gi];
-    val = ws.value[gi];
+  if (lane < W) {  // read with the count: entries past it are not used
+    const int i = ws.layer_order[lb * LW + lane];
+    const int t = ws.layer_tok[lb * LW + lane];
+    const float v = ws.layer_val[lb * LW + lane];
+    if (lane < min(avail, W) && i >= 0) {
+      id = i;
+      tok = t;
+      val = v;
+    }
   }
   return avail;
 }

@@ -40,15 +40,12 @@ __global__ void __launch_bounds__(kSortThreads) sort_nodes_kernel(SortArgs a) {
     const int d = 1 + f / a.LW, p = f % a.LW;
     const int64_t lb = (int64_t)b * (a.D + 1) + d;
     uint64_t k = 0ull;
-    if (p < ws.layer_count[lb]) {
-      const int id = ws.layer_order[lb * a.LW + p];
-      if (id > 0 && id < a.N) {
-        const int64_t gi = (int64_t)b * a.N + id;
-        const int tok = ws.token[gi];
-        const float v = ws.value[gi];
-        if (tok >= 0) k = make_key(v, (uint32_t)id);
-      }
-    }
+    const int64_t li = lb * a.LW + p;
+    const int lc = ws.layer_count[lb];
+    const int id = ws.layer_order[li];  // read with the count: not used past it
+    const int tok = ws.layer_tok[li];
+    const float v = ws.layer_val[li];
+    if (p < lc && id > 0 && id < a.N && tok >= 0) k = make_key(v, (uint32_t)id);
     keys[f] = k;
   }
   __syncthreads();
@@ -159,7 +156,9 @@ __device__ void batch_items(double* items, double* part, int cap, int B, F vb) {
       if (s2 < cap) {
         double acc = 0.0;
         for (int w = 0; w < nw; ++w) acc += part[w * kItemChunk + j];
-        items[s2] = acc / (double)B;
+        // dividing by a power of two is multiplying by its exact inverse (a long fp64 division saved)
+        items[s2] = (B & (B - 1)) == 0 ? acc * __hiloint2double((1023 - (31 - __clz(B))) << 20, 0)
+                                       : acc / (double)B;
       }
     }
     __syncthreads();
@@ -170,8 +169,8 @@ __device__ void batch_items(double* items, double* part, int cap, int B, F vb) {
 // c_k <= c_k0 or (u_k - u_k0) / (c_k - c_k0) >= thr, with u_k = items[0] + ... + items[k-1]. For
 // c_k > c_k0 the second test is u_k - thr c_k >= u_k0 - thr c_k0, so with q_k = u_k - thr c_k both
 // tests compare precomputed values. Warp 0 builds u (prefix sums, u[0] = 0), q and the ordered
-// images of c and q; thread 0 then walks k while warp 1 runs `during_walk` (work that needs u and
-// may overlap the walk). `u`, `cimg`, `qimg` ([cap+1] each) are shared scratch. All threads call
+// images of c and q; thread 0 then walks k while the other warps run during_walk(warp) (work that
+// needs u and may overlap the walk). `u`, `cimg`, `qimg` ([cap+1] each) are shared scratch. All threads call
 // it; every thread gets k0.
 template <class DuringWalk>
 __device__ int selection_rule(const double* items, const double* cost, double thr, int cap, double* u,
@@ -211,8 +210,8 @@ __device__ int selection_rule(const double* items, const double* cost, double th
       }
     }
     *result = k0;
-  } else if ((tid >> 5) == 1) {
-    during_walk();
+  } else if ((tid >> 5) >= 1) {
+    during_walk(tid >> 5);
   }
   __syncthreads();
   return *result;
@@ -273,32 +272,43 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
   batch_items(items, part, wcap, a.B, [&](int b, int s) {
     const int64_t lb = (int64_t)b * (a.D + 1) + a.d;
     const int cnt = ws.layer_count[lb];
-    const int id = ws.layer_order[lb * a.LW + s];  // read with the count: -1 past it
-    if (s >= cnt || id < 0) return 0.0;
-    return (double)expf(ws.value[(int64_t)b * a.N + id]);
+    const float v = ws.layer_val[lb * a.LW + s];  // read with the count: not used past it
+    if (s >= cnt) return 0.0;
+    return (double)expf(v);
   });
   __syncthreads();
   const int cap = min(a.p.width_cap, s_maxcand);
-  // While thread 0 walks the selection, warp 1 evaluates the grow test for every width k the walk
-  // may choose (the FIFO as it would be after appending u_k / u_prev), so that no fp64 division is
-  // left for after the walk. Same operations, in the same order, as the update below.
-  auto grow_for_all_widths = [&]() {
+  // While thread 0 walks the selection, warp 1 evaluates the grow test for every width k the walk may
+  // choose, and warp 2 the FIFO entry u_k / u_prev that width would append. The test is
+  // alpha u_k / c_k >= C2 with alpha the mean of the FIFO after the append; with S the sum of the
+  // entries that stay (the oldest drops out when the FIFO is full) and L its new length it reads
+  // (S u_prev + u_k) u_k >= C2 c_k L u_prev for u_prev > 0, and S u_k >= C2 c_k L before the first
+  // append, which needs no fp64 division (equal to the quotient form up to rounding).
+  auto grow_for_all_widths = [&](int w) {
     const int len = cs.fifo_len;
-    for (int k = 1 + lane; k <= cap; k += 32) {
-      const double uk = u[k];
-      double sum = 0.0;
-      int nlen = len;
-      if (cs.u_prev >= 0.0) {
-        const double r = uk / cs.u_prev;
-        ratio_k[k] = r;
-        for (int j = len < a.p.R ? 0 : 1; j < len; ++j) sum += cs.fifo[j];
-        sum += r;
-        nlen = len < a.p.R ? len + 1 : len;
-      } else {
-        for (int j = 0; j < len; ++j) sum += cs.fifo[j];
+    const double up = cs.u_prev;
+    if (w == 1) {
+      const bool app = up >= 0.0;  // this layer appends a ratio
+      double kept = 0.0;
+      for (int j = app && len >= a.p.R ? 1 : 0; j < len; ++j) kept += cs.fifo[j];
+      const int nlen = app ? (len < a.p.R ? len + 1 : len) : len;
+      for (int k = 1 + lane; k <= cap; k += 32) {
+        const double uk = u[k];
+        bool g;
+        if (nlen <= 0) {
+          g = false;  // the mean of an empty FIFO is NaN
+        } else if (app && up > 0.0) {
+          g = (kept * up + uk) * uk >= a.p.C2 * cost[k] * (double)nlen * up;
+        } else if (app) {  // u_prev = 0: the ratio is not finite; the quotient form as written
+          const double alpha = (kept + uk / up) / (double)nlen;
+          g = alpha * uk >= a.p.C2 * cost[k];
+        } else {
+          g = kept * uk >= a.p.C2 * cost[k] * (double)nlen;
+        }
+        grow_k[k] = (a.d < a.p.D_max) && g;
       }
-      const double alpha = sum / (double)nlen;
-      grow_k[k] = (a.d < a.p.D_max) && (alpha * uk >= a.p.C2 * cost[k]);  // alpha * u / c_k >= C2
+    } else if (w == 2 && up >= 0.0) {
+      for (int k = 1 + lane; k <= cap; k += 32) ratio_k[k] = u[k] / up;
     }
   };
   int n = 0;
@@ -363,7 +373,7 @@ __global__ void __launch_bounds__(kPruneThreads) cast_verify_kernel(PruneArgs a)
   const int cap = min(a.p.m_cap, maxn);
   batch_items(items, part, cap, a.B, [&](int b, int s) { return lin[(int64_t)b * a.p.m_cap + s]; });
   int m = 0;
-  if (cap > 0) m = selection_rule(items, cost, a.p.C3, cap, u, cimg, qimg, &s_k0, [] {});
+  if (cap > 0) m = selection_rule(items, cost, a.p.C3, cap, u, cimg, qimg, &s_k0, [](int) {});
   if (tid == 0) a.out.m[0] = m;
   if (a.sel) {  // the rerank, as dt_rerank(m) would write it: each request's top-m ids, ascending
     const int lane = tid & 31;
@@ -397,7 +407,7 @@ __global__ void graft_checkpoint_kernel(PruneArgs a) {
     if (a.p.ckpt_layer[s] != li) continue;
     const int64_t lb = (int64_t)b * (a.D + 1) + a.d;
     double c = 0.0;
-    if (ws.layer_count[lb] > 0) c = (double)expf(ws.value[(int64_t)b * a.N + ws.layer_order[lb * a.LW]]);
+    if (ws.layer_count[lb] > 0) c = (double)expf(ws.layer_val[lb * a.LW]);
     if (!(c > a.p.tau[s])) {
       a.out.stop[b] = 1;
       if (a.out.stage) a.out.stage[b] = s;

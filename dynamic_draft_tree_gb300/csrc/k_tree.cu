@@ -167,18 +167,23 @@ __global__ void __launch_bounds__(kRowThreads, 4) expand_kernel(ExpandArgs a) {
     if (sm.last) {  // last row of the request: order the new layer by (value desc, id asc)
       if (tid == 0) ws.req_counter[b] = 0;
       const int n = active * a.K;
-      int32_t* order = ws.layer_order + ((int64_t)b * (a.D + 1) + a.d) * a.LW;
-      // keys staged in the candidate buffer (n <= W*K <= 1024 = kCandCap)
+      const int64_t lo = ((int64_t)b * (a.D + 1) + a.d) * a.LW;
+      // keys staged in the candidate buffer (n <= W*K <= 1024 = kCandCap), the tokens after it (the
+      // stage memory holds both); the layer's values and tokens are written in order next to the ids
+      int32_t* tok_s = reinterpret_cast<int32_t*>(sm.cand + kCandCap);
       for (int i = tid; i < n; i += blockDim.x) {
-        const int id = a.base + i;
-        sm.cand[i] = make_key(__ldcg(&ws.value[(int64_t)b * a.N + id]), (uint32_t)id);
+        const int64_t gi = (int64_t)b * a.N + a.base + i;
+        sm.cand[i] = make_key(__ldcg(&ws.value[gi]), (uint32_t)(a.base + i));
+        tok_s[i] = __ldcg(&ws.token[gi]);
       }
       __syncthreads();
       for (int i = tid; i < n; i += blockDim.x) {
         const uint64_t k = sm.cand[i];
         int rank = 0;
         for (int j = 0; j < n; ++j) rank += (sm.cand[j] > k);
-        order[rank] = (int32_t)key_id(k);
+        ws.layer_order[lo + rank] = (int32_t)key_id(k);
+        ws.layer_val[lo + rank] = key_value(k);
+        ws.layer_tok[lo + rank] = tok_s[i];
       }
       if (tid == 0) ws.layer_count[(int64_t)b * (a.D + 1) + a.d] = n;
     }
