@@ -239,8 +239,9 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
   __shared__ uint64_t cimg[kMaxW + 2], qimg[kMaxW + 2];
   __shared__ double ratio_k[kMaxW + 2];
   __shared__ uint8_t grow_k[kMaxW + 2];
+  __shared__ double cost_all[kPruneThreads];  // c_k of every table row, when they fit the idle warps
   __shared__ CastState cs;
-  __shared__ int s_maxcand, s_grow, s_k0, s_width;
+  __shared__ int s_maxcand, s_grow, s_k0, s_width, s_row;
   const Workspace& ws = a.ws;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nwarps = (int)(blockDim.x >> 5);
@@ -254,12 +255,25 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
   const bool f_pref = a.select && a.B <= nwarps;
   if (f_pref && warp < a.B) f_avail = frontier_candidates(ws, warp, a.N, a.W, a.LW, a.D, a.d, f_id, f_tok, f_val);
   const int wcap = min(a.p.width_cap, a.LW);
+  // normalised draft cost of k frontier nodes at the current context: c_k = S_D[row][k-1] / S_T[row][0].
+  // When the table's rows x wcap entries fit the warps between the request warps and the two helper
+  // warps, those compute every row's entries while the last warp finds the row (the row needs the
+  // context sum, so this takes the loads off the chain); otherwise the last warp does both in turn.
+  const int free0 = a.B * 32, nfree = (nwarps - 2) * 32 - free0;
+  const bool par_cost = a.p.M_rows * wcap <= nfree;
+  if (par_cost && tid >= free0 && tid < free0 + a.p.M_rows * wcap) {
+    const int t = tid - free0, r = t / wcap, k = t - r * wcap + 1;
+    cost_all[t] = a.p.S_D[(int64_t)r * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)r * a.p.N_cols];
+  }
   if (warp == nwarps - 1) {
-    // normalised draft cost of k frontier nodes at the current context: c_k = S_D[row][k-1] / S_T[row][0]
     const int64_t ctx = ws.cast->ctx_sum;
     const int row = table_row((double)(a.p.n0 + ctx), a.p.L, a.p.M_rows);
-    for (int k = 1 + lane; k <= wcap; k += 32)
-      cost[k] = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
+    if (par_cost) {
+      if (lane == 0) s_row = row;
+    } else {
+      for (int k = 1 + lane; k <= wcap; k += 32)
+        cost[k] = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
+    }
   }
   if (warp == nwarps - 2) {
     int mc = 0;
@@ -278,6 +292,7 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
   });
   __syncthreads();
   const int cap = min(a.p.width_cap, s_maxcand);
+  const double* costp = par_cost ? cost_all + (int64_t)s_row * wcap - 1 : cost;  // costp[k] = c_k
   // While thread 0 walks the selection, warp 1 evaluates the grow test for every width k the walk may
   // choose, and warp 2 the FIFO entry u_k / u_prev that width would append. The test is
   // alpha u_k / c_k >= C2 with alpha the mean of the FIFO after the append; with S the sum of the
@@ -298,12 +313,12 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
         if (nlen <= 0) {
           g = false;  // the mean of an empty FIFO is NaN
         } else if (app && up > 0.0) {
-          g = (kept * up + uk) * uk >= a.p.C2 * cost[k] * (double)nlen * up;
+          g = (kept * up + uk) * uk >= a.p.C2 * costp[k] * (double)nlen * up;
         } else if (app) {  // u_prev = 0: the ratio is not finite; the quotient form as written
           const double alpha = (kept + uk / up) / (double)nlen;
-          g = alpha * uk >= a.p.C2 * cost[k];
+          g = alpha * uk >= a.p.C2 * costp[k];
         } else {
-          g = kept * uk >= a.p.C2 * cost[k] * (double)nlen;
+          g = kept * uk >= a.p.C2 * costp[k] * (double)nlen;
         }
         grow_k[k] = (a.d < a.p.D_max) && g;
       }
@@ -312,7 +327,7 @@ __global__ void __launch_bounds__(kPruneThreads) cast_width_depth_kernel(PruneAr
     }
   };
   int n = 0;
-  if (cap > 0) n = selection_rule(items, cost, a.p.C1, cap, u, cimg, qimg, &s_k0, grow_for_all_widths);
+  if (cap > 0) n = selection_rule(items, costp, a.p.C1, cap, u, cimg, qimg, &s_k0, grow_for_all_widths);
   if (tid == 0) {
     bool grow = false;
     if (cap > 0) {
@@ -358,20 +373,28 @@ __global__ void __launch_bounds__(kPruneThreads) cast_verify_kernel(PruneArgs a)
   __shared__ double part[32 * kItemChunk];
   __shared__ double u[kMaxP + 2];
   __shared__ uint64_t cimg[kMaxP + 2], qimg[kMaxP + 2];
-  __shared__ int maxn, s_k0;
+  __shared__ int s_maxn, s_k0;
   const Workspace& ws = a.ws;
-  const int tid = threadIdx.x;
-  if (tid == 0) maxn = 0;
-  __syncthreads();
-  for (int b = tid; b < a.B; b += blockDim.x) atomicMax(&maxn, ws.sorted_cnt[b]);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nwarps = (int)(blockDim.x >> 5);
   const double* lin = ws.sorted_lin;
-  const int row = table_row((double)a.p.n0, a.p.L, a.p.M_rows);
   const int mcap = a.p.m_cap;
-  for (int k = 1 + tid; k <= mcap; k += blockDim.x)
-    cost[k] = a.p.S_T[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
-  __syncthreads();
-  const int cap = min(a.p.m_cap, maxn);
-  batch_items(items, part, cap, a.B, [&](int b, int s) { return lin[(int64_t)b * a.p.m_cap + s]; });
+  // No barrier before the loads: the last two warps compute the cost vector, the third-last the
+  // largest count, while batch_items reads the linear values of every slot up to m_cap (the sort
+  // left 0 past each request's count); its first barrier publishes all of it.
+  if (warp >= nwarps - 2) {
+    const int row = table_row((double)a.p.n0, a.p.L, a.p.M_rows);
+    for (int k = 1 + (tid - (nwarps - 2) * 32); k <= mcap; k += 64)
+      cost[k] = a.p.S_T[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
+  }
+  if (warp == nwarps - 3) {
+    int mc = 0;
+    for (int b = lane; b < a.B; b += 32) mc = max(mc, ws.sorted_cnt[b]);
+    mc = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)max(mc, 0));
+    if (lane == 0) s_maxn = mc;
+  }
+  batch_items(items, part, mcap, a.B, [&](int b, int s) { return lin[(int64_t)b * a.p.m_cap + s]; });
+  const int cap = min(a.p.m_cap, s_maxn);
   int m = 0;
   if (cap > 0) m = selection_rule(items, cost, a.p.C3, cap, u, cimg, qimg, &s_k0, [](int) {});
   if (tid == 0) a.out.m[0] = m;
