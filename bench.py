@@ -111,8 +111,8 @@ class Clocks:
 
 # DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte of each row-pass
 # kernel, from the captures summarised in profiles/ (None once the kernel has changed since).
-TRAFFIC_PER_ALGO_BYTE = {"dt_expand_layer": 20.671488e6 / (80 * 256512),   # layer 2 of a CAST round, 80 rows
-                         "dt_verify": (84.241664e6 + 1.554432e6) / (328 * 256512)}  # 328 used rows
+TRAFFIC_PER_ALGO_BYTE = {"dt_expand_layer": 20.685056e6 / (80 * 256512),   # layer 2 of a CAST round, 80 rows
+                         "dt_verify": (84.258048e6 + 1.573120e6) / (328 * 256512)}  # 328 used rows
 
 
 def measured_peaks():
