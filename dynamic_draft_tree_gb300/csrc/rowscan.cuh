@@ -211,22 +211,6 @@ __device__ __forceinline__ void combine_partial_sums(ScanSmem& sm, float m0, flo
 }
 
 // ---------------------------------------------------------------- warp top-K list ----
-__device__ __forceinline__ uint64_t shfl_up_u64(uint64_t v, int d) {
-  uint32_t lo = __shfl_up_sync(0xFFFFFFFFu, (uint32_t)v, d);
-  uint32_t hi = __shfl_up_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), d);
-  return ((uint64_t)hi << 32) | lo;
-}
-
-// Inserts key k (same value in every lane) into the lane-distributed descending list L of K keys.
-__device__ __forceinline__ void wl_insert(uint64_t& L, uint64_t k, int K, int lane) {
-  const unsigned gt = __ballot_sync(0xFFFFFFFFu, lane < K && L > k);
-  const int p = __popc(gt);
-  if (p >= K) return;  // warp-uniform
-  const uint64_t up = shfl_up_u64(L, 1);
-  if (lane > p && lane < K) L = up;
-  if (lane == p) L = k;
-}
-
 // Result of a segment scan; the segment's top-K keys are left in sm.topk (descending, 0-padded).
 struct SegOut {
   float m;            // softmax scans: thread 0 holds the max; otherwise every thread: the best key's value
