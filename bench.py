@@ -294,7 +294,7 @@ def run_ours(args):
     roofline = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                 "traffic": None if tr is None else tr * bpl, "kernel": kname, "peak_source": peak_kind,
                 "bytes_per_launch": bpl, "avg_launch_us": us}
-    launches_per_round = 1 + (D - 1 if w["policy"] != "cast" else 0) + D + \
+    launches_per_round = 1 + (D if w["policy"] != "cast" else 1) + D + \
         (D if w["policy"] in ("cast", "graft") else 0) + \
         (2 if w["policy"] == "cast" else 1) + 1 + (3 if w["T"] == 1 else 2) + \
         (2 if w["policy"] == "graft" else 0)

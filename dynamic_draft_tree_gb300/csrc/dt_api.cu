@@ -221,7 +221,6 @@ int dt_select_frontier(dt_handle* h, const int32_t* width, int32_t width_len, co
                        int32_t* frontier_token, cudaStream_t s) {
   if (!h) return fail(DT_ERR_ARG, "dt_select_frontier: null handle");
   if (h->B < 1) return fail(DT_ERR_ARG, "dt_select_frontier: no tree (call dt_tree_reset)");
-  if (h->depth < 1) return fail(DT_ERR_ARG, "dt_select_frontier: no layer built yet");
   if (h->depth >= h->cfg.D_max) return fail(DT_ERR_ARG, "dt_select_frontier: tree at D_max");
   if (width && width_len != 1 && width_len != h->B) return fail(DT_ERR_ARG, "width_len must be 1 or B");
   cudaError_t e = dt::launch_select_frontier(h, width, width_len, stop, frontier_token, s);

@@ -38,10 +38,20 @@ __global__ void tree_reset_kernel(Workspace ws, const int32_t* __restrict__ root
     ws.parent[i] = -1;
     ws.node_depth[i] = layer_of(id, K, LW);
   }
+  // layer orders invalid, except layer 0 = {root}: id 0, value 0, the root token (so that the
+  // frontier of layer 1 is selected like any other)
   const int64_t lo_total = (int64_t)B * (D + 1) * LW;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < lo_total;
-       i += (int64_t)gridDim.x * blockDim.x)
-    ws.layer_order[i] = -1;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t lb = i / LW;
+    if (lb % (D + 1) == 0 && i % LW == 0) {
+      ws.layer_order[i] = 0;
+      ws.layer_val[i] = 0.0f;
+      ws.layer_tok[i] = root[lb / (D + 1)];
+    } else {
+      ws.layer_order[i] = -1;
+    }
+  }
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)B * (D + 1);
        i += (int64_t)gridDim.x * blockDim.x)
     ws.layer_count[i] = (i % (D + 1)) == 0 ? 1 : 0;

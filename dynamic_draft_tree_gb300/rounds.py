@@ -93,8 +93,7 @@ class RoundRunner:
                     dt_select_frontier(h, self.width, self.stop, self.frontier_token)
                 F = self.k
             else:
-                self.frontier_token.fill_(-1)
-                self.frontier_token[:, 0] = roots
+                dt_select_frontier(h, None, None, self.frontier_token)  # layer 0 = {root}: the root in slot 0
                 F = 1
             dt_expand_layer(h, draft_rows(d, self.frontier_token), F)
             if after_expand is not None:

@@ -173,7 +173,9 @@ int dt_clear_status(dt_handle* h, cudaStream_t s);
 int dt_tree_reset(dt_handle* h, int32_t B, const int32_t* root_token, cudaStream_t s);
 
 /* a2 (EAGLE-2 §扩展阶段): choose the frontier of the next layer: for request b, the first
- * w_b nodes of the newest layer in (value desc, id asc) order, slotted in ascending id.
+ * w_b nodes of the newest layer in (value desc, id asc) order, slotted in ascending id. Right
+ * after dt_tree_reset the newest layer is layer 0 = {root}: the call then gives the frontier of
+ * layer 1 (the root in slot 0, its token in frontier_token[b][0]).
  * w_b = min(width, W, nodes in the layer), 0 where stop[b] != 0. width: device [width_len]
  * with width_len 1 (batch-wide) or B, or NULL for W. stop: device [B] or NULL.
  * frontier_token: device [B][W] out (tokens of the slots, -1 padded) or NULL. */

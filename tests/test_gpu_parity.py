@@ -137,8 +137,14 @@ def test_host_argument_errors(torch):
     dt.dt_tree_reset(h, torch.zeros(2, dtype=torch.int32, device="cuda"))
     with pytest.raises(dt.DtError):
         dt.dt_expand_layer(h, x, 3)                     # F > W
-    with pytest.raises(dt.DtError):
-        dt.dt_select_frontier(h)                        # no layer built
+    # right after the reset the newest layer is layer 0 = {root}: the layer-1 frontier is the root
+    ft = torch.full((2, 2), 7, dtype=torch.int32, device="cuda")
+    dt.dt_tree_reset(h, torch.tensor([5, 9], dtype=torch.int32, device="cuda"))
+    dt.dt_select_frontier(h, frontier_token=ft)
+    assert ft.cpu().tolist() == [[5, -1], [9, -1]]
+    t = dt.dt_get_tree(h)
+    assert t["frontier"][:2].cpu().tolist() == [[0, -1], [0, -1]]
+    assert t["frontier_count"][:2].cpu().tolist() == [1, 1]
     with pytest.raises(dt.DtError):
         dt.dt_expand_layer(h, x, 1, ld=999)             # ld < V
     with pytest.raises(dt.DtError):
