@@ -129,7 +129,10 @@ __device__ __forceinline__ uint64_t d2ord(double x) {
   return (u & 0x8000000000000000ull) ? ~u : (u | 0x8000000000000000ull);
 }
 
-constexpr int kPruneThreads = 1024;  // 32 warps
+constexpr int kPruneThreads = 1024;  // 32 warps (most threads a prune launch uses)
+// Threads of a prune launch: 16 warps while they hold one warp per request plus the helper warps
+// (B <= 16; fewer warps make every block barrier shorter), 32 beyond.
+inline int prune_threads(int B) { return B <= 16 ? kPruneThreads / 2 : kPruneThreads; }
 constexpr int kItemChunk = 64;       // items per pass (two per lane)
 
 // items[s] = (1/B) sum_b vb(b, s) for s < cap, in fp64. Warp w sums requests b = w, w + 32, ... for
@@ -492,13 +495,13 @@ cudaError_t launch_cast_prune(dt_handle* h, int policy, const dt_prune_params* p
   a.ftok = nullptr;
   a.sel = nullptr;
   if (policy == DT_POLICY_CAST_WIDTH_DEPTH) {
-    launch_k(cast_width_depth_kernel, dim3(1), dim3(kPruneThreads), 0, s, a);
+    launch_k(cast_width_depth_kernel, dim3(1), dim3(prune_threads(h->B)), 0, s, a);
     return cudaGetLastError();
   }
   if (policy == DT_POLICY_CAST_VERIFY) {
     cudaError_t e = launch_sort(h, 1, nullptr, 1, p->m_cap, nullptr, s);
     if (e != cudaSuccess) return e;
-    launch_k(cast_verify_kernel, dim3(1), dim3(kPruneThreads), 0, s, a);
+    launch_k(cast_verify_kernel, dim3(1), dim3(prune_threads(h->B)), 0, s, a);
     return cudaGetLastError();
   }
   launch_k(graft_checkpoint_kernel, dim3((h->B + 127) / 128), dim3(128), 0, s, a);
@@ -521,7 +524,7 @@ cudaError_t launch_cast_prune_select(dt_handle* h, const dt_prune_params* p, con
   a.select = 1;
   a.ftok = frontier_token;
   a.sel = nullptr;
-  launch_k(cast_width_depth_kernel, dim3(1), dim3(kPruneThreads), 0, s, a);
+  launch_k(cast_width_depth_kernel, dim3(1), dim3(prune_threads(h->B)), 0, s, a);
   return cudaGetLastError();
 }
 
@@ -543,7 +546,7 @@ cudaError_t launch_cast_verify_rerank(dt_handle* h, const dt_prune_params* p, co
   a.select = 0;
   a.ftok = nullptr;
   a.sel = selected;
-  launch_k(cast_verify_kernel, dim3(1), dim3(kPruneThreads), 0, s, a);
+  launch_k(cast_verify_kernel, dim3(1), dim3(prune_threads(h->B)), 0, s, a);
   return cudaGetLastError();
 }
 
