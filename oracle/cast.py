@@ -16,7 +16,7 @@ in Large Language Models", §关键设计:
 4. verify count: u_k = sum_{j<=k} v_(j), c_k = S_T[select(n_0)][k] / S_T[select(n_0)][1],
    threshold C3, same selection rule.
 
-Readings (listed in the design doc; the body of Algorithm 1 is not on the page):
+Readings taken where the page is silent or garbled (the body of Algorithm 1 is not on the page):
 
 * select(): the printed form max(floor(c/L), M-1) maps every c past the table;
   read as row = min(floor(c/L), M_rows - 1).

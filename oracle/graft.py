@@ -13,7 +13,7 @@ Decoding", the three-step method description:
     verified token refresh its row of M with the top-k successors of the
     target's next-token distribution at that position.
 
-Readings (listed in DESIGN.md):
+Readings taken where the page is silent or garbled:
 
 * Checkpoints d0/d1/d5 are layer indices 0, 1, 5, i.e. draft layers 1, 2, 6
   of the D_E = 8 layer base tree; the test is strict ">" as printed; it is

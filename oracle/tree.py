@@ -8,7 +8,7 @@ value(parent) * confidence(child)), §"重排阶段" (top-m over all nodes, shal
 first on ties, connected subtree, flatten + ancestor-only mask), and the
 implementation flow in §"一段更贴近实现的流程".
 
-Readings taken where the page is silent (each is listed in the design doc):
+Readings taken where the page is silent:
 
 * Values are kept in log form, root value 0, value = sum of log c on the path
   (Graft's page writes the same score as S_d = S_{d-1} + log q).

@@ -7,7 +7,7 @@ shape, makes the output distribution equal the target's; greedy is
 deterministic) and step 3 of §"一段更贴近实现的流程" (apply the rule along
 the candidate paths, commit the accepted tokens).
 
-Readings (listed in DESIGN.md):
+Readings taken where the page is silent or garbled:
 
 * Greedy: for every root-to-leaf retrieve row, count the leading positions
   whose token equals the argmax (ties to the lower id) of the target row of

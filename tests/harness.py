@@ -1,7 +1,7 @@
 """Test harness: the same seeded rows fed to the oracle (host generator) and the GPU path
 (device generator), round drivers for both, and the comparison rules.
 
-Comparison rules (readings listed in the design doc):
+Comparison rules:
   * index outputs (tokens, parents, frontier sets, selections, masks, position ids, retrieve rows,
     accepted lengths and paths, bonus tokens, M rows) must be equal;
   * log confidences and log values: |gpu - oracle| <= 2e-6 * max(1, |oracle|);
