@@ -49,6 +49,25 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, world):
+    """The largest x over all ranks (the slowest rank's time); x itself on one rank. Works on the
+    NCCL (device tensor) and gloo (host tensor) process groups."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as tdist
+
+    dev = "cuda" if tdist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms_max):
+    """Whole-job rate: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank / (ms_max / 1e3)
+
+
 def workload_config(w, g):
     return {"workload": f"{w['policy']} tree round, B={w['B']}, V={w['V']}, bf16 logits, K={w['K']}, "
                         f"k<={w['k']}, depth<={w['D']}, m<={g['m_cap']}, greedy verify",
@@ -269,11 +288,8 @@ def run_ours(args):
     ms = t0.elapsed_time(t1)
     graph_ev.replay()  # per-kernel events (not part of the timed region)
     torch.cuda.synchronize()
-    if world > 1:
-        tt = torch.tensor([ms], device="cuda")
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = world * args.steps / (ms / 1e3)
+    ms = max_over_ranks(ms, world)
+    value = job_throughput(args.steps, world, ms)
 
     # per-kernel figures from the live events
     exp_ms = [a.elapsed_time(b) for a, b in ev_exp]
@@ -353,7 +369,8 @@ def run_ours(args):
         e1.record()
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1)
-        e2e = {"value": world * args.e2e_steps / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(bi),
+        e_ms = max_over_ranks(e_ms, world)
+        e2e = {"value": job_throughput(args.e2e_steps, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": int(bi),
                "d2h_bytes_per_step": int(bo), "double_buffered": True}
         e2e["consistent"] = bool(torch.equal(out_len.cuda(), rec_out[0][0]) and
                                  torch.equal(out_bonus.cuda(), rec_out[0][1]))
