@@ -18,7 +18,10 @@ What it restates, and from where (page titles, sections):
     attention mask.
   - §"先把投机解码的账本摆清楚" and §"无损性为什么没有被动态树破坏":
     speculative-sampling acceptance min(1, p/q) with residual
-    norm(max(0, p - q)); greedy decoding is deterministic.
+    norm(max(0, p - q)); greedy decoding is deterministic. ``sampled``
+    applies the same rule to children drawn from the draft distribution
+    without replacement (each sibling against the distribution it was drawn
+    from).
 * CAST ("Inference-Cost-Aware Dynamic Tree Construction ..."), §关键设计 1-4:
   cost lookup table with the grid quantiser select(c), width pruning by
   marginal utility against C1, depth pruning with the FIFO ratio buffer
