@@ -19,8 +19,12 @@ repeated applications of it, each against the distribution the child was actuall
 * An accepted child becomes the current node (its own target and draft distributions and
   children next). When every child of the current node is rejected, or it has none, the bonus
   token is drawn from the last residual and the round ends.
-* Only a prefix of a node's draw order can be verified: a later draw without the earlier ones
-  does not have the distribution q_j.
+* The verified tree is every drawn node: the frontier still chooses by value which nodes get
+  children (a node's children are drawn after that choice, so it cannot bias them), but no node
+  is dropped after its draw. Dropping drawn nodes by their own values (a rerank) makes whether a
+  child is tested depend on the child itself, and the first emitted token is then no longer
+  distributed as the target's (exact enumeration on a three-token vocabulary shows errors up to
+  0.09). The size of the verified tree is set by the frontier widths and the depth.
 
 Uniforms (Philox4x32-10, key = seed, round r; see ``philox``):
 
@@ -178,3 +182,38 @@ def walk(children, target, draft, seed, rnd, b, V, gaps=None):
             return chain, bonus_from_residual(r, philox.gumbel_uniforms(seed, rnd, b, cur, V), gaps)
         cur = kids[j][0]
         chain.append(cur)
+
+
+def verify_tree(tree, meta, target_row, seed, rnd, gaps=None):
+    """Sampled-draft verify of every request of a flattened tree (``tree.build_meta`` layout).
+
+    ``tree`` is the ``OracleTree`` whose expansion drew the children (it keeps, for every expanded
+    node, the draft row its children were drawn from) and ``meta`` its flattening with every drawn
+    node selected; ``target_row(b, i)`` is the target row at position i. A position's children are tested in position order, which is their draw order
+    (ids grow with the draw rank and positions with the id). Returns accepted lengths, accepted
+    positions (root first, -1 padded) and bonus tokens.
+    """
+    B, P, D_path = meta["retrieve"].shape
+    acc = np.zeros(B, np.int64)
+    path = np.full((B, D_path), -1, np.int64)
+    bonus = np.zeros(B, np.int64)
+    for b in range(B):
+        n_pos = int(meta["n_pos"][b])
+        tok, par, node = meta["tokens"][b], meta["parents"][b], meta["node_id"][b]
+        children = {}
+        for j in range(1, n_pos):
+            children.setdefault(int(par[j]), []).append((j, int(tok[j])))
+        V = np.asarray(target_row(b, 0)).size
+
+        def target(i):
+            return softmax(target_row(b, i))
+
+        def draft(i):
+            row = tree.draft_row[b].get(int(node[i]))
+            return softmax(row) if row is not None else np.full(V, 1.0 / V)  # unused: no children
+
+        chain, bt = walk(children, target, draft, seed, rnd, b, V, gaps)
+        acc[b] = len(chain) - 1
+        path[b, :len(chain)] = chain
+        bonus[b] = bt
+    return acc, path, bonus

@@ -114,6 +114,7 @@ class OracleTree:
         self.cur_depth = 0
         self.frontier = [[0] for _ in range(B)]      # layer 1 expands the root
         self.layer_sorted = [dict() for _ in range(B)]
+        self.draft_row = [dict() for _ in range(B)]  # sampled drafts: node -> the row its children came from
 
     # -- helpers ---------------------------------------------------------------
     def valid(self, b, i):
@@ -139,11 +140,14 @@ class OracleTree:
         return out[::-1]
 
     # -- expansion (a1 + a2) ---------------------------------------------------
-    def expand_layer(self, rows):
+    def expand_layer(self, rows, sampler=None):
         """Expand the current frontier into layer d = cur_depth + 1.
 
         ``rows`` is an array [B][F][V] of logits, or a callable (b, f) -> row;
-        row f of request b is the draft row of frontier slot f.
+        row f of request b is the draft row of frontier slot f. With ``sampler``
+        (sampled drafts, ``oracle.sampled``), sampler(b, node, row) gives the
+        node's children in draw order (at most K; missing ones stay invalid)
+        instead of the top-K, and each expanded node keeps its row.
         """
         d = self.cur_depth + 1
         if d > self.D:
@@ -153,8 +157,13 @@ class OracleTree:
         for b in range(self.B):
             for f, pid in enumerate(self.frontier[b]):
                 row = rows(b, f) if callable(rows) else rows[b][f]
-                toks, logc, _, _ = row_softmax_topk(row, K)
-                for r in range(K):
+                toks, logc, m, logS = row_softmax_topk(row, K)
+                if sampler is not None:
+                    x = np.asarray(row, dtype=np.float64)
+                    toks = np.asarray(sampler(b, pid, x), dtype=np.int64)[:K]
+                    logc = (x[toks] - m) - logS
+                    self.draft_row[b][pid] = x
+                for r in range(len(toks)):
                     i = base + f * K + r
                     self.token[b, i] = toks[r]
                     self.parent[b, i] = pid

@@ -8,9 +8,12 @@ What fixes them (not the oracle itself):
   the number of siblings, the emitted token is distributed exactly as the target's p. Checked by
   exact enumeration of every ordered draw, and by Monte Carlo with the Philox uniforms over a
   two-level tree (first token ~ p_root; second token, after an accepted first one, ~ p(.|t1)).
+* The same for a whole round: with the frontier chosen by value and every drawn node verified,
+  exact enumeration of every draw at two layers gives the target's first-token distribution.
 * Special cases: q = p accepts the first child always; a single child (K = 1) is the page's
-  one-token rule; a proposal that ignores the earlier siblings (a plausible mistake, planted here
-  on the CPU) is not lossless, so the pins above would catch it.
+  one-token rule. Two plausible mistakes, planted here on the CPU, are not lossless, so the pins
+  above would catch them: a proposal that ignores the earlier siblings, and a rerank that drops
+  drawn nodes by their own values.
 """
 import itertools
 
@@ -157,3 +160,99 @@ def test_two_level_walk_monte_carlo():
         exp = m * p_next[t]
         c2 = float(((second[t] - exp) ** 2 / exp).sum())
         assert c2 < 25.0, (t, c2)
+
+
+# ------------------------------------------------------------------ the tree side ----
+from oracle import tree as otree  # noqa: E402
+
+
+def _exact_first_token(V, K, xs_draft, x_target_root, keep=None):
+    """Exact first-token distribution of a round with one frontier node at layer 2 (W = 1, D = 2):
+    every ordered draw at both layers enumerated with its Plackett-Luce probability. ``keep``
+    (optional) maps (tree, root draw, layer-2 draw) to the root children actually verified."""
+    p = sampled.softmax(x_target_root)
+    q0 = sampled.softmax(xs_draft[0])
+    out = np.zeros(V)
+    for s1 in itertools.permutations(range(V), K):
+        w1 = sampled.plackett_luce(q0, s1)
+        t = otree.OracleTree(1, K, 1, 2, root_tokens=[0])
+        t.expand_layer(lambda b, f: xs_draft[0], sampler=lambda b, node, x: list(s1))
+        t.select_frontier(1)
+        fnode = int(t.frontier[0][0])
+        q1 = sampled.softmax(xs_draft[int(t.token[0, fnode])])
+        for s2 in itertools.permutations(range(V), K):
+            w = w1 * sampled.plackett_luce(q1, s2)
+            t2 = otree.OracleTree(1, K, 1, 2, root_tokens=[0])
+            t2.expand_layer(lambda b, f: xs_draft[0], sampler=lambda b, node, x: list(s1))
+            t2.select_frontier(1)
+            t2.expand_layer(lambda b, f: xs_draft[int(t2.token[0, fnode])], sampler=lambda b, node, x: list(s2))
+            kids = list(s1) if keep is None else keep(t2)
+            r, qj, stay = p.copy(), q0.copy(), 1.0
+            for tok in kids:
+                a = sampled.accept_probability(r, qj, tok)
+                out[tok] += w * stay * a
+                stay *= 1.0 - a
+                r = sampled.residual(r, qj)
+                qj = sampled.without(qj, tok)
+            out += w * stay * r
+    return out, p
+
+
+@pytest.mark.parametrize("trial", range(4))
+def test_whole_drawn_tree_is_exactly_lossless(trial):
+    """Frontier by value, every drawn node verified: the first token is exactly the target's."""
+    rng = np.random.default_rng(40 + trial)
+    V, K = 3, 2
+    xs = {tok: rng.normal(size=V) * 1.5 for tok in range(V)}
+    out, p = _exact_first_token(V, K, xs, rng.normal(size=V) * 1.5)
+    np.testing.assert_allclose(out, p, atol=1e-12, rtol=0)
+
+
+def test_pruning_drawn_nodes_by_value_is_not_lossless():
+    """Planted mistake: keep only the best m drawn nodes by value (a rerank after the draws); the
+    root children that survive then depend on their own draws, and the first token is biased."""
+    rng = np.random.default_rng(43)
+    V, K, m = 3, 2, 3
+    xs = {tok: rng.normal(size=V) * 1.5 for tok in range(V)}
+
+    def keep(t):
+        ids = t.sorted_nodes(0, t.nodes(0))[:m]
+        kept = sorted(i for i in ids if t.parent[0, i] == 0)
+        # a later-drawn root child without the earlier one is not a prefix: keep the prefix only
+        pref = []
+        for r, i in enumerate(range(1, 1 + K)):
+            if i not in kept:
+                break
+            pref.append(int(t.token[0, i]))
+        return pref
+
+    out, p = _exact_first_token(V, K, xs, rng.normal(size=V) * 1.5, keep=keep)
+    assert np.abs(out - p).max() > 1e-3
+
+
+def test_sampled_round_first_token_is_the_target_distribution():
+    """Whole round with sampled drafts and the Philox draws (expand 2 layers, frontier, every drawn
+    node verified, flatten, verify): the first emitted token is distributed as the target row at
+    the root."""
+    V, K, W, D = 4, 2, 2, 2
+    rng = np.random.default_rng(23)
+    x_draft = {tok: rng.normal(size=V) for tok in range(-1, V)}
+    x_target = {tok: rng.normal(size=V) * 1.3 for tok in range(-1, V)}
+    p_root = sampled.softmax(x_target[0])
+    n = 6000
+    first = np.zeros(V)
+    for rnd in range(n):
+        t = otree.OracleTree(1, K, W, D, root_tokens=[0])
+        drawn = lambda b, node, x, rnd=rnd: sampled.sample_children(x, K, seed=8, rnd=rnd, b=b, node=node)
+        t.expand_layer(lambda b, f: x_draft[int(t.token[b, t.frontier[b][f]])], sampler=drawn)
+        t.select_frontier(W)
+        t.expand_layer(lambda b, f: x_draft[int(t.token[b, t.frontier[b][f]])], sampler=drawn)
+        n_all = len(t.nodes(0))
+        sel = t.rerank(n_all, n_all)  # every drawn node
+        meta = otree.build_meta(t, sel, np.zeros(1, np.int64), n_all + 1, D + 1)
+        acc, path, bonus = sampled.verify_tree(
+            t, meta, lambda b, i: x_target[int(meta["tokens"][b, i]) if i > 0 else 0], seed=8, rnd=rnd)
+        tok0 = int(meta["tokens"][0, path[0, 1]]) if acc[0] >= 1 else int(bonus[0])
+        first[tok0] += 1
+    chi2 = float(((first - n * p_root) ** 2 / (n * p_root)).sum())
+    assert chi2 < 25.0, (chi2, first / n, p_root)
