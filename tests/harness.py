@@ -35,6 +35,14 @@ def round_id(rnd):
 
 _ROWS = {"owner": None, "rows": {}}
 
+# Seed redraws of the parity runs of this process: (label, rounds compared, requests redrawn, rounds
+# with at least one redraw). Printed at the end of the test session.
+REDRAW_LOG = []
+
+
+def log_redraws(label, rounds, redrawn, rounds_hit):
+    REDRAW_LOG.append((label, int(rounds), int(redrawn), int(rounds_hit)))
+
 
 class HostRows:
     """Row providers for the oracle, keyed like the device generator.

@@ -158,28 +158,39 @@ SMALL = [("pr1", dict(V=4099)), ("pr1", dict(V=32000)), ("vicuna", dict(V=32000)
          ("vicuna", dict(V=8192, T=1)), ("pr1", dict(V=3001, K=1, k=1, m=1)), ("pr1", dict(V=3001, m=60))]
 
 
-def _run_rounds(torch, w, rounds):
+def _run_rounds(torch, w, rounds, label=None, compare_from=0, chain_roots=True):
+    """GPU rounds against the oracle's, element by element; ``rounds`` is a count or the list of
+    round indices. Graft chains its rounds: M comes from the previous round, and so does the next
+    root (its bonus token) unless ``chain_roots`` is false (then every round drafts from the same
+    root tokens). Rounds before ``compare_from`` run on both sides (warm-up) but are compared only
+    through M. Logs the seed redraws under ``label``."""
     import harness
+    from dynamic_draft_tree_gb300 import dt_get_status
 
     gr = harness.GpuRound(w)
     M = None
     if w["policy"] == "graft":
         M = np.full((w["B"], w["V"], 8), -1, np.int64)
     roots = None
-    rejections = 0
-    for rnd in range(rounds):
+    redrawn = hit = 0
+    idx = list(range(rounds)) if isinstance(rounds, int) else list(rounds)
+    for n, rnd in enumerate(idx):
         ref, attempts, rej = harness.oracle_round(w, rnd, roots=roots, M=M)
-        rejections += rej
+        redrawn += rej
+        hit += rej > 0
         gr.round(rnd, attempts, ref["roots"])
-        from dynamic_draft_tree_gb300 import dt_get_status
-
         assert dt_get_status(gr.run.h) == 0
-        harness.compare_round(gr, ref)
+        if n >= compare_from:
+            harness.compare_round(gr, ref)
+        elif w["policy"] == "graft":  # warm-up: the refreshed M must still agree
+            np.testing.assert_array_equal(gr.M.cpu().numpy(), ref["M"], err_msg="M after warm-up round")
         if w["policy"] == "graft":
             M = ref["M"]
-            roots = ref["bonus"].astype(np.int32)
+            roots = ref["bonus"].astype(np.int32) if chain_roots else ref["roots"]
     gr.run.h.close()
-    return rejections
+    harness.log_redraws(label or f"{w['policy']} B={w['B']} V={w['V']} T={w['T']}", len(idx) - compare_from,
+                        redrawn, hit)
+    return redrawn
 
 
 @pytest.mark.parametrize("name,over", SMALL)
@@ -187,7 +198,70 @@ def test_round_parity_small(torch, name, over):
     w = with_sizes(name, **over)
     if w["m"] > 1 and name == "pr1" and over.get("m") == 60:
         w["D"] = 6
-    _run_rounds(torch, w, 3)
+    _run_rounds(torch, w, 3, label=f"small {name} {over}")
+
+
+# Stochastic verify (T = 1): 24 rounds each of a Vicuna-shaped and a stress-shaped batch at reduced
+# V, so that a few hundred acceptance tests and residual draws are compared (EAGLE-2 page,
+# §无损性为什么没有被动态树破坏).
+@pytest.mark.parametrize("name,over", [("vicuna", dict(V=4096, T=1)), ("stress", dict(V=3001, B=8, D=5))])
+def test_round_parity_sampling_many_rounds(torch, name, over):
+    _run_rounds(torch, with_sizes(name, **over), 24, label=f"T=1 {name} {over}")
+
+
+def test_round_parity_graft_after_warmup(torch):
+    """Graft page step (3): every round drafts again from the same root tokens, so the refresh of M
+    from the verified positions fills the rows the template reads: after five warm-up rounds
+    (about 80 % of the grafted nodes are real tokens by then, all of them two rounds later) eight
+    more rounds run with accepted paths through grafted nodes. Every round is compared in full."""
+    w = with_sizes("graft", V=2003, B=4)
+    _run_rounds(torch, w, 13, label="graft, 5 warm-up + 8 rounds, filled M", chain_roots=False)
+
+
+def test_round_parity_cast_table_rows(torch):
+    """CAST page §关键设计 1: rounds whose prefix lengths n0 = 512 (1 + r mod 16) select eight
+    different cost-table rows (r = 0, 2, ..., 14 -> rows 1, 3, ..., 15), plus the rows the growing
+    context reaches within each round."""
+    w = with_sizes("cast", V=12007)
+    _run_rounds(torch, w, range(0, 16, 2), label="cast table rows 1..15")
+
+
+def test_sampling_first_token_law_on_gpu(torch):
+    """Monte Carlo on the GPU alone: the first token a T = 1 round emits (the accepted child, or the
+    bonus if every child of the root is rejected) is distributed as the target's root row,
+    whatever the tree (EAGLE-2 page, §无损性为什么没有被动态树破坏). V = 8, a draft row unlike the
+    target, 1024 requests per round (independent Philox counters per request), 12 rounds; chi-square
+    with 7 degrees of freedom against softmax(target root row)."""
+    import dynamic_draft_tree_gb300 as dt
+    from dynamic_draft_tree_gb300.rounds import RoundRunner
+
+    V, B, K, k, D, m = 8, 1024, 3, 2, 2, 5
+    P, D_path = m + 1, D + 1
+    draft_row = torch.tensor([2.0, 1.5, 1.0, 0.2, -0.5, -1.0, 0.1, 0.0])
+    target_root = torch.tensor([0.3, 1.2, -0.4, 0.8, 0.0, -1.5, 0.5, 0.9])
+    other = torch.tensor([0.0, 0.5, 1.0, -0.5, 0.2, 0.1, -0.2, 0.3])
+    run = RoundRunner("eagle", B, V, K, k, D, P, D_path, m, dt.DT_F32, T=1)
+    draft = draft_row.repeat(B, k, 1).cuda().contiguous()
+    target = other.repeat(B, P, 1).clone()
+    target[:, 0] = target_root
+    target = target.cuda().contiguous()
+    roots = torch.zeros(B, dtype=torch.int32, device="cuda")
+    counts = np.zeros(V, np.int64)
+    for rnd in range(12):
+        run.run(roots, lambda d, ft: draft, lambda meta: target, seed=99, rnd=rnd << 8)
+        assert dt.dt_get_status(run.h) == 0
+        acc = run.accept_len.cpu().numpy()
+        path = run.accept_path.cpu().numpy()
+        tok = run.meta.tokens.cpu().numpy()
+        bonus = run.bonus.cpu().numpy()
+        first = np.where(acc >= 1, tok[np.arange(B), np.maximum(path[:, 1], 0)], bonus)
+        counts += np.bincount(first, minlength=V)
+    run.h.close()
+    p = torch.softmax(target_root.double(), 0).numpy()
+    n = counts.sum()
+    chi2 = float(((counts - n * p) ** 2 / (n * p)).sum())
+    assert n == 12 * B
+    assert chi2 < 29.9, (chi2, counts, n * p)   # 7 dof: P(chi2 > 29.9) ~ 1e-4
 
 
 def test_full_size_round_is_deterministic(torch):
@@ -243,7 +317,7 @@ FULL = [("pr1", {}, 3), ("vicuna", {}, 2), ("vicuna", dict(T=1), 2), ("cast", {}
 @pytest.mark.parametrize("name,over,rounds", FULL)
 def test_round_parity_full_size(torch, name, over, rounds):
     w = with_sizes(name, **over)
-    _run_rounds(torch, w, rounds)
+    _run_rounds(torch, w, rounds, label=f"full size {name} {over}")
 
 
 @pytest.mark.parametrize("V,K", [(128256, 32), (128256, 10), (70001, 8)])

@@ -55,12 +55,39 @@ def test_draw_order_frequencies_match_plackett_luce():
     assert chi2 < 110.0, chi2  # 59 degrees of freedom: p ~ 1e-4 at 104
 
 
+def _draw_counter_word2(b, node):
+    return sampled.DRAW_STREAM + 4096 * b + node
+
+
 def test_draw_uniforms_are_a_separate_stream():
-    """The draw noise does not reuse the residual or the acceptance uniforms of any position."""
-    u = sampled.draw_uniforms(5, 3, 1, 2, 64)
-    g = philox.gumbel_uniforms(5, 3, 1, 2, 64)
+    """The draw noise does not reuse the residual or the acceptance uniforms of any position.
+
+    The three streams share a round (counter words 0-1) and the key; they differ in words 2-3:
+      draw noise   word 2 = 0x40000000 + 4096 b + node, word 3 = v >> 2      (node < 4096)
+      residual     word 2 = 512 b + pos,                word 3 = v >> 2      (pos < 512)
+      acceptance   word 2 = 512 b + pos,                word 3 = 0x80000000
+    For every request b < 2^18, node < 4096 and pos < 512 the draw stream's word 2 lies in
+    [2^30, 2^31), the others' below 2^27 + 512; the acceptance stream's word 3 is 2^31, every
+    token group's below 2^29 (V < 2^31). So no two streams ever use the same counter."""
+    seed, rnd, b, node, V = 5, 3, 1, 2, 64
+    u = sampled.draw_uniforms(seed, rnd, b, node, V)
+    # the layout itself: each uniform is the published Philox block at the stated counter
+    for v in (0, 1, 5, 63):
+        w = philox.philox4x32_10((rnd, 0, _draw_counter_word2(b, node), v >> 2), (seed, 0))
+        assert u[v] == ((int(w[v & 3]) >> 9) + 0.5) * 2.0 ** -23
+    # range arithmetic at the extremes of every index
+    b_max, node_max, pos_max = (1 << 18) - 1, 4095, 511
+    lo_draw, hi_draw = _draw_counter_word2(0, 0), _draw_counter_word2(b_max, node_max)
+    assert lo_draw == 1 << 30 and hi_draw == (1 << 31) - 1
+    hi_other = 512 * b_max + pos_max
+    assert hi_other < lo_draw
+    assert ((1 << 31) - 1) >> 2 < 0x80000000
+    # and the values differ from the other two streams at the same (round, request, index)
+    g = philox.gumbel_uniforms(seed, rnd, b, node, V)
     assert (u > 0).all() and (u < 1).all()
     assert not np.allclose(u, g)
+    a = philox.accept_uniform(seed, rnd, b, node)
+    assert not np.any(np.abs(u - a) < 2.0 ** -22)
     with pytest.raises(ValueError):
         sampled.draw_uniforms(5, 3, 1, 4096, 8)
 
