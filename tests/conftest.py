@@ -31,6 +31,8 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
         tr.write_line(f"{label}: {rounds} rounds compared, {hit} redrawn, {redrawn} request redraws")
         tot_r, tot_q, tot_h = tot_r + rounds, tot_q + redrawn, tot_h + hit
     tr.write_line(f"total: {tot_r} rounds compared, {tot_h} redrawn, {tot_q} request redraws")
-    config.cache.set("dt/seed_redraws", {"runs": [list(x) for x in log],
-                                          "total": {"rounds": tot_r, "rounds_redrawn": tot_h,
-                                                    "request_redraws": tot_q}})
+    cache = getattr(config, "cache", None)
+    if cache is not None:
+        cache.set("dt/seed_redraws", {"runs": [list(x) for x in log],
+                                      "total": {"rounds": tot_r, "rounds_redrawn": tot_h,
+                                                "request_redraws": tot_q}})
