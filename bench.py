@@ -1,19 +1,24 @@
-"""Benchmark of the draft-tree hot path on the CAST batch workload (B=8, V=128256, bf16).
+"""Benchmark of the draft-tree hot path; headline on the CAST batch workload (B=8, V=128256, bf16).
 
 One step = one complete round of the path (EAGLE-2 expansion with CAST width/depth pruning for up
 to 8 layers, CAST verify count, rerank, flatten + metadata, greedy verify) over one batch of B=8
 requests, with its inputs already in HBM. The draft and target model forwards are not part of the
-path: their logits are produced by the seeded generator in an untimed recording pass (R rounds,
-each ~289 MB, so every timed step reads a different round: inputs larger than L2), and the timed
-steps replay the path on them. The replay must reproduce the recording pass's outputs bit for bit.
+path: their logits are produced by the seeded generator in an untimed recording pass (R rounds, so
+that the recorded inputs exceed L2 and every timed step reads a different round), and the timed
+steps replay the path on them. A replayed round must reproduce its recording bit for bit.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+The same measurement runs for the four other workloads (PR1, Vicuna greedy and sampling, Graft
+after its warm-up rounds, the fp32 B=64 stress batch with sampling); they are reported in the
+line's "per_config" block.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workloads a,b,...]
 
 Under torchrun each rank runs its own independent batch (requests shard across GPUs with no
 exchange: weak scaling). The reference arm times the fp64 CPU oracle on a bounded sample.
 """
 import argparse
 import json
+import math
 import os
 import subprocess
 import sys
@@ -27,6 +32,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "draft-tree rounds/s (expand+rerank+verify) at B=8,V=128256; logits HBM GB/s"
 UNIT = "rounds/s"
+HEADLINE = "cast"
+OTHERS = ["pr1", "vicuna", "vicuna_t1", "graft", "stress"]
+L2_BYTES = 129 * 2 ** 20
 
 
 def parse():
@@ -35,8 +43,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="cast")
-    ap.add_argument("--rec-rounds", type=int, default=16)
+    ap.add_argument("--workload", default=HEADLINE, help="workload of the headline line")
+    ap.add_argument("--workloads", default=",".join(OTHERS),
+                    help="comma-separated workloads measured for the per_config block ('' for none)")
+    ap.add_argument("--per-config-steps", type=int, default=100)
+    ap.add_argument("--min-replay-s", type=float, default=1.0, help="time the K-step graph for at least this long")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     return ap.parse_args()
@@ -68,12 +79,24 @@ def job_throughput(units_per_rank, world, ms_max):
     return world * units_per_rank / (ms_max / 1e3)
 
 
-def workload_config(w, g):
-    return {"workload": f"{w['policy']} tree round, B={w['B']}, V={w['V']}, bf16 logits, K={w['K']}, "
-                        f"k<={w['k']}, depth<={w['D']}, m<={g['m_cap']}, greedy verify",
+def workload_of(name):
+    """(workload dict, label) of a bench workload name; vicuna_t1 is Vicuna with sampling (T = 1)."""
+    from synth.workloads import WORKLOADS
+
+    if name == "vicuna_t1":
+        w = dict(WORKLOADS["vicuna"])
+        w["T"] = 1
+        return w, "vicuna_t1"
+    return dict(WORKLOADS[name]), name
+
+
+def workload_config(w, g, label):
+    dt = "bf16" if w["dtype"] == 0 else "fp32"
+    verify = "greedy verify" if w["T"] == 0 else "speculative-sampling verify (T=1)"
+    return {"workload": f"{label}: {w['policy']} tree round, B={w['B']}, V={w['V']}, {dt} logits, K={w['K']}, "
+                        f"k<={w['k']}, depth<={w['D']}, m<={g['m_cap']}, {verify}",
             "B": w["B"], "V": w["V"], "K": w["K"], "k_max": w["k"], "D_max": w["D"], "m_cap": g["m_cap"],
-            "global_batch": w["B"], "inputs": "recorded synthetic rounds replayed from HBM; every step reads a "
-                                              "different round (inputs larger than L2, no flush needed)"}
+            "global_batch": w["B"]}
 
 
 class Clocks:
@@ -91,7 +114,7 @@ class Clocks:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -128,10 +151,9 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte of each row-pass
-# kernel, from the captures summarised in profiles/ (None once the kernel has changed since).
-TRAFFIC_PER_ALGO_BYTE = {"dt_expand_layer": 20.685056e6 / (80 * 256512),   # layer 2 of a CAST round, 80 rows
-                         "dt_verify": (84.258048e6 + 1.573120e6) / (328 * 256512)}  # 328 used rows
+# DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte of the streaming
+# kernels, from the captures summarised in profiles/ (None while no capture of the current kernel exists).
+TRAFFIC_PER_ALGO_BYTE = {"expand_rows": None, "verify_rows": None}
 
 
 def measured_peaks():
@@ -142,23 +164,44 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def run_ours(args):
+class EventTiming:
+    """Events around the halves of the split expansion / verify calls (see RoundRunner.run)."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.ev = {}
+
+    def _new(self):
+        try:
+            return self.torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return self.torch.cuda.Event(enable_timing=True)
+
+    def start(self, kind):
+        e = self._new()
+        e.record()
+        self.ev.setdefault(kind, []).append([e, None])
+
+    def stop(self, kind):
+        e = self._new()
+        e.record()
+        self.ev[kind][-1][1] = e
+
+    def ms(self, kind):
+        return [a.elapsed_time(b) for a, b in self.ev.get(kind, [])]
+
+
+def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
+    """Record rounds of workload `name`, replay them as a CUDA graph of `steps` rounds, time it."""
     import torch
     import torch.distributed as tdist
 
     import synth
-    from synth.workloads import WORKLOADS, spec_for, geometry, cast_tables, chain_template
-    import __graft_entry__
-
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    if world > 1:
-        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    __graft_entry__.build()  # every rank builds (or finds) the library before importing it
+    from synth.workloads import spec_for, geometry, cast_tables, chain_template
     from dynamic_draft_tree_gb300 import dt_get_status
     from dynamic_draft_tree_gb300.rounds import RoundRunner
 
-    w = dict(WORKLOADS[args.workload])
+    w, label = workload_of(name)
     w["seed"] = w["seed"] + 1000 * rank  # independent batch per rank
     g = geometry(w)
     spec = spec_for(w)
@@ -167,236 +210,294 @@ def run_ours(args):
     if w["policy"] == "cast":
         cc = w["cast"]
         kw = dict(cast=dict(cc), cast_tables=cast_tables(B, cc["M_rows"], cc["N_cols"], cc["L"]))
-    if w["policy"] == "graft":
+    graft = w["policy"] == "graft"
+    if graft:
         kw = dict(graft=w["graft"], template=chain_template(k, w["D"]))
     run = RoundRunner(w["policy"], B, V, w["K"], k, D, P, g["D_path"], g["m_cap"], spec.dtype, T=w["T"], **kw)
     dt = torch.int16 if spec.dtype == synth.BF16 else torch.float32
     esz = 2 if spec.dtype == synth.BF16 else 4
-    R = args.rec_rounds
+    round_bytes = (D * B * k + B * P) * V * esz
+    # recorded rounds: at least 16 (a mix of rounds) and at least 3x L2 of inputs, at most 48 GiB
+    R = int(max(2, min(max(16, math.ceil(3 * L2_BYTES / round_bytes)), 256, (48 << 30) // round_bytes)))
     rec_draft = torch.empty((R, D, B, k, V), dtype=dt, device="cuda")
     rec_target = torch.empty((R, B, P, V), dtype=dt, device="cuda")
     roots = torch.empty((R, B), dtype=torch.int32, device="cuda")
-    M = None
-    if w["policy"] == "graft":
-        M = torch.full((B, V, 8), -1, dtype=torch.int32, device="cuda")
+    M = torch.full((B, V, 8), -1, dtype=torch.int32, device="cuda") if graft else None
     dk = w["recipe"]["depthkey"]
 
-    # ---- recording pass (untimed): the model forwards are stood in for by the generator ----
-    rec_out, rows_expand, rows_verify = [], [], []
-    for r in range(R):
-        salt = (r << 8)
-        roots[r] = torch.from_numpy(synth.root_tokens(w["seed"], salt, B, V)).cuda()
-        widths = []
+    def salt_of(r):
+        # Graft: successors are stationary and every round drafts from the same root tokens, so M learns
+        # the rows its template reads (as when one position is drafted again); others: a new round each time
+        return 0 if graft else (r << 8)
 
-        def draft_rows(d, ftok, r=r, salt=salt):
+    def record(r, slot, widths=None):
+        salt = salt_of(r)
+        roots[slot] = torch.from_numpy(synth.root_tokens(w["seed"], salt, B, V)).cuda()
+
+        def draft_rows(d, ftok):
             F = 1 if d == 1 else k
             ctx = ftok[:, :F].contiguous().view(-1)
-            widths.append(int((ctx >= 0).sum()))
-            synth.gen_rows_gpu(torch, spec, w["seed"], salt, synth.DRAFT, ctx, rec_draft[r, d - 1], V,
+            if widths is not None:
+                widths.append((ftok[:, :F] >= 0).sum(1).cpu().numpy())
+            synth.gen_rows_gpu(torch, spec, w["seed"], salt, synth.DRAFT, ctx, rec_draft[slot, d - 1], V,
                                depth_add=d if dk else 0, rows_per_b=F)
-            return rec_draft[r, d - 1]
+            return rec_draft[slot, d - 1]
 
-        def target_rows(meta, r=r, salt=salt):
-            synth.gen_rows_gpu(torch, spec, w["seed"], salt, synth.TARGET, meta.tokens.view(-1), rec_target[r],
+        def target_rows(meta):
+            synth.gen_rows_gpu(torch, spec, w["seed"], salt, synth.TARGET, meta.tokens.view(-1), rec_target[slot],
                                V, depth_dev=meta.depth.view(-1) if dk else None, depth_add=1 if dk else 0,
                                rows_per_b=P)
-            return rec_target[r]
+            return rec_target[slot]
 
-        run.run(roots[r], draft_rows, target_rows, seed=w["seed"], rnd=r, M=M, n0=512 * (1 + r % 16))
+        run.run(roots[slot], draft_rows, target_rows, seed=w["seed"], rnd=r, M=M, n0=512 * (1 + r % 16))
+
+    # Graft: the configured warm-up rounds seed M, then more until it no longer changes (a steady M, so
+    # that replayed rounds reproduce their recording); untimed
+    warm = 0
+    if graft:
+        for warm in range(1, 41):
+            before = M.clone()
+            record(0, 0)
+            torch.cuda.synchronize()
+            if warm >= w.get("warmup_rounds", 5) and torch.equal(before, M):
+                break
+
+    # ---- recording pass (untimed): the model forwards are stood in for by the generator ----
+    rec_out, rows_expand, rows_verify, npos_rec, act_rec = [], [], [], [], []
+    for r in range(R):
+        widths = []
+        record(r, r, widths)
         torch.cuda.synchronize()
         rec_out.append((run.accept_len.clone(), run.bonus.clone(), run.m_dev.clone()))
-        # rows each kernel actually reads in this round
         rows_verify.append(int((run.meta.tokens >= 0).sum()))
-        rows_expand.append(widths)
+        rows_expand.append([int(x.sum()) for x in widths])
+        npos_rec.append(run.meta.n_pos.cpu().numpy().copy())
+        act_rec.append(widths)
     assert dt_get_status(run.h) == 0, "device status set during recording"
 
     # ---- timed replay: the path only, on recorded inputs, captured as one CUDA graph ----
-    ev_exp = []   # [start, end] events around each expand launch (graph event-record nodes)
-    ev_ver = []
+    def replay(r, timing=None):
+        run.run(roots[r], lambda d, ftok: rec_draft[r, d - 1], lambda meta: rec_target[r], seed=w["seed"], rnd=r,
+                M=M, n0=512 * (1 + r % 16), timing=timing)
 
-    def new_event():
-        try:
-            return torch.cuda.Event(enable_timing=True, external=True)
-        except TypeError:
-            return torch.cuda.Event(enable_timing=True)
-
-    def replay(r, timed):
-        def draft_rows(d, ftok):
-            if timed:
-                e0 = new_event()
-                e0.record()
-                ev_exp.append([e0, None])
-            return rec_draft[r, d - 1]
-
-        def target_rows(meta):
-            if timed:
-                e0 = new_event()
-                e0.record()
-                ev_ver.append([e0, None])
-            return rec_target[r]
-
-        run.run(roots[r], draft_rows, target_rows, seed=w["seed"], rnd=r, M=M, n0=512 * (1 + r % 16),
-                after_expand=(lambda: _close(ev_exp)) if timed else None,
-                after_verify=(lambda: _close(ev_ver)) if timed else None)
-
-    def _close(lst):
-        e1 = new_event()
-        e1.record()
-        lst[-1][1] = e1
-
-    for i in range(args.warmup):
-        replay(i % R, False)
+    for i in range(warmup):
+        replay(i % R)
     torch.cuda.synchronize()
     # consistency: a replayed round equals its recording
-    replay(0, False)
+    replay(R - 1)
     torch.cuda.synchronize()
-    consistent = bool(torch.equal(run.accept_len, rec_out[0][0]) and torch.equal(run.bonus, rec_out[0][1]))
+    consistent = bool(torch.equal(run.accept_len, rec_out[R - 1][0]) and torch.equal(run.bonus, rec_out[R - 1][1]))
 
-    # two graphs of the same K steps: the timed one holds the path only; the other adds event records
-    # around each expansion and verify launch for the per-kernel figures (events between launches
-    # would also split the programmatic launch overlap of the kernels they separate)
-    def capture(with_events):
-        g = torch.cuda.CUDAGraph()
+    timing = EventTiming(torch)
+
+    def capture(tm):
+        gph = torch.cuda.CUDAGraph()
         cap_stream = torch.cuda.Stream()
         cap_stream.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(cap_stream):
-            with torch.cuda.graph(g, stream=cap_stream):
-                for s in range(args.steps):
-                    replay(s % R, with_events)
+            with torch.cuda.graph(gph, stream=cap_stream):
+                for s in range(steps):
+                    replay(s % R, tm)
         torch.cuda.current_stream().wait_stream(cap_stream)
-        g.replay()  # untimed: uploads the graph
+        gph.replay()  # untimed: uploads the graph
         torch.cuda.synchronize()
-        return g
+        return gph
 
-    graph = capture(False)
-    graph_ev = capture(True)
+    graph = capture(None)
+    graph_ev = capture(timing)
 
+    # K-step replays, each timed with events, for at least min_replay_s and 20 replays
     clocks = Clocks(local)
     if world > 1:
         tdist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    graph.replay()
-    t1.record()
+    reps, t_begin = [], time.perf_counter()
+    while len(reps) < 20 or (time.perf_counter() - t_begin < args.min_replay_s and len(reps) < 2000):
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        graph.replay()
+        t1.record()
+        t1.synchronize()
+        reps.append(t0.elapsed_time(t1))
     torch.cuda.synchronize()
     if world > 1:
         tdist.barrier()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1)
+    ms = float(np.median(reps))
+    ms = max_over_ranks(ms, world)
+    value = job_throughput(steps, world, ms)
+    spread = {"replays": len(reps), "ms_min": float(np.min(reps)), "ms_p10": float(np.percentile(reps, 10)),
+              "ms_median": float(np.median(reps)), "ms_p90": float(np.percentile(reps, 90)),
+              "ms_max": float(np.max(reps))}
     graph_ev.replay()  # per-kernel events (not part of the timed region)
     torch.cuda.synchronize()
-    ms = max_over_ranks(ms, world)
-    value = job_throughput(args.steps, world, ms)
 
-    # per-kernel figures from the live events
-    exp_ms = [a.elapsed_time(b) for a, b in ev_exp]
-    ver_ms = [a.elapsed_time(b) for a, b in ev_ver]
-    exp_bytes = sum(sum(rows_expand[s % R]) for s in range(args.steps)) * V * esz
-    ver_bytes = sum(rows_verify[s % R] for s in range(args.steps)) * V * esz
     peak, peak_kind = measured_peaks()
-    ver_gbs = ver_bytes / (sum(ver_ms) / 1e3) / 1e9
-    exp_gbs = exp_bytes / (sum(exp_ms) / 1e3) / 1e9
-    # roofline of the kernel with the most time per round (expansion: D launches; verify: one)
-    rl = {"dt_expand_layer": (exp_gbs, exp_bytes / len(exp_ms), 1e3 * sum(exp_ms) / len(exp_ms), sum(exp_ms),
-                              "expand_kernel (vocab softmax + top-K per frontier node)"),
-          "dt_verify": (ver_gbs, ver_bytes / len(ver_ms), 1e3 * sum(ver_ms) / len(ver_ms), sum(ver_ms),
-                        "dt_verify (verify row pass + acceptance walk)")}
-    top = max(rl, key=lambda k: rl[k][3])
-    gbs, bpl, us, _, kname = rl[top]
+    kern = {}
+    exp_bytes = sum(sum(rows_expand[s % R]) for s in range(steps)) * V * esz
+    ver_bytes = sum(rows_verify[s % R] for s in range(steps)) * V * esz
+    for kind, nbytes in (("expand_rows", exp_bytes), ("expand_finish", None), ("verify_rows", ver_bytes),
+                         ("verify_accept", None)):
+        t = timing.ms(kind)
+        if not t:
+            continue
+        d = {"launches": len(t), "avg_us": 1e3 * float(np.mean(t)), "total_us_per_round": 1e3 * sum(t) / steps}
+        if nbytes is not None:
+            gbs = nbytes / (sum(t) / 1e3) / 1e9
+            d.update(gbs=gbs, frac=gbs / peak, bytes_per_launch=nbytes / len(t))
+        kern[kind] = d
+    # the expansion layer as a whole (streaming + finishing kernels)
+    if "expand_rows" in kern and "expand_finish" in kern:
+        lay = sum(timing.ms("expand_rows")) + sum(timing.ms("expand_finish"))
+        kern["expand_layer"] = {"avg_us": 1e3 * lay / len(timing.ms("expand_rows")),
+                                "gbs": exp_bytes / (lay / 1e3) / 1e9}
+    streaming = [k_ for k_ in ("expand_rows", "verify_rows") if k_ in kern]
+    top = max(streaming, key=lambda k_: kern[k_]["total_us_per_round"])
     tr = TRAFFIC_PER_ALGO_BYTE.get(top)
-    roofline = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                "traffic": None if tr is None else tr * bpl, "kernel": kname, "peak_source": peak_kind,
-                "bytes_per_launch": bpl, "avg_launch_us": us}
-    launches_per_round = 1 + (D if w["policy"] != "cast" else 1) + D + \
-        (D if w["policy"] in ("cast", "graft") else 0) + \
-        (2 if w["policy"] == "cast" else 1) + 1 + (3 if w["T"] == 1 else 2) + \
-        (2 if w["policy"] == "graft" else 0)
+    names = {"expand_rows": "expand_stream_kernel (vocab max, softmax sum and top-K pieces of the frontier rows)",
+             "verify_rows": "verify_stream_kernel (argmax / softmax pieces of the used target rows)"}
+    roofline = {"bound": "hbm", "achieved": kern[top]["gbs"], "peak": peak, "unit": "GB/s", "frac": kern[top]["frac"],
+                "traffic": None if tr is None else tr * kern[top]["bytes_per_launch"], "kernel": names[top],
+                "peak_source": peak_kind, "bytes_per_launch": kern[top]["bytes_per_launch"],
+                "avg_launch_us": kern[top]["avg_us"]}
+    # kernels of the library launched per round: reset + layer-1 frontier, 2 per layer (CAST: 3 when the
+    # batch does not fit one finishing CTA), verify count + rerank (CAST) or rerank, retrieval (Graft),
+    # meta, 2 or 3 for the verify (the bonus draw with sampling), the M refresh (Graft)
+    launches = 2 + 2 * D + (2 if w["policy"] == "cast" else 1) + (1 if graft else 0) + 1 + \
+        (3 if w["T"] == 1 else 2) + (1 if graft else 0)
+
+    out = {"label": label, "value": value, "unit": UNIT, "ms_per_step": ms / steps, "steps": steps,
+           "dtype": "bf16" if spec.dtype == synth.BF16 else "f32",
+           "config": dict(workload_config(w, g, label),
+                          inputs=f"{R} recorded synthetic rounds ({R * round_bytes / 2**30:.2f} GiB, > L2) replayed "
+                                 "from HBM; every step reads a different round's buffers, no flush needed"),
+           "roofline": roofline, "kernels": kern, "replay": spread, "replay_consistent": consistent,
+           "rows_per_round": {"expand": rows_expand[:min(R, 16)], "verify": rows_verify[:min(R, 16)]},
+           "gpu_launches": launches * steps, "clocks": clk}
+    if graft:
+        out["graft_warmup_rounds"] = warm
 
     # ---- end to end through the public API with host buffers ----
-    e2e = None
-    if args.e2e_steps > 0:
-        h_draft = torch.empty_like(rec_draft[0], device="cpu").pin_memory()
-        h_target = torch.empty_like(rec_target[0], device="cpu").pin_memory()
-        h_draft.copy_(rec_draft[0])
-        h_target.copy_(rec_target[0])
-        h_roots = roots[0].cpu().pin_memory()
-        out_len = torch.empty((B,), dtype=torch.int32).pin_memory()
-        out_bonus = torch.empty((B,), dtype=torch.int32).pin_memory()
-        out_path = torch.empty(tuple(run.accept_path.shape), dtype=torch.int32).pin_memory()
-        d_draft = torch.empty_like(rec_draft[0])
-        d_target = torch.empty_like(rec_target[0])
-        d_roots = torch.empty_like(roots[0])
-        bi = h_draft.numel() * esz + h_target.numel() * esz + h_roots.numel() * 4
-        bo = (out_len.numel() + out_bonus.numel() + out_path.numel()) * 4
-        # Double-buffered inputs: step s + 1's rows are copied (on a copy stream) while step s runs,
-        # into the other buffer set, which step s - 1 has finished reading (every step ends with a
-        # synchronisation on its results). Every step's copy is inside the timed region.
-        d_draft2, d_target2, d_roots2 = torch.empty_like(d_draft), torch.empty_like(d_target), torch.empty_like(d_roots)
-        bufs = [(d_roots, d_draft, d_target), (d_roots2, d_draft2, d_target2)]
-        copy_stream = torch.cuda.Stream()
-        copied = [torch.cuda.Event(), torch.cuda.Event()]
-
-        def copy_inputs(i):
-            r_, dr_, tg_ = bufs[i % 2]
-            with torch.cuda.stream(copy_stream):
-                r_.copy_(h_roots, non_blocking=True)
-                dr_.copy_(h_draft, non_blocking=True)
-                tg_.copy_(h_target, non_blocking=True)
-                copied[i % 2].record(copy_stream)
-
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        copy_stream.wait_event(e0)
-        copy_inputs(0)
-        for s in range(args.e2e_steps):
-            cur = torch.cuda.current_stream()
-            cur.wait_event(copied[s % 2])
-            r_, dr_, tg_ = bufs[s % 2]
-            if s + 1 < args.e2e_steps:
-                copy_inputs(s + 1)
-            run.run(r_, lambda d, ftok, dr_=dr_: dr_[d - 1], lambda meta, tg_=tg_: tg_, seed=w["seed"], rnd=0, M=M,
-                    n0=512)
-            out_len.copy_(run.accept_len, non_blocking=True)
-            out_bonus.copy_(run.bonus, non_blocking=True)
-            out_path.copy_(run.accept_path, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-        copy_stream.synchronize()
-        e1.record()
-        torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1)
-        e_ms = max_over_ranks(e_ms, world)
-        e2e = {"value": job_throughput(args.e2e_steps, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": int(bi),
-               "d2h_bytes_per_step": int(bo), "double_buffered": True}
-        e2e["consistent"] = bool(torch.equal(out_len.cuda(), rec_out[0][0]) and
-                                 torch.equal(out_bonus.cuda(), rec_out[0][1]))
-        if not e2e["consistent"]:
-            print("e2e mismatch:", out_len.tolist(), rec_out[0][0].tolist(), out_bonus.tolist(),
-                  rec_out[0][1].tolist(), file=sys.stderr)
-
+    if with_e2e and args.e2e_steps > 0:
+        out["e2e"] = e2e_run(torch, run, w, rec_draft, rec_target, roots, rec_out, act_rec, npos_rec, esz, M,
+                             args.e2e_steps, world)
     assert dt_get_status(run.h) == 0, "device status set during the timed region"
+    del rec_draft, rec_target
+    run.h.close()
+    torch.cuda.empty_cache()
+    return out
+
+
+def e2e_run(torch, run, w, rec_draft, rec_target, roots, rec_out, act_rec, npos_rec, esz, M, steps, world):
+    """The recorded round 0 through the public API from pinned host buffers, every step: the rows the
+    round reads (each request's active frontier rows per layer, its used target positions) and the roots
+    copied host -> device, the round, and the accepted lengths, paths and bonus tokens copied back.
+    The inputs are double-buffered: step s + 1's copies run on a copy stream while step s runs."""
+    B, k, V = w["B"], w["k"], w["V"]
+    h_draft = rec_draft[0].cpu().pin_memory()
+    h_target = rec_target[0].cpu().pin_memory()
+    h_roots = roots[0].cpu().pin_memory()
+    out_len = torch.empty((B,), dtype=torch.int32).pin_memory()
+    out_bonus = torch.empty((B,), dtype=torch.int32).pin_memory()
+    out_path = torch.empty(tuple(run.accept_path.shape), dtype=torch.int32).pin_memory()
+    # contiguous row blocks the round reads: layer d, request b, frontier slots 0..cnt-1 (row (b F + f) of
+    # that layer's [B][F][V] buffer); target rows 0..n_pos[b]-1 of request b
+    chunks = []
+    for d, cnt in enumerate(act_rec[0]):
+        F = 1 if d == 0 else k
+        for b in range(B):
+            if cnt[b] > 0:
+                chunks.append(("d", d, b * F, int(cnt[b])))
+    for b in range(B):
+        if npos_rec[0][b] > 0:
+            chunks.append(("t", 0, b * run.P, int(npos_rec[0][b])))
+    bi = sum(c[3] for c in chunks) * V * esz + h_roots.numel() * 4
+    bo = (out_len.numel() + out_bonus.numel() + out_path.numel()) * 4
+    bufs = [(torch.zeros_like(roots[0]), torch.zeros_like(rec_draft[0]), torch.zeros_like(rec_target[0]))
+            for _ in range(2)]
+    hd = h_draft.view(h_draft.shape[0], -1, V)
+    ht = h_target.view(-1, V)
+    copy_stream = torch.cuda.Stream()
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def copy_inputs(i):
+        r_, dr_, tg_ = bufs[i % 2]
+        dd = dr_.view(dr_.shape[0], -1, V)
+        tt = tg_.view(-1, V)
+        with torch.cuda.stream(copy_stream):
+            r_.copy_(h_roots, non_blocking=True)
+            for kind, d, r0, n in chunks:
+                if kind == "d":
+                    dd[d, r0:r0 + n].copy_(hd[d, r0:r0 + n], non_blocking=True)
+                else:
+                    tt[r0:r0 + n].copy_(ht[r0:r0 + n], non_blocking=True)
+            copied[i % 2].record(copy_stream)
+
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    copy_stream.wait_event(e0)
+    copy_inputs(0)
+    for s in range(steps):
+        cur = torch.cuda.current_stream()
+        cur.wait_event(copied[s % 2])
+        r_, dr_, tg_ = bufs[s % 2]
+        if s + 1 < steps:  # the other buffer set: step s - 1 finished reading it (synchronised below)
+            copy_inputs(s + 1)
+        run.run(r_, lambda d, ftok, dr_=dr_: dr_[d - 1], lambda meta, tg_=tg_: tg_, seed=w["seed"], rnd=0, M=M,
+                n0=512)
+        out_len.copy_(run.accept_len, non_blocking=True)
+        out_bonus.copy_(run.bonus, non_blocking=True)
+        out_path.copy_(run.accept_path, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    copy_stream.synchronize()
+    e1.record()
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    consistent = bool(torch.equal(out_len.cuda(), rec_out[0][0]) and torch.equal(out_bonus.cuda(), rec_out[0][1]))
+    if not consistent:
+        print("e2e mismatch:", out_len.tolist(), rec_out[0][0].tolist(), out_bonus.tolist(), rec_out[0][1].tolist(),
+              file=sys.stderr)
+    return {"value": job_throughput(steps, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": int(bi),
+            "d2h_bytes_per_step": int(bo), "double_buffered": True, "consistent": consistent,
+            "copies": "the rows the round reads (active frontier rows per layer and request, used target "
+                      "positions), as recorded"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as tdist
+
+    import __graft_entry__
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    __graft_entry__.build()  # every rank builds (or finds) the library before importing it
+
+    head = measure_workload(args.workload, args.steps, args.warmup, args, rank, world, local, with_e2e=True)
+    per_config = {}
+    for name in [x for x in args.workloads.split(",") if x and x != args.workload]:
+        r = measure_workload(name, min(args.steps, args.per_config_steps), args.warmup, args, rank, world, local,
+                             with_e2e=False)
+        per_config[r.pop("label")] = r
     if rank != 0:
         return None
+    head.pop("label")
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if spec.dtype == synth.BF16 else "f32",
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
         "data": "synthetic (seeded counter-hash logits standing in for the draft/target forwards)",
-        "config": dict(workload_config(w, g), parallelism=f"replicas x{world} (independent batches)"),
-        "roofline": roofline,
-        "kernels": {"dt_verify": {"gbs": ver_gbs, "avg_us": 1e3 * float(np.mean(ver_ms)),
-                                  "avg_bytes": ver_bytes / len(ver_ms), "rows_per_round": rows_verify},
-                    "dt_expand_layer": {"gbs": exp_gbs, "avg_us": 1e3 * float(np.mean(exp_ms)),
-                                        "avg_bytes": exp_bytes / len(exp_ms), "launches_per_round": D,
-                                        "rows_per_round": rows_expand}},
-        "e2e": e2e,
-        "gpu_launches": launches_per_round * args.steps,
-        "replay_consistent": consistent,
-        "clocks": clk,
+        "config": dict(head["config"], parallelism=f"replicas x{world} (independent batches)"),
+        "roofline": head["roofline"], "kernels": head["kernels"], "replay": head["replay"],
+        "e2e": head.get("e2e"), "gpu_launches": head["gpu_launches"],
+        "replay_consistent": head["replay_consistent"], "rows_per_round": head["rows_per_round"],
+        "clocks": head["clocks"], "per_config": per_config,
     }
     return line
 
@@ -408,9 +509,9 @@ def run_reference(args):
         return None
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import harness
-    from synth.workloads import WORKLOADS, geometry
+    from synth.workloads import geometry
 
-    w = dict(WORKLOADS[args.workload])
+    w, label = workload_of(args.workload)
     g = geometry(w)
     # the oracle's rows come from a warm cache so that only the oracle itself is timed; the run is
     # bounded in time (the oracle takes seconds per round), so at most `budget` seconds of rounds are
@@ -436,30 +537,36 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": dict(workload_config(w, g), parallelism="1 host process"),
+            "data": "synthetic", "config": dict(workload_config(w, g, label), parallelism="1 host process"),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"{len(times)} of {args.steps} requested rounds of the workload, "
                                        f"time-bounded to {budget:.0f} s (rows pre-generated)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def cpu_baseline_sample(seconds=12.0):
-    """Oracle rounds/s on the host, single process, rows pre-generated: bounded to ~seconds."""
+def cpu_baseline_sample(name, seconds=12.0):
+    """Oracle rounds/s on the host, single process, rows pre-generated: bounded to ~seconds. Also counts
+    the rounds whose oracle decision gaps fall below 1e-5 relative (the parity tests redraw those): the
+    sampled rounds are the benchmark's own rounds 0, 1, ... (same seeds, salts and prefix lengths)."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import harness
-    from synth.workloads import WORKLOADS
 
-    w = dict(WORKLOADS["cast"])
-    n, sec, rnd = 0, 0.0, 0
+    w, _ = workload_of(name)
+    n, sec, rnd, redrawn, hit = 0, 0.0, 0, 0, 0
     while sec < seconds and n < 50:
-        harness.oracle_round(w, rnd)
+        _, _, rej = harness.oracle_round(w, rnd)
+        redrawn += rej
+        hit += rej > 0
         t = time.perf_counter()
         harness.oracle_round(w, rnd)
         sec += time.perf_counter() - t
         n += 1
         rnd += 1
-    return {"value": n / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} full rounds of the CAST workload, rows pre-generated (only the oracle timed)"}
+    base = {"value": n / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} full rounds of the {name} workload, rows pre-generated (only the oracle timed)"}
+    seeds = {"rounds_checked": n, "rounds_with_near_tie": hit, "request_redraws": redrawn,
+             "rule": "a round is redrawn when an oracle decision gap is below 1e-5 relative"}
+    return base, seeds
 
 
 def main():
@@ -469,7 +576,7 @@ def main():
     else:
         line = run_ours(args)
         if line is not None and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline_sample()
+            line["cpu_baseline"], line["seed_redraws"] = cpu_baseline_sample(args.workload)
     if line is not None:
         print(json.dumps(line))
 

@@ -12,7 +12,7 @@ import torch
 from ._lib import (lib, check, DtError, DtConfig, DtTreeView, DtPruneParams, DtPruneOut, DtTemplate,  # noqa
                    DtTreeMeta, EXPORTS, DT_OK, DT_ERR_ARG, DT_ERR_CUDA, DT_ERR_DEVICE,
                    DT_ERR_DEVICE_TIMEOUT, DT_BF16, DT_F32, DT_GREEDY, DT_SAMPLE,
-                   DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT,
+                   DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT, DT_POLICY_NONE,
                    DT_DEV_BAD_LOGITS, DT_DEV_BAD_TOKEN, DT_DEV_BAD_TREE, DT_DEV_TIMEOUT, DT_DEV_INTERNAL,
                    DT_FLAG_TEST_TIMEOUT, LIB_PATH)
 
@@ -113,6 +113,34 @@ def dt_expand_layer(h, logits, F, ld=None, stream=None):
     check(lib.dt_expand_layer(h.h, _ptr(logits), ld, F, _stream(stream)))
 
 
+def dt_expand_prune_select(h, logits, F, policy, params=None, out=None, width=None, frontier_token=None, ld=None,
+                           stream=None):
+    """Expansion, then the policy's pruning (DT_POLICY_NONE: none), then the next frontier."""
+    ld = logits.shape[-1] if ld is None else ld
+    wl = 0 if width is None else width.numel()
+    check(lib.dt_expand_prune_select(h.h, _ptr(logits), ld, F, policy,
+                                     None if params is None else ctypes.byref(params),
+                                     None if out is None else ctypes.byref(out), _ptr(width), wl,
+                                     _ptr(frontier_token), _stream(stream)))
+
+
+def dt_expand_rows(h, logits, F, ld=None, stream=None):
+    """Streaming half of an expansion (reads the frontier rows; the tree is unchanged)."""
+    ld = logits.shape[-1] if ld is None else ld
+    check(lib.dt_expand_rows(h.h, _ptr(logits), ld, F, _stream(stream)))
+
+
+def dt_expand_finish(h, F, select=False, policy=DT_POLICY_NONE, params=None, out=None, width=None,
+                     frontier_token=None, stream=None):
+    """Finishing half of an expansion (after dt_expand_rows): the layer, and with ``select`` the
+    policy's pruning and the next frontier."""
+    wl = 0 if width is None else width.numel()
+    check(lib.dt_expand_finish(h.h, F, 1 if select else 0, policy,
+                               None if params is None else ctypes.byref(params),
+                               None if out is None else ctypes.byref(out), _ptr(width), wl, _ptr(frontier_token),
+                               _stream(stream)))
+
+
 def dt_cast_prune(h, policy, params, out, stream=None):
     check(lib.dt_cast_prune(h.h, policy, ctypes.byref(params), ctypes.byref(out), _stream(stream)))
 
@@ -151,6 +179,21 @@ def dt_verify(h, meta, logits, mode, seed, round_, accept_len, accept_path, bonu
     ld = logits.shape[-1] if ld is None else ld
     check(lib.dt_verify(h.h, ctypes.byref(meta.c), _ptr(logits), ld, mode, seed, round_, _ptr(accept_len),
                         _ptr(accept_path), _ptr(bonus), _ptr(top8), _stream(stream)))
+
+
+def dt_verify_rows(h, meta, logits, mode, with_top8=False, ld=None, stream=None):
+    """Streaming half of dt_verify (one read of every used target row)."""
+    ld = logits.shape[-1] if ld is None else ld
+    check(lib.dt_verify_rows(h.h, ctypes.byref(meta.c), _ptr(logits), ld, mode, 1 if with_top8 else 0,
+                             _stream(stream)))
+
+
+def dt_verify_accept(h, meta, logits, mode, seed, round_, accept_len, accept_path, bonus, top8=None, ld=None,
+                     stream=None):
+    """Acceptance half of dt_verify (after dt_verify_rows)."""
+    ld = logits.shape[-1] if ld is None else ld
+    check(lib.dt_verify_accept(h.h, ctypes.byref(meta.c), _ptr(logits), ld, mode, seed, round_, _ptr(accept_len),
+                               _ptr(accept_path), _ptr(bonus), _ptr(top8), _stream(stream)))
 
 
 def dt_adj_update(h, M, meta, top8, stream=None):

@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(HERE, "libdt.so")
 DT_OK, DT_ERR_ARG, DT_ERR_CUDA, DT_ERR_DEVICE, DT_ERR_DEVICE_TIMEOUT = 0, -1, -2, -3, -4
 DT_BF16, DT_F32 = 0, 1
 DT_GREEDY, DT_SAMPLE = 0, 1
-DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT = 0, 1, 2
+DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT, DT_POLICY_NONE = 0, 1, 2, 3
 DT_DEV_BAD_LOGITS, DT_DEV_BAD_TOKEN, DT_DEV_BAD_TREE, DT_DEV_TIMEOUT, DT_DEV_INTERNAL = 1, 2, 4, 8, 16
 DT_FLAG_TEST_TIMEOUT = 1
 
@@ -21,7 +21,8 @@ EXPORTS = ["dt_last_error_string", "dt_create", "dt_destroy", "dt_get_tree", "dt
            "dt_clear_status", "dt_tree_reset", "dt_select_frontier", "dt_expand_layer", "dt_cast_prune",
            "dt_rerank", "dt_graft_retrieve", "dt_build_tree_meta", "dt_verify", "dt_adj_update",
            "dt_row_topk_static", "dt_cast_prune_select",
-           "dt_cast_verify_rerank"]
+           "dt_cast_verify_rerank", "dt_expand_prune_select", "dt_expand_rows", "dt_expand_finish",
+           "dt_verify_rows", "dt_verify_accept"]
 
 c_i32p = ctypes.c_void_p
 vp = ctypes.c_void_p
@@ -91,6 +92,15 @@ def _load():
                        ctypes.c_uint64, vp, vp, vp, vp, vp], I),
         "dt_adj_update": ([vp, vp, ctypes.POINTER(DtTreeMeta), vp, vp], I),
         "dt_cast_prune_select": ([vp, ctypes.POINTER(DtPruneParams), ctypes.POINTER(DtPruneOut), vp, vp], I),
+        "dt_expand_prune_select": ([vp, vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                    ctypes.POINTER(DtPruneParams), ctypes.POINTER(DtPruneOut), vp, ctypes.c_int32,
+                                    vp, vp], I),
+        "dt_expand_rows": ([vp, vp, ctypes.c_int64, ctypes.c_int32, vp], I),
+        "dt_expand_finish": ([vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(DtPruneParams),
+                              ctypes.POINTER(DtPruneOut), vp, ctypes.c_int32, vp, vp], I),
+        "dt_verify_rows": ([vp, ctypes.POINTER(DtTreeMeta), vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp], I),
+        "dt_verify_accept": ([vp, ctypes.POINTER(DtTreeMeta), vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64,
+                              ctypes.c_uint64, vp, vp, vp, vp, vp], I),
         "dt_cast_verify_rerank": ([vp, ctypes.POINTER(DtPruneParams), ctypes.POINTER(DtPruneOut), vp, vp], I),
         "dt_row_topk_static": ([vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                 vp, vp, vp, vp], I),

@@ -18,7 +18,7 @@ ARCH = "103a"
 
 SOURCES = ["dt_api.cu", "k_tree.cu", "k_select.cu", "k_meta.cu", "k_verify.cu", "k_graft.cu",
            "k_rowtopk_static.cu"]
-HEADERS = ["dt_internal.cuh", "rowscan.cuh"]
+HEADERS = ["dt_internal.cuh", "rowscan.cuh", "rowstream.cuh", "cast_block.cuh"]
 
 
 def nvcc_flags(verbose_ptxas=False):

@@ -85,6 +85,12 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
 
   const size_t BN = (size_t)c.B_max * h->N;
   const size_t rows_max = (size_t)c.B_max * std::max(c.W, c.P_max);
+  // the streaming passes place elements with 64-bit products (rows x V) x warps
+  const double place = (double)rows_max * (double)c.V * (double)dt::stream_grid(h) * 8.0;
+  if (place >= 9.0e18) {
+    delete h;
+    return fail(DT_ERR_ARG, "B_max * max(W, P_max) * V too large for 64-bit row placement");
+  }
   Carver cv;
   const size_t o_token = cv.take<int32_t>(BN), o_parent = cv.take<int32_t>(BN), o_depth = cv.take<int32_t>(BN);
   const size_t o_logc = cv.take<float>(BN), o_value = cv.take<float>(BN);
@@ -241,6 +247,90 @@ int dt_expand_layer(dt_handle* h, const void* logits, int64_t ld, int32_t F, cud
   return DT_OK;
 }
 
+// Host checks shared by the CAST width/depth entry points.
+static int check_cast_width_params(const dt_handle* h, const dt_prune_params* p, const dt_prune_out* out) {
+  if (!p->S_T || !p->S_D) return fail(DT_ERR_ARG, "cost tables missing");
+  if (p->M_rows < 1 || p->N_cols < 1) return fail(DT_ERR_ARG, "table shape must be positive");
+  if (!(p->L > 0.0)) return fail(DT_ERR_ARG, "L must be > 0");
+  if (p->n0 < 0) return fail(DT_ERR_ARG, "n0 must be >= 0");
+  if (p->width_cap < 1 || p->width_cap > h->cfg.W || p->width_cap > p->N_cols)
+    return fail(DT_ERR_ARG, "width_cap must be in [1, min(W, N_cols)]");
+  if (p->R < 1 || p->R > dt::kMaxFifo) return fail(DT_ERR_ARG, "R must be in [1, 16]");
+  if (!out->width || !out->stop) return fail(DT_ERR_ARG, "width and stop outputs required");
+  return DT_OK;
+}
+
+static int check_expand_args(const dt_handle* h, const char* who, int32_t F) {
+  if (h->B < 1) return fail(DT_ERR_ARG, "%s: no tree (call dt_tree_reset)", who);
+  if (h->depth >= h->cfg.D_max) return fail(DT_ERR_ARG, "%s: tree already has D_max layers", who);
+  if (F < 1 || F > h->cfg.W) return fail(DT_ERR_ARG, "F=%d outside [1, W=%d]", F, h->cfg.W);
+  return DT_OK;
+}
+
+static int check_policy_args(const dt_handle* h, int32_t policy, const dt_prune_params* p, const dt_prune_out* out,
+                             const int32_t* width, int32_t width_len) {
+  if (width && width_len != 1 && width_len != h->B) return fail(DT_ERR_ARG, "width_len must be 1 or B");
+  if (policy == DT_POLICY_CAST_WIDTH_DEPTH) {
+    if (!p || !out) return fail(DT_ERR_ARG, "CAST pruning needs params and outputs");
+    return check_cast_width_params(h, p, out);
+  }
+  if (policy == DT_POLICY_GRAFT_CHECKPOINT) {
+    if (!p || !out) return fail(DT_ERR_ARG, "the Graft checkpoint needs params and outputs");
+    if (p->n_ckpt < 0 || p->n_ckpt > 4) return fail(DT_ERR_ARG, "n_ckpt must be in [0, 4]");
+    if (!out->stop) return fail(DT_ERR_ARG, "stop output required");
+    return DT_OK;
+  }
+  if (policy != DT_POLICY_NONE)
+    return fail(DT_ERR_ARG, "policy must be DT_POLICY_NONE, DT_POLICY_CAST_WIDTH_DEPTH or "
+                            "DT_POLICY_GRAFT_CHECKPOINT");
+  return DT_OK;
+}
+
+int dt_expand_rows(dt_handle* h, const void* logits, int64_t ld, int32_t F, cudaStream_t s) {
+  if (!h || !logits) return fail(DT_ERR_ARG, "dt_expand_rows: null argument");
+  int rc = check_expand_args(h, "dt_expand_rows", F);
+  if (rc != DT_OK) return rc;
+  if (ld < h->cfg.V) return fail(DT_ERR_ARG, "ld=%lld < V", (long long)ld);
+  const size_t esz = h->cfg.dtype == DT_BF16 ? 2 : 4;
+  if (!aligned(logits, esz)) return fail(DT_ERR_ARG, "logits not aligned to its element size");
+  cudaError_t e = dt::launch_expand_rows(h, logits, ld, F, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dt_expand_rows");
+  return DT_OK;
+}
+
+int dt_expand_finish(dt_handle* h, int32_t F, int32_t select, int32_t policy, const dt_prune_params* p,
+                     const dt_prune_out* out, const int32_t* width, int32_t width_len, int32_t* frontier_token,
+                     cudaStream_t s) {
+  if (!h) return fail(DT_ERR_ARG, "dt_expand_finish: null handle");
+  int rc = check_expand_args(h, "dt_expand_finish", F);
+  if (rc != DT_OK) return rc;
+  if (select) {
+    rc = check_policy_args(h, policy, p, out, width, width_len);
+    if (rc != DT_OK) return rc;
+  }
+  cudaError_t e = dt::launch_expand_finish(h, F, select ? policy : dt::DT_EXPAND_ONLY, p, out, width, width_len,
+                                           frontier_token, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dt_expand_finish");
+  return DT_OK;
+}
+
+int dt_expand_prune_select(dt_handle* h, const void* logits, int64_t ld, int32_t F, int32_t policy,
+                           const dt_prune_params* p, const dt_prune_out* out, const int32_t* width,
+                           int32_t width_len, int32_t* frontier_token, cudaStream_t s) {
+  if (!h || !logits) return fail(DT_ERR_ARG, "dt_expand_prune_select: null argument");
+  if (h->B < 1) return fail(DT_ERR_ARG, "dt_expand_prune_select: no tree (call dt_tree_reset)");
+  if (h->depth >= h->cfg.D_max) return fail(DT_ERR_ARG, "dt_expand_prune_select: tree already has D_max layers");
+  if (F < 1 || F > h->cfg.W) return fail(DT_ERR_ARG, "F=%d outside [1, W=%d]", F, h->cfg.W);
+  if (ld < h->cfg.V) return fail(DT_ERR_ARG, "ld=%lld < V", (long long)ld);
+  const size_t esz = h->cfg.dtype == DT_BF16 ? 2 : 4;
+  if (!aligned(logits, esz)) return fail(DT_ERR_ARG, "logits not aligned to its element size");
+  const int rc = check_policy_args(h, policy, p, out, width, width_len);
+  if (rc != DT_OK) return rc;
+  cudaError_t e = dt::launch_expand_ex(h, logits, ld, F, policy, p, out, width, width_len, frontier_token, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dt_expand_prune_select");
+  return DT_OK;
+}
+
 int dt_cast_prune(dt_handle* h, int32_t policy, const dt_prune_params* p, const dt_prune_out* out,
                   cudaStream_t s) {
   if (!h || !p || !out) return fail(DT_ERR_ARG, "dt_cast_prune: null argument");
@@ -294,15 +384,9 @@ int dt_cast_prune_select(dt_handle* h, const dt_prune_params* p, const dt_prune_
                          cudaStream_t s) {
   if (!h || !p || !out) return fail(DT_ERR_ARG, "dt_cast_prune_select: null argument");
   if (h->B < 1) return fail(DT_ERR_ARG, "dt_cast_prune_select: no tree (call dt_tree_reset)");
-  if (!p->S_T || !p->S_D) return fail(DT_ERR_ARG, "cost tables missing");
-  if (p->M_rows < 1 || p->N_cols < 1) return fail(DT_ERR_ARG, "table shape must be positive");
-  if (!(p->L > 0.0)) return fail(DT_ERR_ARG, "L must be > 0");
-  if (p->n0 < 0) return fail(DT_ERR_ARG, "n0 must be >= 0");
   if (h->depth < 1) return fail(DT_ERR_ARG, "no layer to prune");
-  if (p->width_cap < 1 || p->width_cap > h->cfg.W || p->width_cap > p->N_cols)
-    return fail(DT_ERR_ARG, "width_cap must be in [1, min(W, N_cols)]");
-  if (p->R < 1 || p->R > dt::kMaxFifo) return fail(DT_ERR_ARG, "R must be in [1, 16]");
-  if (!out->width || !out->stop) return fail(DT_ERR_ARG, "width and stop outputs required");
+  const int rc = check_cast_width_params(h, p, out);
+  if (rc != DT_OK) return rc;
   cudaError_t e = dt::launch_cast_prune_select(h, p, out, frontier_token, s);
   if (e != cudaSuccess) return cuda_fail(e, "dt_cast_prune_select");
   return DT_OK;
@@ -358,12 +442,10 @@ int dt_build_tree_meta(dt_handle* h, const int32_t* selected, int32_t m_cap, con
   return DT_OK;
 }
 
-int dt_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int32_t mode,
-              uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path, int32_t* bonus,
-              int32_t* top8, cudaStream_t s) {
-  if (!h || !meta || !logits || !accept_len || !accept_path || !bonus)
-    return fail(DT_ERR_ARG, "dt_verify: null argument");
-  if (h->B < 1) return fail(DT_ERR_ARG, "dt_verify: no tree (call dt_tree_reset)");
+static int check_verify_args(const dt_handle* h, const char* who, const dt_tree_meta* meta, const void* logits,
+                             int64_t ld, int32_t mode) {
+  if (!meta || !logits) return fail(DT_ERR_ARG, "%s: null argument", who);
+  if (h->B < 1) return fail(DT_ERR_ARG, "%s: no tree (call dt_tree_reset)", who);
   if (mode != DT_GREEDY && mode != DT_SAMPLE) return fail(DT_ERR_ARG, "mode must be DT_GREEDY or DT_SAMPLE");
   if (meta->P < 1 || meta->P > h->cfg.P_max) return fail(DT_ERR_ARG, "meta P must be in [1, P_max]");
   if (meta->D_path < 1 || meta->D_path > 64) return fail(DT_ERR_ARG, "D_path must be in [1, 64]");
@@ -371,6 +453,37 @@ int dt_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_
   const size_t esz = h->cfg.dtype == DT_BF16 ? 2 : 4;
   if (!aligned(logits, esz)) return fail(DT_ERR_ARG, "logits not aligned to its element size");
   if ((int64_t)h->B * meta->P > (int64_t)h->ws.row_counter_cap) return fail(DT_ERR_ARG, "B*P too large");
+  return DT_OK;
+}
+
+int dt_verify_rows(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int32_t mode,
+                   int32_t with_top8, cudaStream_t s) {
+  if (!h) return fail(DT_ERR_ARG, "dt_verify_rows: null handle");
+  const int rc = check_verify_args(h, "dt_verify_rows", meta, logits, ld, mode);
+  if (rc != DT_OK) return rc;
+  cudaError_t e = dt::launch_verify_rows(h, meta, logits, ld, mode, with_top8 ? 1 : 0, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dt_verify_rows");
+  return DT_OK;
+}
+
+int dt_verify_accept(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int32_t mode,
+                     uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path, int32_t* bonus,
+                     int32_t* top8, cudaStream_t s) {
+  if (!h || !accept_len || !accept_path || !bonus) return fail(DT_ERR_ARG, "dt_verify_accept: null argument");
+  const int rc = check_verify_args(h, "dt_verify_accept", meta, logits, ld, mode);
+  if (rc != DT_OK) return rc;
+  cudaError_t e = dt::launch_verify_accept(h, meta, logits, ld, mode, seed, round, accept_len, accept_path, bonus,
+                                           top8, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dt_verify_accept");
+  return DT_OK;
+}
+
+int dt_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int32_t mode,
+              uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path, int32_t* bonus,
+              int32_t* top8, cudaStream_t s) {
+  if (!h || !accept_len || !accept_path || !bonus) return fail(DT_ERR_ARG, "dt_verify: null argument");
+  const int rc = check_verify_args(h, "dt_verify", meta, logits, ld, mode);
+  if (rc != DT_OK) return rc;
   cudaError_t e = dt::launch_verify(h, meta, logits, ld, mode, seed, round, accept_len, accept_path, bonus, top8, s);
   if (e != cudaSuccess) return cuda_fail(e, "dt_verify");
   return DT_OK;

@@ -8,71 +8,45 @@
 // rejection. Graft page step (3): every verified row also yields its top-k successor ids.
 #include <algorithm>
 
-#include "rowscan.cuh"
+#include "rowstream.cuh"
 
 namespace dt {
 namespace {
 
-struct RowPassArgs {
+struct StreamArgs {
   Workspace ws;
   const void* logits;
   int64_t ld;
-  int B, P, V, K, Smax;
+  int B, P, V, K, maxp;
+  int64_t Gtot;           // warps of the grid
   const int32_t* tokens;  // meta [B][P]
   const int32_t* n_pos;   // meta [B]
-  int32_t* top8;          // [B][P][8] or null
-  uint32_t first_wait_cap;
+  int test_timeout;
 };
 
-// Balanced over the used positions (request b reads rows i < n_pos[b]; a position without a valid
-// token is counted but not read); see the balanced row pass in rowscan.cuh.
+// Streaming pass of the verify: request b's rows are its used positions i < n_pos[b] (a position
+// without a valid token is counted but not read); every warp leaves the statistics and top-K keys
+// (K = 1, or 8 for the Graft refresh) of the row pieces it reads.
 template <typename T, bool SOFTMAX>
-__global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(RowPassArgs a) {
+__global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) verify_stream_kernel(StreamArgs a) {
   pdl_begin();
-  extern __shared__ __align__(128) uint8_t dyn_smem[];
-  __shared__ ScanSmem sm;
-  __shared__ RowPlan plan;
-  const int tid = threadIdx.x;
+  __shared__ WarpRing rings[kStreamWarps];
+  WarpRing& rg = rings[threadIdx.x >> 5];
   Workspace& ws = a.ws;
+  const int lane = threadIdx.x & 31;
   auto cnt = [&](int b) -> int { return min(max(a.n_pos[b], 0), a.P); };
-  if (tid < 32) {
-    RowPlan p;
-    plan_rows(p, a.B, a.V, a.Smax, (int)sizeof(T), cnt);
-    if (tid == 0) plan = p;
-  }
-  __syncthreads();
-  const RowPlan p = plan;
-  if ((int)blockIdx.x >= p.G) return;
-
   auto row_of = [&](int b, int i) -> const T* {
     const int64_t r = (int64_t)b * a.P + i;
-    if (a.tokens[r] < 0) return nullptr;  // invalid token: row not needed
+    if (a.test_timeout || a.tokens[r] < 0) return nullptr;  // invalid token: row not needed
     return reinterpret_cast<const T*>(a.logits) + r * a.ld;
   };
-  auto finish = [&](int b, int i, const SoftmaxStat& stt) {
-    const int64_t r = (int64_t)b * a.P + i;
-    if (a.tokens[r] < 0) return;  // block-uniform
-    if (tid == 0) {
-      RowStat st;
-      st.amax = (int32_t)key_id(sm.topk[0]);
-      st.m = stt.m;
-      if (SOFTMAX) {
-        if (stt.nan || !(stt.m > -INFINITY) || stt.m == INFINITY || !(stt.s_hi > 0.0f) || stt.s_hi == INFINITY)
-          set_status(ws.status, DT_DEV_BAD_LOGITS);
-        st.s = (double)stt.s_hi + (double)stt.s_lo;
-      } else {
-        st.s = 0.0;
-        if (sm.topk[0] == 0ull || !(st.m > -INFINITY)) set_status(ws.status, DT_DEV_BAD_LOGITS);
-      }
-      ws.row_stats[r] = st;
-    }
-    if (a.top8 && tid < 8) {
-      const uint64_t k = sm.topk[tid];
-      a.top8[r * 8 + tid] = (tid < a.K && k != 0ull) ? (int32_t)key_id(k) : -1;
-    }
-  };
-  scan_pieces<T, SOFTMAX>(p, a.V, a.K, a.B, ws.partials, ws.row_counter, ws.row_tau, sm, dyn_smem, a.first_wait_cap,
-                          ws.status, row_of, cnt, finish);
+  if (a.test_timeout && blockIdx.x == 0 && threadIdx.x == 0) set_status(ws.status, DT_DEV_TIMEOUT);
+  stream_rows<T, SOFTMAX>(a.B, a.V, a.K, a.maxp, a.Gtot, rg, ws.row_tau, cnt, row_of,
+                          [&](int64_t j, int64_t g, int b, int i, const PieceOut& o) {
+                            publish_partial(ws.partials + j + g, rg, o, a.K);
+                            if (lane == 0 && o.internal) set_status(ws.status, DT_DEV_INTERNAL);
+                            if (lane == 0 && o.bad) set_status(ws.status, DT_DEV_BAD_LOGITS);
+                          });
 }
 
 struct WalkArgs {
@@ -80,11 +54,14 @@ struct WalkArgs {
   dt_tree_meta meta;
   const void* logits;
   int64_t ld;
-  int P, V, dtype, mode;
+  int B, P, V, dtype, mode;
+  int K, maxp, esz, vecel;  // pieces of the streaming pass: keys per piece, pieces per row at most
+  int64_t Gtot;             // warps of the streaming launch
   uint32_t key0, key1, r0, r1;
   int32_t* accept_len;
   int32_t* accept_path;
   int32_t* bonus;
+  int32_t* top8;            // [B][P][8] or null
 };
 
 __device__ __forceinline__ float load_logit(const void* logits, int dtype, int64_t idx) {
@@ -118,9 +95,19 @@ __device__ double residual_rescan(const WalkArgs& a, int64_t r, float M, const i
   return (double)tot * 1.4210854715202004e-14;  // 2^-46
 }
 
-// One CTA per request.
+constexpr int kWalkWarps = kWalkThreads / 32;
+
+// One CTA per request. The statistics of the target rows come from the streaming pass's pieces:
+// greedy verify merges every used row first (argmax, and the top-8 ids for the Graft refresh);
+// sampling merges the softmax statistics of each row the walk visits.
 __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
   pdl_begin();
+  __shared__ uint64_t s_mbuf[kWalkWarps][256];  // per-warp merge scratch (pieces x keys <= 32 x 8)
+  __shared__ uint64_t s_mtop[kWalkWarps][kMaxK];
+  __shared__ uint64_t s_key[kMaxP];
+  __shared__ int64_t s_A, s_base;
+  __shared__ float s_m;
+  __shared__ double s_S;
   __shared__ int32_t s_first_child[kMaxP], s_next_sib[kMaxP];
   __shared__ int32_t s_path[kMaxP];
   __shared__ int32_t s_rej[kMaxP];
@@ -137,18 +124,66 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
   const int64_t rb = (int64_t)b * P;
   const int npos = min(a.meta.n_pos[b], P);
 
-  // stage the flattened tree (coalesced, independent loads)
+  const int lane = tid & 31, warp = tid >> 5;
+  auto cnt = [&](int bb) -> int { return min(max(a.meta.n_pos[bb], 0), a.P); };
+  // stage the flattened tree (coalesced, independent loads); warp 0 places this request's rows in the
+  // streaming pass's row order
+  if (warp == 0) {
+    const int64_t A = warp_total_rows(a.B, cnt);
+    const int64_t base = warp_rows_before(b, cnt);
+    if (lane == 0) {
+      s_A = A;
+      s_base = base;
+    }
+  }
   for (int p = tid; p < P; p += blockDim.x) {
     const bool used = p < npos;
     s_tok[p] = used ? a.meta.tokens[rb + p] : -1;
     s_par[p] = used ? a.meta.parents[rb + p] : -1;
     s_depth[p] = used ? a.meta.depth[rb + p] : -1;
     s_haschild[p] = 0;
+    s_key[p] = 0ull;
   }
   __syncthreads();
+  const int64_t rowA = s_A, rowbase = s_base;
+  const int64_t G = stream_warps(rowA, a.V, a.esz, a.Gtot, a.maxp);
+  for (int p = tid; p < npos; p += blockDim.x) ws.row_tau[rowbase + p] = 0ull;  // the pass is over
   if (a.mode == DT_GREEDY) {
+    if (a.top8 == nullptr) {
+      // argmax of every used row: the best of its pieces' keys (one load per piece)
+      for (int p = tid; p < npos; p += blockDim.x) {
+        if (s_tok[p] < 0) continue;
+        const RowPieces rp = row_pieces(rowbase + p, a.V, rowA, G, a.vecel);
+        uint64_t best = 0ull;
+        for (int q = 0; q < rp.S; ++q) {
+          const uint64_t k = ws.partials[rp.slot0 + q].keys[0];
+          best = k > best ? k : best;
+        }
+        s_key[p] = best;
+      }
+    } else {
+      // the top-8 of every used row (the Graft refresh) and its argmax: one warp per row
+      for (int p = warp; p < npos; p += kWalkWarps) {
+        if (s_tok[p] < 0) {
+          if (lane < 8) a.top8[(rb + p) * 8 + lane] = -1;
+          continue;
+        }
+        const RowPieces rp = row_pieces(rowbase + p, a.V, rowA, G, a.vecel);
+        float M, sh, sl;
+        if (rp.S > a.maxp) {  // never: the streaming plan bounds the pieces of a row
+          if (lane == 0) set_status(ws.status, DT_DEV_INTERNAL);
+          continue;
+        }
+        warp_merge_row(ws.partials + rp.slot0, rp.S, a.K, s_mbuf[warp], s_mtop[warp], false, M, sh, sl);
+        const uint64_t k = lane < 8 ? s_mtop[warp][lane] : 0ull;
+        if (lane < 8) a.top8[(rb + p) * 8 + lane] = (lane < a.K && k != 0ull) ? (int32_t)key_id(k) : -1;
+        if (lane == 0) s_key[p] = s_mtop[warp][0];
+      }
+    }
+    __syncthreads();
     for (int p = tid; p < npos; p += blockDim.x) {
-      s_amax[p] = s_tok[p] >= 0 ? ws.row_stats[rb + p].amax : -1;
+      if (s_tok[p] >= 0 && s_key[p] == 0ull) set_status(ws.status, DT_DEV_BAD_LOGITS);  // no finite entry
+      s_amax[p] = (s_tok[p] >= 0 && s_key[p] != 0ull) ? (int32_t)key_id(s_key[p]) : -1;
       if (p > 0 && s_par[p] >= 0) s_haschild[s_par[p]] = 1;
     }
     if (tid == 0) s_best = 0ull;
@@ -213,7 +248,26 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
   __syncthreads();
   for (int guard = 0; guard < kMaxP; ++guard) {
     const int cur = s_cur;
-    const RowStat st = ws.row_stats[rb + cur];
+    if (warp == 0) {  // the softmax statistics of the row at the current position, from its pieces
+      const RowPieces rp = row_pieces(rowbase + cur, a.V, rowA, G, a.vecel);
+      float M = -INFINITY, sh = 0.0f, sl = 0.0f;
+      if (s_tok[cur] < 0 || rp.S > a.maxp) {
+        if (lane == 0) set_status(ws.status, s_tok[cur] < 0 ? DT_DEV_BAD_TOKEN : DT_DEV_INTERNAL);
+      } else {
+        warp_merge_row(ws.partials + rp.slot0, rp.S, a.K, s_mbuf[0], s_mtop[0], true, M, sh, sl);
+      }
+      if (lane == 0) {
+        if (sh != sh || !(M > -INFINITY) || M == INFINITY || !(sh > 0.0f) || sh == INFINITY)
+          set_status(ws.status, DT_DEV_BAD_LOGITS);
+        s_m = M;
+        s_S = (double)sh + (double)sl;
+      }
+    }
+    __syncthreads();
+    RowStat st;
+    st.m = s_m;
+    st.s = s_S;
+    st.amax = -1;
     const double S = st.s;
     __syncthreads();
     if (tid == 0) {
@@ -359,44 +413,32 @@ __global__ void __launch_bounds__(kBonusThreads) verify_bonus_kernel(BonusArgs a
 }  // namespace
 
 cudaError_t init_verify_attributes() {
-  const int smem = kScanSmemBytes;
-  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  cudaError_t e = cudaFuncSetAttribute(verify_rows_kernel<uint16_t, false>, a, smem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<uint16_t, true>, a, smem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<float, false>, a, smem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<float, true>, a, smem);
-  // all of the unified L1 as shared memory, so that 4 CTAs fit on an SM
+  // all of the unified L1 as cache for the streaming passes (they use a few KB of shared memory)
   const cudaFuncAttribute c = cudaFuncAttributePreferredSharedMemoryCarveout;
-  const int mx = cudaSharedmemCarveoutMaxShared;
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<uint16_t, false>, c, mx);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<uint16_t, true>, c, mx);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<float, false>, c, mx);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_rows_kernel<float, true>, c, mx);
+  cudaError_t e = cudaFuncSetAttribute(verify_stream_kernel<uint16_t, false>, c, 10);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<uint16_t, true>, c, 10);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<float, false>, c, 10);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<float, true>, c, 10);
   return e;
 }
 
-cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int mode,
-                          uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path,
-                          int32_t* bonus, int32_t* top8, cudaStream_t s) {
-  const int P = meta->P;
-  const int V = h->cfg.V;
-  RowPassArgs ra;
+cudaError_t launch_verify_rows(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int mode,
+                               int with_top8, cudaStream_t s) {
+  StreamArgs ra;
   ra.ws = h->ws;
   ra.logits = logits;
   ra.ld = ld;
   ra.B = h->B;
-  ra.P = P;
-  ra.V = V;
-  ra.K = top8 ? 8 : 1;
-  ra.Smax = row_pass_smax(ra.K);
+  ra.P = meta->P;
+  ra.V = h->cfg.V;
+  ra.K = with_top8 ? 8 : 1;
+  ra.maxp = stream_max_pieces(ra.K);
+  const unsigned grid = (unsigned)stream_grid(h);
+  ra.Gtot = (int64_t)grid * kStreamWarps;
   ra.tokens = meta->tokens;
   ra.n_pos = meta->n_pos;
-  ra.top8 = top8;
-  ra.first_wait_cap = (h->cfg.flags & DT_FLAG_TEST_TIMEOUT) ? 0u : kSpinCap;
-  const unsigned grid = (unsigned)row_pass_grid(h);
-  const size_t smem = (size_t)kScanSmemBytes;
-  cudaError_t e;
-#define DT_LAUNCH_ROWS(T, SM) e = launch_k(verify_rows_kernel<T, SM>, dim3(grid), dim3(kRowThreads), smem, s, ra)
+  ra.test_timeout = (h->cfg.flags & DT_FLAG_TEST_TIMEOUT) ? 1 : 0;
+#define DT_LAUNCH_ROWS(T, SM) launch_k(verify_stream_kernel<T, SM>, dim3(grid), dim3(kStreamThreads), 0, s, ra)
   const bool sm_on = mode == DT_SAMPLE;
   if (h->cfg.dtype == DT_BF16) {
     if (sm_on) DT_LAUNCH_ROWS(uint16_t, true);
@@ -406,9 +448,16 @@ cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* lo
     else DT_LAUNCH_ROWS(float, false);
   }
 #undef DT_LAUNCH_ROWS
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
+cudaError_t launch_verify_accept(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld,
+                                 int mode, uint64_t seed, uint64_t round, int32_t* accept_len,
+                                 int32_t* accept_path, int32_t* bonus, int32_t* top8, cudaStream_t s) {
+  const int P = meta->P;
+  const int V = h->cfg.V;
+  const int esz = h->cfg.dtype == DT_BF16 ? 2 : 4;
+  cudaError_t e;
   WalkArgs wa;
   wa.ws = h->ws;
   wa.meta = *meta;
@@ -425,6 +474,13 @@ cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* lo
   wa.accept_len = accept_len;
   wa.accept_path = accept_path;
   wa.bonus = bonus;
+  wa.top8 = top8;
+  wa.B = h->B;
+  wa.K = top8 ? 8 : 1;
+  wa.maxp = stream_max_pieces(wa.K);
+  wa.esz = esz;
+  wa.vecel = 16 / esz;
+  wa.Gtot = (int64_t)stream_grid(h) * kStreamWarps;
   launch_k(verify_walk_kernel, dim3(h->B), dim3(kWalkThreads), 0, s, wa);
   e = cudaGetLastError();
   if (e != cudaSuccess || mode != DT_SAMPLE) return e;
@@ -448,6 +504,14 @@ cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* lo
   ba.bonus = bonus;
   launch_k(verify_bonus_kernel, dim3((unsigned)(h->B * Sb)), dim3(kBonusThreads), 0, s, ba);
   return cudaGetLastError();
+}
+
+cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int mode,
+                          uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path,
+                          int32_t* bonus, int32_t* top8, cudaStream_t s) {
+  cudaError_t e = launch_verify_rows(h, meta, logits, ld, mode, top8 != nullptr, s);
+  if (e != cudaSuccess) return e;
+  return launch_verify_accept(h, meta, logits, ld, mode, seed, round, accept_len, accept_path, bonus, top8, s);
 }
 
 }  // namespace dt

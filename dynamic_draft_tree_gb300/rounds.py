@@ -4,8 +4,11 @@ Call order (EAGLE-2 page Â§"ä¸€æ®µæ›´è´´è¿‘å®žçŽ°çš„æµç¨‹"; CAST page Â§å…³é”®è
 steps (1)-(3)):
 
   reset -> [frontier -> draft rows -> expand -> prune]* -> (verify count) -> rerank
-  (CAST prunes a layer and chooses the next frontier in one call, and reranks with the verify count)
   -> (retrieve) -> meta -> target rows -> verify -> (M refresh)
+
+By default a layer's expansion, its pruning and the next frontier are one call
+(dt_expand_prune_select, two kernels), and CAST's verify count and rerank are one call; with
+``fused=False`` every step is its own call.
 
 The draft and target model forwards are outside the library: ``draft_rows(d,
 frontier_token)`` must return the logits tensor [B][F][V] of layer d (row f =
@@ -17,9 +20,10 @@ a round, so a round can be captured in a CUDA graph.
 import torch
 
 from . import (Handle, Meta, Template, make_prune_params, make_prune_out, dt_tree_reset, dt_select_frontier,
-               dt_expand_layer, dt_cast_prune, dt_cast_prune_select, dt_cast_verify_rerank, dt_rerank, dt_graft_retrieve, dt_build_tree_meta, dt_verify,
-               dt_adj_update, DT_GREEDY, DT_SAMPLE, DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY,
-               DT_POLICY_GRAFT_CHECKPOINT)
+               dt_expand_layer, dt_expand_prune_select, dt_expand_rows, dt_expand_finish, dt_cast_prune,
+               dt_cast_verify_rerank, dt_rerank, dt_graft_retrieve, dt_build_tree_meta, dt_verify, dt_verify_rows,
+               dt_verify_accept, dt_adj_update, DT_GREEDY, DT_SAMPLE, DT_POLICY_CAST_WIDTH_DEPTH,
+               DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT, DT_POLICY_NONE)
 
 
 class RoundRunner:
@@ -27,8 +31,9 @@ class RoundRunner:
 
     def __init__(self, policy, B, V, K, k, D, P, D_path, m, dtype, T=0, cast=None, cast_tables=None,
                  graft=None, template=None, flags=0, device="cuda", fused=True):
-        """``fused`` (CAST): prune + frontier and verify count + rerank as single calls
-        (dt_cast_prune_select, dt_cast_verify_rerank) instead of the separate calls."""
+        """``fused``: each layer's expansion, pruning and next frontier as one call
+        (dt_expand_prune_select), and CAST's verify count + rerank as one (dt_cast_verify_rerank),
+        instead of the separate calls."""
         self.fused = fused
         self.policy, self.B, self.V, self.K, self.k, self.D = policy, B, V, K, k, D
         self.P, self.D_path, self.T = P, D_path, T
@@ -48,6 +53,7 @@ class RoundRunner:
         self.pos_offset = torch.zeros((B,), **i32)
         self.top8 = None
         self.params = None
+        self.prune_out = None
         if policy == "cast":
             S_T, S_D = cast_tables
             self.S_T = torch.as_tensor(S_T, dtype=torch.float64, device=device).contiguous()
@@ -73,12 +79,14 @@ class RoundRunner:
         self.prune_out = make_prune_out(width=self.width, stop=self.stop)
         self.verify_out = make_prune_out(m=self.m_dev)
 
-    def run(self, roots, draft_rows, target_rows, seed=0, rnd=0, M=None, n0=0, after_expand=None,
-            after_verify=None):
+    def run(self, roots, draft_rows, target_rows, seed=0, rnd=0, M=None, n0=0, timing=None):
         """Launch one round; returns nothing (outputs live in this object's tensors).
 
-        ``after_expand`` / ``after_verify`` (optional) are called right after those launches are
-        enqueued, e.g. to record timing events on the stream.
+        ``timing`` (optional): an object with ``start(kind)`` and ``stop(kind)``; the expansions
+        and the verify are then issued as their two halves (dt_expand_rows + dt_expand_finish,
+        dt_verify_rows + dt_verify_accept, the same kernels as the composite calls) and each half
+        is bracketed by start/stop with kind "expand_rows", "expand_finish", "verify_rows" or
+        "verify_accept", e.g. to record events around them.
         """
         h = self.h
         pol = self.policy
@@ -86,25 +94,28 @@ class RoundRunner:
             self.set_n0(n0)
         if pol == "graft":  # the checkpoints only ever set stop; CAST writes every entry, EAGLE none
             self.stop.zero_()
+        policy = {"cast": DT_POLICY_CAST_WIDTH_DEPTH, "graft": DT_POLICY_GRAFT_CHECKPOINT}.get(pol, DT_POLICY_NONE)
+        width = None if pol == "cast" else self.width
         dt_tree_reset(h, roots)
+        dt_select_frontier(h, None, None, self.frontier_token)  # layer 0 = {root}: the root in slot 0
         for d in range(1, self.D + 1):
-            if d > 1:
-                if pol != "cast" or not self.fused:  # fused CAST chose it when pruning layer d - 1
-                    dt_select_frontier(h, self.width, self.stop, self.frontier_token)
-                F = self.k
+            F = 1 if d == 1 else self.k
+            if d > 1 and not self.fused:
+                dt_select_frontier(h, self.width, self.stop, self.frontier_token)
+            logits = draft_rows(d, self.frontier_token)
+            if not self.fused:
+                dt_expand_layer(h, logits, F)
+                if pol in ("cast", "graft"):
+                    dt_cast_prune(h, policy, self.params, self.prune_out)
+            elif timing is not None:
+                timing.start("expand_rows")
+                dt_expand_rows(h, logits, F)
+                timing.stop("expand_rows")
+                timing.start("expand_finish")
+                dt_expand_finish(h, F, True, policy, self.params, self.prune_out, width, self.frontier_token)
+                timing.stop("expand_finish")
             else:
-                dt_select_frontier(h, None, None, self.frontier_token)  # layer 0 = {root}: the root in slot 0
-                F = 1
-            dt_expand_layer(h, draft_rows(d, self.frontier_token), F)
-            if after_expand is not None:
-                after_expand()
-            if pol == "cast":
-                if d < self.D and self.fused:  # prune layer d and choose the frontier of layer d + 1
-                    dt_cast_prune_select(h, self.params, self.prune_out, self.frontier_token)
-                else:
-                    dt_cast_prune(h, DT_POLICY_CAST_WIDTH_DEPTH, self.params, self.prune_out)
-            elif pol == "graft":
-                dt_cast_prune(h, DT_POLICY_GRAFT_CHECKPOINT, self.params, self.prune_out)
+                dt_expand_prune_select(h, logits, F, policy, self.params, self.prune_out, width, self.frontier_token)
         if pol == "cast" and self.fused:  # verify count and the rerank to it
             dt_cast_verify_rerank(h, self.params, self.verify_out, self.selected)
         else:
@@ -119,9 +130,17 @@ class RoundRunner:
         else:
             dt_build_tree_meta(h, self.selected, self.m_cap, self.meta, self.pos_offset)
         logits = target_rows(self.meta)
-        dt_verify(h, self.meta, logits, DT_SAMPLE if self.T == 1 else DT_GREEDY, seed, rnd, self.accept_len,
-                  self.accept_path, self.bonus, self.top8)
-        if after_verify is not None:
-            after_verify()
+        mode = DT_SAMPLE if self.T == 1 else DT_GREEDY
+        if timing is not None:
+            timing.start("verify_rows")
+            dt_verify_rows(h, self.meta, logits, mode, self.top8 is not None)
+            timing.stop("verify_rows")
+            timing.start("verify_accept")
+            dt_verify_accept(h, self.meta, logits, mode, seed, rnd, self.accept_len, self.accept_path, self.bonus,
+                             self.top8)
+            timing.stop("verify_accept")
+        else:
+            dt_verify(h, self.meta, logits, mode, seed, rnd, self.accept_len, self.accept_path, self.bonus,
+                      self.top8)
         if pol == "graft":
             dt_adj_update(h, M, self.meta, self.top8)

@@ -55,7 +55,8 @@ enum { DT_GREEDY = 0, DT_SAMPLE = 1 };
 enum {
   DT_POLICY_CAST_WIDTH_DEPTH = 0, /* CAST width n_d and grow/stop after layer d */
   DT_POLICY_CAST_VERIFY = 1,      /* CAST batch-wide verify count m            */
-  DT_POLICY_GRAFT_CHECKPOINT = 2  /* Graft confidence checkpoint after layer d */
+  DT_POLICY_GRAFT_CHECKPOINT = 2, /* Graft confidence checkpoint after layer d */
+  DT_POLICY_NONE = 3              /* no pruning (EAGLE-2): dt_expand_prune_select only */
 };
 /* Bits of the device status word. */
 enum {
@@ -66,8 +67,9 @@ enum {
   DT_DEV_INTERNAL = 16     /* an internal iteration bound was hit                              */
 };
 /* dt_config.flags */
-enum { DT_FLAG_TEST_TIMEOUT = 1 }; /* test only: the first copy wait of each row kernel gives up at
-                                      once (it still drains its copies), exercising DT_DEV_TIMEOUT */
+enum { DT_FLAG_TEST_TIMEOUT = 1 }; /* test only: the streaming row passes (expansion and verify)
+                                      behave as if their reads had timed out: they read nothing, leave
+                                      empty results and set DT_DEV_TIMEOUT, exercising that path */
 
 typedef struct dt_handle dt_handle;
 
@@ -206,6 +208,37 @@ int dt_expand_layer(dt_handle* h, const void* logits, int64_t ld, int32_t F, cud
 int dt_cast_prune(dt_handle* h, int32_t policy, const dt_prune_params* p, const dt_prune_out* out,
                   cudaStream_t s);
 
+/* The two halves of an expansion, for callers that time or schedule them apart.
+ * dt_expand_rows (a1, EAGLE-2 §扩展阶段): the streaming pass of the next layer: every frontier row
+ * (same logits layout as dt_expand_layer) is read once, in equal contiguous ranges of the rows laid
+ * end to end, one per warp; each row piece's max, sum exp(x - max) and top-K keys are left in the
+ * handle's workspace. The tree is unchanged.
+ * dt_expand_finish (a1 + a2 [+ a3/a4]): merges those pieces and completes the layer exactly as
+ * dt_expand_layer does (select = 0; policy, p, out, width, frontier_token ignored), or as
+ * dt_expand_prune_select does (select = 1). It must follow dt_expand_rows with the same F on the same
+ * stream, with no other call of this handle between them. */
+int dt_expand_rows(dt_handle* h, const void* logits, int64_t ld, int32_t F, cudaStream_t s);
+int dt_expand_finish(dt_handle* h, int32_t F, int32_t select, int32_t policy, const dt_prune_params* p,
+                     const dt_prune_out* out, const int32_t* width, int32_t width_len, int32_t* frontier_token,
+                     cudaStream_t s);
+
+/* a1 + a2, then a3/a4, then the next frontier, in two launches: exactly
+ *   dt_expand_layer(h, logits, ld, F, s);
+ *   policy DT_POLICY_CAST_WIDTH_DEPTH: dt_cast_prune(h, policy, p, out, s), then
+ *     dt_select_frontier(h, out->width, 1, out->stop, frontier_token, s);
+ *   policy DT_POLICY_GRAFT_CHECKPOINT: dt_cast_prune(h, policy, p, out, s), then
+ *     dt_select_frontier(h, width, width_len, out->stop, frontier_token, s);
+ *   policy DT_POLICY_NONE (EAGLE-2, no pruning): dt_select_frontier(h, width, width_len, NULL,
+ *     frontier_token, s);
+ * except that no frontier is selected once the tree has D_max layers. width: device [width_len]
+ * (1 or B) or NULL for W; p and out may be NULL for DT_POLICY_NONE. The expansion's rows are read
+ * by one streaming kernel; a second kernel merges them, writes the children, orders the layer and
+ * applies the policy and the selection (CAST in the same CTA when B <= 32 and B * W * K <= 4096,
+ * otherwise the pruning kernel follows). */
+int dt_expand_prune_select(dt_handle* h, const void* logits, int64_t ld, int32_t F, int32_t policy,
+                           const dt_prune_params* p, const dt_prune_out* out, const int32_t* width,
+                           int32_t width_len, int32_t* frontier_token, cudaStream_t s);
+
 /* a3 + a2 in one launch: exactly dt_cast_prune(h, DT_POLICY_CAST_WIDTH_DEPTH, p, out, s) followed by
  * dt_select_frontier(h, out->width, 1, out->stop, frontier_token, s): CAST width and grow/stop after
  * the newest layer, then the next layer's frontier (none for stopped requests). One kernel instead of
@@ -256,6 +289,20 @@ int dt_build_tree_meta(dt_handle* h, const int32_t* selected, int32_t m_cap, con
 int dt_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int32_t mode,
               uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path, int32_t* bonus,
               int32_t* top8, cudaStream_t s);
+
+/* The two halves of dt_verify, for callers that time or schedule them apart (same arguments).
+ * dt_verify_rows (a8): the streaming pass over the used target rows (one read of each), leaving each
+ * row piece's statistics in the handle's workspace: the argmax key, the top-8 keys when with_top8,
+ * and for DT_SAMPLE the max and sum exp(x - max).
+ * dt_verify_accept (a9 + the bonus): merges the pieces of the rows it needs and runs the acceptance
+ * walk; with top8 non-NULL it also writes the top-8 ids of every used row (then dt_verify_rows must
+ * have had with_top8 = 1). It must follow dt_verify_rows with the same meta, logits and mode on the
+ * same stream, with no other call of this handle between them. */
+int dt_verify_rows(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int32_t mode,
+                   int32_t with_top8, cudaStream_t s);
+int dt_verify_accept(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int32_t mode,
+                     uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path, int32_t* bonus,
+                     int32_t* top8, cudaStream_t s);
 
 /* a10 (Graft step (3)): M[b][token_i][0..7] = top8[b][i][0..7] for every used position i with a
  * valid token; when a token repeats the highest position wins. M: device [B][V][8]. */
