@@ -153,7 +153,7 @@ class Clocks:
 
 # DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte of the streaming
 # kernels, from the captures summarised in profiles/ (None while no capture of the current kernel exists).
-TRAFFIC_PER_ALGO_BYTE = {"expand_rows": None, "verify_rows": None}
+TRAFFIC_PER_ALGO_BYTE = {"expand": None, "verify_rows": None}
 
 
 def measured_peaks():
@@ -338,7 +338,7 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
     kern = {}
     exp_bytes = sum(sum(rows_expand[s % R]) for s in range(steps)) * V * esz
     ver_bytes = sum(rows_verify[s % R] for s in range(steps)) * V * esz
-    for kind, nbytes in (("expand_rows", exp_bytes), ("expand_finish", None), ("verify_rows", ver_bytes),
+    for kind, nbytes in (("expand", exp_bytes), ("prune_select", None), ("verify_rows", ver_bytes),
                          ("verify_accept", None)):
         t = timing.ms(kind)
         if not t:
@@ -348,24 +348,27 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
             gbs = nbytes / (sum(t) / 1e3) / 1e9
             d.update(gbs=gbs, frac=gbs / peak, bytes_per_launch=nbytes / len(t))
         kern[kind] = d
-    # the expansion layer as a whole (streaming + finishing kernels)
-    if "expand_rows" in kern and "expand_finish" in kern:
-        lay = sum(timing.ms("expand_rows")) + sum(timing.ms("expand_finish"))
-        kern["expand_layer"] = {"avg_us": 1e3 * lay / len(timing.ms("expand_rows")),
+    # the expansion layer as a whole (expansion kernel + pruning / frontier kernels)
+    if "expand" in kern and "prune_select" in kern:
+        lay = sum(timing.ms("expand")) + sum(timing.ms("prune_select"))
+        kern["expand_layer"] = {"avg_us": 1e3 * lay / len(timing.ms("expand")),
                                 "gbs": exp_bytes / (lay / 1e3) / 1e9}
-    streaming = [k_ for k_ in ("expand_rows", "verify_rows") if k_ in kern]
+    streaming = [k_ for k_ in ("expand", "verify_rows") if k_ in kern]
     top = max(streaming, key=lambda k_: kern[k_]["total_us_per_round"])
     tr = TRAFFIC_PER_ALGO_BYTE.get(top)
-    names = {"expand_rows": "expand_stream_kernel (vocab max, softmax sum and top-K pieces of the frontier rows)",
+    names = {"expand": "expand_kernel (vocab softmax + top-K of the frontier rows, children, layer order)",
              "verify_rows": "verify_stream_kernel (argmax / softmax pieces of the used target rows)"}
     roofline = {"bound": "hbm", "achieved": kern[top]["gbs"], "peak": peak, "unit": "GB/s", "frac": kern[top]["frac"],
                 "traffic": None if tr is None else tr * kern[top]["bytes_per_launch"], "kernel": names[top],
                 "peak_source": peak_kind, "bytes_per_launch": kern[top]["bytes_per_launch"],
                 "avg_launch_us": kern[top]["avg_us"]}
-    # kernels of the library launched per round: reset + layer-1 frontier, 2 per layer (CAST: 3 when the
-    # batch does not fit one finishing CTA), verify count + rerank (CAST) or rerank, retrieval (Graft),
-    # meta, 2 or 3 for the verify (the bonus draw with sampling), the M refresh (Graft)
-    launches = 2 + 2 * D + (2 if w["policy"] == "cast" else 1) + (1 if graft else 0) + 1 + \
+    # kernels of the library launched per round: reset + layer-1 frontier; per layer the expansion and
+    # the pruning / frontier kernels (CAST: 1 fused; Graft: checkpoint + frontier; EAGLE: frontier; none
+    # after the last layer except CAST's and Graft's pruning); verify count + rerank (CAST) or rerank,
+    # retrieval (Graft), meta, 2 or 3 for the verify (the bonus draw with sampling), the M refresh (Graft)
+    per_layer = {"cast": 1, "graft": 2, "eagle": 1}[w["policy"]]
+    last = 1 if w["policy"] in ("cast", "graft") else 0
+    launches = 2 + D + per_layer * (D - 1) + last + (2 if w["policy"] == "cast" else 1) + (1 if graft else 0) + 1 + \
         (3 if w["T"] == 1 else 2) + (1 if graft else 0)
 
     out = {"label": label, "value": value, "unit": UNIT, "ms_per_step": ms / steps, "steps": steps,

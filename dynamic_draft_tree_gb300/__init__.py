@@ -124,23 +124,6 @@ def dt_expand_prune_select(h, logits, F, policy, params=None, out=None, width=No
                                      _ptr(frontier_token), _stream(stream)))
 
 
-def dt_expand_rows(h, logits, F, ld=None, stream=None):
-    """Streaming half of an expansion (reads the frontier rows; the tree is unchanged)."""
-    ld = logits.shape[-1] if ld is None else ld
-    check(lib.dt_expand_rows(h.h, _ptr(logits), ld, F, _stream(stream)))
-
-
-def dt_expand_finish(h, F, select=False, policy=DT_POLICY_NONE, params=None, out=None, width=None,
-                     frontier_token=None, stream=None):
-    """Finishing half of an expansion (after dt_expand_rows): the layer, and with ``select`` the
-    policy's pruning and the next frontier."""
-    wl = 0 if width is None else width.numel()
-    check(lib.dt_expand_finish(h.h, F, 1 if select else 0, policy,
-                               None if params is None else ctypes.byref(params),
-                               None if out is None else ctypes.byref(out), _ptr(width), wl, _ptr(frontier_token),
-                               _stream(stream)))
-
-
 def dt_cast_prune(h, policy, params, out, stream=None):
     check(lib.dt_cast_prune(h.h, policy, ctypes.byref(params), ctypes.byref(out), _stream(stream)))
 

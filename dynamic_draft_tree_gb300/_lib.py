@@ -21,8 +21,7 @@ EXPORTS = ["dt_last_error_string", "dt_create", "dt_destroy", "dt_get_tree", "dt
            "dt_clear_status", "dt_tree_reset", "dt_select_frontier", "dt_expand_layer", "dt_cast_prune",
            "dt_rerank", "dt_graft_retrieve", "dt_build_tree_meta", "dt_verify", "dt_adj_update",
            "dt_row_topk_static", "dt_cast_prune_select",
-           "dt_cast_verify_rerank", "dt_expand_prune_select", "dt_expand_rows", "dt_expand_finish",
-           "dt_verify_rows", "dt_verify_accept"]
+           "dt_cast_verify_rerank", "dt_expand_prune_select", "dt_verify_rows", "dt_verify_accept"]
 
 c_i32p = ctypes.c_void_p
 vp = ctypes.c_void_p
@@ -95,9 +94,6 @@ def _load():
         "dt_expand_prune_select": ([vp, vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                     ctypes.POINTER(DtPruneParams), ctypes.POINTER(DtPruneOut), vp, ctypes.c_int32,
                                     vp, vp], I),
-        "dt_expand_rows": ([vp, vp, ctypes.c_int64, ctypes.c_int32, vp], I),
-        "dt_expand_finish": ([vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(DtPruneParams),
-                              ctypes.POINTER(DtPruneOut), vp, ctypes.c_int32, vp, vp], I),
         "dt_verify_rows": ([vp, ctypes.POINTER(DtTreeMeta), vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp], I),
         "dt_verify_accept": ([vp, ctypes.POINTER(DtTreeMeta), vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64,
                               ctypes.c_uint64, vp, vp, vp, vp, vp], I),

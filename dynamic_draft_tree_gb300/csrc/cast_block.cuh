@@ -1,5 +1,4 @@
-// CAST width/depth pruning as a block-level device function, shared by the standalone pruning kernel
-// and the expansion's finishing kernel (which runs it right after ordering the new layer).
+// CAST width/depth pruning and the Graft checkpoint test as device functions of the pruning kernels.
 //
 // CAST page §关键设计 2-3: marginal utility (u_k - u_k0)/(c_k - c_k0) against C1 for the width, the
 // FIFO gain buffer against C2 for the depth; costs from the S_T/S_D lookup tables.

@@ -260,13 +260,6 @@ static int check_cast_width_params(const dt_handle* h, const dt_prune_params* p,
   return DT_OK;
 }
 
-static int check_expand_args(const dt_handle* h, const char* who, int32_t F) {
-  if (h->B < 1) return fail(DT_ERR_ARG, "%s: no tree (call dt_tree_reset)", who);
-  if (h->depth >= h->cfg.D_max) return fail(DT_ERR_ARG, "%s: tree already has D_max layers", who);
-  if (F < 1 || F > h->cfg.W) return fail(DT_ERR_ARG, "F=%d outside [1, W=%d]", F, h->cfg.W);
-  return DT_OK;
-}
-
 static int check_policy_args(const dt_handle* h, int32_t policy, const dt_prune_params* p, const dt_prune_out* out,
                              const int32_t* width, int32_t width_len) {
   if (width && width_len != 1 && width_len != h->B) return fail(DT_ERR_ARG, "width_len must be 1 or B");
@@ -283,34 +276,6 @@ static int check_policy_args(const dt_handle* h, int32_t policy, const dt_prune_
   if (policy != DT_POLICY_NONE)
     return fail(DT_ERR_ARG, "policy must be DT_POLICY_NONE, DT_POLICY_CAST_WIDTH_DEPTH or "
                             "DT_POLICY_GRAFT_CHECKPOINT");
-  return DT_OK;
-}
-
-int dt_expand_rows(dt_handle* h, const void* logits, int64_t ld, int32_t F, cudaStream_t s) {
-  if (!h || !logits) return fail(DT_ERR_ARG, "dt_expand_rows: null argument");
-  int rc = check_expand_args(h, "dt_expand_rows", F);
-  if (rc != DT_OK) return rc;
-  if (ld < h->cfg.V) return fail(DT_ERR_ARG, "ld=%lld < V", (long long)ld);
-  const size_t esz = h->cfg.dtype == DT_BF16 ? 2 : 4;
-  if (!aligned(logits, esz)) return fail(DT_ERR_ARG, "logits not aligned to its element size");
-  cudaError_t e = dt::launch_expand_rows(h, logits, ld, F, s);
-  if (e != cudaSuccess) return cuda_fail(e, "dt_expand_rows");
-  return DT_OK;
-}
-
-int dt_expand_finish(dt_handle* h, int32_t F, int32_t select, int32_t policy, const dt_prune_params* p,
-                     const dt_prune_out* out, const int32_t* width, int32_t width_len, int32_t* frontier_token,
-                     cudaStream_t s) {
-  if (!h) return fail(DT_ERR_ARG, "dt_expand_finish: null handle");
-  int rc = check_expand_args(h, "dt_expand_finish", F);
-  if (rc != DT_OK) return rc;
-  if (select) {
-    rc = check_policy_args(h, policy, p, out, width, width_len);
-    if (rc != DT_OK) return rc;
-  }
-  cudaError_t e = dt::launch_expand_finish(h, F, select ? policy : dt::DT_EXPAND_ONLY, p, out, width, width_len,
-                                           frontier_token, s);
-  if (e != cudaSuccess) return cuda_fail(e, "dt_expand_finish");
   return DT_OK;
 }
 

@@ -127,16 +127,10 @@ cudaError_t launch_select_frontier(dt_handle* h, const int32_t* width, int width
                                    int32_t* frontier_token, cudaStream_t s);
 cudaError_t launch_expand(dt_handle* h, const void* logits, int64_t ld, int F, cudaStream_t s);
 // Expansion followed, by policy, by no pruning (DT_POLICY_NONE), the Graft checkpoint or CAST's width
-// and depth pruning, then the next frontier (not after D_max). DT_EXPAND_ONLY: the expansion alone.
-constexpr int DT_EXPAND_ONLY = -1;
+// and depth pruning, then the next frontier (not after D_max).
 cudaError_t launch_expand_ex(dt_handle* h, const void* logits, int64_t ld, int F, int policy,
                              const dt_prune_params* p, const dt_prune_out* out, const int32_t* width,
                              int width_len, int32_t* frontier_token, cudaStream_t s);
-cudaError_t launch_expand_rows(dt_handle* h, const void* logits, int64_t ld, int F, cudaStream_t s);
-cudaError_t launch_expand_finish(dt_handle* h, int F, int policy, const dt_prune_params* p,
-                                 const dt_prune_out* out, const int32_t* width, int width_len,
-                                 int32_t* frontier_token, cudaStream_t s);
-bool expand_fuses_cast(const dt_handle* h);
 // CTAs of a streaming row pass (one wave).
 int stream_grid(const dt_handle* h);
 cudaError_t launch_cast_prune(dt_handle* h, int policy, const dt_prune_params* p, const dt_prune_out* out,
@@ -163,6 +157,11 @@ cudaError_t launch_verify_accept(dt_handle* h, const dt_tree_meta* meta, const v
                                  int32_t* accept_path, int32_t* bonus, int32_t* top8, cudaStream_t s);
 cudaError_t launch_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta, const int32_t* top8,
                               cudaStream_t s);
+// Expansion row pass: CTAs per launch (one wave) and the most pieces a row may be cut into when its
+// partial lists hold K keys.
+int row_pass_grid(const dt_handle* h);
+int row_pass_smax(int K);
+
 cudaError_t launch_row_topk_static(const void* logits, int64_t ld, int rows, int V, int K, int dtype, float* logp,
                                    int32_t* ids, int32_t* status, cudaStream_t s);
 

@@ -30,8 +30,9 @@ struct StreamArgs {
 template <typename T, bool SOFTMAX>
 __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) verify_stream_kernel(StreamArgs a) {
   pdl_begin();
-  __shared__ WarpRing rings[kStreamWarps];
-  WarpRing& rg = rings[threadIdx.x >> 5];
+  extern __shared__ __align__(16) uint8_t stream_smem[];
+  WarpStream& wsm = reinterpret_cast<WarpStream*>(stream_smem)[threadIdx.x >> 5];
+  WarpRing& rg = wsm.rg;
   Workspace& ws = a.ws;
   const int lane = threadIdx.x & 31;
   auto cnt = [&](int b) -> int { return min(max(a.n_pos[b], 0), a.P); };
@@ -41,7 +42,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) verify_strea
     return reinterpret_cast<const T*>(a.logits) + r * a.ld;
   };
   if (a.test_timeout && blockIdx.x == 0 && threadIdx.x == 0) set_status(ws.status, DT_DEV_TIMEOUT);
-  stream_rows<T, SOFTMAX>(a.B, a.V, a.K, a.maxp, a.Gtot, rg, ws.row_tau, cnt, row_of,
+  stream_rows<T, SOFTMAX>(a.B, a.V, a.K, a.maxp, a.Gtot, wsm, ws.row_tau, cnt, row_of,
                           [&](int64_t j, int64_t g, int b, int i, const PieceOut& o) {
                             publish_partial(ws.partials + j + g, rg, o, a.K);
                             if (lane == 0 && o.internal) set_status(ws.status, DT_DEV_INTERNAL);
@@ -147,17 +148,21 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
   __syncthreads();
   const int64_t rowA = s_A, rowbase = s_base;
   const int64_t G = stream_warps(rowA, a.V, a.esz, a.Gtot, a.maxp);
+  const PieceMap pm(rowA, a.V, G, a.vecel);
   for (int p = tid; p < npos; p += blockDim.x) ws.row_tau[rowbase + p] = 0ull;  // the pass is over
   if (a.mode == DT_GREEDY) {
     if (a.top8 == nullptr) {
       // argmax of every used row: the best of its pieces' keys (one load per piece)
       for (int p = tid; p < npos; p += blockDim.x) {
         if (s_tok[p] < 0) continue;
-        const RowPieces rp = row_pieces(rowbase + p, a.V, rowA, G, a.vecel);
+        const RowPieces rp = pm.row(rowbase + p);
         uint64_t best = 0ull;
-        for (int q = 0; q < rp.S; ++q) {
-          const uint64_t k = ws.partials[rp.slot0 + q].keys[0];
-          best = k > best ? k : best;
+        for (int q0 = 0; q0 < rp.S; q0 += 8) {  // independent loads, eight at a time
+          uint64_t k8[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) k8[u] = q0 + u < rp.S ? ws.partials[rp.slot0 + q0 + u].keys[0] : 0ull;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) best = k8[u] > best ? k8[u] : best;
         }
         s_key[p] = best;
       }
@@ -168,13 +173,13 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
           if (lane < 8) a.top8[(rb + p) * 8 + lane] = -1;
           continue;
         }
-        const RowPieces rp = row_pieces(rowbase + p, a.V, rowA, G, a.vecel);
+        const RowPieces rp = pm.row(rowbase + p);
         float M, sh, sl;
         if (rp.S > a.maxp) {  // never: the streaming plan bounds the pieces of a row
           if (lane == 0) set_status(ws.status, DT_DEV_INTERNAL);
           continue;
         }
-        warp_merge_row(ws.partials + rp.slot0, rp.S, a.K, s_mbuf[warp], s_mtop[warp], false, M, sh, sl);
+        warp_merge_row(ws.partials + rp.slot0, rp.S, a.K, s_mbuf[warp], 256, s_mtop[warp], false, M, sh, sl);
         const uint64_t k = lane < 8 ? s_mtop[warp][lane] : 0ull;
         if (lane < 8) a.top8[(rb + p) * 8 + lane] = (lane < a.K && k != 0ull) ? (int32_t)key_id(k) : -1;
         if (lane == 0) s_key[p] = s_mtop[warp][0];
@@ -249,12 +254,12 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
   for (int guard = 0; guard < kMaxP; ++guard) {
     const int cur = s_cur;
     if (warp == 0) {  // the softmax statistics of the row at the current position, from its pieces
-      const RowPieces rp = row_pieces(rowbase + cur, a.V, rowA, G, a.vecel);
+      const RowPieces rp = pm.row(rowbase + cur);
       float M = -INFINITY, sh = 0.0f, sl = 0.0f;
       if (s_tok[cur] < 0 || rp.S > a.maxp) {
         if (lane == 0) set_status(ws.status, s_tok[cur] < 0 ? DT_DEV_BAD_TOKEN : DT_DEV_INTERNAL);
       } else {
-        warp_merge_row(ws.partials + rp.slot0, rp.S, a.K, s_mbuf[0], s_mtop[0], true, M, sh, sl);
+        warp_merge_row(ws.partials + rp.slot0, rp.S, a.K, s_mbuf[0], 256, s_mtop[0], true, M, sh, sl);
       }
       if (lane == 0) {
         if (sh != sh || !(M > -INFINITY) || M == INFINITY || !(sh > 0.0f) || sh == INFINITY)
@@ -412,13 +417,21 @@ __global__ void __launch_bounds__(kBonusThreads) verify_bonus_kernel(BonusArgs a
 
 }  // namespace
 
+int stream_grid(const dt_handle* h) { return std::max(1, h->num_sms * kStreamCtasPerSm); }
+
 cudaError_t init_verify_attributes() {
-  // all of the unified L1 as cache for the streaming passes (they use a few KB of shared memory)
-  const cudaFuncAttribute c = cudaFuncAttributePreferredSharedMemoryCarveout;
-  cudaError_t e = cudaFuncSetAttribute(verify_stream_kernel<uint16_t, false>, c, 10);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<uint16_t, true>, c, 10);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<float, false>, c, 10);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<float, true>, c, 10);
+  // the streaming kernels: two CTAs of eight warps with their copy rings per SM
+  const cudaFuncAttribute dyn = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  const cudaFuncAttribute carve = cudaFuncAttributePreferredSharedMemoryCarveout;
+  const int mx = cudaSharedmemCarveoutMaxShared, sb = (int)stream_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(verify_stream_kernel<uint16_t, false>, dyn, sb);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<uint16_t, true>, dyn, sb);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<float, false>, dyn, sb);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<float, true>, dyn, sb);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<uint16_t, false>, carve, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<uint16_t, true>, carve, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<float, false>, carve, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_stream_kernel<float, true>, carve, mx);
   return e;
 }
 
@@ -438,7 +451,8 @@ cudaError_t launch_verify_rows(dt_handle* h, const dt_tree_meta* meta, const voi
   ra.tokens = meta->tokens;
   ra.n_pos = meta->n_pos;
   ra.test_timeout = (h->cfg.flags & DT_FLAG_TEST_TIMEOUT) ? 1 : 0;
-#define DT_LAUNCH_ROWS(T, SM) launch_k(verify_stream_kernel<T, SM>, dim3(grid), dim3(kStreamThreads), 0, s, ra)
+#define DT_LAUNCH_ROWS(T, SM) \
+  launch_k(verify_stream_kernel<T, SM>, dim3(grid), dim3(kStreamThreads), stream_smem_bytes(), s, ra)
   const bool sm_on = mode == DT_SAMPLE;
   if (h->cfg.dtype == DT_BF16) {
     if (sm_on) DT_LAUNCH_ROWS(uint16_t, true);

@@ -20,8 +20,7 @@ a round, so a round can be captured in a CUDA graph.
 import torch
 
 from . import (Handle, Meta, Template, make_prune_params, make_prune_out, dt_tree_reset, dt_select_frontier,
-               dt_expand_layer, dt_expand_prune_select, dt_expand_rows, dt_expand_finish, dt_cast_prune,
-               dt_cast_verify_rerank, dt_rerank, dt_graft_retrieve, dt_build_tree_meta, dt_verify, dt_verify_rows,
+               dt_expand_layer, dt_expand_prune_select, dt_cast_prune, dt_cast_prune_select, dt_cast_verify_rerank, dt_rerank, dt_graft_retrieve, dt_build_tree_meta, dt_verify, dt_verify_rows,
                dt_verify_accept, dt_adj_update, DT_GREEDY, DT_SAMPLE, DT_POLICY_CAST_WIDTH_DEPTH,
                DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT, DT_POLICY_NONE)
 
@@ -82,11 +81,11 @@ class RoundRunner:
     def run(self, roots, draft_rows, target_rows, seed=0, rnd=0, M=None, n0=0, timing=None):
         """Launch one round; returns nothing (outputs live in this object's tensors).
 
-        ``timing`` (optional): an object with ``start(kind)`` and ``stop(kind)``; the expansions
-        and the verify are then issued as their two halves (dt_expand_rows + dt_expand_finish,
-        dt_verify_rows + dt_verify_accept, the same kernels as the composite calls) and each half
-        is bracketed by start/stop with kind "expand_rows", "expand_finish", "verify_rows" or
-        "verify_accept", e.g. to record events around them.
+        ``timing`` (optional): an object with ``start(kind)`` and ``stop(kind)``; the composite
+        calls are then issued as their parts (dt_expand_layer + the pruning / frontier calls,
+        dt_verify_rows + dt_verify_accept: the same kernels) and each part is bracketed by
+        start/stop with kind "expand", "prune_select", "verify_rows" or "verify_accept", e.g. to
+        record events around them.
         """
         h = self.h
         pol = self.policy
@@ -107,13 +106,23 @@ class RoundRunner:
                 dt_expand_layer(h, logits, F)
                 if pol in ("cast", "graft"):
                     dt_cast_prune(h, policy, self.params, self.prune_out)
-            elif timing is not None:
-                timing.start("expand_rows")
-                dt_expand_rows(h, logits, F)
-                timing.stop("expand_rows")
-                timing.start("expand_finish")
-                dt_expand_finish(h, F, True, policy, self.params, self.prune_out, width, self.frontier_token)
-                timing.stop("expand_finish")
+            elif timing is not None:  # the kernels of dt_expand_prune_select, as separate calls
+                timing.start("expand")
+                dt_expand_layer(h, logits, F)
+                timing.stop("expand")
+                timing.start("prune_select")
+                if pol == "cast":
+                    if d < self.D:
+                        dt_cast_prune_select(h, self.params, self.prune_out, self.frontier_token)
+                    else:
+                        dt_cast_prune(h, policy, self.params, self.prune_out)
+                else:
+                    if pol == "graft":
+                        dt_cast_prune(h, policy, self.params, self.prune_out)
+                    if d < self.D:
+                        dt_select_frontier(h, self.width, self.stop if pol == "graft" else None,
+                                           self.frontier_token)
+                timing.stop("prune_select")
             else:
                 dt_expand_prune_select(h, logits, F, policy, self.params, self.prune_out, width, self.frontier_token)
         if pol == "cast" and self.fused:  # verify count and the rerank to it

@@ -208,33 +208,16 @@ int dt_expand_layer(dt_handle* h, const void* logits, int64_t ld, int32_t F, cud
 int dt_cast_prune(dt_handle* h, int32_t policy, const dt_prune_params* p, const dt_prune_out* out,
                   cudaStream_t s);
 
-/* The two halves of an expansion, for callers that time or schedule them apart.
- * dt_expand_rows (a1, EAGLE-2 §扩展阶段): the streaming pass of the next layer: every frontier row
- * (same logits layout as dt_expand_layer) is read once, in equal contiguous ranges of the rows laid
- * end to end, one per warp; each row piece's max, sum exp(x - max) and top-K keys are left in the
- * handle's workspace. The tree is unchanged.
- * dt_expand_finish (a1 + a2 [+ a3/a4]): merges those pieces and completes the layer exactly as
- * dt_expand_layer does (select = 0; policy, p, out, width, frontier_token ignored), or as
- * dt_expand_prune_select does (select = 1). It must follow dt_expand_rows with the same F on the same
- * stream, with no other call of this handle between them. */
-int dt_expand_rows(dt_handle* h, const void* logits, int64_t ld, int32_t F, cudaStream_t s);
-int dt_expand_finish(dt_handle* h, int32_t F, int32_t select, int32_t policy, const dt_prune_params* p,
-                     const dt_prune_out* out, const int32_t* width, int32_t width_len, int32_t* frontier_token,
-                     cudaStream_t s);
-
-/* a1 + a2, then a3/a4, then the next frontier, in two launches: exactly
+/* a1 + a2, then a3/a4, then the next frontier, as one call: exactly
  *   dt_expand_layer(h, logits, ld, F, s);
- *   policy DT_POLICY_CAST_WIDTH_DEPTH: dt_cast_prune(h, policy, p, out, s), then
- *     dt_select_frontier(h, out->width, 1, out->stop, frontier_token, s);
+ *   policy DT_POLICY_CAST_WIDTH_DEPTH: dt_cast_prune_select(h, p, out, frontier_token, s)
+ *     (after the last layer, D_max: dt_cast_prune(h, policy, p, out, s) alone);
  *   policy DT_POLICY_GRAFT_CHECKPOINT: dt_cast_prune(h, policy, p, out, s), then
  *     dt_select_frontier(h, width, width_len, out->stop, frontier_token, s);
  *   policy DT_POLICY_NONE (EAGLE-2, no pruning): dt_select_frontier(h, width, width_len, NULL,
  *     frontier_token, s);
- * except that no frontier is selected once the tree has D_max layers. width: device [width_len]
- * (1 or B) or NULL for W; p and out may be NULL for DT_POLICY_NONE. The expansion's rows are read
- * by one streaming kernel; a second kernel merges them, writes the children, orders the layer and
- * applies the policy and the selection (CAST in the same CTA when B <= 32 and B * W * K <= 4096,
- * otherwise the pruning kernel follows). */
+ * no frontier is selected once the tree has D_max layers. width: device [width_len] (1 or B) or
+ * NULL for W; p and out may be NULL for DT_POLICY_NONE. */
 int dt_expand_prune_select(dt_handle* h, const void* logits, int64_t ld, int32_t F, int32_t policy,
                            const dt_prune_params* p, const dt_prune_out* out, const int32_t* width,
                            int32_t width_len, int32_t* frontier_token, cudaStream_t s);
