@@ -26,6 +26,8 @@ What it restates, and from where (page titles, sections):
   cost lookup table with the grid quantiser select(c), width pruning by
   marginal utility against C1, depth pruning with the FIFO ratio buffer
   against C2, verify-count selection against C3.
+* EAGLE-2, §"一段更贴近实现的流程" (after verification): ``kv`` commits the root's and the accepted
+  positions' temporary KV rows to the cache, in path order, and discards the rest.
 * Graft ("Draft Less, Retrieve More"), the three-step method description:
   confidence checkpoints c_d = exp(max_j S_{d,j}) against tau_d, retrieval
   x_u = M[x_{F(u)}, r_u] over a template, hybrid flatten to K_max tokens,
