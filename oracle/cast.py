@@ -31,6 +31,11 @@ Readings taken where the page is silent or garbled (the body of Algorithm 1 is n
   items directly.
 * Width cap = the per-node K (10 for the CAST workload); n_i is batch-wide.
   Verify cap m_cap = 60, minimum 1, batch-wide m.
+* Per-request rule (the page's stated limitation, §局限与展望: padded equal-length batches, no
+  continuous batching): every request applies the same rules to its own utilities alone (a
+  "batch" of one: u_k = sum_{s<=k} v^(b)(s)), with its own context sum, its own FIFO and its own
+  stop, and its own verify count m_b; the cost tables are the running batch's, as in the batch-wide
+  rule.
 * Depth: layer 1 always exists; after layer i (i >= 2) is pruned the ratio
   phi_{i-1} is pushed (oldest dropped beyond R), then the C2 test decides
   whether layer i+1 is built; layer D_max is the last.
@@ -46,7 +51,7 @@ def select_row(c, L, M_rows):
     return min(int(math.floor(c / L)), M_rows - 1)
 
 
-def selection_rule(item_sums, cost, threshold, cap, gaps=None, kind="C"):
+def selection_rule(item_sums, cost, threshold, cap, gaps=None, kind="C", b=None):
     """Marginal-utility selection over k = 1..cap.
 
     ``item_sums[s]`` is the batch-averaged utility of the s-th item (0-based),
@@ -61,7 +66,7 @@ def selection_rule(item_sums, cost, threshold, cap, gaps=None, kind="C"):
         du = float(np.sum(item_sums[k0:k]))
         marg = du / (cost[k] - cost[k0])
         if gaps is not None:
-            gaps.add(kind, marg - threshold, marg)
+            gaps.add(kind, marg - threshold, marg, b)
         if marg >= threshold:
             k0 = k
     return k0
@@ -90,25 +95,29 @@ class CastState:
         self.u_prev = None
 
 
-def width_depth(tree, d, state, p, gaps=None):
+def width_depth(tree, d, state, p, gaps=None, reqs=None):
     """Width n_d and the grow decision after layer d (CAST key designs 2 and 3).
 
     ``p`` holds S_T, S_D (arrays [M_rows][N_cols]), L, n0, C1, C2, R,
-    width_cap, D_max. Returns (n_d, grow).
+    width_cap, D_max. ``reqs``: the requests whose utilities are averaged (all of the batch by
+    default; one request for the per-request rule, with that request's own state). Returns
+    (n_d, grow).
     """
-    B = tree.B
-    per_req = [sorted_linear_values(tree, b, tree.layer_ids(b, d)) for b in range(B)]
+    reqs = list(range(tree.B)) if reqs is None else list(reqs)
+    B = len(reqs)
+    per_req = [sorted_linear_values(tree, b, tree.layer_ids(b, d)) for b in reqs]
     maxcand = max(v.size for v in per_req)
     if maxcand == 0:
         return 0, False
     cap = min(p["width_cap"], maxcand)
     items = batch_item_sums(per_req, B, cap)
+    gb = reqs[0] if len(reqs) == 1 and reqs != list(range(tree.B)) else None
     u = np.concatenate([[0.0], np.cumsum(items)])          # u[k], k = 0..cap
     row = select_row(p["n0"] + state.ctx_sum, p["L"], p["S_T"].shape[0])
     cost = np.zeros(cap + 1)
     for k in range(1, cap + 1):
         cost[k] = p["S_D"][row][k - 1] / p["S_T"][row][0]
-    n = selection_rule(items, cost, p["C1"], cap, gaps, "C1")
+    n = selection_rule(items, cost, p["C1"], cap, gaps, "C1", gb)
     if state.u_prev is not None:
         state.fifo.append(u[n] / state.u_prev)
         while len(state.fifo) > p["R"]:
@@ -118,17 +127,20 @@ def width_depth(tree, d, state, p, gaps=None):
     grow = False
     if d < p["D_max"]:
         if gaps is not None:
-            gaps.add("C2", key - p["C2"], key)
+            gaps.add("C2", key - p["C2"], key, gb)
         grow = key >= p["C2"]
     state.u_prev = u[n]
     state.ctx_sum += n
     return n, grow
 
 
-def verify_count(tree, p, gaps=None):
-    """Batch-wide verify budget m (CAST key design 4)."""
-    B = tree.B
-    per_req = [sorted_linear_values(tree, b, tree.nodes(b)) for b in range(B)]
+def verify_count(tree, p, gaps=None, reqs=None):
+    """Verify budget m (CAST key design 4): batch-wide, or for the requests ``reqs`` alone (the
+    per-request rule passes one request)."""
+    reqs = list(range(tree.B)) if reqs is None else list(reqs)
+    B = len(reqs)
+    per_req = [sorted_linear_values(tree, b, tree.nodes(b)) for b in reqs]
+    gb = reqs[0] if len(reqs) == 1 and reqs != list(range(tree.B)) else None
     maxn = max(v.size for v in per_req)
     if maxn == 0:
         return 0
@@ -138,7 +150,7 @@ def verify_count(tree, p, gaps=None):
     cost = np.zeros(cap + 1)
     for k in range(1, cap + 1):
         cost[k] = p["S_T"][row][k - 1] / p["S_T"][row][0]
-    return selection_rule(items, cost, p["C3"], cap, gaps, "C3")
+    return selection_rule(items, cost, p["C3"], cap, gaps, "C3", gb)
 
 
 def linear_table(M_rows, N_cols, L, a, b_coef, e):

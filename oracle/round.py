@@ -33,6 +33,8 @@ def run_round(cfg, roots, draft_row, target_row, rnd=0, M=None, pos_offset=None,
     stage = [-1] * B
     m_req = [cfg["m_cap"]] * B
     widths, cast_state = [], cast_mod.CastState()
+    per_request = policy == "cast" and bool(cfg["cast"].get("per_request", False))
+    cast_states = [cast_mod.CastState() for _ in range(B)]
     frontiers = []
     p_graft = None
     if policy == "graft":
@@ -45,7 +47,17 @@ def run_round(cfg, roots, draft_row, target_row, rnd=0, M=None, pos_offset=None,
 
     d = expand()
     while True:
-        if policy == "cast":
+        if policy == "cast" and per_request:  # every running request decides for itself
+            width = [0] * B
+            for b in range(B):
+                if stop[b]:
+                    continue
+                n, grow = cast_mod.width_depth(tree, d, cast_states[b], cfg["cast"], gaps, reqs=[b])
+                width[b] = n
+                if not grow:
+                    stop[b] = True
+            widths.append(list(width))
+        elif policy == "cast":
             n, grow = cast_mod.width_depth(tree, d, cast_state, cfg["cast"], gaps)
             widths.append(n)
             width = n
@@ -63,7 +75,10 @@ def run_round(cfg, roots, draft_row, target_row, rnd=0, M=None, pos_offset=None,
         frontiers.append(tree.select_frontier(width, stop, gaps))
         d = expand()
 
-    if policy == "cast":
+    if policy == "cast" and per_request:
+        m_sel = [cast_mod.verify_count(tree, cfg["cast"], gaps, reqs=[b]) for b in range(B)]
+        m = list(m_sel)
+    elif policy == "cast":
         m = cast_mod.verify_count(tree, cfg["cast"], gaps)
         m_sel = [m] * B
     elif policy == "graft":

@@ -85,7 +85,8 @@ def oracle_cfg(w):
         cc = w["cast"]
         S_T, S_D = cast_tables(w["B"], cc["M_rows"], cc["N_cols"], cc["L"])
         c["cast"] = dict(S_T=S_T, S_D=S_D, L=cc["L"], n0=0, C1=cc["C1"], C2=cc["C2"], C3=cc["C3"], R=cc["R"],
-                         width_cap=cc["width_cap"], m_cap=cc["m_cap"], D_max=g["D_max"])
+                         width_cap=cc["width_cap"], m_cap=cc["m_cap"], D_max=g["D_max"],
+                         per_request=bool(cc.get("per_request", False)))
     if w["policy"] == "graft":
         c["graft"] = dict(w["graft"], template=chain_template(w["k"], w["D"]))
     return c
@@ -127,7 +128,8 @@ def oracle_round(w, rnd, roots=None, M=None, max_attempts=16):
             ref["salts"] = salts
             return ref, attempts, redraws
         bs = {it[3] for it in near}
-        if None in bs or w["policy"] == "cast":
+        batch_coupled = w["policy"] == "cast" and not w["cast"].get("per_request", False)
+        if None in bs or batch_coupled:
             attempts += 1
             redraws += B
         else:
