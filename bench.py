@@ -268,7 +268,7 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
         widths = []
         record(r, r, widths)
         torch.cuda.synchronize()
-        rec_out.append((run.accept_len.clone(), run.bonus.clone(), run.m_dev.clone()))
+        rec_out.append((run.accept_len.clone(), run.bonus.clone(), run.m_dev.clone(), run.accept_path.clone()))
         rows_verify.append(int((run.meta.tokens >= 0).sum()))
         rows_expand.append([int(x.sum()) for x in widths])
         npos_rec.append(run.meta.n_pos.cpu().numpy().copy())
@@ -382,6 +382,9 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
     if graft:
         out["graft_warmup_rounds"] = warm
 
+    if with_e2e:
+        out["kv_commit"] = kv_commit_run(torch, run, rec_out, steps, R)
+
     # ---- end to end through the public API with host buffers ----
     if with_e2e and args.e2e_steps > 0:
         out["e2e"] = e2e_run(torch, run, w, rec_draft, rec_target, roots, rec_out, act_rec, npos_rec, esz, M,
@@ -391,6 +394,43 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
     run.h.close()
     torch.cuda.empty_cache()
     return out
+
+
+KV_ROW_BYTES = 32 * 2 * 8 * 128 * 2  # one token's keys and values: 32 layers, 8 KV heads of 128, bf16
+
+
+def kv_commit_run(torch, run, rec_out, steps, R):
+    """Accepted-path KV compaction (dt_commit_kv) after each recorded round's verify, with KV rows of
+    KV_ROW_BYTES (an 8B-parameter model's cache row): the calls of `steps` rounds back to back, timed
+    with events; bytes moved = 2 x rows committed x row size."""
+    from dynamic_draft_tree_gb300 import dt_commit_kv, dt_get_status
+
+    B, P = run.meta.tokens.shape
+    Dp = run.accept_path.shape[1]
+    L = steps * Dp
+    tmp = torch.empty((B, P, KV_ROW_BYTES), dtype=torch.uint8, device="cuda")
+    cache = torch.empty((B, L, KV_ROW_BYTES), dtype=torch.uint8, device="cuda")
+    cache_len = torch.zeros((B,), dtype=torch.int32, device="cuda")
+    rows = sum(int((rec_out[s % R][0] + 1).sum()) for s in range(steps))
+    for s in range(3):  # warm-up, then start again from an empty cache
+        dt_commit_kv(run.h, tmp, cache, cache_len, rec_out[s % R][0], rec_out[s % R][3])
+    cache_len.zero_()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(steps):
+        dt_commit_kv(run.h, tmp, cache, cache_len, rec_out[s % R][0], rec_out[s % R][3])
+    e1.record()
+    torch.cuda.synchronize()
+    assert dt_get_status(run.h) == 0
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    nbytes = 2.0 * rows / steps * KV_ROW_BYTES
+    peak, _ = measured_peaks()
+    del tmp, cache
+    return {"row_bytes": KV_ROW_BYTES, "rows_per_call": rows / steps, "avg_us": us,
+            "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak,
+            "note": "calls back to back (two launches each), not in the round's graph"}
 
 
 def e2e_run(torch, run, w, rec_draft, rec_target, roots, rec_out, act_rec, npos_rec, esz, M, steps, world):
@@ -500,6 +540,7 @@ def run_ours(args):
         "roofline": head["roofline"], "kernels": head["kernels"], "replay": head["replay"],
         "e2e": head.get("e2e"), "gpu_launches": head["gpu_launches"],
         "replay_consistent": head["replay_consistent"], "rows_per_round": head["rows_per_round"],
+        "kv_commit": head.get("kv_commit"),
         "clocks": head["clocks"], "per_config": per_config,
     }
     return line

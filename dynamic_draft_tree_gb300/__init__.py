@@ -13,7 +13,7 @@ from ._lib import (lib, check, DtError, DtConfig, DtTreeView, DtPruneParams, DtP
                    DtTreeMeta, EXPORTS, DT_OK, DT_ERR_ARG, DT_ERR_CUDA, DT_ERR_DEVICE,
                    DT_ERR_DEVICE_TIMEOUT, DT_BF16, DT_F32, DT_GREEDY, DT_SAMPLE,
                    DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT, DT_POLICY_NONE,
-                   DT_DEV_BAD_LOGITS, DT_DEV_BAD_TOKEN, DT_DEV_BAD_TREE, DT_DEV_TIMEOUT, DT_DEV_INTERNAL,
+                   DT_DEV_BAD_LOGITS, DT_DEV_BAD_TOKEN, DT_DEV_BAD_TREE, DT_DEV_TIMEOUT, DT_DEV_INTERNAL, DT_DEV_KV_FULL,
                    DT_FLAG_TEST_TIMEOUT, LIB_PATH)
 
 
@@ -183,6 +183,28 @@ def dt_adj_update(h, M, meta, top8, stream=None):
     check(lib.dt_adj_update(h.h, _ptr(M), ctypes.byref(meta.c), _ptr(top8), _stream(stream)))
 
 
+def dt_commit_kv(h, tmp_kv, cache, cache_len, accept_len, accept_path, stream=None):
+    """Append the root's and the accepted positions' KV rows to each request's cache.
+
+    tmp_kv [B][P][...] and cache [B][L_max][...] are device tensors whose trailing dimensions form
+    one row (contiguous, a multiple of 16 bytes); cache_len [B] int32 is updated in place."""
+    if tmp_kv.dim() < 3 or cache.dim() < 3:
+        raise ValueError("tmp_kv and cache need [B][positions][row...] shapes")
+    esz = tmp_kv.element_size()
+    row_bytes = tmp_kv[0, 0].numel() * esz
+    if cache[0, 0].numel() * cache.element_size() != row_bytes:
+        raise ValueError("tmp_kv and cache rows differ in size")
+    if not tmp_kv[0, 0].is_contiguous() or not cache[0, 0].is_contiguous():
+        raise ValueError("KV rows must be contiguous")
+    for t in (tmp_kv, cache):
+        if not t.is_cuda:
+            raise ValueError("device tensor required")
+    check(lib.dt_commit_kv(h.h, tmp_kv.data_ptr(), tmp_kv.stride(1) * esz, tmp_kv.stride(0) * esz, tmp_kv.shape[1],
+                           cache.data_ptr(), cache.stride(1) * cache.element_size(),
+                           cache.stride(0) * cache.element_size(), cache.shape[1], row_bytes, _ptr(cache_len),
+                           _ptr(accept_len), _ptr(accept_path), accept_path.shape[-1], _stream(stream)))
+
+
 def dt_row_topk_static(logits, K, logp, ids, V=None, status=None, stream=None):
     """Row log-softmax top-K with no handle and no allocation: logits [rows][ld] (bf16 or fp32),
     logp [rows][K] fp32 and ids [rows][K] int32 caller-owned; status an int32 device word or None."""
@@ -224,7 +246,7 @@ class Meta:
 
 
 def make_prune_params(S_T=None, S_D=None, L=512.0, n0=0, C1=0.0, C2=0.0, C3=0.0, R=3, width_cap=1, m_cap=1,
-                      D_max=1, ckpt_layers=(), tau=(), k_draft=(), K_total=0):
+                      D_max=1, ckpt_layers=(), tau=(), k_draft=(), K_total=0, per_request=False):
     """dt_prune_params from device tables (float64 tensors [M_rows][N_cols]) and scalars."""
     p = DtPruneParams()
     p.S_T = _ptr(S_T)
@@ -237,6 +259,7 @@ def make_prune_params(S_T=None, S_D=None, L=512.0, n0=0, C1=0.0, C2=0.0, C3=0.0,
     for i, (c, t, k) in enumerate(zip(ckpt_layers, tau, k_draft)):
         p.ckpt_layer[i], p.tau[i], p.k_draft[i] = c, t, k
     p.K_total = K_total
+    p.per_request = 1 if per_request else 0
     return p
 
 

@@ -15,13 +15,15 @@ DT_BF16, DT_F32 = 0, 1
 DT_GREEDY, DT_SAMPLE = 0, 1
 DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT, DT_POLICY_NONE = 0, 1, 2, 3
 DT_DEV_BAD_LOGITS, DT_DEV_BAD_TOKEN, DT_DEV_BAD_TREE, DT_DEV_TIMEOUT, DT_DEV_INTERNAL = 1, 2, 4, 8, 16
+DT_DEV_KV_FULL = 32
 DT_FLAG_TEST_TIMEOUT = 1
 
 EXPORTS = ["dt_last_error_string", "dt_create", "dt_destroy", "dt_get_tree", "dt_get_status",
            "dt_clear_status", "dt_tree_reset", "dt_select_frontier", "dt_expand_layer", "dt_cast_prune",
            "dt_rerank", "dt_graft_retrieve", "dt_build_tree_meta", "dt_verify", "dt_adj_update",
            "dt_row_topk_static", "dt_cast_prune_select",
-           "dt_cast_verify_rerank", "dt_expand_prune_select", "dt_verify_rows", "dt_verify_accept"]
+           "dt_cast_verify_rerank", "dt_expand_prune_select", "dt_verify_rows", "dt_verify_accept",
+           "dt_commit_kv"]
 
 c_i32p = ctypes.c_void_p
 vp = ctypes.c_void_p
@@ -48,7 +50,7 @@ class DtPruneParams(ctypes.Structure):
                 ("width_cap", ctypes.c_int32), ("m_cap", ctypes.c_int32), ("D_max", ctypes.c_int32),
                 ("n_ckpt", ctypes.c_int32), ("ckpt_layer", ctypes.c_int32 * 4),
                 ("tau", ctypes.c_double * 4), ("k_draft", ctypes.c_int32 * 4),
-                ("K_total", ctypes.c_int32)]
+                ("K_total", ctypes.c_int32), ("per_request", ctypes.c_int32)]
 
 
 class DtPruneOut(ctypes.Structure):
@@ -97,6 +99,8 @@ def _load():
         "dt_verify_rows": ([vp, ctypes.POINTER(DtTreeMeta), vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp], I),
         "dt_verify_accept": ([vp, ctypes.POINTER(DtTreeMeta), vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64,
                               ctypes.c_uint64, vp, vp, vp, vp, vp], I),
+        "dt_commit_kv": ([vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, vp, ctypes.c_int64, ctypes.c_int64,
+                          ctypes.c_int32, ctypes.c_int64, vp, vp, vp, ctypes.c_int32, vp], I),
         "dt_cast_verify_rerank": ([vp, ctypes.POINTER(DtPruneParams), ctypes.POINTER(DtPruneOut), vp, vp], I),
         "dt_row_topk_static": ([vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                 vp, vp, vp, vp], I),

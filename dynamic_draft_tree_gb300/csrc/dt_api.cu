@@ -112,6 +112,7 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   const size_t o_scnt = cv.take<int32_t>(c.B_max);
   const size_t o_sids = cv.take<int32_t>((size_t)c.B_max * c.P_max);
   const size_t o_cast = cv.take<dt::CastState>(1);
+  const size_t o_castr = cv.take<dt::CastState>(c.B_max);
   const size_t o_walk = cv.take<dt::WalkState>(c.B_max);
   const size_t o_bkey = cv.take<unsigned long long>(c.B_max);
   const size_t o_bcnt = cv.take<int32_t>(c.B_max);
@@ -155,6 +156,7 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   w.sorted_cnt = reinterpret_cast<int32_t*>(bp + o_scnt);
   w.sorted_ids = reinterpret_cast<int32_t*>(bp + o_sids);
   w.cast = reinterpret_cast<dt::CastState*>(bp + o_cast);
+  w.cast_req = reinterpret_cast<dt::CastState*>(bp + o_castr);
   w.walk = reinterpret_cast<dt::WalkState*>(bp + o_walk);
   w.bonus_key = reinterpret_cast<unsigned long long*>(bp + o_bkey);
   w.bonus_counter = reinterpret_cast<int32_t*>(bp + o_bcnt);
@@ -461,6 +463,30 @@ int dt_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta, const int3
   if (!aligned(M, 16) || !aligned(top8, 16)) return fail(DT_ERR_ARG, "M and top8 must be 16-byte aligned");
   cudaError_t e = dt::launch_adj_update(h, M, meta, top8, s);
   if (e != cudaSuccess) return cuda_fail(e, "dt_adj_update");
+  return DT_OK;
+}
+
+int dt_commit_kv(dt_handle* h, const void* tmp_kv, int64_t tmp_pos_stride, int64_t tmp_req_stride, int32_t P,
+                 void* cache, int64_t cache_pos_stride, int64_t cache_req_stride, int32_t L_max, int64_t row_bytes,
+                 int32_t* cache_len, const int32_t* accept_len, const int32_t* accept_path, int32_t D_path,
+                 cudaStream_t s) {
+  if (!h || !tmp_kv || !cache || !cache_len || !accept_len || !accept_path)
+    return fail(DT_ERR_ARG, "dt_commit_kv: null argument");
+  if (h->B < 1) return fail(DT_ERR_ARG, "dt_commit_kv: no tree (call dt_tree_reset)");
+  if (P < 1 || L_max < 1 || D_path < 1 || D_path > 64) return fail(DT_ERR_ARG, "P, L_max >= 1 and D_path in [1, 64]");
+  if (row_bytes < 16) return fail(DT_ERR_ARG, "row_bytes must be >= 16");
+  if (!aligned(tmp_kv, 16) || !aligned(cache, 16) || tmp_pos_stride % 16 || tmp_req_stride % 16 ||
+      cache_pos_stride % 16 || cache_req_stride % 16 || row_bytes % 16)
+    return fail(DT_ERR_ARG, "dt_commit_kv: pointers, strides and row_bytes must be multiples of 16 bytes");
+  if (tmp_pos_stride < row_bytes || cache_pos_stride < row_bytes || tmp_req_stride < tmp_pos_stride * P ||
+      cache_req_stride < cache_pos_stride * L_max)
+    return fail(DT_ERR_ARG, "dt_commit_kv: strides smaller than the rows they hold");
+  if (!aligned(cache_len, 4) || !aligned(accept_len, 4) || !aligned(accept_path, 4))
+    return fail(DT_ERR_ARG, "dt_commit_kv: int32 arrays must be 4-byte aligned");
+  cudaError_t e = dt::launch_commit_kv(h, tmp_kv, tmp_pos_stride, tmp_req_stride, P, cache, cache_pos_stride,
+                                       cache_req_stride, L_max, row_bytes, cache_len, accept_len, accept_path,
+                                       D_path, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dt_commit_kv");
   return DT_OK;
 }
 

@@ -83,6 +83,7 @@ struct Workspace {
   int32_t* sorted_cnt;   // [B_max]
   int32_t* sorted_ids;   // [B_max][P_max] ids of each request's top nodes in rank order
   CastState* cast;
+  CastState* cast_req;   // [B_max] per-request CAST state (per_request rule)
   WalkState* walk;
   unsigned long long* bonus_key;  // [B_max]
   int32_t* bonus_counter;         // [B_max]
@@ -162,6 +163,10 @@ cudaError_t launch_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta
 int row_pass_grid(const dt_handle* h);
 int row_pass_smax(int K);
 
+cudaError_t launch_commit_kv(dt_handle* h, const void* tmp_kv, int64_t tmp_pos_stride, int64_t tmp_req_stride, int P,
+                             void* cache, int64_t cache_pos_stride, int64_t cache_req_stride, int L_max,
+                             int64_t row_bytes, int32_t* cache_len, const int32_t* accept_len,
+                             const int32_t* accept_path, int D_path, cudaStream_t s);
 cudaError_t launch_row_topk_static(const void* logits, int64_t ld, int rows, int V, int K, int dtype, float* logp,
                                    int32_t* ids, int32_t* status, cudaStream_t s);
 

@@ -172,6 +172,169 @@ __global__ void __launch_bounds__(kPruneThreads) cast_verify_kernel(PruneArgs a)
   }
 }
 
+// CAST width + depth, per-request rule: one warp per request applies the batch rule to the request
+// alone (a batch of one: its items are its own sorted path values, the batch mean of one value being
+// that value), with its own state (context sum, FIFO, last utility) and its own stop; then, with
+// select, its next frontier. A request stopped at an earlier layer stays stopped.
+constexpr int kReqWarps = 8;
+__global__ void __launch_bounds__(32 * kReqWarps) cast_width_depth_req_kernel(PruneArgs a) {
+  pdl_begin();
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kReqWarps + (threadIdx.x >> 5);
+  if (b >= a.B) return;
+  const Workspace& ws = a.ws;
+  CastState* cst = ws.cast_req + b;
+  int f_id = -1, f_tok = -1, f_avail = 0;
+  float f_val = -INFINITY;
+  if (a.select) f_avail = frontier_candidates(ws, b, a.N, a.W, a.LW, a.D, a.d, f_id, f_tok, f_val);
+  const bool stopped = a.d > 1 && a.out.stop[b] != 0;
+  int n = 0;
+  bool grow = false;
+  if (!stopped) {
+    const int wcap = min(a.p.width_cap, a.LW);
+    const int64_t lb = (int64_t)b * (a.D + 1) + a.d;
+    const int cnt = ws.layer_count[lb];
+    const float v = lane < a.LW ? ws.layer_val[lb * a.LW + lane] : 0.0f;  // read with the count
+    const int row = table_row((double)(a.p.n0 + cst->ctx_sum), a.p.L, a.p.M_rows);
+    const int cap = min(a.p.width_cap, cnt);
+    const int k = lane + 1;  // lane k - 1 holds u_k and c_k
+    const double item = (lane < wcap && lane < cnt) ? 0.0 + (double)expf(v) : 0.0;
+    double ck = 0.0;
+    if (k <= wcap) ck = a.p.S_D[(int64_t)row * a.p.N_cols + (k - 1)] / a.p.S_T[(int64_t)row * a.p.N_cols];
+    double x = k <= cap ? item : 0.0;  // u_k: inclusive prefix (the batch rule's scan)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    x += 0.0;
+    const uint64_t cimg = d2ord(ck), qimg = d2ord(x - a.p.C1 * ck);
+    if (cap > 0) {
+      int k0 = 1;
+      uint64_t c0 = __shfl_sync(0xFFFFFFFFu, cimg, 0), q0 = __shfl_sync(0xFFFFFFFFu, qimg, 0);
+      for (int kk = 2; kk <= cap; ++kk) {
+        const uint64_t c = __shfl_sync(0xFFFFFFFFu, cimg, kk - 1), q = __shfl_sync(0xFFFFFFFFu, qimg, kk - 1);
+        if (c <= c0 || q >= q0) {
+          k0 = kk;
+          c0 = c;
+          q0 = q;
+        }
+      }
+      n = k0;
+    }
+    const double un = __shfl_sync(0xFFFFFFFFu, x, max(n, 1) - 1);
+    const double cn = __shfl_sync(0xFFFFFFFFu, ck, max(n, 1) - 1);
+    int g = 0;
+    if (lane == 0 && cap > 0) {
+      CastState cs = *cst;
+      const int len = cs.fifo_len;
+      const double up = cs.u_prev;
+      const bool app = up >= 0.0;  // this layer appends a ratio
+      double kept = 0.0;
+      for (int j = app && len >= a.p.R ? 1 : 0; j < len; ++j) kept += cs.fifo[j];
+      const int nlen = app ? (len < a.p.R ? len + 1 : len) : len;
+      bool gg;
+      if (nlen <= 0) {
+        gg = false;  // the mean of an empty FIFO is NaN
+      } else if (app && up > 0.0) {
+        gg = (kept * up + un) * un >= a.p.C2 * cn * (double)nlen * up;
+      } else if (app) {  // u_prev = 0: the ratio is not finite; the quotient form as written
+        const double alpha = (kept + un / up) / (double)nlen;
+        gg = alpha * un >= a.p.C2 * cn;
+      } else {
+        gg = kept * un >= a.p.C2 * cn * (double)nlen;
+      }
+      g = ((a.d < a.p.D_max) && gg) ? 1 : 0;
+      if (app) {
+        const double ratio = un / up;
+        int l2 = len;
+        if (l2 < a.p.R) {
+          cs.fifo[l2++] = ratio;
+        } else {
+          for (int j = 1; j < l2; ++j) cs.fifo[j - 1] = cs.fifo[j];
+          cs.fifo[l2 - 1] = ratio;
+        }
+        cs.fifo_len = l2;
+      }
+      cs.u_prev = un;
+      cs.u_layer = un;
+      cs.ctx_sum += n;
+      *cst = cs;
+    }
+    grow = __shfl_sync(0xFFFFFFFFu, g, 0) != 0;
+  }
+  if (lane == 0) {
+    a.out.width[b] = n;
+    a.out.stop[b] = grow ? 0 : 1;
+  }
+  if (a.select)  // the next layer's frontier, as dt_select_frontier(width[b], stop[b]) would choose it
+    select_frontier_write(ws, b, a.W, max(0, min(min(grow ? n : 0, a.W), f_avail)), f_id, f_tok, f_val, a.ftok);
+}
+
+// CAST verify count, per-request rule: one warp per request runs the selection over the request's own
+// sorted path values (a batch of one), then, with sel, writes its top-m_b ids in ascending order.
+__global__ void __launch_bounds__(32) cast_verify_req_kernel(PruneArgs a) {
+  pdl_begin();
+  __shared__ uint64_t cimg[kMaxP + 2], qimg[kMaxP + 2];
+  const int b = blockIdx.x, lane = threadIdx.x;
+  const Workspace& ws = a.ws;
+  const int mcap = a.p.m_cap;
+  const double* lin = ws.sorted_lin + (int64_t)b * mcap;
+  const int cnt = ws.sorted_cnt[b];
+  const int cap = min(mcap, cnt);
+  const int row = table_row((double)a.p.n0, a.p.L, a.p.M_rows);
+  const double t0 = a.p.S_T[(int64_t)row * a.p.N_cols];
+  double carry = 0.0;
+  for (int c0 = 0; c0 < cap; c0 += 32) {  // u_k, chunk by chunk (the batch rule's scan)
+    const int k = c0 + lane + 1;
+    double x = k <= cap ? (0.0 + (0.0 + lin[k - 1])) : 0.0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    x += carry;
+    if (k <= cap) {
+      const double ck = a.p.S_T[(int64_t)row * a.p.N_cols + (k - 1)] / t0;
+      cimg[k] = d2ord(ck);
+      qimg[k] = d2ord(x - a.p.C3 * ck);
+    }
+    carry = __shfl_sync(0xFFFFFFFFu, x, 31);
+  }
+  __syncwarp();
+  int m = 0;
+  if (lane == 0 && cap > 0) {
+    int k0 = 1;
+    uint64_t c0 = cimg[1], q0 = qimg[1];
+    for (int k = 2; k <= cap; ++k) {
+      const uint64_t ck = cimg[k], qk = qimg[k];
+      if (ck <= c0 || qk >= q0) {
+        k0 = k;
+        c0 = ck;
+        q0 = qk;
+      }
+    }
+    m = k0;
+  }
+  m = __shfl_sync(0xFFFFFFFFu, m, 0);
+  if (lane == 0) a.out.m[b] = m;
+  if (a.sel) {  // the rerank, as dt_rerank(m[b]) would write it: the request's top-m ids, ascending
+    const int mb = max(0, min(m, cnt));
+    const int32_t* ids = ws.sorted_ids + (int64_t)b * mcap;
+    int32_t* out = a.sel + (int64_t)b * mcap;
+    for (int i = lane; i < mcap; i += 32) {
+      if (i < mb) {
+        const int32_t id = ids[i];
+        int r = 0;
+        for (int j = 0; j < mb; ++j) r += ids[j] < id;
+        out[r] = id;
+      } else {
+        out[i] = -1;
+      }
+    }
+  }
+}
+
 // Graft checkpoint after layer d: one thread per request.
 __global__ void graft_checkpoint_kernel(PruneArgs a) {
   pdl_begin();
@@ -226,13 +389,19 @@ cudaError_t launch_cast_prune(dt_handle* h, int policy, const dt_prune_params* p
   a.ftok = nullptr;
   a.sel = nullptr;
   if (policy == DT_POLICY_CAST_WIDTH_DEPTH) {
-    launch_k(cast_width_depth_kernel, dim3(1), dim3(prune_threads(h->B)), 0, s, a);
+    if (p->per_request)
+      launch_k(cast_width_depth_req_kernel, dim3((h->B + kReqWarps - 1) / kReqWarps), dim3(32 * kReqWarps), 0, s, a);
+    else
+      launch_k(cast_width_depth_kernel, dim3(1), dim3(prune_threads(h->B)), 0, s, a);
     return cudaGetLastError();
   }
   if (policy == DT_POLICY_CAST_VERIFY) {
     cudaError_t e = launch_sort(h, 1, nullptr, 1, p->m_cap, nullptr, s);
     if (e != cudaSuccess) return e;
-    launch_k(cast_verify_kernel, dim3(1), dim3(prune_threads(h->B)), 0, s, a);
+    if (p->per_request)
+      launch_k(cast_verify_req_kernel, dim3(h->B), dim3(32), 0, s, a);
+    else
+      launch_k(cast_verify_kernel, dim3(1), dim3(prune_threads(h->B)), 0, s, a);
     return cudaGetLastError();
   }
   launch_k(graft_checkpoint_kernel, dim3((h->B + 127) / 128), dim3(128), 0, s, a);
@@ -255,7 +424,10 @@ cudaError_t launch_cast_prune_select(dt_handle* h, const dt_prune_params* p, con
   a.select = 1;
   a.ftok = frontier_token;
   a.sel = nullptr;
-  launch_k(cast_width_depth_kernel, dim3(1), dim3(prune_threads(h->B)), 0, s, a);
+  if (p->per_request)
+    launch_k(cast_width_depth_req_kernel, dim3((h->B + kReqWarps - 1) / kReqWarps), dim3(32 * kReqWarps), 0, s, a);
+  else
+    launch_k(cast_width_depth_kernel, dim3(1), dim3(prune_threads(h->B)), 0, s, a);
   return cudaGetLastError();
 }
 
@@ -277,7 +449,10 @@ cudaError_t launch_cast_verify_rerank(dt_handle* h, const dt_prune_params* p, co
   a.select = 0;
   a.ftok = nullptr;
   a.sel = selected;
-  launch_k(cast_verify_kernel, dim3(1), dim3(prune_threads(h->B)), 0, s, a);
+  if (p->per_request)
+    launch_k(cast_verify_req_kernel, dim3(h->B), dim3(32), 0, s, a);
+  else
+    launch_k(cast_verify_kernel, dim3(1), dim3(prune_threads(h->B)), 0, s, a);
   return cudaGetLastError();
 }
 

@@ -63,6 +63,15 @@ __global__ void tree_reset_kernel(Workspace ws, const int32_t* __restrict__ root
   }
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < B; i += (int64_t)gridDim.x * blockDim.x)
     ws.frontier_count[i] = 1;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < B; i += (int64_t)gridDim.x * blockDim.x) {
+    CastState* cs = ws.cast_req + i;  // per-request rule: FIFO = {1}, no ratio yet, no context yet
+    for (int j = 0; j < kMaxFifo; ++j) cs->fifo[j] = 0.0;
+    cs->fifo[0] = 1.0;
+    cs->fifo_len = 1;
+    cs->u_prev = -1.0;
+    cs->ctx_sum = 0;
+    cs->u_layer = 0.0;
+  }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     CastState* cs = ws.cast;
     for (int j = 0; j < kMaxFifo; ++j) cs->fifo[j] = 0.0;

@@ -39,10 +39,11 @@ class RoundRunner:
         self.h = Handle(B, V, K, k, D, P, dtype, flags)
         i32 = dict(dtype=torch.int32, device=device)
         self.frontier_token = torch.full((B, k), -1, **i32)
-        self.width = torch.full((1,), k, **i32)
+        per_req = policy == "cast" and bool((cast or {}).get("per_request", False))
+        self.width = torch.full((B if per_req else 1,), k, **i32)
         self.stop = torch.zeros((B,), **i32)
         self.stage = torch.full((B,), -1, **i32)
-        self.m_dev = torch.full((B if policy == "graft" else 1,), m, **i32)
+        self.m_dev = torch.full((B if policy == "graft" or per_req else 1,), m, **i32)
         self.m_cap = m
         self.selected = torch.empty((B, m), **i32)
         self.meta = Meta(B, P, D_path, device)
@@ -74,7 +75,7 @@ class RoundRunner:
         c = self.cast
         self.params = make_prune_params(S_T=self.S_T, S_D=self.S_D, L=c["L"], n0=n0, C1=c["C1"], C2=c["C2"],
                                         C3=c["C3"], R=c["R"], width_cap=c["width_cap"], m_cap=c["m_cap"],
-                                        D_max=self.D)
+                                        D_max=self.D, per_request=bool(c.get("per_request", False)))
         self.prune_out = make_prune_out(width=self.width, stop=self.stop)
         self.verify_out = make_prune_out(m=self.m_dev)
 

@@ -64,7 +64,8 @@ enum {
   DT_DEV_BAD_TOKEN = 2,    /* a token id outside [0, V) where a token was required            */
   DT_DEV_BAD_TREE = 4,     /* selection not parent-closed, or a tree deeper than D_path - 1    */
   DT_DEV_TIMEOUT = 8,      /* a bounded wait on an asynchronous copy ran out                   */
-  DT_DEV_INTERNAL = 16     /* an internal iteration bound was hit                              */
+  DT_DEV_INTERNAL = 16,    /* an internal iteration bound was hit                              */
+  DT_DEV_KV_FULL = 32      /* dt_commit_kv: a request's rows would pass the cache's capacity   */
 };
 /* dt_config.flags */
 enum { DT_FLAG_TEST_TIMEOUT = 1 }; /* test only: the streaming row passes (expansion and verify)
@@ -125,14 +126,20 @@ typedef struct {
   double tau[4];        /* confidence thresholds: request continues iff exp(max value) > tau   */
   int32_t k_draft[4];   /* draft nodes kept when stopped at checkpoint s                       */
   int32_t K_total;      /* K_max: draft + retrieved nodes per request                         */
+  /* CAST, per-request rule (CAST page §局限与展望: padded equal-length batches are a limit of the
+   * batch rule): nonzero = every request applies the width/depth and verify-count rules to its own
+   * utilities, context, FIFO and stop; width, stop and m are then [B] outputs. */
+  int32_t per_request;
 } dt_prune_params;
 
 /* Outputs of dt_cast_prune (device pointers; NULL where a policy does not write). */
 typedef struct {
-  int32_t* width; /* [1]  CAST_WIDTH_DEPTH: n_d                                           */
-  int32_t* stop;  /* [B]  CAST_WIDTH_DEPTH: 1 = do not grow (batch-wide); GRAFT: per request,
+  int32_t* width; /* [1]  CAST_WIDTH_DEPTH: n_d ([B] with per_request)                     */
+  int32_t* stop;  /* [B]  CAST_WIDTH_DEPTH: 1 = do not grow (batch-wide, or per request with
+                          per_request: a stopped request stays stopped); GRAFT: per request,
                           set once a request stops                                          */
-  int32_t* m;     /* [1]  CAST_VERIFY: m;  [B] GRAFT: K_draft of each request (set on stop) */
+  int32_t* m;     /* [1]  CAST_VERIFY: m ([B] with per_request); [B] GRAFT: K_draft of each
+                          request (set on stop)                                             */
   int32_t* stage; /* [B]  GRAFT: checkpoint index that stopped the request, n_ckpt if none  */
 } dt_prune_out;
 
@@ -291,6 +298,25 @@ int dt_verify_accept(dt_handle* h, const dt_tree_meta* meta, const void* logits,
  * valid token; when a token repeats the highest position wins. M: device [B][V][8]. */
 int dt_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta, const int32_t* top8,
                   cudaStream_t s);
+
+/* After a9 (EAGLE-2 §一段更贴近实现的流程: commit the accepted tokens' KV, discard the rejected
+ * candidates'; §工程实现里的几个难点: the tree's KV is temporary while it is verified): append to each
+ * request's KV cache the rows of the root and of the accepted positions, in path order.
+ *   tmp_kv: device bytes, row of position i of request b at b * tmp_req_stride + i * tmp_pos_stride
+ *           (the verify forward's temporary KV, P positions per request); read only.
+ *   cache:  device bytes, row j of request b at b * cache_req_stride + j * cache_pos_stride, L_max
+ *           rows per request; rows cache_len[b] .. cache_len[b] + accept_len[b] are written.
+ *   row_bytes: bytes of one row (one token's keys and values of every layer). Every pointer, stride and
+ *           row_bytes must be a multiple of 16 bytes (DT_ERR_ARG otherwise).
+ *   cache_len: device [B] int32, in/out: increased by accept_len[b] + 1.
+ *   accept_len, accept_path: device, as written by dt_verify ([B], [B][D_path]).
+ * A request whose rows would pass L_max, or whose accept_len + 1 exceeds D_path, commits nothing,
+ * keeps its cache_len and sets DT_DEV_KV_FULL; a path position outside [0, P) sets DT_DEV_BAD_TREE.
+ * Two launches (the copy, then the lengths). */
+int dt_commit_kv(dt_handle* h, const void* tmp_kv, int64_t tmp_pos_stride, int64_t tmp_req_stride, int32_t P,
+                 void* cache, int64_t cache_pos_stride, int64_t cache_req_stride, int32_t L_max, int64_t row_bytes,
+                 int32_t* cache_len, const int32_t* accept_len, const int32_t* accept_path, int32_t D_path,
+                 cudaStream_t s);
 
 /* Standalone row log-softmax top-K that allocates nothing. This entry point has no counterpart in
  * the method's pages: it is the expansion's row pass (EAGLE-2 §扩展阶段: the children of a node

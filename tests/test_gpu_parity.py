@@ -226,6 +226,43 @@ def test_round_parity_cast_table_rows(torch):
     _run_rounds(torch, w, range(0, 16, 2), label="cast table rows 1..15")
 
 
+def _cast_per_request(**over):
+    from synth.workloads import WORKLOADS
+
+    return with_sizes("cast", cast=dict(WORKLOADS["cast"]["cast"], per_request=True), **over)
+
+
+@pytest.mark.parametrize("over,rounds", [(dict(V=12007), range(0, 16, 2)), ({}, 2)])
+def test_round_parity_cast_per_request(torch, over, rounds):
+    """CAST page §局限与展望: the per-request rule (each request's own widths, stop and verify count)
+    against the oracle's, at reduced and at full size."""
+    w = _cast_per_request(**over)
+    _run_rounds(torch, w, rounds, label=f"cast per request {over}")
+
+
+def test_cast_per_request_fused_calls_equal_separate_calls(torch):
+    import harness
+
+    w = _cast_per_request(V=32000)
+    outs = []
+    for fused in (True, False):
+        gr = harness.GpuRound(w, fused=fused)
+        res = []
+        for rnd in range(3):
+            attempts = np.zeros(w["B"], np.int64)
+            roots = harness.root_tokens(w, harness.salts_of(w, rnd, attempts))
+            gr.round(rnd, attempts, roots)
+            t = harness.tree_numpy(gr.run.h)
+            res.append((t["token"].copy(), t["value"].copy(), gr.run.selected.cpu().numpy().copy(),
+                        gr.run.m_dev.cpu().numpy().copy(), gr.run.width.cpu().numpy().copy(),
+                        gr.run.accept_len.cpu().numpy().copy(), gr.run.bonus.cpu().numpy().copy()))
+        outs.append(res)
+        gr.run.h.close()
+    for ra, rb in zip(*outs):
+        for a, b in zip(ra, rb):
+            np.testing.assert_array_equal(a, b)
+
+
 def test_sampling_first_token_law_on_gpu(torch):
     """Monte Carlo on the GPU alone: the first token a T = 1 round emits (the accepted child, or the
     bonus if every child of the root is rejected) is distributed as the target's root row,
