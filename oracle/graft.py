@@ -29,6 +29,29 @@ Readings taken where the page is silent or garbled:
 * M is one matrix per request, starts all -1, and is refreshed for every
   used position with a valid token (root included), in increasing position,
   so the highest position wins when a token repeats.
+
+Block drafters (the page's extension direction 1, Grafting for block drafters,
+and weakness 4, whose remedy is token-level confidence inside the block and
+templates fitted to the block's topology). Readings:
+
+* A block drafter gives in one pass one row per block position j = 1..L
+  (L = 16 for DFlash), its distribution for the token at j; the rows do not
+  depend on the tokens picked at earlier positions of the block.
+* Block tree: layer j holds the top-K tokens of row j, children of the block's
+  token at position j - 1 (the root for j = 1); the block's token at j is the
+  top-1 of row j. K = 1 is the plain block (a chain); K > 1 adds the top-K
+  alternatives at every position (the "tree-shaped expansion inside the
+  block"). This is the EAGLE-2 expansion with frontier width 1 fed with the
+  block's rows, since the highest-value node of a layer is the top-1 child of
+  the block token above it.
+* Token-level pruning: every block position can be a checkpoint, with the
+  rule of step (1): S_j is the block path's score at j, the first position
+  whose exp(S_j) is not above tau_j truncates the block after layer j.
+* Templates: root-anchored (step (2), template root = x_t) or tail-anchored
+  (the page contrasts G_ret^root and G_ret^tail): the template root is the
+  deepest kept draft node, ties broken by the total order (value desc, id
+  asc), i.e. the end of the kept block prefix; level-1 template nodes become
+  its children.
 """
 
 import numpy as np
@@ -74,8 +97,19 @@ def default_template(width=8, depth=8):
     return parent, rank
 
 
+def tail_anchor(tree, selected_b, b):
+    """The deepest kept draft node of request b (ties: value desc, then id asc); 0 (the root) when
+    no draft node is kept."""
+    best = 0
+    for i in (int(x) for x in selected_b if x >= 0):
+        if (tree.depth[b, i], tree.value[b, i], -i) > (tree.depth[b, best], tree.value[b, best], -best):
+            best = i
+    return best
+
+
 def retrieve(M, root_tokens, k_ret, template):
-    """Gather the first k_ret[b] template nodes from M[b]; returns per-request (tokens, parents)."""
+    """Gather the first k_ret[b] template nodes from M[b], the template root's token being
+    root_tokens[b] (the root's, or the anchor node's); returns per-request (tokens, parents)."""
     parent, rank = template
     out = []
     for b in range(len(root_tokens)):

@@ -19,14 +19,20 @@ Readings taken where the page is silent:
 import numpy as np
 
 
-def commit_kv(tmp_kv, cache, cache_len, accept_len, accept_path):
+def commit_kv(tmp_kv, cache, cache_len, accept_len, accept_path, row_off=None):
     """Append the root's and the accepted positions' KV rows to each request's cache (in place).
 
     tmp_kv [B][P][row], cache [B][L_max][row] (any dtype), cache_len [B] (updated), accept_len [B],
-    accept_path [B][D_path] (positions, root first, -1 padded). Returns the list of requests whose
-    commit was refused for lack of room.
+    accept_path [B][D_path] (positions, root first, -1 padded). With ``row_off`` ([B+1], the
+    padding-free layout of ``oracle.tree.packed_row_offsets``) tmp_kv is [rows][row] and position i
+    of request b is its row row_off[b] + i. Returns the list of requests whose commit was refused
+    for lack of room.
     """
     B, L_max = cache.shape[0], cache.shape[1]
+
+    def tmp_row(b, i):
+        return tmp_kv[int(row_off[b]) + i] if row_off is not None else tmp_kv[b, i]
+
     refused = []
     for b in range(B):
         n = int(accept_len[b]) + 1
@@ -35,6 +41,6 @@ def commit_kv(tmp_kv, cache, cache_len, accept_len, accept_path):
             refused.append(b)
             continue
         for j in range(n):
-            cache[b, start + j] = tmp_kv[b, int(accept_path[b, j])]
+            cache[b, start + j] = tmp_row(b, int(accept_path[b, j]))
         cache_len[b] = start + n
     return refused

@@ -39,10 +39,16 @@ def run_round(cfg, roots, draft_row, target_row, rnd=0, M=None, pos_offset=None,
     p_graft = None
     if policy == "graft":
         p_graft = dict(cfg["graft"], gaps=gaps, D_max=D)
+    # block drafter (Graft page, extension direction 1): the row of layer d is the block's row for
+    # position d, the same whatever tokens were picked above it; frontier width 1 (the block token)
+    block = bool(cfg.get("block", False))
 
     def expand():
         d = tree.cur_depth + 1
-        tree.expand_layer(lambda b, f: draft_row(b, d, int(tree.token[b, tree.frontier[b][f]])))
+        if block:
+            tree.expand_layer(lambda b, f: draft_row(b, d, int(roots[b])))
+        else:
+            tree.expand_layer(lambda b, f: draft_row(b, d, int(tree.token[b, tree.frontier[b][f]])))
         return d
 
     d = expand()
@@ -65,7 +71,7 @@ def run_round(cfg, roots, draft_row, target_row, rnd=0, M=None, pos_offset=None,
                 stop = [True] * B
         elif policy == "graft":
             graft_mod.checkpoint(tree, d, p_graft, stop, stage, m_req)
-            width = cfg["k"]
+            width = 1 if block else cfg["k"]
         else:
             width = cfg["k"]
             if d >= D:
@@ -93,7 +99,13 @@ def run_round(cfg, roots, draft_row, target_row, rnd=0, M=None, pos_offset=None,
     if policy == "graft":
         K_total = cfg["graft"]["K_total"]
         k_ret = [K_total - int(np.sum(selected[b] >= 0)) for b in range(B)]
-        retrieved = graft_mod.retrieve(M, roots, k_ret, cfg["graft"]["template"])
+        if cfg["graft"].get("anchor", "root") == "tail":
+            anchors = [graft_mod.tail_anchor(tree, selected[b], b) for b in range(B)]
+        else:
+            anchors = [0] * B
+        retrieved = graft_mod.retrieve(M, [int(tree.token[b, a]) for b, a in enumerate(anchors)], k_ret,
+                                       cfg["graft"]["template"])
+        retrieved = [(t, p, a) for (t, p), a in zip(retrieved, anchors)]
     if pos_offset is None:
         pos_offset = np.zeros(B, np.int64)
     meta = build_meta(tree, selected, pos_offset, cfg["P"], cfg["D_path"], retrieved)

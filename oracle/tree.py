@@ -25,6 +25,9 @@ Readings taken where the page is silent:
 * Flattening: position 0 is the root, then the selected nodes in ascending
   node id (a topological order), then retrieved nodes (Graft) in template
   order.
+* Padding-free target rows (CAST page §局限与展望 names padded batches as a
+  limit): request b's used positions take consecutive rows after those of
+  requests 0..b-1, in position order (``packed_row_offsets``).
 
 Node-id layout (an interface format: the GPU path writes the same layout from
 its own code): with K = per-node top-K, W = maximum frontier width and D =
@@ -223,8 +226,9 @@ def build_meta(tree, selected, pos_offset, P, D_path, retrieved=None):
     """Flatten each request's verify tree and build its attention metadata (a7).
 
     Positions: 0 = root, then the selected draft nodes in ascending id, then the
-    retrieved nodes (``retrieved[b] = (tokens, parents)``, parents index the
-    retrieved list, -1 = root) in template order. Positions past the request's
+    retrieved nodes (``retrieved[b] = (tokens, parents)`` or ``(tokens, parents,
+    anchor)``: parents index the retrieved list, -1 = the template root, which
+    is the root or the draft node ``anchor``) in template order. Positions past the request's
     count are unused: token, parent, depth and position id -1, empty mask row.
 
     mask[i][j] = 1 iff position j is an ancestor of position i or i itself.
@@ -258,10 +262,11 @@ def build_meta(tree, selected, pos_offset, P, D_path, retrieved=None):
             node_id[b, p] = i
             p += 1
         if retrieved is not None:
-            rt, rp = retrieved[b]
+            rt, rp = retrieved[b][0], retrieved[b][1]
+            anchor = retrieved[b][2] if len(retrieved[b]) > 2 else 0
             first = p
             for u in range(len(rt)):
-                par = 0 if rp[u] < 0 else first + rp[u]
+                par = pos_of[anchor] if rp[u] < 0 else first + rp[u]
                 tokens[b, p] = rt[u]
                 parents[b, p] = par
                 depth[b, p] = depth[b, par] + 1
@@ -288,4 +293,18 @@ def build_meta(tree, selected, pos_offset, P, D_path, retrieved=None):
                 row += 1
         n_leaves[b] = row
     return dict(tokens=tokens, parents=parents, depth=depth, node_id=node_id, mask=mask,
-                position_ids=posid, retrieve=retrieve, n_leaves=n_leaves, n_pos=n_pos)
+                position_ids=posid, retrieve=retrieve, n_leaves=n_leaves, n_pos=n_pos,
+                row_off=packed_row_offsets(n_pos))
+
+
+def packed_row_offsets(n_pos):
+    """Padding-free layout of a ragged batch's target rows.
+
+    CAST page §局限与展望 names padded equal-length batches as a limit of the method; without padding,
+    request b's n_pos[b] used positions take consecutive rows after those of requests 0..b-1, so the
+    row of (b, i) is row_off[b] + i. Returns row_off[0..B], row_off[B] = the rows in all.
+    """
+    off = [0]
+    for n in n_pos:
+        off.append(off[-1] + int(n))
+    return np.array(off, np.int64)

@@ -73,3 +73,42 @@ def test_two_requests_follow_their_own_trajectories():
     # the batch-wide rule averages the two requests and decides otherwise
     c = run(2, [CAST_DRAFT, REQ1_DRAFT], [CAST_TARGET, CAST_TARGET], per_request=False)
     assert c["widths"] != [w[0] for w in a["widths"]] or c["m"] != 7
+
+
+# ---- padding-free target rows (the verify layout of ragged batches) ----
+def test_packed_row_offsets_of_the_two_request_round():
+    """Request 0 uses 8 positions and request 1 uses 4: without padding their target rows are rows
+    0..7 and 8..11 of one buffer."""
+    a = run(2, [CAST_DRAFT, REQ1_DRAFT], [CAST_TARGET, CAST_TARGET], per_request=True)
+    assert list(a["meta"]["row_off"]) == [0, 8, 12]
+
+
+def test_packed_rows_cover_the_used_positions_once_and_verify_alike():
+    """Every used position (b, i) gets its own row row_off[b] + i, the rows of all requests cover
+    0..row_off[B]-1 exactly once, and the greedy verify reading packed rows decides exactly what it
+    decides on the padded rows (same rows, other addresses)."""
+    from oracle.tree import OracleTree, build_meta, packed_row_offsets
+    from oracle.verify import verify_greedy
+
+    for seed in range(5):
+        rng = np.random.default_rng(100 + seed)
+        B, V, K, W, D = 4, 10, 3, 2, 3
+        t = OracleTree(B, K, W, D, rng.integers(0, V, B))
+        for d in range(1, D + 1):
+            t.expand_layer(lambda b, f: rng.normal(0, 2, V))
+            if d < D:
+                t.select_frontier(W)
+        m = [int(x) for x in rng.integers(0, 9, B)]
+        sel = t.rerank(m, 8)
+        meta = build_meta(t, sel, np.zeros(B, np.int64), P=9, D_path=D + 1)
+        n_pos = meta["n_pos"]
+        off = packed_row_offsets(n_pos)
+        assert list(n_pos) == [1 + x for x in m]
+        seen = sorted(int(off[b]) + i for b in range(B) for i in range(int(n_pos[b])))
+        assert seen == list(range(int(off[B])))
+        padded = rng.normal(0, 2, (B, 9, V))
+        packed = np.concatenate([padded[b, :int(n_pos[b])] for b in range(B)])
+        g1 = verify_greedy(meta, lambda b, i: padded[b, i])
+        g2 = verify_greedy(meta, lambda b, i: packed[int(off[b]) + i])
+        for x, y in zip(g1, g2):
+            np.testing.assert_array_equal(x, y)

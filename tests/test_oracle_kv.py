@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 from oracle.kv import commit_kv
-from oracle.tree import OracleTree, build_meta
+from oracle.tree import OracleTree, build_meta, packed_row_offsets
 from oracle.verify import verify_greedy
 
 ROW = 16  # bytes of a synthetic KV row
@@ -32,11 +32,17 @@ def random_round(seed, B=3, V=12, K=3, W=2, D=3, m=8):
         t.expand_layer(lambda b, f: rng.normal(0, 2, V))
         if d < D:
             t.select_frontier(W)
-    sel = t.rerank(m, m)
-    meta = build_meta(t, sel, np.zeros(B, np.int64), P=m + 1, D_path=D + 1)
-    rows = rng.normal(0, 2, (B, m + 1, V))  # target rows: argmax decides the accepted path
+    m_cap = int(np.max(m))
+    sel = t.rerank(m, m_cap)
+    meta = build_meta(t, sel, np.zeros(B, np.int64), P=m_cap + 1, D_path=D + 1)
+    rows = rng.normal(0, 2, (B, m_cap + 1, V))  # target rows: argmax decides the accepted path
     acc, path, bonus = verify_greedy(meta, lambda b, i: rows[b, i])
     return t, meta, acc, path, rng
+
+
+def rng_m(seed):
+    """Verify counts: 8 for every request, or per-request counts (ragged requests) for the packed cases."""
+    return 8 if seed < 6 else [2 + seed % 3, 8, 1 + seed % 5]
 
 
 def path_tokens(meta, b, i):
@@ -48,15 +54,22 @@ def path_tokens(meta, b, i):
     return out[::-1]
 
 
-@pytest.mark.parametrize("seed", range(6))
-def test_commit_equals_sequential_decode(seed):
-    t, meta, acc, path, rng = random_round(seed)
+@pytest.mark.parametrize("seed,packed", [(s, False) for s in range(6)] + [(s, True) for s in range(6, 10)])
+def test_commit_equals_sequential_decode(seed, packed):
+    """Padded temporary rows ([B][P]), or padding-free ones (request b's used positions at
+    row_off[b] + i, one request after the other, nothing in between)."""
+    t, meta, acc, path, rng = random_round(seed, m=rng_m(seed))
     B, P = meta["tokens"].shape
     ctx = [list(rng.integers(0, 12, rng.integers(0, 5))) for _ in range(B)]  # already committed tokens
     tmp = np.zeros((B, P, ROW), np.uint8)
     for b in range(B):
         for i in range(int(meta["n_pos"][b])):
             tmp[b, i] = kv_row(ctx[b] + path_tokens(meta, b, i))
+    row_off = None
+    if packed:
+        row_off = packed_row_offsets(meta["n_pos"])
+        tmp = np.concatenate([tmp[b, :int(meta["n_pos"][b])] for b in range(B)])  # used rows, in order
+        assert tmp.shape[0] == row_off[B] and len(set(meta["n_pos"].tolist())) > 1  # ragged
     L = 16
     cache = np.zeros((B, L, ROW), np.uint8)
     cache_len = np.array([len(c) for c in ctx], np.int64)
@@ -64,7 +77,7 @@ def test_commit_equals_sequential_decode(seed):
         for j in range(len(ctx[b])):
             cache[b, j] = kv_row(ctx[b][:j + 1])
     before = cache.copy()
-    refused = commit_kv(tmp, cache, cache_len, acc, path)
+    refused = commit_kv(tmp, cache, cache_len, acc, path, row_off=row_off)
     assert refused == []
     for b in range(B):
         committed = [int(meta["tokens"][b, 0])] + [int(meta["tokens"][b, p]) for p in path[b, 1:acc[b] + 1]]

@@ -217,8 +217,8 @@ def test_graft_round_composition_by_hand():
     ref = run_graft()
     assert ref["stage"] == [1] and ref["m_sel"] == [8] and ref["depth"] == 2
     assert int(np.sum(ref["selected"][0] >= 0)) == 6
-    toks, pars = ref["retrieved"][0]
-    assert toks == [1, 0, 2, -1] and pars == [-1, -1, 0, 1]
+    toks, pars, anchor = ref["retrieved"][0]
+    assert toks == [1, 0, 2, -1] and pars == [-1, -1, 0, 1] and anchor == 0
     meta = ref["meta"]
     assert int(meta["n_pos"][0]) == 11
     assert list(meta["tokens"][0]) == [2, 0, 1, 0, 1, 1, 0, 1, 0, 2, -1]
