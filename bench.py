@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "draft-tree rounds/s (expand+rerank+verify) at B=8,V=128256; logits HBM GB/s"
 UNIT = "rounds/s"
 HEADLINE = "cast"
-OTHERS = ["pr1", "vicuna", "vicuna_t1", "graft", "stress"]
+OTHERS = ["pr1", "vicuna", "vicuna_t1", "graft", "stress", "cast_req", "graft_block"]
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -80,20 +80,29 @@ def job_throughput(units_per_rank, world, ms_max):
 
 
 def workload_of(name):
-    """(workload dict, label) of a bench workload name; vicuna_t1 is Vicuna with sampling (T = 1)."""
+    """(workload dict, label) of a bench workload name; vicuna_t1 is Vicuna with sampling (T = 1);
+    cast_req is the CAST batch with the per-request rule and padding-free target rows."""
     from synth.workloads import WORKLOADS
 
     if name == "vicuna_t1":
         w = dict(WORKLOADS["vicuna"])
         w["T"] = 1
         return w, "vicuna_t1"
+    if name == "cast_req":
+        w = dict(WORKLOADS["cast"])
+        w["cast"] = dict(w["cast"], per_request=True)
+        w["packed"] = True
+        return w, "cast_req"
     return dict(WORKLOADS[name]), name
 
 
 def workload_config(w, g, label):
     dt = "bf16" if w["dtype"] == 0 else "fp32"
     verify = "greedy verify" if w["T"] == 0 else "speculative-sampling verify (T=1)"
-    return {"workload": f"{label}: {w['policy']} tree round, B={w['B']}, V={w['V']}, {dt} logits, K={w['K']}, "
+    if w.get("packed"):
+        verify += " of padding-free target rows"
+    rule = ", per-request CAST rule" if w.get("cast", {}).get("per_request") else ""
+    return {"workload": f"{label}: {w['policy']} tree round{rule}, B={w['B']}, V={w['V']}, {dt} logits, K={w['K']}, "
                         f"k<={w['k']}, depth<={w['D']}, m<={g['m_cap']}, {verify}",
             "B": w["B"], "V": w["V"], "K": w["K"], "k_max": w["k"], "D_max": w["D"], "m_cap": g["m_cap"],
             "global_batch": w["B"]}
@@ -197,7 +206,7 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
     import torch.distributed as tdist
 
     import synth
-    from synth.workloads import spec_for, geometry, cast_tables, chain_template
+    from synth.workloads import spec_for, geometry, cast_tables, graft_template
     from dynamic_draft_tree_gb300 import dt_get_status
     from dynamic_draft_tree_gb300.rounds import RoundRunner
 
@@ -212,14 +221,18 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
         kw = dict(cast=dict(cc), cast_tables=cast_tables(B, cc["M_rows"], cc["N_cols"], cc["L"]))
     graft = w["policy"] == "graft"
     if graft:
-        kw = dict(graft=w["graft"], template=chain_template(k, w["D"]))
-    run = RoundRunner(w["policy"], B, V, w["K"], k, D, P, g["D_path"], g["m_cap"], spec.dtype, T=w["T"], **kw)
+        kw = dict(graft=w["graft"], template=graft_template(w), block=bool(w.get("block", False)))
+    packed = bool(w.get("packed", False))
+    run = RoundRunner(w["policy"], B, V, w["K"], k, D, P, g["D_path"], g["m_cap"], spec.dtype, T=w["T"],
+                      packed=packed, **kw)
     dt = torch.int16 if spec.dtype == synth.BF16 else torch.float32
     esz = 2 if spec.dtype == synth.BF16 else 4
     round_bytes = (D * B * k + B * P) * V * esz
     # recorded rounds: at least 16 (a mix of rounds) and at least 3x L2 of inputs, at most 48 GiB
     R = int(max(2, min(max(16, math.ceil(3 * L2_BYTES / round_bytes)), 256, (48 << 30) // round_bytes)))
-    rec_draft = torch.empty((R, D, B, k, V), dtype=dt, device="cuda")
+    block = bool(w.get("block", False))
+    # a block drafter's rows: one [B][L][V] set per round (L = D), at rec_draft[r, 0]
+    rec_draft = torch.empty((R, 1, B, D, V) if block else (R, D, B, k, V), dtype=dt, device="cuda")
     rec_target = torch.empty((R, B, P, V), dtype=dt, device="cuda")
     roots = torch.empty((R, B), dtype=torch.int32, device="cuda")
     M = torch.full((B, V, 8), -1, dtype=torch.int32, device="cuda") if graft else None
@@ -235,6 +248,14 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
         roots[slot] = torch.from_numpy(synth.root_tokens(w["seed"], salt, B, V)).cuda()
 
         def draft_rows(d, ftok):
+            if d == 0:  # block rows: position j + 1 of request b, keyed on its root token
+                ctx = roots[slot].repeat_interleave(D)
+                pos = torch.arange(1, D + 1, dtype=torch.int32, device="cuda").repeat(B)
+                synth.gen_rows_gpu(torch, spec, w["seed"], salt, synth.DRAFT, ctx, rec_draft[slot, 0], V,
+                                   depth_dev=pos if dk else None, rows_per_b=D)
+                if widths is not None:
+                    widths.append(np.full(B, D))
+                return rec_draft[slot, 0]
             F = 1 if d == 1 else k
             ctx = ftok[:, :F].contiguous().view(-1)
             if widths is not None:
@@ -244,6 +265,11 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
             return rec_draft[slot, d - 1]
 
         def target_rows(meta):
+            if packed:  # padding-free: request b's rows at meta.row_off[b] + i
+                req, ctx, dep = synth.packed_row_map(torch, meta.row_off, meta.tokens, meta.depth)
+                synth.gen_rows_gpu(torch, spec, w["seed"], salt, synth.TARGET, ctx, rec_target[slot], V,
+                                   depth_dev=dep if dk else None, depth_add=1 if dk else 0, row_req_dev=req)
+                return rec_target[slot]
             synth.gen_rows_gpu(torch, spec, w["seed"], salt, synth.TARGET, meta.tokens.view(-1), rec_target[slot],
                                V, depth_dev=meta.depth.view(-1) if dk else None, depth_add=1 if dk else 0,
                                rows_per_b=P)
@@ -370,6 +396,8 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
     last = 1 if w["policy"] in ("cast", "graft") else 0
     launches = 2 + D + per_layer * (D - 1) + last + (2 if w["policy"] == "cast" else 1) + (1 if graft else 0) + 1 + \
         (3 if w["T"] == 1 else 2) + (1 if graft else 0)
+    if block:  # reset, the block expansion, rerank, retrieval, meta, the verify, the M refresh
+        launches = 5 + (3 if w["T"] == 1 else 2) + 1
 
     out = {"label": label, "value": value, "unit": UNIT, "ms_per_step": ms / steps, "steps": steps,
            "dtype": "bf16" if spec.dtype == synth.BF16 else "f32",
@@ -412,25 +440,38 @@ def kv_commit_run(torch, run, rec_out, steps, R):
     cache = torch.empty((B, L, KV_ROW_BYTES), dtype=torch.uint8, device="cuda")
     cache_len = torch.zeros((B,), dtype=torch.int32, device="cuda")
     rows = sum(int((rec_out[s % R][0] + 1).sum()) for s in range(steps))
-    for s in range(3):  # warm-up, then start again from an empty cache
+    for s in range(3):  # warm-up
         dt_commit_kv(run.h, tmp, cache, cache_len, rec_out[s % R][0], rec_out[s % R][3])
-    cache_len.zero_()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for s in range(steps):
-        dt_commit_kv(run.h, tmp, cache, cache_len, rec_out[s % R][0], rec_out[s % R][3])
-    e1.record()
-    torch.cuda.synchronize()
+    # the calls of `steps` rounds captured as one CUDA graph (device time, not the host's call rate),
+    # each replay starting again from an empty cache
+    gph = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(gph, stream=cs):
+            for s in range(steps):
+                dt_commit_kv(run.h, tmp, cache, cache_len, rec_out[s % R][0], rec_out[s % R][3])
+    torch.cuda.current_stream().wait_stream(cs)
+    times = []
+    for _ in range(6):
+        cache_len.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        gph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
     assert dt_get_status(run.h) == 0
-    us = e0.elapsed_time(e1) * 1e3 / steps
+    us = float(np.median(times[1:])) * 1e3 / steps
     nbytes = 2.0 * rows / steps * KV_ROW_BYTES
     peak, _ = measured_peaks()
     del tmp, cache
     return {"row_bytes": KV_ROW_BYTES, "rows_per_call": rows / steps, "avg_us": us,
             "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak,
-            "note": "calls back to back (two launches each), not in the round's graph"}
+            "note": "the calls of `steps` rounds (two launches each) as one CUDA graph, median of 5 replays; "
+                    "not part of the round's graph"}
 
 
 def e2e_run(torch, run, w, rec_draft, rec_target, roots, rec_out, act_rec, npos_rec, esz, M, steps, world):
@@ -449,13 +490,16 @@ def e2e_run(torch, run, w, rec_draft, rec_target, roots, rec_out, act_rec, npos_
     # that layer's [B][F][V] buffer); target rows 0..n_pos[b]-1 of request b
     chunks = []
     for d, cnt in enumerate(act_rec[0]):
-        F = 1 if d == 0 else k
+        F = w["D"] if run.block else (1 if d == 0 else k)  # a block drafter: one [B][L][V] set
         for b in range(B):
             if cnt[b] > 0:
                 chunks.append(("d", d, b * F, int(cnt[b])))
-    for b in range(B):
-        if npos_rec[0][b] > 0:
-            chunks.append(("t", 0, b * run.P, int(npos_rec[0][b])))
+    if run.packed:  # padding-free: the used target rows are rows 0 .. sum n_pos - 1
+        chunks.append(("t", 0, 0, int(np.sum(npos_rec[0]))))
+    else:
+        for b in range(B):
+            if npos_rec[0][b] > 0:
+                chunks.append(("t", 0, b * run.P, int(npos_rec[0][b])))
     bi = sum(c[3] for c in chunks) * V * esz + h_roots.numel() * 4
     bo = (out_len.numel() + out_bonus.numel() + out_path.numel()) * 4
     bufs = [(torch.zeros_like(roots[0]), torch.zeros_like(rec_draft[0]), torch.zeros_like(rec_target[0]))

@@ -11,10 +11,10 @@ import torch
 
 from ._lib import (lib, check, DtError, DtConfig, DtTreeView, DtPruneParams, DtPruneOut, DtTemplate,  # noqa
                    DtTreeMeta, EXPORTS, DT_OK, DT_ERR_ARG, DT_ERR_CUDA, DT_ERR_DEVICE,
-                   DT_ERR_DEVICE_TIMEOUT, DT_BF16, DT_F32, DT_GREEDY, DT_SAMPLE,
+                   DT_ERR_DEVICE_TIMEOUT, DT_BF16, DT_F32, DT_GREEDY, DT_SAMPLE, DT_VERIFY_PACKED,
                    DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT, DT_POLICY_NONE,
                    DT_DEV_BAD_LOGITS, DT_DEV_BAD_TOKEN, DT_DEV_BAD_TREE, DT_DEV_TIMEOUT, DT_DEV_INTERNAL, DT_DEV_KV_FULL,
-                   DT_FLAG_TEST_TIMEOUT, LIB_PATH)
+                   DT_FLAG_TEST_TIMEOUT, DT_ANCHOR_ROOT, DT_ANCHOR_TAIL, LIB_PATH)
 
 
 def _ptr(t):
@@ -145,16 +145,26 @@ def dt_rerank(h, m, m_cap, selected, stream=None):
     check(lib.dt_rerank(h.h, _ptr(m), ml, m_cap, _ptr(selected), _stream(stream)))
 
 
-def dt_graft_retrieve(h, M, m_draft, K_total, template, R_cap, ret_token, ret_parent, ret_count, stream=None):
-    check(lib.dt_graft_retrieve(h.h, _ptr(M), _ptr(m_draft), K_total, ctypes.byref(template.c), R_cap,
-                                _ptr(ret_token), _ptr(ret_parent), _ptr(ret_count), _stream(stream)))
+def dt_graft_retrieve(h, M, template, R_cap, ret_token, ret_parent, ret_count, selected=None, m_cap=0,
+                      ret_anchor=None, stream=None):
+    """Retrieval envelope from M; a tail-anchored template needs ``selected`` / ``m_cap``."""
+    check(lib.dt_graft_retrieve(h.h, _ptr(M), ctypes.byref(template.c), R_cap, _ptr(selected), m_cap,
+                                _ptr(ret_token), _ptr(ret_parent), _ptr(ret_count), _ptr(ret_anchor),
+                                _stream(stream)))
 
 
 def dt_build_tree_meta(h, selected, m_cap, meta, pos_offset=None, ret_token=None, ret_parent=None,
-                       ret_count=None, R_cap=0, stream=None):
+                       ret_count=None, R_cap=0, ret_anchor=None, K_total=0, stream=None):
     check(lib.dt_build_tree_meta(h.h, _ptr(selected), m_cap, _ptr(ret_token), _ptr(ret_parent),
-                                 _ptr(ret_count), R_cap, _ptr(pos_offset), ctypes.byref(meta.c),
-                                 _stream(stream)))
+                                 _ptr(ret_count), _ptr(ret_anchor), R_cap, K_total, _ptr(pos_offset),
+                                 ctypes.byref(meta.c), _stream(stream)))
+
+
+def dt_block_expand(h, logits, L, params=None, out=None, ld=None, stream=None):
+    """Draft layers 1..L from a block drafter's rows [B][L][V] (one call; Graft gates with params)."""
+    ld = logits.shape[-1] if ld is None else ld
+    check(lib.dt_block_expand(h.h, _ptr(logits), ld, L, None if params is None else ctypes.byref(params),
+                              None if out is None else ctypes.byref(out), _stream(stream)))
 
 
 def dt_verify(h, meta, logits, mode, seed, round_, accept_len, accept_path, bonus, top8=None, ld=None,
@@ -183,26 +193,40 @@ def dt_adj_update(h, M, meta, top8, stream=None):
     check(lib.dt_adj_update(h.h, _ptr(M), ctypes.byref(meta.c), _ptr(top8), _stream(stream)))
 
 
-def dt_commit_kv(h, tmp_kv, cache, cache_len, accept_len, accept_path, stream=None):
+def dt_commit_kv(h, tmp_kv, cache, cache_len, accept_len, accept_path, row_off=None, P=None, stream=None):
     """Append the root's and the accepted positions' KV rows to each request's cache.
 
     tmp_kv [B][P][...] and cache [B][L_max][...] are device tensors whose trailing dimensions form
-    one row (contiguous, a multiple of 16 bytes); cache_len [B] int32 is updated in place."""
-    if tmp_kv.dim() < 3 or cache.dim() < 3:
-        raise ValueError("tmp_kv and cache need [B][positions][row...] shapes")
+    one row (contiguous, a multiple of 16 bytes); cache_len [B] int32 is updated in place. With
+    ``row_off`` ([B+1] int32 device, dt_tree_meta.row_off) tmp_kv is packed: [rows][...], the row of
+    position i of request b being row_off[b] + i; P (positions per request of the tree) is then
+    required."""
+    packed = row_off is not None
+    lead = 1 if packed else 2
+    if tmp_kv.dim() < lead + 1 or cache.dim() < 3:
+        raise ValueError("tmp_kv needs [B][positions][row...] ([rows][row...] packed), cache [B][L_max][row...]")
     esz = tmp_kv.element_size()
-    row_bytes = tmp_kv[0, 0].numel() * esz
+    row0 = tmp_kv[0] if packed else tmp_kv[0, 0]
+    row_bytes = row0.numel() * esz
     if cache[0, 0].numel() * cache.element_size() != row_bytes:
         raise ValueError("tmp_kv and cache rows differ in size")
-    if not tmp_kv[0, 0].is_contiguous() or not cache[0, 0].is_contiguous():
+    if not row0.is_contiguous() or not cache[0, 0].is_contiguous():
         raise ValueError("KV rows must be contiguous")
     for t in (tmp_kv, cache):
         if not t.is_cuda:
             raise ValueError("device tensor required")
-    check(lib.dt_commit_kv(h.h, tmp_kv.data_ptr(), tmp_kv.stride(1) * esz, tmp_kv.stride(0) * esz, tmp_kv.shape[1],
+    if packed:
+        if P is None:
+            raise ValueError("P is required with row_off")
+        pos_stride, req_stride = tmp_kv.stride(0) * esz, 0
+    else:
+        P = tmp_kv.shape[1]
+        pos_stride, req_stride = tmp_kv.stride(1) * esz, tmp_kv.stride(0) * esz
+    check(lib.dt_commit_kv(h.h, tmp_kv.data_ptr(), pos_stride, req_stride, P,
                            cache.data_ptr(), cache.stride(1) * cache.element_size(),
                            cache.stride(0) * cache.element_size(), cache.shape[1], row_bytes, _ptr(cache_len),
-                           _ptr(accept_len), _ptr(accept_path), accept_path.shape[-1], _stream(stream)))
+                           _ptr(accept_len), _ptr(accept_path), accept_path.shape[-1], _ptr(row_off),
+                           _stream(stream)))
 
 
 def dt_row_topk_static(logits, K, logp, ids, V=None, status=None, stream=None):
@@ -235,14 +259,15 @@ class Meta:
         self.retrieve = torch.empty((B, P, D_path), **i32)
         self.n_leaves = torch.empty((B,), **i32)
         self.n_pos = torch.empty((B,), **i32)
+        self.row_off = torch.empty((B + 1,), **i32)
         self.c = DtTreeMeta(P, D_path, *[_ptr(t) for t in (self.tokens, self.parents, self.depth, self.node_id,
                                                             self.mask, self.position_ids, self.retrieve,
-                                                            self.n_leaves, self.n_pos)])
+                                                            self.n_leaves, self.n_pos, self.row_off)])
 
     def numpy(self):
         return {k: getattr(self, k).cpu().numpy() for k in
                 ("tokens", "parents", "depth", "node_id", "mask", "position_ids", "retrieve", "n_leaves",
-                 "n_pos")}
+                 "n_pos", "row_off")}
 
 
 def make_prune_params(S_T=None, S_D=None, L=512.0, n0=0, C1=0.0, C2=0.0, C3=0.0, R=3, width_cap=1, m_cap=1,
@@ -268,10 +293,13 @@ def make_prune_out(width=None, stop=None, m=None, stage=None):
 
 
 class Template:
-    """Host-side retrieval template (parent, rank) in breadth-first order."""
+    """Host-side retrieval template (parent, rank) in breadth-first order, hanging from the root or
+    (anchor DT_ANCHOR_TAIL) from the deepest kept draft node."""
 
-    def __init__(self, parent, rank):
+    def __init__(self, parent, rank, anchor=DT_ANCHOR_ROOT):
         self.n = len(parent)
+        self.anchor = anchor
         self._p = (ctypes.c_int32 * max(1, self.n))(*parent)
         self._r = (ctypes.c_int32 * max(1, self.n))(*rank)
-        self.c = DtTemplate(self.n, ctypes.cast(self._p, ctypes.c_void_p), ctypes.cast(self._r, ctypes.c_void_p))
+        self.c = DtTemplate(self.n, ctypes.cast(self._p, ctypes.c_void_p), ctypes.cast(self._r, ctypes.c_void_p),
+                            anchor)

@@ -13,17 +13,19 @@ LIB_PATH = os.path.join(HERE, "libdt.so")
 DT_OK, DT_ERR_ARG, DT_ERR_CUDA, DT_ERR_DEVICE, DT_ERR_DEVICE_TIMEOUT = 0, -1, -2, -3, -4
 DT_BF16, DT_F32 = 0, 1
 DT_GREEDY, DT_SAMPLE = 0, 1
+DT_VERIFY_PACKED = 2
 DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT, DT_POLICY_NONE = 0, 1, 2, 3
 DT_DEV_BAD_LOGITS, DT_DEV_BAD_TOKEN, DT_DEV_BAD_TREE, DT_DEV_TIMEOUT, DT_DEV_INTERNAL = 1, 2, 4, 8, 16
 DT_DEV_KV_FULL = 32
 DT_FLAG_TEST_TIMEOUT = 1
+DT_ANCHOR_ROOT, DT_ANCHOR_TAIL = 0, 1
 
 EXPORTS = ["dt_last_error_string", "dt_create", "dt_destroy", "dt_get_tree", "dt_get_status",
            "dt_clear_status", "dt_tree_reset", "dt_select_frontier", "dt_expand_layer", "dt_cast_prune",
            "dt_rerank", "dt_graft_retrieve", "dt_build_tree_meta", "dt_verify", "dt_adj_update",
            "dt_row_topk_static", "dt_cast_prune_select",
            "dt_cast_verify_rerank", "dt_expand_prune_select", "dt_verify_rows", "dt_verify_accept",
-           "dt_commit_kv"]
+           "dt_commit_kv", "dt_block_expand"]
 
 c_i32p = ctypes.c_void_p
 vp = ctypes.c_void_p
@@ -48,8 +50,8 @@ class DtPruneParams(ctypes.Structure):
                 ("L", ctypes.c_double), ("n0", ctypes.c_int64), ("C1", ctypes.c_double),
                 ("C2", ctypes.c_double), ("C3", ctypes.c_double), ("R", ctypes.c_int32),
                 ("width_cap", ctypes.c_int32), ("m_cap", ctypes.c_int32), ("D_max", ctypes.c_int32),
-                ("n_ckpt", ctypes.c_int32), ("ckpt_layer", ctypes.c_int32 * 4),
-                ("tau", ctypes.c_double * 4), ("k_draft", ctypes.c_int32 * 4),
+                ("n_ckpt", ctypes.c_int32), ("ckpt_layer", ctypes.c_int32 * 16),
+                ("tau", ctypes.c_double * 16), ("k_draft", ctypes.c_int32 * 16),
                 ("K_total", ctypes.c_int32), ("per_request", ctypes.c_int32)]
 
 
@@ -58,13 +60,13 @@ class DtPruneOut(ctypes.Structure):
 
 
 class DtTemplate(ctypes.Structure):
-    _fields_ = [("n", ctypes.c_int32), ("parent", vp), ("rank", vp)]
+    _fields_ = [("n", ctypes.c_int32), ("parent", vp), ("rank", vp), ("anchor", ctypes.c_int32)]
 
 
 class DtTreeMeta(ctypes.Structure):
     _fields_ = [("P", ctypes.c_int32), ("D_path", ctypes.c_int32), ("tokens", vp), ("parents", vp),
                 ("depth", vp), ("node_id", vp), ("mask", vp), ("position_ids", vp),
-                ("retrieve", vp), ("n_leaves", vp), ("n_pos", vp)]
+                ("retrieve", vp), ("n_leaves", vp), ("n_pos", vp), ("row_off", vp)]
 
 
 def _load():
@@ -85,10 +87,12 @@ def _load():
         "dt_expand_layer": ([vp, vp, ctypes.c_int64, ctypes.c_int32, vp], I),
         "dt_cast_prune": ([vp, ctypes.c_int32, ctypes.POINTER(DtPruneParams), ctypes.POINTER(DtPruneOut), vp], I),
         "dt_rerank": ([vp, vp, ctypes.c_int32, ctypes.c_int32, vp, vp], I),
-        "dt_graft_retrieve": ([vp, vp, vp, ctypes.c_int32, ctypes.POINTER(DtTemplate), ctypes.c_int32,
-                               vp, vp, vp, vp], I),
-        "dt_build_tree_meta": ([vp, vp, ctypes.c_int32, vp, vp, vp, ctypes.c_int32, vp,
+        "dt_graft_retrieve": ([vp, vp, ctypes.POINTER(DtTemplate), ctypes.c_int32, vp, ctypes.c_int32,
+                               vp, vp, vp, vp, vp], I),
+        "dt_build_tree_meta": ([vp, vp, ctypes.c_int32, vp, vp, vp, vp, ctypes.c_int32, ctypes.c_int32, vp,
                                 ctypes.POINTER(DtTreeMeta), vp], I),
+        "dt_block_expand": ([vp, vp, ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(DtPruneParams),
+                             ctypes.POINTER(DtPruneOut), vp], I),
         "dt_verify": ([vp, ctypes.POINTER(DtTreeMeta), vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64,
                        ctypes.c_uint64, vp, vp, vp, vp, vp], I),
         "dt_adj_update": ([vp, vp, ctypes.POINTER(DtTreeMeta), vp, vp], I),
@@ -100,7 +104,7 @@ def _load():
         "dt_verify_accept": ([vp, ctypes.POINTER(DtTreeMeta), vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64,
                               ctypes.c_uint64, vp, vp, vp, vp, vp], I),
         "dt_commit_kv": ([vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, vp, ctypes.c_int64, ctypes.c_int64,
-                          ctypes.c_int32, ctypes.c_int64, vp, vp, vp, ctypes.c_int32, vp], I),
+                          ctypes.c_int32, ctypes.c_int64, vp, vp, vp, ctypes.c_int32, vp, vp], I),
         "dt_cast_verify_rerank": ([vp, ctypes.POINTER(DtPruneParams), ctypes.POINTER(DtPruneOut), vp, vp], I),
         "dt_row_topk_static": ([vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                 vp, vp, vp, vp], I),

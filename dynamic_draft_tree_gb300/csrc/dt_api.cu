@@ -78,6 +78,7 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   if (e == cudaSuccess) e = dt::init_verify_attributes();
   if (e == cudaSuccess) e = dt::init_select_attributes();
   if (e == cudaSuccess) e = dt::init_meta_attributes();
+  if (e == cudaSuccess) e = dt::init_block_attributes();
   if (e != cudaSuccess) {
     delete h;
     return cuda_fail(e, "cudaFuncSetAttribute");
@@ -93,7 +94,7 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   }
   Carver cv;
   const size_t o_token = cv.take<int32_t>(BN), o_parent = cv.take<int32_t>(BN), o_depth = cv.take<int32_t>(BN);
-  const size_t o_logc = cv.take<float>(BN), o_value = cv.take<float>(BN);
+  const size_t o_logc = cv.take<float>(BN), o_value = cv.take<float>(BN), o_dd = cv.take<float2>(BN);
   const size_t o_lorder = cv.take<int32_t>((size_t)c.B_max * (c.D_max + 1) * h->LW);
   const size_t o_lval = cv.take<float>((size_t)c.B_max * (c.D_max + 1) * h->LW);
   const size_t o_ltok = cv.take<int32_t>((size_t)c.B_max * (c.D_max + 1) * h->LW);
@@ -138,6 +139,7 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   w.node_depth = reinterpret_cast<int32_t*>(bp + o_depth);
   w.logc = reinterpret_cast<float*>(bp + o_logc);
   w.value = reinterpret_cast<float*>(bp + o_value);
+  w.node_dd = reinterpret_cast<float2*>(bp + o_dd);
   w.layer_order = reinterpret_cast<int32_t*>(bp + o_lorder);
   w.layer_val = reinterpret_cast<float*>(bp + o_lval);
   w.layer_tok = reinterpret_cast<int32_t*>(bp + o_ltok);
@@ -271,7 +273,7 @@ static int check_policy_args(const dt_handle* h, int32_t policy, const dt_prune_
   }
   if (policy == DT_POLICY_GRAFT_CHECKPOINT) {
     if (!p || !out) return fail(DT_ERR_ARG, "the Graft checkpoint needs params and outputs");
-    if (p->n_ckpt < 0 || p->n_ckpt > 4) return fail(DT_ERR_ARG, "n_ckpt must be in [0, 4]");
+    if (p->n_ckpt < 0 || p->n_ckpt > 16) return fail(DT_ERR_ARG, "n_ckpt must be in [0, 16]");
     if (!out->stop) return fail(DT_ERR_ARG, "stop output required");
     return DT_OK;
   }
@@ -298,6 +300,25 @@ int dt_expand_prune_select(dt_handle* h, const void* logits, int64_t ld, int32_t
   return DT_OK;
 }
 
+int dt_block_expand(dt_handle* h, const void* logits, int64_t ld, int32_t L, const dt_prune_params* p,
+                    const dt_prune_out* out, cudaStream_t s) {
+  if (!h || !logits) return fail(DT_ERR_ARG, "dt_block_expand: null argument");
+  if (h->B < 1) return fail(DT_ERR_ARG, "dt_block_expand: no tree (call dt_tree_reset)");
+  if (h->depth != 0) return fail(DT_ERR_ARG, "dt_block_expand: the tree must be right after dt_tree_reset");
+  if (L < 1 || L > h->cfg.D_max) return fail(DT_ERR_ARG, "L=%d outside [1, D_max=%d]", L, h->cfg.D_max);
+  if ((int64_t)h->B * L > h->ws.row_counter_cap) return fail(DT_ERR_ARG, "B*L exceeds B_max*max(W, P_max)");
+  if (ld < h->cfg.V) return fail(DT_ERR_ARG, "ld=%lld < V", (long long)ld);
+  const size_t esz = h->cfg.dtype == DT_BF16 ? 2 : 4;
+  if (!aligned(logits, esz)) return fail(DT_ERR_ARG, "logits not aligned to its element size");
+  if (p) {
+    if (!out || !out->stop) return fail(DT_ERR_ARG, "dt_block_expand: the gates need out->stop");
+    if (p->n_ckpt < 0 || p->n_ckpt > 16) return fail(DT_ERR_ARG, "n_ckpt must be in [0, 16]");
+  }
+  cudaError_t e = dt::launch_block_expand(h, logits, ld, L, p, out, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dt_block_expand");
+  return DT_OK;
+}
+
 int dt_cast_prune(dt_handle* h, int32_t policy, const dt_prune_params* p, const dt_prune_out* out,
                   cudaStream_t s) {
   if (!h || !p || !out) return fail(DT_ERR_ARG, "dt_cast_prune: null argument");
@@ -321,7 +342,7 @@ int dt_cast_prune(dt_handle* h, int32_t policy, const dt_prune_params* p, const 
     if (!out->m) return fail(DT_ERR_ARG, "m output required");
   } else if (policy == DT_POLICY_GRAFT_CHECKPOINT) {
     if (h->depth < 1) return fail(DT_ERR_ARG, "no layer to check");
-    if (p->n_ckpt < 0 || p->n_ckpt > 4) return fail(DT_ERR_ARG, "n_ckpt must be in [0, 4]");
+    if (p->n_ckpt < 0 || p->n_ckpt > 16) return fail(DT_ERR_ARG, "n_ckpt must be in [0, 16]");
     if (!out->stop) return fail(DT_ERR_ARG, "stop output required");
   } else {
     return fail(DT_ERR_ARG, "unknown policy %d", policy);
@@ -369,10 +390,10 @@ int dt_rerank(dt_handle* h, const int32_t* m, int32_t m_len, int32_t m_cap, int3
   return DT_OK;
 }
 
-int dt_graft_retrieve(dt_handle* h, const int32_t* M, const int32_t* m_draft, int32_t K_total,
-                      const dt_template* tpl, int32_t R_cap, int32_t* ret_token, int32_t* ret_parent,
-                      int32_t* ret_count, cudaStream_t s) {
-  if (!h || !M || !m_draft || !tpl || !ret_token || !ret_parent || !ret_count)
+int dt_graft_retrieve(dt_handle* h, const int32_t* M, const dt_template* tpl, int32_t R_cap, const int32_t* selected,
+                      int32_t m_cap, int32_t* ret_token, int32_t* ret_parent, int32_t* ret_count,
+                      int32_t* ret_anchor, cudaStream_t s) {
+  if (!h || !M || !tpl || !ret_token || !ret_parent || !ret_count)
     return fail(DT_ERR_ARG, "dt_graft_retrieve: null argument");
   if (h->B < 1) return fail(DT_ERR_ARG, "dt_graft_retrieve: no tree (call dt_tree_reset)");
   if (tpl->n < 0 || tpl->n > 256) return fail(DT_ERR_ARG, "template size must be in [0, 256]");
@@ -381,17 +402,21 @@ int dt_graft_retrieve(dt_handle* h, const int32_t* M, const int32_t* m_draft, in
     if (tpl->parent[u] < -1 || tpl->parent[u] >= u) return fail(DT_ERR_ARG, "template parent[%d] invalid", u);
     if (tpl->rank[u] < 0 || tpl->rank[u] >= 8) return fail(DT_ERR_ARG, "template rank[%d] invalid", u);
   }
+  if (tpl->anchor != DT_ANCHOR_ROOT && tpl->anchor != DT_ANCHOR_TAIL)
+    return fail(DT_ERR_ARG, "template anchor must be DT_ANCHOR_ROOT or DT_ANCHOR_TAIL");
+  if (tpl->anchor == DT_ANCHOR_TAIL && (!selected || m_cap < 1 || m_cap > h->N - 1))
+    return fail(DT_ERR_ARG, "a tail-anchored template needs selected and m_cap in [1, N-1]");
   if (R_cap < 1 || R_cap > dt::kMaxP) return fail(DT_ERR_ARG, "R_cap must be in [1, 512]");
-  if (K_total < 0) return fail(DT_ERR_ARG, "K_total must be >= 0");
-  cudaError_t e = dt::launch_graft_retrieve(h, M, m_draft, K_total, tpl, R_cap, ret_token, ret_parent,
-                                            ret_count, s);
+  cudaError_t e = dt::launch_graft_retrieve(h, M, tpl, R_cap, selected, m_cap, ret_token, ret_parent, ret_count,
+                                            ret_anchor, s);
   if (e != cudaSuccess) return cuda_fail(e, "dt_graft_retrieve");
   return DT_OK;
 }
 
 int dt_build_tree_meta(dt_handle* h, const int32_t* selected, int32_t m_cap, const int32_t* ret_token,
-                       const int32_t* ret_parent, const int32_t* ret_count, int32_t R_cap,
-                       const int32_t* pos_offset, const dt_tree_meta* meta, cudaStream_t s) {
+                       const int32_t* ret_parent, const int32_t* ret_count, const int32_t* ret_anchor,
+                       int32_t R_cap, int32_t K_total, const int32_t* pos_offset, const dt_tree_meta* meta,
+                       cudaStream_t s) {
   if (!h || !selected || !meta) return fail(DT_ERR_ARG, "dt_build_tree_meta: null argument");
   if (h->B < 1) return fail(DT_ERR_ARG, "dt_build_tree_meta: no tree (call dt_tree_reset)");
   if (!meta->tokens || !meta->parents || !meta->depth || !meta->node_id || !meta->mask ||
@@ -403,8 +428,9 @@ int dt_build_tree_meta(dt_handle* h, const int32_t* selected, int32_t m_cap, con
   const bool graft = ret_token != nullptr;
   if (graft && (!ret_parent || !ret_count || R_cap < 1)) return fail(DT_ERR_ARG, "retrieval arrays incomplete");
   if (1 + m_cap > meta->P) return fail(DT_ERR_ARG, "1 + m_cap exceeds P");
-  cudaError_t e = dt::launch_build_meta(h, selected, m_cap, ret_token, ret_parent, ret_count, graft ? R_cap : 0,
-                                        pos_offset, meta, s);
+  cudaError_t e = dt::launch_build_meta(h, selected, m_cap, ret_token, ret_parent, ret_count,
+                                        graft ? ret_anchor : nullptr, graft ? R_cap : 0, K_total, pos_offset, meta,
+                                        s);
   if (e != cudaSuccess) return cuda_fail(e, "dt_build_tree_meta");
   return DT_OK;
 }
@@ -413,7 +439,9 @@ static int check_verify_args(const dt_handle* h, const char* who, const dt_tree_
                              int64_t ld, int32_t mode) {
   if (!meta || !logits) return fail(DT_ERR_ARG, "%s: null argument", who);
   if (h->B < 1) return fail(DT_ERR_ARG, "%s: no tree (call dt_tree_reset)", who);
-  if (mode != DT_GREEDY && mode != DT_SAMPLE) return fail(DT_ERR_ARG, "mode must be DT_GREEDY or DT_SAMPLE");
+  const int32_t base_mode = mode & ~DT_VERIFY_PACKED;
+  if (base_mode != DT_GREEDY && base_mode != DT_SAMPLE)
+    return fail(DT_ERR_ARG, "mode must be DT_GREEDY or DT_SAMPLE, optionally | DT_VERIFY_PACKED");
   if (meta->P < 1 || meta->P > h->cfg.P_max) return fail(DT_ERR_ARG, "meta P must be in [1, P_max]");
   if (meta->D_path < 1 || meta->D_path > 64) return fail(DT_ERR_ARG, "D_path must be in [1, 64]");
   if (ld < h->cfg.V) return fail(DT_ERR_ARG, "ld < V");
@@ -469,7 +497,7 @@ int dt_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta, const int3
 int dt_commit_kv(dt_handle* h, const void* tmp_kv, int64_t tmp_pos_stride, int64_t tmp_req_stride, int32_t P,
                  void* cache, int64_t cache_pos_stride, int64_t cache_req_stride, int32_t L_max, int64_t row_bytes,
                  int32_t* cache_len, const int32_t* accept_len, const int32_t* accept_path, int32_t D_path,
-                 cudaStream_t s) {
+                 const int32_t* tmp_row_off, cudaStream_t s) {
   if (!h || !tmp_kv || !cache || !cache_len || !accept_len || !accept_path)
     return fail(DT_ERR_ARG, "dt_commit_kv: null argument");
   if (h->B < 1) return fail(DT_ERR_ARG, "dt_commit_kv: no tree (call dt_tree_reset)");
@@ -478,14 +506,14 @@ int dt_commit_kv(dt_handle* h, const void* tmp_kv, int64_t tmp_pos_stride, int64
   if (!aligned(tmp_kv, 16) || !aligned(cache, 16) || tmp_pos_stride % 16 || tmp_req_stride % 16 ||
       cache_pos_stride % 16 || cache_req_stride % 16 || row_bytes % 16)
     return fail(DT_ERR_ARG, "dt_commit_kv: pointers, strides and row_bytes must be multiples of 16 bytes");
-  if (tmp_pos_stride < row_bytes || cache_pos_stride < row_bytes || tmp_req_stride < tmp_pos_stride * P ||
-      cache_req_stride < cache_pos_stride * L_max)
+  if (tmp_pos_stride < row_bytes || cache_pos_stride < row_bytes ||
+      (!tmp_row_off && tmp_req_stride < tmp_pos_stride * P) || cache_req_stride < cache_pos_stride * L_max)
     return fail(DT_ERR_ARG, "dt_commit_kv: strides smaller than the rows they hold");
-  if (!aligned(cache_len, 4) || !aligned(accept_len, 4) || !aligned(accept_path, 4))
+  if (!aligned(cache_len, 4) || !aligned(accept_len, 4) || !aligned(accept_path, 4) || !aligned(tmp_row_off, 4))
     return fail(DT_ERR_ARG, "dt_commit_kv: int32 arrays must be 4-byte aligned");
   cudaError_t e = dt::launch_commit_kv(h, tmp_kv, tmp_pos_stride, tmp_req_stride, P, cache, cache_pos_stride,
                                        cache_req_stride, L_max, row_bytes, cache_len, accept_len, accept_path,
-                                       D_path, s);
+                                       D_path, tmp_row_off, s);
   if (e != cudaSuccess) return cuda_fail(e, "dt_commit_kv");
   return DT_OK;
 }

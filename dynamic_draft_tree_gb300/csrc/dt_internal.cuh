@@ -51,6 +51,7 @@ struct CastState {
 
 // Sampled walk result handed to the bonus kernel.
 struct WalkState {
+  int64_t row;        // its row of the target logits (padded or packed layout)
   int32_t cur;        // position whose residual is sampled
   int32_t n_rej;      // rejected tokens at that position
   int32_t rej[kMaxP];
@@ -63,6 +64,7 @@ struct Workspace {
   int32_t* node_depth;
   float* logc;
   float* value;
+  float2* node_dd;       // [B_max][N] log c of a block layer's child as a double-float (block expansion)
   int32_t* layer_order;
   float* layer_val;      // [B_max][D_max+1][LW] value of layer_order's node at the same place
   int32_t* layer_tok;    // [B_max][D_max+1][LW] token of layer_order's node at the same place
@@ -142,12 +144,15 @@ cudaError_t launch_cast_verify_rerank(dt_handle* h, const dt_prune_params* p, co
                                      int32_t* selected, cudaStream_t s);
 cudaError_t launch_cast_prune_select(dt_handle* h, const dt_prune_params* p, const dt_prune_out* out,
                                      int32_t* frontier_token, cudaStream_t s);
-cudaError_t launch_graft_retrieve(dt_handle* h, const int32_t* M, const int32_t* m_draft, int K_total,
-                                  const dt_template* tpl, int R_cap, int32_t* ret_token,
-                                  int32_t* ret_parent, int32_t* ret_count, cudaStream_t s);
+cudaError_t launch_graft_retrieve(dt_handle* h, const int32_t* M, const dt_template* tpl, int R_cap,
+                                  const int32_t* selected, int m_cap, int32_t* ret_token, int32_t* ret_parent,
+                                  int32_t* ret_count, int32_t* ret_anchor, cudaStream_t s);
 cudaError_t launch_build_meta(dt_handle* h, const int32_t* selected, int m_cap, const int32_t* ret_token,
-                              const int32_t* ret_parent, const int32_t* ret_count, int R_cap,
-                              const int32_t* pos_offset, const dt_tree_meta* meta, cudaStream_t s);
+                              const int32_t* ret_parent, const int32_t* ret_count, const int32_t* ret_anchor,
+                              int R_cap, int K_total, const int32_t* pos_offset, const dt_tree_meta* meta,
+                              cudaStream_t s);
+cudaError_t launch_block_expand(dt_handle* h, const void* logits, int64_t ld, int L, const dt_prune_params* p,
+                                const dt_prune_out* out, cudaStream_t s);
 cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int mode,
                           uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path,
                           int32_t* bonus, int32_t* top8, cudaStream_t s);
@@ -166,7 +171,8 @@ int row_pass_smax(int K);
 cudaError_t launch_commit_kv(dt_handle* h, const void* tmp_kv, int64_t tmp_pos_stride, int64_t tmp_req_stride, int P,
                              void* cache, int64_t cache_pos_stride, int64_t cache_req_stride, int L_max,
                              int64_t row_bytes, int32_t* cache_len, const int32_t* accept_len,
-                             const int32_t* accept_path, int D_path, cudaStream_t s);
+                             const int32_t* accept_path, int D_path, const int32_t* tmp_row_off,
+                             cudaStream_t s);
 cudaError_t launch_row_topk_static(const void* logits, int64_t ld, int rows, int V, int K, int dtype, float* logp,
                                    int32_t* ids, int32_t* status, cudaStream_t s);
 
@@ -176,6 +182,7 @@ cudaError_t init_tree_attributes();
 cudaError_t init_verify_attributes();
 cudaError_t init_select_attributes();
 cudaError_t init_meta_attributes();
+cudaError_t init_block_attributes();
 
 
 }  // namespace dt

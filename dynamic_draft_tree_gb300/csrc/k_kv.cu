@@ -27,10 +27,13 @@ struct KvArgs {
   const int32_t* cache_len;
   const int32_t* accept_len;
   const int32_t* accept_path;
+  const int32_t* tmp_row_off;    // [B+1] packed temporary rows (row_off[b] + i), or null: [B][P]
   int32_t* len_out;              // cache_len updated by the second kernel
 };
 
 constexpr int kKvThreads = 256;
+constexpr int kKvPer = 8;                         // 16-byte vectors per thread
+constexpr int kKvChunk = kKvThreads * kKvPer;     // vectors per CTA (32 KB)
 
 // Request b commits n = accept_len[b] + 1 rows when they fit (len0 + n <= L_max) and its path is valid.
 __device__ __forceinline__ bool kv_commit_ok(const KvArgs& a, int b, int& n, int& len0) {
@@ -39,7 +42,7 @@ __device__ __forceinline__ bool kv_commit_ok(const KvArgs& a, int b, int& n, int
   return n >= 1 && n <= a.D_path && len0 >= 0 && (int64_t)len0 + n <= a.L_max;
 }
 
-// Grid: B * D_path * chunks CTAs; CTA (b, j, c) copies chunk c of the j-th committed row of b.
+// Grid: B * D_path * chunks CTAs; CTA (b, j, c) copies chunk c (32 KB) of the j-th committed row of b.
 __global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(KvArgs a) {
   pdl_begin();
   const int c = (int)(blockIdx.x % a.chunks);
@@ -53,15 +56,28 @@ __global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(KvArgs a) {
   }
   if (j >= n) return;
   const int pos = a.accept_path[(int64_t)b * a.D_path + j];
-  if (pos < 0 || pos >= a.P) {
+  const int rows_b = a.tmp_row_off ? a.tmp_row_off[b + 1] - a.tmp_row_off[b] : a.P;
+  if (pos < 0 || pos >= a.P || pos >= rows_b) {
     if (c == 0 && threadIdx.x == 0) set_status(a.ws.status, DT_DEV_BAD_TREE);
     return;
   }
-  const uint4* src = a.tmp + b * a.tmp_req + pos * a.tmp_pos;
+  const uint4* src = a.tmp_row_off ? a.tmp + ((int64_t)a.tmp_row_off[b] + pos) * a.tmp_pos
+                                   : a.tmp + b * a.tmp_req + pos * a.tmp_pos;
   uint4* dst = a.cache + b * a.cache_req + (int64_t)(len0 + j) * a.cache_pos;
-  const int64_t per = (a.nv + a.chunks - 1) / a.chunks;
-  const int64_t v0 = (int64_t)c * per, v1 = min(a.nv, v0 + per);
-  for (int64_t v = v0 + threadIdx.x; v < v1; v += kKvThreads) __stcs(dst + v, __ldcs(src + v));
+  // chunk c: vectors [c * kKvChunk, (c + 1) * kKvChunk); each thread loads its eight vectors before it
+  // stores any (independent loads in flight, not a load-store chain)
+  const int64_t v0 = (int64_t)c * kKvChunk + threadIdx.x;
+  uint4 r[kKvPer];
+#pragma unroll
+  for (int u = 0; u < kKvPer; ++u) {
+    const int64_t v = v0 + (int64_t)u * kKvThreads;
+    if (v < a.nv) r[u] = __ldcs(src + v);
+  }
+#pragma unroll
+  for (int u = 0; u < kKvPer; ++u) {
+    const int64_t v = v0 + (int64_t)u * kKvThreads;
+    if (v < a.nv) __stcs(dst + v, r[u]);
+  }
 }
 
 // cache_len[b] += accept_len[b] + 1 for every request whose rows were committed.
@@ -78,7 +94,8 @@ __global__ void kv_len_kernel(KvArgs a, int B) {
 cudaError_t launch_commit_kv(dt_handle* h, const void* tmp_kv, int64_t tmp_pos_stride, int64_t tmp_req_stride, int P,
                              void* cache, int64_t cache_pos_stride, int64_t cache_req_stride, int L_max,
                              int64_t row_bytes, int32_t* cache_len, const int32_t* accept_len,
-                             const int32_t* accept_path, int D_path, cudaStream_t s) {
+                             const int32_t* accept_path, int D_path, const int32_t* tmp_row_off,
+                             cudaStream_t s) {
   KvArgs a;
   a.ws = h->ws;
   a.tmp = reinterpret_cast<const uint4*>(tmp_kv);
@@ -91,13 +108,16 @@ cudaError_t launch_commit_kv(dt_handle* h, const void* tmp_kv, int64_t tmp_pos_s
   a.L_max = L_max;
   a.nv = row_bytes / 16;
   a.D_path = D_path;
-  // about 4096 vectors (64 KB) per CTA, at most 64 CTAs per row
-  a.chunks = (int)std::max<int64_t>(1, std::min<int64_t>(64, (a.nv + 4095) / 4096));
+  const int64_t chunks = std::max<int64_t>(1, (a.nv + kKvChunk - 1) / kKvChunk);
+  if (chunks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+  a.chunks = (int)chunks;
   a.cache_len = cache_len;
   a.accept_len = accept_len;
   a.accept_path = accept_path;
+  a.tmp_row_off = tmp_row_off;
   a.len_out = cache_len;
   const int64_t grid = (int64_t)h->B * D_path * a.chunks;
+  if (grid > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;  // rows of more than ~2^31 / (B D_path) x 32 KB
   launch_k(kv_commit_kernel, dim3((unsigned)grid), dim3(kKvThreads), 0, s, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

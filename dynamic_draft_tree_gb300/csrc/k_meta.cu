@@ -18,9 +18,18 @@ struct MetaArgs {
   const int32_t* ret_token;
   const int32_t* ret_parent;
   const int32_t* ret_count;
+  const int32_t* ret_anchor;  // [B] draft node the template root stands for, or null (the root)
+  int K_total;                // > 0: at most K_total - selected nodes retrieved ones are used
   const int32_t* pos_offset;
   dt_tree_meta meta;
 };
+
+// Retrieved nodes request b uses when it keeps n selected draft nodes.
+__device__ __forceinline__ int used_retrieved(const MetaArgs& a, int b, int n) {
+  int rc = a.ret_count ? max(0, min(a.ret_count[b], a.R_cap)) : 0;
+  if (a.K_total > 0) rc = min(rc, max(0, a.K_total - n));
+  return rc;
+}
 
 constexpr int kMetaThreads = 512;
 constexpr int kWords = kMaxP / 32;
@@ -33,7 +42,7 @@ __global__ void __launch_bounds__(kMetaThreads) build_meta_kernel(MetaArgs a) {
   __shared__ uint32_t anc[kMaxP][kWords];
   __shared__ int32_t has_child[kMaxP];
   __shared__ int32_t leaf_idx[kMaxP];
-  __shared__ int32_t s_nsel, s_npos, s_bad, s_rc;
+  __shared__ int32_t s_nsel, s_npos, s_bad, s_rc, s_off;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const Workspace& ws = a.ws;
@@ -44,10 +53,7 @@ __global__ void __launch_bounds__(kMetaThreads) build_meta_kernel(MetaArgs a) {
   if (tid == 0) {
     s_nsel = a.m_cap;
     s_bad = 0;
-  }
-  if (tid == 32) {
-    const int rc = a.ret_count ? a.ret_count[b] : 0;
-    s_rc = max(0, min(rc, a.R_cap));
+    s_off = 0;
   }
   for (int i = tid; i < P; i += blockDim.x) has_child[i] = 0;
   __syncthreads();
@@ -57,12 +63,30 @@ __global__ void __launch_bounds__(kMetaThreads) build_meta_kernel(MetaArgs a) {
   __syncthreads();
   if (tid == 0) {
     const int n = s_nsel;
-    const int rc = s_rc;
+    const int rc = used_retrieved(a, b, n);
+    s_rc = rc;
     s_npos = min(P, 1 + n + rc);
     if (1 + n + rc > P) s_bad = 1;  // positions would not fit: flagged, the extra ones dropped
   }
   __syncthreads();
   const int nsel = s_nsel, npos = s_npos;
+  if (a.meta.row_off) {
+    // packed row offset: the positions of requests 0..b-1, counted as their own CTAs count them (root +
+    // the selected entries before the first -1 + the retrieved nodes, at most P); one warp per request
+    const int lane = tid & 31;
+    for (int bb = tid >> 5; bb < b; bb += kMetaThreads / 32) {
+      int n = a.m_cap;
+      for (int c = 0; c < a.m_cap; c += 32) {
+        const bool neg = c + lane < a.m_cap && a.selected[(int64_t)bb * a.m_cap + c + lane] < 0;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, neg);
+        if (m) {
+          n = c + __ffs(m) - 1;
+          break;
+        }
+      }
+      if (lane == 0) atomicAdd(&s_off, min(P, 1 + n + used_retrieved(a, bb, n)));
+    }
+  }
   if (tid == 0) pos_of[0] = 0;
   for (int j = tid; j < nsel; j += blockDim.x) {
     const int id = a.selected[(int64_t)b * a.m_cap + j];
@@ -94,7 +118,18 @@ __global__ void __launch_bounds__(kMetaThreads) build_meta_kernel(MetaArgs a) {
       const int u = p - nsel - 1;
       t = a.ret_token[(int64_t)b * a.R_cap + u];
       const int rp = a.ret_parent[(int64_t)b * a.R_cap + u];
-      pp = rp < 0 ? 0 : nsel + 1 + rp;
+      int ap = 0;  // position of the template root: the root, or the anchor draft node
+      if (a.ret_anchor) {
+        const int an = a.ret_anchor[b];
+        if (an > 0) {
+          ap = an < a.N ? pos_of[an] : -1;
+          if (ap < 0) {  // the anchor was not kept
+            s_bad = 1;
+            ap = 0;
+          }
+        }
+      }
+      pp = rp < 0 ? ap : nsel + 1 + rp;
       if (pp >= p) {
         s_bad = 1;
         pp = 0;
@@ -182,6 +217,10 @@ __global__ void __launch_bounds__(kMetaThreads) build_meta_kernel(MetaArgs a) {
   __syncthreads();
   if (tid == 0) {
     a.meta.n_pos[b] = npos;
+    if (a.meta.row_off) {
+      a.meta.row_off[b] = s_off;
+      if (b == (int)gridDim.x - 1) a.meta.row_off[b + 1] = s_off + npos;
+    }
     if (s_bad) set_status(ws.status, DT_DEV_BAD_TREE);
   }
 }
@@ -194,8 +233,9 @@ cudaError_t init_meta_attributes() {
 }
 
 cudaError_t launch_build_meta(dt_handle* h, const int32_t* selected, int m_cap, const int32_t* ret_token,
-                              const int32_t* ret_parent, const int32_t* ret_count, int R_cap,
-                              const int32_t* pos_offset, const dt_tree_meta* meta, cudaStream_t s) {
+                              const int32_t* ret_parent, const int32_t* ret_count, const int32_t* ret_anchor,
+                              int R_cap, int K_total, const int32_t* pos_offset, const dt_tree_meta* meta,
+                              cudaStream_t s) {
   MetaArgs a;
   a.ws = h->ws;
   a.N = h->N;
@@ -205,6 +245,8 @@ cudaError_t launch_build_meta(dt_handle* h, const int32_t* selected, int m_cap, 
   a.ret_token = ret_token;
   a.ret_parent = ret_parent;
   a.ret_count = ret_token ? ret_count : nullptr;
+  a.ret_anchor = ret_token ? ret_anchor : nullptr;
+  a.K_total = ret_token ? K_total : 0;
   a.pos_offset = pos_offset;
   a.meta = *meta;
   const size_t smem = ((size_t)h->N * sizeof(int16_t) + 15) / 16 * 16;

@@ -143,30 +143,13 @@ __global__ void __launch_bounds__(kRowThreads, 4) expand_kernel(ExpandArgs a) {
     if (tid == 0 && (st.nan || !(M > -INFINITY) || M == INFINITY || !(st.s_hi > 0.0f) || st.s_hi == INFINITY))
       set_status(ws.status, DT_DEV_BAD_LOGITS);
     if (tid < a.K) {
-      // log S as a double-float: S = mant * 2^e with mant in [1, 2) (exact scaling), log S =
-      // e * ln2 (Cody-Waite split: e * LN2_HI is exact for |e| < 2^9) + log(mant_hi) + mant_lo / mant_hi
-      constexpr float LN2_HI = 0.693145751953125f, LN2_LO = 1.4286068203094173e-06f;
-      float lh, ll;
-      const float sh = st.s_hi, sl = st.s_lo;
-      if (sh > 0.0f && sh < INFINITY) {
-        const int e = (int)((__float_as_uint(sh) >> 23) & 0xFF) - 127;
-        const float scale = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
-        const float mh = __fmul_rn(sh, scale), ml = __fmul_rn(sl, scale);
-        const float lm = __fadd_rn(logf(mh), __fdiv_rn(ml, mh));
-        two_sum(__fmul_rn((float)e, LN2_HI), fmaf((float)e, LN2_LO, lm), lh, ll);
-      } else {
-        lh = logf(sh);
-        ll = 0.0f;
-      }
       const uint64_t k = sm.topk[tid];
       const int id = a.base + f * a.K + tid;
       const int64_t gi = (int64_t)b * a.N + id;
-      const float x = key_value(k);
       // log c = (x - M) - log S and value = value(parent) + log c, each kept as a double-float until
       // the final rounding
       float dh, dl;
-      two_sum(x, -M, dh, dl);
-      ff_add(dh, dl, -lh, -ll);
+      log_softmax_dd(st, key_value(k), dh, dl);
       const float lc = __fadd_rn(dh, dl);
       float vh = pval, vl = 0.0f;
       ff_add(vh, vl, dh, dl);

@@ -21,12 +21,14 @@ struct StreamArgs {
   int64_t Gtot;           // warps of the grid
   const int32_t* tokens;  // meta [B][P]
   const int32_t* n_pos;   // meta [B]
+  int packed;             // logits rows packed (row (b, i) = the pass's row j) instead of [B][P]
   int test_timeout;
 };
 
 // Streaming pass of the verify: request b's rows are its used positions i < n_pos[b] (a position
-// without a valid token is counted but not read); every warp leaves the statistics and top-K keys
-// (K = 1, or 8 for the Graft refresh) of the row pieces it reads.
+// without a valid token is counted but not read), numbered in request order, which is the packed
+// layout's row order; every warp leaves the statistics and top-K keys (K = 1, or 8 for the Graft
+// refresh) of the row pieces it reads.
 template <typename T, bool SOFTMAX>
 __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) verify_stream_kernel(StreamArgs a) {
   pdl_begin();
@@ -36,10 +38,10 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) verify_strea
   Workspace& ws = a.ws;
   const int lane = threadIdx.x & 31;
   auto cnt = [&](int b) -> int { return min(max(a.n_pos[b], 0), a.P); };
-  auto row_of = [&](int b, int i) -> const T* {
+  auto row_of = [&](int b, int i, int64_t j) -> const T* {
     const int64_t r = (int64_t)b * a.P + i;
     if (a.test_timeout || a.tokens[r] < 0) return nullptr;  // invalid token: row not needed
-    return reinterpret_cast<const T*>(a.logits) + r * a.ld;
+    return reinterpret_cast<const T*>(a.logits) + (a.packed ? j : r) * a.ld;
   };
   if (a.test_timeout && blockIdx.x == 0 && threadIdx.x == 0) set_status(ws.status, DT_DEV_TIMEOUT);
   stream_rows<T, SOFTMAX>(a.B, a.V, a.K, a.maxp, a.Gtot, wsm, ws.row_tau, cnt, row_of,
@@ -55,7 +57,7 @@ struct WalkArgs {
   dt_tree_meta meta;
   const void* logits;
   int64_t ld;
-  int B, P, V, dtype, mode;
+  int B, P, V, dtype, mode, packed;
   int K, maxp, esz, vecel;  // pieces of the streaming pass: keys per piece, pieces per row at most
   int64_t Gtot;             // warps of the streaming launch
   uint32_t key0, key1, r0, r1;
@@ -147,6 +149,7 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
   }
   __syncthreads();
   const int64_t rowA = s_A, rowbase = s_base;
+  const int64_t lrow0 = a.packed ? rowbase : rb;  // logits row of position 0
   const int64_t G = stream_warps(rowA, a.V, a.esz, a.Gtot, a.maxp);
   const PieceMap pm(rowA, a.V, G, a.vecel);
   for (int p = tid; p < npos; p += blockDim.x) ws.row_tau[rowbase + p] = 0ull;  // the pass is over
@@ -297,14 +300,14 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
       __syncthreads();
       const int st0 = s_state;
       if (st0 == 4) {  // the running residual lost too much to cancellation: recompute it exactly
-        const double v = residual_rescan(a, rb + cur, st.m, s_rej, s_nrej);
+        const double v = residual_rescan(a, lrow0 + cur, st.m, s_rej, s_nrej);
         if (tid == 0) s_sres = v;
         s_ref = v;
       }
       __syncthreads();
       if (tid == 0 && st0 != 3) {
         const int t = s_tok[child];
-        const float x = load_logit(a.logits, a.dtype, (rb + cur) * a.ld + t);
+        const float x = load_logit(a.logits, a.dtype, (lrow0 + cur) * a.ld + t);
         const float e = ex2((x - st.m) * kLog2e);
         const Philox4 w = philox4x32_10(a.r0, a.r1, (uint32_t)(512 * b + child), 0x80000000u, a.key0, a.key1);
         const double u = (double)(w.v[0] >> 8) * 5.9604644775390625e-08;  // 2^-24
@@ -335,6 +338,7 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
     // residual draw happens in the bonus kernel
     if (tid == 0) {
       WalkState* wsb = ws.walk + b;
+      wsb->row = lrow0 + cur;
       wsb->cur = cur;
       wsb->n_rej = s_nrej;
       for (int j = 0; j < s_nrej; ++j) wsb->rej[j] = s_rej[j];
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kBonusThreads) verify_bonus_kernel(BonusArgs a
   for (int j = tid; j < n_rej; j += blockDim.x) s_rej[j] = wsb->rej[j];
   if (tid == 0) s_best = 0ull;
   __syncthreads();
-  const int64_t r = (int64_t)b * a.P + cur;
+  const int64_t r = wsb->row;
   const int64_t v0 = (int64_t)seg * a.seg_len;
   const int64_t v1 = min((int64_t)a.V, v0 + a.seg_len);
   unsigned long long best = 0ull;
@@ -437,7 +441,10 @@ cudaError_t init_verify_attributes() {
 
 cudaError_t launch_verify_rows(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int mode,
                                int with_top8, cudaStream_t s) {
+  const int packed = (mode & DT_VERIFY_PACKED) ? 1 : 0;
+  mode &= ~DT_VERIFY_PACKED;
   StreamArgs ra;
+  ra.packed = packed;
   ra.ws = h->ws;
   ra.logits = logits;
   ra.ld = ld;
@@ -471,8 +478,11 @@ cudaError_t launch_verify_accept(dt_handle* h, const dt_tree_meta* meta, const v
   const int P = meta->P;
   const int V = h->cfg.V;
   const int esz = h->cfg.dtype == DT_BF16 ? 2 : 4;
+  const int packed = (mode & DT_VERIFY_PACKED) ? 1 : 0;
+  mode &= ~DT_VERIFY_PACKED;
   cudaError_t e;
   WalkArgs wa;
+  wa.packed = packed;
   wa.ws = h->ws;
   wa.meta = *meta;
   wa.logits = logits;

@@ -167,6 +167,27 @@ struct SoftmaxStat {
   bool nan;  // the sum was poisoned by a NaN
 };
 
+// log softmax(x) = (x - M) - log S of a row with statistics st, as a double-float (dh, dl).
+// log S: S = mant * 2^e with mant in [1, 2) (exact scaling), log S = e * ln2 (Cody-Waite split:
+// e * LN2_HI is exact for |e| < 2^9) + log(mant_hi) + mant_lo / mant_hi.
+__device__ __forceinline__ void log_softmax_dd(const SoftmaxStat& st, float x, float& dh, float& dl) {
+  constexpr float LN2_HI = 0.693145751953125f, LN2_LO = 1.4286068203094173e-06f;
+  float lh, ll;
+  const float sh = st.s_hi, sl = st.s_lo;
+  if (sh > 0.0f && sh < INFINITY) {
+    const int e = (int)((__float_as_uint(sh) >> 23) & 0xFF) - 127;
+    const float scale = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+    const float mh = __fmul_rn(sh, scale), ml = __fmul_rn(sl, scale);
+    const float lm = __fadd_rn(logf(mh), __fdiv_rn(ml, mh));
+    two_sum(__fmul_rn((float)e, LN2_HI), fmaf((float)e, LN2_LO, lm), lh, ll);
+  } else {
+    lh = logf(sh);
+    ll = 0.0f;
+  }
+  two_sum(x, -st.m, dh, dl);
+  ff_add(dh, dl, -lh, -ll);
+}
+
 // (h, l) * f for a float factor f, renormalised (the product's rounding error is kept by an fma).
 __device__ __forceinline__ void ff_scale(float& h, float& l, float f) {
   const float p = __fmul_rn(h, f);

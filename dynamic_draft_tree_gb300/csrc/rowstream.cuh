@@ -221,7 +221,8 @@ __device__ __forceinline__ void ring_issue(WarpStream& ws_, int nseg, int t) {
 }
 
 // The streaming pass of one launch, for warp g of the grid. cnt(b): rows of request b;
-// row_of(b, i): row i of request b, or null when it is not to be read (no partial is written);
+// row_of(b, i, j): row i of request b, the j-th row of the pass, or null when it is not to be read
+// (no partial is written);
 // publish(j, g, b, i, out): called by all lanes after each piece, with rg.list holding its keys.
 // The warp's range is described kMaxSeg pieces at a time; the ring runs on across the pieces of a
 // description.
@@ -256,7 +257,7 @@ __device__ void stream_rows(int B, int64_t V, int K, int maxp, int64_t Gtot, War
       sd.j = j;
       sd.b = b;
       sd.i = i;
-      const T* row = b < B ? row_of(b, i) : nullptr;
+      const T* row = b < B ? row_of(b, i, j) : nullptr;
       sd.row = row;
       sd.a0 = sd.s0;
       sd.nvec = 0;

@@ -8,11 +8,15 @@ steps (1)-(3)):
 
 By default a layer's expansion, its pruning and the next frontier are one call
 (dt_expand_prune_select, two kernels), and CAST's verify count and rerank are one call; with
-``fused=False`` every step is its own call.
+``fused=False`` every step is its own call. Graft's root-anchored retrieval is issued on a second
+stream right after the reset (it needs the root tokens and M only) and joined before the tree is
+flattened, so it runs beside the draft layers; a tail-anchored one follows the rerank. A block
+drafter (Graft with ``block``) builds all draft layers with one dt_block_expand call.
 
 The draft and target model forwards are outside the library: ``draft_rows(d,
 frontier_token)`` must return the logits tensor [B][F][V] of layer d (row f =
-the draft row of frontier slot f), and ``target_rows(meta)`` the tensor
+the draft row of frontier slot f), or for a block drafter, called once with d = 0,
+the block's rows [B][L][V]; ``target_rows(meta)`` the tensor
 [B][P][V] (row i = the target's next-token row after position i). Every call
 is asynchronous on the current stream; no host synchronisation happens inside
 a round, so a round can be captured in a CUDA graph.
@@ -21,19 +25,24 @@ import torch
 
 from . import (Handle, Meta, Template, make_prune_params, make_prune_out, dt_tree_reset, dt_select_frontier,
                dt_expand_layer, dt_expand_prune_select, dt_cast_prune, dt_cast_prune_select, dt_cast_verify_rerank, dt_rerank, dt_graft_retrieve, dt_build_tree_meta, dt_verify, dt_verify_rows,
-               dt_verify_accept, dt_adj_update, DT_GREEDY, DT_SAMPLE, DT_POLICY_CAST_WIDTH_DEPTH,
-               DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT, DT_POLICY_NONE)
+               dt_verify_accept, dt_adj_update, dt_block_expand, DT_GREEDY, DT_SAMPLE, DT_VERIFY_PACKED,
+               DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT, DT_POLICY_NONE,
+               DT_ANCHOR_ROOT, DT_ANCHOR_TAIL)
 
 
 class RoundRunner:
     """Device buffers and call sequence of one round for a policy ('eagle' | 'cast' | 'graft')."""
 
     def __init__(self, policy, B, V, K, k, D, P, D_path, m, dtype, T=0, cast=None, cast_tables=None,
-                 graft=None, template=None, flags=0, device="cuda", fused=True):
+                 graft=None, template=None, flags=0, device="cuda", fused=True, packed=False, block=False):
         """``fused``: each layer's expansion, pruning and next frontier as one call
         (dt_expand_prune_select), and CAST's verify count + rerank as one (dt_cast_verify_rerank),
-        instead of the separate calls."""
+        instead of the separate calls. ``packed``: the target rows are padding-free
+        (DT_VERIFY_PACKED): ``target_rows`` returns them at meta.row_off[b] + i. ``block`` (Graft):
+        the D draft layers come from a block drafter's rows in one dt_block_expand call."""
         self.fused = fused
+        self.packed = packed
+        self.block = block
         self.policy, self.B, self.V, self.K, self.k, self.D = policy, B, V, K, k, D
         self.P, self.D_path, self.T = P, D_path, T
         self.h = Handle(B, V, K, k, D, P, dtype, flags)
@@ -62,7 +71,11 @@ class RoundRunner:
         if policy == "graft":
             self.graft = graft
             self.R_cap = graft["K_total"]
-            self.template = Template(*template)
+            anchor = DT_ANCHOR_TAIL if graft.get("anchor", "root") == "tail" else DT_ANCHOR_ROOT
+            self.template = Template(*template, anchor=anchor)
+            self.ret_anchor = torch.zeros((B,), **i32)
+            self.retrieve_stream = torch.cuda.Stream(device=device) if anchor == DT_ANCHOR_ROOT else None
+            self.retrieved = torch.cuda.Event() if anchor == DT_ANCHOR_ROOT else None
             self.ret_token = torch.empty((B, self.R_cap), **i32)
             self.ret_parent = torch.empty((B, self.R_cap), **i32)
             self.ret_count = torch.empty((B,), **i32)
@@ -97,8 +110,24 @@ class RoundRunner:
         policy = {"cast": DT_POLICY_CAST_WIDTH_DEPTH, "graft": DT_POLICY_GRAFT_CHECKPOINT}.get(pol, DT_POLICY_NONE)
         width = None if pol == "cast" else self.width
         dt_tree_reset(h, roots)
-        dt_select_frontier(h, None, None, self.frontier_token)  # layer 0 = {root}: the root in slot 0
-        for d in range(1, self.D + 1):
+        tail = pol == "graft" and self.template.anchor == DT_ANCHOR_TAIL
+        if pol == "graft" and not tail:  # root-centred retrieval beside the draft layers (Graft step (2))
+            main = torch.cuda.current_stream()
+            self.retrieve_stream.wait_stream(main)
+            with torch.cuda.stream(self.retrieve_stream):
+                dt_graft_retrieve(h, M, self.template, self.R_cap, self.ret_token, self.ret_parent, self.ret_count,
+                                  ret_anchor=self.ret_anchor)
+                self.retrieved.record(self.retrieve_stream)
+        if self.block:  # a block drafter: every draft layer from one set of rows, gated per position
+            rows = draft_rows(0, None)
+            if timing is not None:
+                timing.start("expand")
+            dt_block_expand(h, rows, self.D, self.params, self.prune_out)
+            if timing is not None:
+                timing.stop("expand")
+        else:
+            dt_select_frontier(h, None, None, self.frontier_token)  # layer 0 = {root}: the root in slot 0
+        for d in range(1, 0 if self.block else self.D + 1):
             F = 1 if d == 1 else self.k
             if d > 1 and not self.fused:
                 dt_select_frontier(h, self.width, self.stop, self.frontier_token)
@@ -133,14 +162,18 @@ class RoundRunner:
                 dt_cast_prune(h, DT_POLICY_CAST_VERIFY, self.params, self.verify_out)
             dt_rerank(h, self.m_dev, self.m_cap, self.selected)
         if pol == "graft":
-            dt_graft_retrieve(h, M, self.m_dev, self.graft["K_total"], self.template, self.R_cap, self.ret_token,
-                              self.ret_parent, self.ret_count)
+            if tail:
+                dt_graft_retrieve(h, M, self.template, self.R_cap, self.ret_token, self.ret_parent, self.ret_count,
+                                  selected=self.selected, m_cap=self.m_cap, ret_anchor=self.ret_anchor)
+            else:
+                torch.cuda.current_stream().wait_event(self.retrieved)
             dt_build_tree_meta(h, self.selected, self.m_cap, self.meta, self.pos_offset, self.ret_token,
-                               self.ret_parent, self.ret_count, self.R_cap)
+                               self.ret_parent, self.ret_count, self.R_cap, ret_anchor=self.ret_anchor,
+                               K_total=self.graft["K_total"])
         else:
             dt_build_tree_meta(h, self.selected, self.m_cap, self.meta, self.pos_offset)
         logits = target_rows(self.meta)
-        mode = DT_SAMPLE if self.T == 1 else DT_GREEDY
+        mode = (DT_SAMPLE if self.T == 1 else DT_GREEDY) | (DT_VERIFY_PACKED if self.packed else 0)
         if timing is not None:
             timing.start("verify_rows")
             dt_verify_rows(h, self.meta, logits, mode, self.top8 is not None)

@@ -52,6 +52,11 @@ extern "C" {
 enum { DT_OK = 0, DT_ERR_ARG = -1, DT_ERR_CUDA = -2, DT_ERR_DEVICE = -3, DT_ERR_DEVICE_TIMEOUT = -4 };
 enum { DT_BF16 = 0, DT_F32 = 1 };
 enum { DT_GREEDY = 0, DT_SAMPLE = 1 };
+/* OR-ed into the verify mode: padding-free target rows. Request b's used rows are packed after those
+ * of requests 0..b-1: row (b, i) is row row_off[b] + i of the logits buffer, with
+ * row_off[b] = n_pos[0] + ... + n_pos[b-1] (dt_tree_meta.row_off), so a ragged batch's target
+ * forward computes and stores sum_b n_pos[b] rows instead of B * P. */
+enum { DT_VERIFY_PACKED = 2 };
 enum {
   DT_POLICY_CAST_WIDTH_DEPTH = 0, /* CAST width n_d and grow/stop after layer d */
   DT_POLICY_CAST_VERIFY = 1,      /* CAST batch-wide verify count m            */
@@ -121,10 +126,10 @@ typedef struct {
   int32_t m_cap;      /* largest verify count m, <= N_cols                                     */
   int32_t D_max;      /* last layer: no growth after it                                        */
   /* Graft */
-  int32_t n_ckpt;       /* number of checkpoints, 0..4                                         */
-  int32_t ckpt_layer[4];/* checkpoint layer indices (layer index 0 = draft layer 1)            */
-  double tau[4];        /* confidence thresholds: request continues iff exp(max value) > tau   */
-  int32_t k_draft[4];   /* draft nodes kept when stopped at checkpoint s                       */
+  int32_t n_ckpt;        /* number of checkpoints, 0..16 (a block drafter may gate every position) */
+  int32_t ckpt_layer[16];/* checkpoint layer indices (layer index 0 = draft layer 1)            */
+  double tau[16];        /* confidence thresholds: request continues iff exp(max value) > tau   */
+  int32_t k_draft[16];   /* draft nodes kept when stopped at checkpoint s                       */
   int32_t K_total;      /* K_max: draft + retrieved nodes per request                         */
   /* CAST, per-request rule (CAST page §局限与展望: padded equal-length batches are a limit of the
    * batch rule): nonzero = every request applies the width/depth and verify-count rules to its own
@@ -143,12 +148,18 @@ typedef struct {
   int32_t* stage; /* [B]  GRAFT: checkpoint index that stopped the request, n_ckpt if none  */
 } dt_prune_out;
 
+/* Template anchors (Graft page: root-grafted G_ret^root and tail-grafted G_ret^tail templates). */
+enum { DT_ANCHOR_ROOT = 0, DT_ANCHOR_TAIL = 1 };
 /* Retrieval template (host arrays), nodes in breadth-first order:
- * parent[u] in [-1, u) (-1 = the root), rank[u] in [0, 8): x_u = M[x_parent][rank]. n <= 256. */
+ * parent[u] in [-1, u) (-1 = the template root), rank[u] in [0, 8): x_u = M[x_parent][rank]. n <= 256.
+ * anchor: DT_ANCHOR_ROOT = the template root is the tree's root; DT_ANCHOR_TAIL = it is the deepest
+ * kept draft node (ties: value desc, then id asc), the end of the kept draft path (a block drafter's
+ * kept prefix). Any shape a caller designs or learns fits these arrays. */
 typedef struct {
   int32_t n;
   const int32_t* parent;
   const int32_t* rank;
+  int32_t anchor;
 } dt_template;
 
 /* Flattened verify tree (device arrays, caller-owned), P positions per request. */
@@ -164,6 +175,8 @@ typedef struct {
   int32_t* retrieve;     /* [B][P][D_path] root-to-leaf positions, -1 padded              */
   int32_t* n_leaves;     /* [B]                                                           */
   int32_t* n_pos;        /* [B] positions in use                                          */
+  int32_t* row_off;      /* [B+1] or NULL: exclusive prefix sums of n_pos (row_off[B] = total),
+                            the packed target-row offsets of DT_VERIFY_PACKED                */
 } dt_tree_meta;
 
 const char* dt_last_error_string(void);
@@ -229,6 +242,24 @@ int dt_expand_prune_select(dt_handle* h, const void* logits, int64_t ld, int32_t
                            const dt_prune_params* p, const dt_prune_out* out, const int32_t* width,
                            int32_t width_len, int32_t* frontier_token, cudaStream_t s);
 
+/* Block drafters (Graft page, extension direction 1; weakness 4: token-level confidence inside the
+ * block): draft layers 1..L in one call from a block drafter's rows. logits: device [B][L][V] of dtype,
+ * row (b, j) at element (b*L + j)*ld, the drafter's distribution for block position j + 1 (the same
+ * whatever tokens are picked at earlier positions). Layer j + 1 = the top-K tokens of row j (log c,
+ * ties and the DT_DEV_BAD_LOGITS rule as in dt_expand_layer), children of the block token at position
+ * j (the root for j = 0), the block token being the top node of its layer (value desc, id asc), i.e.
+ * the top-1 of its row; they occupy frontier slot 0's ids. Values: value(parent) + log c. With p and
+ * out (Graft checkpoint parameters and outputs, as dt_cast_prune with DT_POLICY_GRAFT_CHECKPOINT):
+ * the checkpoint rule after every layer; a request stopped after layer j keeps layers 1..j only
+ * (deeper slots invalid) and has no frontier; one that passes layer L gets stage n_ckpt and m =
+ * K_total (layer L plays the part of p->D_max); stop, stage and m are written for every request.
+ * p == NULL: no gate, L layers. Needs the tree right after dt_tree_reset, 1 <= L <= D_max and
+ * B * L <= B_max * max(W, P_max). The tree then has L layers; the frontier is the block token of
+ * layer L - 1 (the root if L = 1). One row pass over the B*L rows (the expansion's kernel design);
+ * the last row of a request to finish builds its layers, values, layer orders and gates. */
+int dt_block_expand(dt_handle* h, const void* logits, int64_t ld, int32_t L, const dt_prune_params* p,
+                    const dt_prune_out* out, cudaStream_t s);
+
 /* a3 + a2 in one launch: exactly dt_cast_prune(h, DT_POLICY_CAST_WIDTH_DEPTH, p, out, s) followed by
  * dt_select_frontier(h, out->width, 1, out->stop, frontier_token, s): CAST width and grow/stop after
  * the newest layer, then the next layer's frontier (none for stopped requests). One kernel instead of
@@ -248,26 +279,39 @@ int dt_cast_verify_rerank(dt_handle* h, const dt_prune_params* p, const dt_prune
 int dt_rerank(dt_handle* h, const int32_t* m, int32_t m_len, int32_t m_cap, int32_t* selected,
               cudaStream_t s);
 
-/* a6 (Graft step (2)): gather k_ret_b = min(K_total - min(m_draft[b], tree nodes of b), tpl->n,
- * R_cap) template nodes from M (device [B][V][8] int32, -1 = unset): token(u) =
- * M[b][token(parent(u))][rank(u)], -1 when the parent is invalid or the entry unset.
- * ret_token/ret_parent: device [B][R_cap] (parent = template parent index, -1 root, -2 unused),
- * ret_count: device [B]. */
-int dt_graft_retrieve(dt_handle* h, const int32_t* M, const int32_t* m_draft, int32_t K_total,
-                      const dt_template* tpl, int32_t R_cap, int32_t* ret_token, int32_t* ret_parent,
-                      int32_t* ret_count, cudaStream_t s);
+/* a6 (Graft step (2)): gather the retrieval envelope, the first e = min(tpl->n, R_cap) template nodes,
+ * from M (device [B][V][8] int32, -1 = unset): token(u) = M[b][token(parent(u))][rank(u)], the template
+ * root's token being that of the anchor; -1 when the parent is invalid or the entry unset. The cut to
+ * K_ret = K_total - kept draft nodes is made by dt_build_tree_meta. With DT_ANCHOR_ROOT the call
+ * depends on the root tokens and M only (selected may be NULL): it can be issued right after
+ * dt_tree_reset, on a second stream, while the draft layers are built (step (2): retrieval adds no
+ * serial stage). With DT_ANCHOR_TAIL it needs the kept draft nodes, selected (device [B][m_cap], as
+ * written by dt_rerank), and follows the rerank.
+ * ret_token/ret_parent: device [B][R_cap] (parent = template parent index, -1 the template root, -2
+ * unused); ret_count: device [B] (= e); ret_anchor: device [B] (the anchor's node id, 0 = the root) or
+ * NULL. */
+int dt_graft_retrieve(dt_handle* h, const int32_t* M, const dt_template* tpl, int32_t R_cap, const int32_t* selected,
+                      int32_t m_cap, int32_t* ret_token, int32_t* ret_parent, int32_t* ret_count,
+                      int32_t* ret_anchor, cudaStream_t s);
 
 /* a7 (EAGLE-2 §重排阶段; Graft step (3)): flatten and build the verify metadata. Position 0 is
  * the root, then selected nodes (device [B][m_cap], ascending id, -1 padded), then retrieved
- * nodes (ret_*: device, NULL when there is no graft) in template order. pos_offset: device [B]
+ * nodes (ret_*: device, NULL when there is no graft) in template order: the first
+ * min(ret_count[b], K_total - selected nodes) of them (all ret_count[b] when K_total <= 0), the
+ * template root's children hanging from the position of draft node ret_anchor[b] (NULL: the root;
+ * an anchor that is not selected sets DT_DEV_BAD_TREE and the root is used). pos_offset: device [B]
  * or NULL (0). Needs 1 + m_cap <= meta->P; a request whose root + selected + retrieved nodes
- * exceed P sets DT_DEV_BAD_TREE and keeps the first P positions. */
+ * exceed P sets DT_DEV_BAD_TREE and keeps the first P positions. meta->row_off, when not NULL,
+ * receives the packed row offsets (DT_VERIFY_PACKED). */
 int dt_build_tree_meta(dt_handle* h, const int32_t* selected, int32_t m_cap, const int32_t* ret_token,
-                       const int32_t* ret_parent, const int32_t* ret_count, int32_t R_cap,
-                       const int32_t* pos_offset, const dt_tree_meta* meta, cudaStream_t s);
+                       const int32_t* ret_parent, const int32_t* ret_count, const int32_t* ret_anchor,
+                       int32_t R_cap, int32_t K_total, const int32_t* pos_offset, const dt_tree_meta* meta,
+                       cudaStream_t s);
 
 /* a8 + a9 (EAGLE-2 §先把投机解码的账本摆清楚, §无损性…): verify against the target rows
- * logits: device [B][P][V], row (b, i) at element (b*P + i)*ld, the target row after position i.
+ * logits: device [B][P][V], row (b, i) at element (b*P + i)*ld, the target row after position i;
+ * with mode | DT_VERIFY_PACKED: device [sum_b n_pos[b]][V], row (b, i) at element
+ * (n_pos[0] + ... + n_pos[b-1] + i)*ld: a ragged batch without padding (CAST page §局限与展望).
  * DT_GREEDY: longest leaf path whose tokens equal the argmax (ties: lower id) of their parent's
  * row (ties: first path), bonus = argmax of the last accepted position's row.
  * DT_SAMPLE: from the root, children in position order are accepted with probability
@@ -308,6 +352,9 @@ int dt_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta, const int3
  *           rows per request; rows cache_len[b] .. cache_len[b] + accept_len[b] are written.
  *   row_bytes: bytes of one row (one token's keys and values of every layer). Every pointer, stride and
  *           row_bytes must be a multiple of 16 bytes (DT_ERR_ARG otherwise).
+ *   tmp_row_off: device [B+1] int32 or NULL. Not NULL: the temporary KV is packed like the target rows
+ *           of DT_VERIFY_PACKED: the row of position i of request b is at (tmp_row_off[b] + i) *
+ *           tmp_pos_stride (tmp_req_stride is ignored; dt_tree_meta.row_off gives the offsets).
  *   cache_len: device [B] int32, in/out: increased by accept_len[b] + 1.
  *   accept_len, accept_path: device, as written by dt_verify ([B], [B][D_path]).
  * A request whose rows would pass L_max, or whose accept_len + 1 exceeds D_path, commits nothing,
@@ -316,7 +363,7 @@ int dt_adj_update(dt_handle* h, int32_t* M, const dt_tree_meta* meta, const int3
 int dt_commit_kv(dt_handle* h, const void* tmp_kv, int64_t tmp_pos_stride, int64_t tmp_req_stride, int32_t P,
                  void* cache, int64_t cache_pos_stride, int64_t cache_req_stride, int32_t L_max, int64_t row_bytes,
                  int32_t* cache_len, const int32_t* accept_len, const int32_t* accept_path, int32_t D_path,
-                 cudaStream_t s);
+                 const int32_t* tmp_row_off, cudaStream_t s);
 
 /* Standalone row log-softmax top-K that allocates nothing. This entry point has no counterpart in
  * the method's pages: it is the expansion's row pass (EAGLE-2 §扩展阶段: the children of a node

@@ -107,7 +107,7 @@ def _gpu_lib():
         lib = ctypes.CDLL(GPU_LIB)
         lib.synth_gen_rows_gpu.argtypes = [ctypes.POINTER(SpecC), ctypes.c_uint64, ctypes.c_uint64,
                                            ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
-                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                            ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p]
         lib.synth_gen_rows_gpu.restype = ctypes.c_int
         _gpu = lib
@@ -184,15 +184,17 @@ def gen_rows_cpu(spec, seed, salt, stream, ctx, depth=None, depth_add=0, rows_pe
 
 
 def gen_rows_gpu(torch, spec, seed, salt, stream, ctx_dev, out_dev, ld, depth_dev=None, depth_add=0,
-                 rows_per_b=1, cuda_stream=None, salts_dev=None):
+                 rows_per_b=1, cuda_stream=None, salts_dev=None, row_req_dev=None):
     """Device rows into ``out_dev`` (row rr at element rr*ld); ctx/depth are device int32 tensors;
-    ``salts_dev`` (device int64 [B], optional) replaces ``salt`` per request."""
+    ``salts_dev`` (device int64 [B], optional) replaces ``salt`` per request; row rr belongs to
+    request rr // rows_per_b, or to ``row_req_dev[rr]`` (device int32 [R]) when given (packed rows)."""
     st = spec.c_struct_device(torch, salts_dev)
     cs = (cuda_stream or torch.cuda.current_stream()).cuda_stream
     R = ctx_dev.numel()
     rc = _gpu_lib().synth_gen_rows_gpu(ctypes.byref(st), seed, salt, stream, ctx_dev.data_ptr(),
                                        None if depth_dev is None else depth_dev.data_ptr(), depth_add,
-                                       rows_per_b, out_dev.data_ptr(), ld, R, cs)
+                                       rows_per_b, None if row_req_dev is None else row_req_dev.data_ptr(),
+                                       out_dev.data_ptr(), ld, R, cs)
     if rc != 0:
         raise RuntimeError(f"synth_gen_rows_gpu failed ({rc})")
 
@@ -205,3 +207,21 @@ def bf16_bits_to_f64(bits):
 
 def to_f64(rows, dtype):
     return bf16_bits_to_f64(rows) if dtype == BF16 else np.asarray(rows, np.float32).astype(np.float64)
+
+
+def packed_row_map(torch, row_off, tokens, depth):
+    """Per-row inputs of a padding-free target batch, on the device (graph-capturable, no sync).
+
+    row_off [B+1] (dt_tree_meta.row_off), tokens/depth [B][P] (the verify tree): for every row j of a
+    [B*P] buffer, the request b with row_off[b] <= j < row_off[b+1], the context token tokens[b][j -
+    row_off[b]] and its depth; rows past row_off[B] get token -1 (not generated). Returns int32
+    (row_req, ctx, depth) of length B*P."""
+    B, P = tokens.shape
+    j = torch.arange(B * P, device=tokens.device, dtype=torch.int64)
+    off = row_off.to(torch.int64)
+    b = torch.searchsorted(off[1:].contiguous(), j, right=True).clamp_(max=B - 1)
+    i = (j - off[b]).clamp_(0, P - 1)
+    valid = j < off[B]
+    ctx = torch.where(valid, tokens[b, i], torch.full_like(j, -1, dtype=tokens.dtype))
+    dep = torch.where(valid, depth[b, i], torch.zeros_like(j, dtype=depth.dtype))
+    return b.to(torch.int32), ctx.to(torch.int32).contiguous(), dep.to(torch.int32).contiguous()

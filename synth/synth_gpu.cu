@@ -90,14 +90,15 @@ constexpr int kPerThread = 8;
 
 __global__ void __launch_bounds__(kThreads) gen_rows_kernel(
     synth_spec sp, uint64_t seed, uint64_t salt, int32_t stream, const int32_t* __restrict__ ctx,
-    const int32_t* __restrict__ depth, int32_t depth_add, int32_t rows_per_b, void* out, int64_t ld) {
+    const int32_t* __restrict__ depth, int32_t depth_add, int32_t rows_per_b, const int32_t* __restrict__ row_req,
+    void* out, int64_t ld) {
   const int rr = blockIdx.y;
   __shared__ RowParams rp;
   if (threadIdx.x == 0) {
     const int32_t c = ctx[rr];
     rp.valid = c >= 0;
     if (rp.valid) {
-      const int64_t b = rr / rows_per_b;
+      const int64_t b = row_req ? row_req[rr] : rr / rows_per_b;
       if (sp.salts) salt = sp.salts[b];
       const int64_t dk = (int64_t)(depth ? depth[rr] : 0) + depth_add;
       const uint64_t r = hk(hk(hk(hk(seed, salt), (uint64_t)b), (uint64_t)dk), (uint64_t)c);
@@ -157,14 +158,14 @@ __global__ void __launch_bounds__(kThreads) gen_rows_kernel(
 
 extern "C" int synth_gen_rows_gpu(const synth_spec* sp, uint64_t seed, uint64_t salt, int32_t stream,
                                   const int32_t* ctx, const int32_t* depth, int32_t depth_add,
-                                  int32_t rows_per_b, void* out, int64_t ld, int32_t R,
-                                  cudaStream_t cs) {
+                                  int32_t rows_per_b, const int32_t* row_req, void* out, int64_t ld,
+                                  int32_t R, cudaStream_t cs) {
   if (R <= 0) return 0;
   if (sp == nullptr || ctx == nullptr || out == nullptr || rows_per_b <= 0 || sp->V < 2 || ld < sp->V)
     return -1;
   if (R > 65535) return -1;
   dim3 grid((unsigned)((sp->V + kThreads * kPerThread - 1) / (kThreads * kPerThread)), (unsigned)R);
   gen_rows_kernel<<<grid, kThreads, 0, cs>>>(*sp, seed, salt, stream, ctx, depth, depth_add, rows_per_b,
-                                              out, ld);
+                                              row_req, out, ld);
   return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }

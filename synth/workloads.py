@@ -1,4 +1,4 @@
-"""The five synthetic workloads (shapes, recipes and method parameters), as plain data.
+"""The synthetic workloads (shapes, recipes and method parameters), as plain data.
 
 Stand-ins for the pages' benchmark runs (MT-bench, HumanEval, GSM8K, Alpaca,
 CNN/DM, NQ, ShareGPT warm-up, LongBench): no dataset or trained model is used;
@@ -58,6 +58,17 @@ WORKLOADS = {
                   warmup_rounds=5,
                   recipe=dict(kind=0, sigma=2 ** 0.5, peak=(2.0, 8.0), per_request_height=False, depthkey=False),
                   graft=dict(ckpt_layers=[0, 1, 5], tau=[0.6, 0.4, 0.2], k_draft=[8, 24, 40], K_total=60)),
+    # Graft with a block drafter (DFlash-like, 16 positions per pass): Qwen3 vocabulary, the top-4
+    # alternatives at every block position, a gate at every position, K_max = 60, an 8 x 8 chain
+    # template hanging from the end of the kept block; block rows: Zipf(1.1) + N(0, 0.5^2) + a peak
+    # of height U[0, 10] per (request, position), so that confidence varies along the block
+    "graft_block": dict(policy="graft", block=True, B=16, V=151936, dtype=BF16, K=4, k=1, D=16, m=60, T=0, seed=6,
+                        rounds=200, warmup_rounds=5,
+                        recipe=dict(kind=2, sigma=0.5, zipf_s=1.1, peak=(0.0, 10.0), per_request_height=False,
+                                    depthkey=True),
+                        graft=dict(ckpt_layers=list(range(16)), tau=[0.05] * 4 + [0.1] * 12,
+                                   k_draft=[min(60, 4 * (j + 1)) for j in range(16)], K_total=60, anchor="tail",
+                                   template_shape=(8, 8))),
     # large-batch stress: fp32, half low-entropy (peak +U[6,12]) and half high-entropy (+U[0,2]), T = 1
     "stress": dict(policy="eagle", B=64, V=128256, dtype=F32, K=8, k=8, D=10, m=64, T=1, seed=5, rounds=500,
                    recipe=dict(kind=0, sigma=2 ** 0.5, peak=None, per_request_height=False, depthkey=True)),
@@ -83,12 +94,24 @@ def spec_for(w):
                 height_per_request=r["per_request_height"], B=B)
 
 
+def graft_template(w):
+    """(parent, rank) of a Graft workload's retrieval template: chains of template_shape = (width,
+    depth), by default (k, D)."""
+    width, depth = w["graft"].get("template_shape", (w["k"], w["D"]))
+    return chain_template(width, depth)
+
+
 def geometry(w):
     """Handle/meta sizes of a workload: W, D_max, P (positions), D_path, m_cap, R_cap."""
     pol = w["policy"]
     if pol == "graft":
         K_total = w["graft"]["K_total"]
-        return dict(W=w["k"], D_max=w["D"], P=K_total + 1, D_path=w["D"] + 2, m_cap=K_total, R_cap=K_total)
+        depth = w["graft"].get("template_shape", (w["k"], w["D"]))[1]
+        if w["graft"].get("anchor", "root") == "tail":  # the template may hang from the deepest layer
+            depth += w["D"]
+        nodes = w["K"] + (w["D"] - 1) * w["k"] * w["K"]  # draft nodes the tree can hold
+        return dict(W=w["k"], D_max=w["D"], P=K_total + 1, D_path=max(w["D"], depth) + 2, m_cap=min(K_total, nodes),
+                    R_cap=K_total)
     m_cap = w["cast"]["m_cap"] if pol == "cast" else w["m"]
     return dict(W=w["k"], D_max=w["D"], P=m_cap + 1, D_path=w["D"] + 1, m_cap=m_cap, R_cap=0)
 

@@ -11,7 +11,7 @@ Comparison rules:
 import numpy as np
 
 import synth
-from synth.workloads import spec_for, geometry, cast_tables, chain_template
+from synth.workloads import spec_for, geometry, cast_tables, graft_template
 from oracle.round import run_round
 from oracle.tree import Gaps
 
@@ -88,7 +88,8 @@ def oracle_cfg(w):
                          width_cap=cc["width_cap"], m_cap=cc["m_cap"], D_max=g["D_max"],
                          per_request=bool(cc.get("per_request", False)))
     if w["policy"] == "graft":
-        c["graft"] = dict(w["graft"], template=chain_template(w["k"], w["D"]))
+        c["graft"] = dict(w["graft"], template=graft_template(w))
+        c["block"] = bool(w.get("block", False))
     return c
 
 
@@ -142,7 +143,7 @@ def oracle_round(w, rnd, roots=None, M=None, max_attempts=16):
 class GpuRound:
     """GPU side of a workload: a RoundRunner plus device row generators."""
 
-    def __init__(self, w, flags=0, fused=True):
+    def __init__(self, w, flags=0, fused=True, packed=False):
         import torch
         from dynamic_draft_tree_gb300.rounds import RoundRunner
 
@@ -156,11 +157,13 @@ class GpuRound:
             cc = w["cast"]
             kw = dict(cast=dict(cc), cast_tables=cast_tables(B, cc["M_rows"], cc["N_cols"], cc["L"]))
         if w["policy"] == "graft":
-            kw = dict(graft=w["graft"], template=chain_template(k, w["D"]))
+            kw = dict(graft=w["graft"], template=graft_template(w), block=bool(w.get("block", False)))
+        self.packed = packed
         self.run = RoundRunner(w["policy"], B, V, w["K"], k, g["D_max"], g["P"], g["D_path"], g["m_cap"],
-                               self.spec.dtype, T=w["T"], flags=flags, fused=fused, **kw)
+                               self.spec.dtype, T=w["T"], flags=flags, fused=fused, packed=packed, **kw)
         dt = torch.int16 if self.spec.dtype == synth.BF16 else torch.float32
-        self.dbuf = torch.zeros((B, k, V), dtype=dt, device="cuda")
+        self.block = bool(w.get("block", False))
+        self.dbuf = torch.zeros((B, w["D"] if self.block else k, V), dtype=dt, device="cuda")
         self.tbuf = torch.zeros((B, g["P"], V), dtype=dt, device="cuda")
         self.M = None
         if w["policy"] == "graft":
@@ -174,6 +177,13 @@ class GpuRound:
         V, k = w["V"], w["k"]
 
         def draft_rows(d, ftok):
+            if d == 0:  # a block drafter's rows: position j + 1 of request b, keyed on the root token
+                L = w["D"]
+                ctx = roots_dev.repeat_interleave(L)
+                pos = torch.arange(1, L + 1, dtype=torch.int32, device="cuda").repeat(w["B"])
+                synth.gen_rows_gpu(torch, self.spec, w["seed"], salt, synth.DRAFT, ctx, self.dbuf, V,
+                                   depth_dev=pos if dk else None, rows_per_b=L, salts_dev=salts_dev)
+                return self.dbuf
             F = 1 if d == 1 else k
             ctx = ftok[:, :F].contiguous().view(-1)
             synth.gen_rows_gpu(torch, self.spec, w["seed"], salt, synth.DRAFT, ctx, self.dbuf, V,
@@ -181,6 +191,14 @@ class GpuRound:
             return self.dbuf
 
         def target_rows(meta):
+            if self.packed:  # padding-free: row j of the buffer belongs to the request whose rows hold it
+                # rows past the used ones hold NaN: a read of one would set DT_DEV_BAD_LOGITS
+                self.tbuf.fill_(-1 if self.tbuf.dtype == torch.int16 else float("nan"))  # int16 -1 = bf16 NaN
+                req, ctx, dep = synth.packed_row_map(torch, meta.row_off, meta.tokens, meta.depth)
+                synth.gen_rows_gpu(torch, self.spec, w["seed"], salt, synth.TARGET, ctx, self.tbuf, V,
+                                   depth_dev=dep if dk else None, depth_add=1 if dk else 0, salts_dev=salts_dev,
+                                   row_req_dev=req)
+                return self.tbuf
             synth.gen_rows_gpu(torch, self.spec, w["seed"], salt, synth.TARGET, meta.tokens.view(-1), self.tbuf,
                                V, depth_dev=meta.depth.view(-1) if dk else None, depth_add=1 if dk else 0,
                                rows_per_b=g["P"], salts_dev=salts_dev)
@@ -228,7 +246,8 @@ def compare_round(gr, ref, check_tree=True):
         assert t["depth"] == ot.cur_depth or w["policy"] != "eagle", "depth"
     meta = run.meta.numpy()
     om = ref["meta"]
-    for key in ("n_pos", "tokens", "parents", "depth", "node_id", "position_ids", "n_leaves", "mask", "retrieve"):
+    for key in ("n_pos", "row_off", "tokens", "parents", "depth", "node_id", "position_ids", "n_leaves", "mask",
+                "retrieve"):
         np.testing.assert_array_equal(meta[key], om[key], err_msg=f"meta {key}")
     np.testing.assert_array_equal(run.accept_len.cpu().numpy(), ref["accept_len"], err_msg="accept_len")
     np.testing.assert_array_equal(run.accept_path.cpu().numpy(), ref["accept_path"], err_msg="accept_path")

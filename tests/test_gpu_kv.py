@@ -23,11 +23,11 @@ def torch():
     return t
 
 
-def _round(torch, name, over, rnd=0):
+def _round(torch, name, over, rnd=0, packed=False):
     import harness
 
     w = with_sizes(name, **over)
-    gr = harness.GpuRound(w)
+    gr = harness.GpuRound(w, packed=packed)
     attempts = np.zeros(w["B"], np.int64)
     roots = harness.root_tokens(w, harness.salts_of(w, rnd, attempts))
     gr.round(rnd, attempts, roots)
@@ -81,4 +81,33 @@ def test_commit_kv_full_cache_is_refused(torch):
     assert commit_kv(tmp, cache, want, acc, run.accept_path.cpu().numpy()) == [0]
     assert d_len.cpu().numpy()[0] == want[0] == cache_len[0]
     assert not d_cache.cpu().numpy().any()
+    run.h.close()
+
+
+def test_commit_kv_packed_matches_oracle(torch):
+    """Padding-free temporary KV (the layout of DT_VERIFY_PACKED): request b's positions at rows
+    row_off[b] + i of one buffer, row_off from the tree metadata; per-request CAST gives ragged trees."""
+    import dynamic_draft_tree_gb300 as dt
+    from oracle.kv import commit_kv
+    from synth.workloads import WORKLOADS
+
+    gr = _round(torch, "cast", dict(V=12007, cast=dict(WORKLOADS["cast"]["cast"], per_request=True)), packed=True)
+    run = gr.run
+    B, P = run.meta.tokens.shape
+    row_off = run.meta.row_off.cpu().numpy()
+    rows = int(row_off[B])
+    row_bytes = 4096
+    rng = np.random.default_rng(7)
+    tmp = rng.integers(0, 256, (rows, row_bytes), dtype=np.uint8)
+    cache = rng.integers(0, 256, (B, 2 * P, row_bytes), dtype=np.uint8)
+    cache_len = rng.integers(0, P, B).astype(np.int32)
+    d_cache, d_len = torch.from_numpy(cache).cuda(), torch.from_numpy(cache_len).cuda()
+    dt.dt_commit_kv(run.h, torch.from_numpy(tmp).cuda(), d_cache, d_len, run.accept_len, run.accept_path,
+                    row_off=run.meta.row_off, P=P)
+    assert dt.dt_get_status(run.h) == 0
+    want_len = cache_len.astype(np.int64).copy()
+    assert commit_kv(tmp, cache, want_len, run.accept_len.cpu().numpy(), run.accept_path.cpu().numpy(),
+                     row_off=row_off) == []
+    np.testing.assert_array_equal(d_len.cpu().numpy(), want_len)
+    np.testing.assert_array_equal(d_cache.cpu().numpy(), cache)
     run.h.close()

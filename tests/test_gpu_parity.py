@@ -158,16 +158,17 @@ SMALL = [("pr1", dict(V=4099)), ("pr1", dict(V=32000)), ("vicuna", dict(V=32000)
          ("vicuna", dict(V=8192, T=1)), ("pr1", dict(V=3001, K=1, k=1, m=1)), ("pr1", dict(V=3001, m=60))]
 
 
-def _run_rounds(torch, w, rounds, label=None, compare_from=0, chain_roots=True):
+def _run_rounds(torch, w, rounds, label=None, compare_from=0, chain_roots=True, packed=False):
     """GPU rounds against the oracle's, element by element; ``rounds`` is a count or the list of
     round indices. Graft chains its rounds: M comes from the previous round, and so does the next
     root (its bonus token) unless ``chain_roots`` is false (then every round drafts from the same
     root tokens). Rounds before ``compare_from`` run on both sides (warm-up) but are compared only
-    through M. Logs the seed redraws under ``label``."""
+    through M. ``packed``: padding-free target rows (DT_VERIFY_PACKED). Logs the seed redraws under
+    ``label``."""
     import harness
     from dynamic_draft_tree_gb300 import dt_get_status
 
-    gr = harness.GpuRound(w)
+    gr = harness.GpuRound(w, packed=packed)
     M = None
     if w["policy"] == "graft":
         M = np.full((w["B"], w["V"], 8), -1, np.int64)
@@ -238,6 +239,21 @@ def test_round_parity_cast_per_request(torch, over, rounds):
     against the oracle's, at reduced and at full size."""
     w = _cast_per_request(**over)
     _run_rounds(torch, w, rounds, label=f"cast per request {over}")
+
+
+@pytest.mark.parametrize("name,over,rounds", [
+    ("cast_req", dict(V=12007), range(0, 8, 2)),  # ragged trees: per-request widths, stops and m
+    ("cast_req", {}, 1),                           # full size
+    ("graft", dict(V=2003, B=4), 6),               # the top-8 refresh reads packed rows
+    ("stress", dict(V=3001, B=8, D=5), 8),         # T = 1: sampled walk and bonus draw on packed rows
+    ("vicuna", dict(V=4096, T=1), 4)])
+def test_round_parity_packed_rows(torch, name, over, rounds):
+    """CAST page §局限与展望 (padded batches are a limit): the verify reads request b's rows at
+    row_off[b] + i of a padding-free buffer (rows past the used ones hold NaN, so a stray read sets
+    a status bit); every output equals the oracle's, and row_off equals its prefix sums."""
+    w = _cast_per_request(**over) if name == "cast_req" else with_sizes(name, **over)
+    _run_rounds(torch, w, rounds, label=f"packed rows {name} {over}", packed=True,
+                chain_roots=name != "graft")
 
 
 def test_cast_per_request_fused_calls_equal_separate_calls(torch):
