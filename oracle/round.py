@@ -18,6 +18,7 @@ import numpy as np
 
 from . import cast as cast_mod
 from . import graft as graft_mod
+from . import sampled as sampled_mod
 from .tree import OracleTree, Gaps, build_meta
 from .verify import verify_greedy, verify_sample, row_top8
 
@@ -42,13 +43,23 @@ def run_round(cfg, roots, draft_row, target_row, rnd=0, M=None, pos_offset=None,
     # block drafter (Graft page, extension direction 1): the row of layer d is the block's row for
     # position d, the same whatever tokens were picked above it; frontier width 1 (the block token)
     block = bool(cfg.get("block", False))
+    # sampled drafts (EAGLE-2 page, the ledger of speculative sampling with drafted tokens drawn from
+    # q): children drawn from the draft row without replacement, every drawn node verified
+    draw = bool(cfg.get("draft_sampling", False))
+    sampler = None
+    if draw:
+        if policy != "eagle" or cfg["T"] != 1:
+            raise ValueError("sampled drafts: EAGLE-2 trees with T = 1 only")
+
+        def sampler(b, node, x):
+            return sampled_mod.sample_children(x, K, cfg["seed"], rnd, b, node, gaps)
 
     def expand():
         d = tree.cur_depth + 1
         if block:
             tree.expand_layer(lambda b, f: draft_row(b, d, int(roots[b])))
         else:
-            tree.expand_layer(lambda b, f: draft_row(b, d, int(tree.token[b, tree.frontier[b][f]])))
+            tree.expand_layer(lambda b, f: draft_row(b, d, int(tree.token[b, tree.frontier[b][f]])), sampler)
         return d
 
     d = expand()
@@ -90,10 +101,13 @@ def run_round(cfg, roots, draft_row, target_row, rnd=0, M=None, pos_offset=None,
     elif policy == "graft":
         m_sel = m_req
         m = None
+    elif draw:  # every drawn node (dropping drawn nodes by value is not lossless)
+        m_sel = [len(tree.nodes(b)) for b in range(B)]
+        m = None
     else:
         m = cfg["m"]
         m_sel = [m] * B
-    selected = tree.rerank(m_sel, cfg["m_cap"], gaps)
+    selected = tree.rerank(m_sel, cfg["m_cap"], None if draw else gaps)
 
     retrieved = None
     if policy == "graft":
@@ -115,6 +129,8 @@ def run_round(cfg, roots, draft_row, target_row, rnd=0, M=None, pos_offset=None,
 
     if cfg["T"] == 0:
         acc, path, bonus = verify_greedy(meta, trow)
+    elif draw:
+        acc, path, bonus = sampled_mod.verify_tree(tree, meta, lambda b, i: trow(b, i), cfg["seed"], rnd, gaps)
     else:
         acc, path, bonus = verify_sample(meta, trow, cfg["seed"], rnd, gaps)
     top8 = None

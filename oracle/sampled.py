@@ -65,19 +65,24 @@ def draw_uniforms(seed, rnd, b, node, V):
     return (k + 0.5) * 2.0 ** -23
 
 
-def draw_order(x, K, u):
-    """The first K tokens by decreasing x_v - log(-log u_v), ties to the lower id (-inf never drawn)."""
+def draw_order(x, K, u, gaps=None, b=None):
+    """The first K tokens by decreasing x_v - log(-log u_v), ties to the lower id (-inf never drawn).
+    With ``gaps``, the distance between consecutive keys of the first K + 1 is recorded (the draw
+    order and the set of K drawn tokens depend on those comparisons)."""
     x = np.asarray(x, dtype=np.float64)
     key = x + (-np.log(-np.log(np.asarray(u, dtype=np.float64))))
     key[~np.isfinite(x)] = -np.inf
     order = np.lexsort((np.arange(x.size), -key))
     order = [int(t) for t in order if np.isfinite(key[t])]
+    if gaps is not None:
+        for a, c in zip(order[:K], order[1:K + 1]):
+            gaps.add("draw", key[a] - key[c], key[a], b)
     return order[:K]
 
 
-def sample_children(x, K, seed, rnd, b, node):
+def sample_children(x, K, seed, rnd, b, node, gaps=None):
     """The K children of node ``node`` (draw order), drawn from softmax(x) without replacement."""
-    return draw_order(x, K, draw_uniforms(seed, rnd, b, node, np.asarray(x).size))
+    return draw_order(x, K, draw_uniforms(seed, rnd, b, node, np.asarray(x).size), gaps, b)
 
 
 def plackett_luce(q, seq):

@@ -283,3 +283,38 @@ def test_sampled_round_first_token_is_the_target_distribution():
         first[tok0] += 1
     chi2 = float(((first - n * p_root) ** 2 / (n * p_root)).sum())
     assert chi2 < 25.0, (chi2, first / n, p_root)
+
+
+def test_run_round_with_sampled_drafts_is_the_pinned_composition():
+    """``run_round`` with ``draft_sampling`` takes exactly the steps of the round whose first token is
+    pinned to the target distribution above (expand with the Philox draws, frontier by value, every
+    drawn node selected, flatten, the sampled walk): same tree, metadata and outputs, round by round."""
+    import oracle.round as oround
+
+    V, K, W, D = 5, 2, 2, 3
+    rng = np.random.default_rng(5)
+    x_draft = {(d, tok): rng.normal(size=V) for d in range(1, D + 1) for tok in range(V)}
+    x_target = {(d, tok): rng.normal(size=V) * 1.3 for d in range(1, D + 2) for tok in range(V)}
+    N = otree.n_nodes(K, W, D)
+    cfg = dict(policy="eagle", draft_sampling=True, B=2, K=K, W=W, D=D, k=W, m=N - 1, m_cap=N - 1, P=N,
+               D_path=D + 1, T=1, seed=11)
+    for rnd in range(12):
+        roots = np.array([rnd % V, (rnd + 2) % V])
+        ref = oround.run_round(cfg, roots, lambda b, d, ctx: x_draft[(d, ctx)],
+                               lambda b, d, ctx: x_target[(d, ctx)], rnd=rnd)
+        t = otree.OracleTree(2, K, W, D, root_tokens=roots)
+        drawn = lambda b, node, x: sampled.sample_children(x, K, seed=11, rnd=rnd, b=b, node=node)  # noqa: E731
+        for d in range(1, D + 1):
+            t.expand_layer(lambda b, f: x_draft[(d, int(t.token[b, t.frontier[b][f]]))], sampler=drawn)
+            if d < D:
+                t.select_frontier(W)
+        sel = t.rerank([len(t.nodes(b)) for b in range(2)], N - 1)
+        meta = otree.build_meta(t, sel, np.zeros(2, np.int64), N, D + 1)
+        acc, path, bonus = sampled.verify_tree(
+            t, meta, lambda b, i: x_target[(int(meta["depth"][b, i]) + 1, int(meta["tokens"][b, i]))], seed=11,
+            rnd=rnd)
+        np.testing.assert_array_equal(ref["tree"].token, t.token)
+        np.testing.assert_array_equal(ref["meta"]["tokens"], meta["tokens"])
+        np.testing.assert_array_equal(ref["accept_len"], acc)
+        np.testing.assert_array_equal(ref["accept_path"], path)
+        np.testing.assert_array_equal(ref["bonus"], bonus)
