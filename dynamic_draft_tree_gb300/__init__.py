@@ -160,6 +160,22 @@ def dt_build_tree_meta(h, selected, m_cap, meta, pos_offset=None, ret_token=None
                                  ctypes.byref(meta.c), _stream(stream)))
 
 
+def dt_expand_layer_sampled(h, logits, F, seed, round_, ld=None, stream=None):
+    """dt_expand_layer with the children drawn from softmax(row) without replacement (Philox draws)."""
+    ld = logits.shape[-1] if ld is None else ld
+    check(lib.dt_expand_layer_sampled(h.h, _ptr(logits), ld, F, seed, round_, _stream(stream)))
+
+
+def dt_verify_sampled(h, meta, logits, draft_rows, seed, round_, accept_len, accept_path, bonus, packed=False,
+                      ld=None, ld_d=None, stream=None):
+    """Verify of sampled drafts: draft_rows is the [D_max][B][W][V] buffer the layers were drawn from."""
+    ld = logits.shape[-1] if ld is None else ld
+    ld_d = draft_rows.shape[-1] if ld_d is None else ld_d
+    check(lib.dt_verify_sampled(h.h, ctypes.byref(meta.c), _ptr(logits), ld, DT_VERIFY_PACKED if packed else 0,
+                                _ptr(draft_rows), ld_d, seed, round_, _ptr(accept_len), _ptr(accept_path),
+                                _ptr(bonus), _stream(stream)))
+
+
 def dt_block_expand(h, logits, L, params=None, out=None, ld=None, stream=None):
     """Draft layers 1..L from a block drafter's rows [B][L][V] (one call; Graft gates with params)."""
     ld = logits.shape[-1] if ld is None else ld

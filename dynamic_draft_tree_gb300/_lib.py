@@ -25,7 +25,7 @@ EXPORTS = ["dt_last_error_string", "dt_create", "dt_destroy", "dt_get_tree", "dt
            "dt_rerank", "dt_graft_retrieve", "dt_build_tree_meta", "dt_verify", "dt_adj_update",
            "dt_row_topk_static", "dt_cast_prune_select",
            "dt_cast_verify_rerank", "dt_expand_prune_select", "dt_verify_rows", "dt_verify_accept",
-           "dt_commit_kv", "dt_block_expand"]
+           "dt_commit_kv", "dt_block_expand", "dt_expand_layer_sampled", "dt_verify_sampled"]
 
 c_i32p = ctypes.c_void_p
 vp = ctypes.c_void_p
@@ -91,6 +91,9 @@ def _load():
                                vp, vp, vp, vp, vp], I),
         "dt_build_tree_meta": ([vp, vp, ctypes.c_int32, vp, vp, vp, vp, ctypes.c_int32, ctypes.c_int32, vp,
                                 ctypes.POINTER(DtTreeMeta), vp], I),
+        "dt_expand_layer_sampled": ([vp, vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64, ctypes.c_uint64, vp], I),
+        "dt_verify_sampled": ([vp, ctypes.POINTER(DtTreeMeta), vp, ctypes.c_int64, ctypes.c_int32, vp, ctypes.c_int64,
+                               ctypes.c_uint64, ctypes.c_uint64, vp, vp, vp, vp], I),
         "dt_block_expand": ([vp, vp, ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(DtPruneParams),
                              ctypes.POINTER(DtPruneOut), vp], I),
         "dt_verify": ([vp, ctypes.POINTER(DtTreeMeta), vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64,

@@ -17,7 +17,7 @@ LIB = os.path.join(HERE, "libdt.so")
 ARCH = "103a"
 
 SOURCES = ["dt_api.cu", "k_tree.cu", "k_select.cu", "k_meta.cu", "k_verify.cu", "k_graft.cu",
-           "k_rowtopk_static.cu", "k_kv.cu", "k_block.cu"]
+           "k_rowtopk_static.cu", "k_kv.cu", "k_block.cu", "k_sampled.cu"]
 HEADERS = ["dt_internal.cuh", "rowscan.cuh", "rowstream.cuh", "cast_block.cuh"]
 
 

@@ -95,6 +95,7 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   Carver cv;
   const size_t o_token = cv.take<int32_t>(BN), o_parent = cv.take<int32_t>(BN), o_depth = cv.take<int32_t>(BN);
   const size_t o_logc = cv.take<float>(BN), o_value = cv.take<float>(BN), o_dd = cv.take<float2>(BN);
+  const size_t o_eslot = cv.take<int32_t>(BN), o_estat = cv.take<float4>(BN);
   const size_t o_lorder = cv.take<int32_t>((size_t)c.B_max * (c.D_max + 1) * h->LW);
   const size_t o_lval = cv.take<float>((size_t)c.B_max * (c.D_max + 1) * h->LW);
   const size_t o_ltok = cv.take<int32_t>((size_t)c.B_max * (c.D_max + 1) * h->LW);
@@ -140,6 +141,8 @@ int dt_create(const dt_config* cfg, dt_handle** out) {
   w.logc = reinterpret_cast<float*>(bp + o_logc);
   w.value = reinterpret_cast<float*>(bp + o_value);
   w.node_dd = reinterpret_cast<float2*>(bp + o_dd);
+  w.exp_slot = reinterpret_cast<int32_t*>(bp + o_eslot);
+  w.exp_stat = reinterpret_cast<float4*>(bp + o_estat);
   w.layer_order = reinterpret_cast<int32_t*>(bp + o_lorder);
   w.layer_val = reinterpret_cast<float*>(bp + o_lval);
   w.layer_tok = reinterpret_cast<int32_t*>(bp + o_ltok);
@@ -297,6 +300,21 @@ int dt_expand_prune_select(dt_handle* h, const void* logits, int64_t ld, int32_t
   if (rc != DT_OK) return rc;
   cudaError_t e = dt::launch_expand_ex(h, logits, ld, F, policy, p, out, width, width_len, frontier_token, s);
   if (e != cudaSuccess) return cuda_fail(e, "dt_expand_prune_select");
+  return DT_OK;
+}
+
+int dt_expand_layer_sampled(dt_handle* h, const void* logits, int64_t ld, int32_t F, uint64_t seed, uint64_t round,
+                            cudaStream_t s) {
+  if (!h || !logits) return fail(DT_ERR_ARG, "dt_expand_layer_sampled: null argument");
+  if (h->B < 1) return fail(DT_ERR_ARG, "dt_expand_layer_sampled: no tree (call dt_tree_reset)");
+  if (h->depth >= h->cfg.D_max) return fail(DT_ERR_ARG, "dt_expand_layer_sampled: tree already has D_max layers");
+  if (F < 1 || F > h->cfg.W) return fail(DT_ERR_ARG, "F=%d outside [1, W=%d]", F, h->cfg.W);
+  if (ld < h->cfg.V) return fail(DT_ERR_ARG, "ld=%lld < V", (long long)ld);
+  if (h->N > 4096) return fail(DT_ERR_ARG, "sampled drafts need at most 4096 nodes per request (draw counter)");
+  const size_t esz = h->cfg.dtype == DT_BF16 ? 2 : 4;
+  if (!aligned(logits, esz)) return fail(DT_ERR_ARG, "logits not aligned to its element size");
+  cudaError_t e = dt::launch_expand(h, logits, ld, F, s, true, seed, round);
+  if (e != cudaSuccess) return cuda_fail(e, "dt_expand_layer_sampled");
   return DT_OK;
 }
 
@@ -481,6 +499,23 @@ int dt_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_
   if (rc != DT_OK) return rc;
   cudaError_t e = dt::launch_verify(h, meta, logits, ld, mode, seed, round, accept_len, accept_path, bonus, top8, s);
   if (e != cudaSuccess) return cuda_fail(e, "dt_verify");
+  return DT_OK;
+}
+
+int dt_verify_sampled(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int32_t mode,
+                      const void* draft_rows, int64_t ld_d, uint64_t seed, uint64_t round, int32_t* accept_len,
+                      int32_t* accept_path, int32_t* bonus, cudaStream_t s) {
+  if (!h || !accept_len || !accept_path || !bonus || !draft_rows)
+    return fail(DT_ERR_ARG, "dt_verify_sampled: null argument");
+  if (mode != 0 && mode != DT_VERIFY_PACKED) return fail(DT_ERR_ARG, "mode must be 0 or DT_VERIFY_PACKED");
+  const int rc = check_verify_args(h, "dt_verify_sampled", meta, logits, ld, DT_SAMPLE | mode);
+  if (rc != DT_OK) return rc;
+  if (ld_d < h->cfg.V) return fail(DT_ERR_ARG, "ld_d < V");
+  const size_t esz = h->cfg.dtype == DT_BF16 ? 2 : 4;
+  if (!aligned(draft_rows, esz)) return fail(DT_ERR_ARG, "draft rows not aligned to their element size");
+  cudaError_t e = dt::launch_verify_sampled(h, meta, logits, ld, mode, draft_rows, ld_d, seed, round, accept_len,
+                                            accept_path, bonus, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dt_verify_sampled");
   return DT_OK;
 }
 

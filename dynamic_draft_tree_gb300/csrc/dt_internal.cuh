@@ -65,6 +65,8 @@ struct Workspace {
   float* logc;
   float* value;
   float2* node_dd;       // [B_max][N] log c of a block layer's child as a double-float (block expansion)
+  int32_t* exp_slot;     // [B_max][N] sampled drafts: frontier slot of each expanded node's row
+  float4* exp_stat;      // [B_max][N] sampled drafts: (max, sum hi, sum lo) of that row's softmax
   int32_t* layer_order;
   float* layer_val;      // [B_max][D_max+1][LW] value of layer_order's node at the same place
   int32_t* layer_tok;    // [B_max][D_max+1][LW] token of layer_order's node at the same place
@@ -128,7 +130,8 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 cudaError_t launch_tree_reset(dt_handle* h, const int32_t* root, cudaStream_t s);
 cudaError_t launch_select_frontier(dt_handle* h, const int32_t* width, int width_len, const int32_t* stop,
                                    int32_t* frontier_token, cudaStream_t s);
-cudaError_t launch_expand(dt_handle* h, const void* logits, int64_t ld, int F, cudaStream_t s);
+cudaError_t launch_expand(dt_handle* h, const void* logits, int64_t ld, int F, cudaStream_t s, bool draw = false,
+                          uint64_t seed = 0, uint64_t round = 0);
 // Expansion followed, by policy, by no pruning (DT_POLICY_NONE), the Graft checkpoint or CAST's width
 // and depth pruning, then the next frontier (not after D_max).
 cudaError_t launch_expand_ex(dt_handle* h, const void* logits, int64_t ld, int F, int policy,
@@ -151,6 +154,9 @@ cudaError_t launch_build_meta(dt_handle* h, const int32_t* selected, int m_cap, 
                               const int32_t* ret_parent, const int32_t* ret_count, const int32_t* ret_anchor,
                               int R_cap, int K_total, const int32_t* pos_offset, const dt_tree_meta* meta,
                               cudaStream_t s);
+cudaError_t launch_verify_sampled(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int mode,
+                                  const void* draft, int64_t ld_d, uint64_t seed, uint64_t round,
+                                  int32_t* accept_len, int32_t* accept_path, int32_t* bonus, cudaStream_t s);
 cudaError_t launch_block_expand(dt_handle* h, const void* logits, int64_t ld, int L, const dt_prune_params* p,
                                 const dt_prune_out* out, cudaStream_t s);
 cudaError_t launch_verify(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int mode,

@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kRowThreads, 4) block_expand_kernel(BlockArgs 
     }
   };
   scan_pieces<T, true>(p, a.V, a.K, a.B, ws.partials, ws.row_counter, ws.row_tau, sm, dyn_smem, a.first_wait_cap,
-                       ws.status, row_of, cnt, finish);
+                       ws.status, row_of, cnt, finish, [](int, int) { return GumbelCtx{}; });
 }
 
 }  // namespace

@@ -104,11 +104,15 @@ struct ExpandArgs {
   int Smax;      // pieces per row at most
   int32_t base;  // first id of layer d
   uint32_t first_wait_cap;
+  GumbelCtx draw;  // sampled drafts: seed and round of the draw noise (c2 set per row)
 };
 
 // Balanced over the active rows (request b expands min(frontier_count[b], F) nodes); see the
 // balanced row pass in rowscan.cuh.
-template <typename T>
+// GUMBEL: sampled drafts, the K children are the first K tokens of x + G (draws without replacement
+// from softmax(x)), in draw order; each expanded node records its slot and its row's statistics for the
+// sampled verify.
+template <typename T, bool GUMBEL>
 __global__ void __launch_bounds__(kRowThreads, 4) expand_kernel(ExpandArgs a) {
   pdl_begin();
   extern __shared__ __align__(128) uint8_t dyn_smem[];
@@ -149,7 +153,13 @@ __global__ void __launch_bounds__(kRowThreads, 4) expand_kernel(ExpandArgs a) {
       // log c = (x - M) - log S and value = value(parent) + log c, each kept as a double-float until
       // the final rounding
       float dh, dl;
-      log_softmax_dd(st, key_value(k), dh, dl);
+      float x = key_value(k);
+      if (GUMBEL) {  // the key holds x + G: the token's own logit
+        const uint32_t t = key_id(k);
+        const T* rowp = reinterpret_cast<const T*>(a.logits) + ((int64_t)b * a.F + f) * a.ld;
+        x = k != 0ull && t < (uint32_t)a.V ? Elt<T>::load(rowp + t) : -INFINITY;
+      }
+      log_softmax_dd(st, x, dh, dl);
       const float lc = __fadd_rn(dh, dl);
       float vh = pval, vl = 0.0f;
       ff_add(vh, vl, dh, dl);
@@ -157,6 +167,10 @@ __global__ void __launch_bounds__(kRowThreads, 4) expand_kernel(ExpandArgs a) {
       ws.parent[gi] = pid;
       ws.logc[gi] = lc;
       ws.value[gi] = __fadd_rn(vh, vl);
+      if (GUMBEL && tid == 0) {  // the row the node's children were drawn from, for the sampled verify
+        ws.exp_slot[(int64_t)b * a.N + pid] = f;
+        ws.exp_stat[(int64_t)b * a.N + pid] = make_float4(st.m, st.s_hi, st.s_lo, 0.0f);
+      }
       __threadfence();  // the children reach L2 before this row's arrival below
     }
     __syncthreads();
@@ -190,8 +204,13 @@ __global__ void __launch_bounds__(kRowThreads, 4) expand_kernel(ExpandArgs a) {
       if (tid == 0) ws.layer_count[(int64_t)b * (a.D + 1) + a.d] = n;
     }
   };
-  scan_pieces<T, true>(p, a.V, a.K, a.B, ws.partials, ws.row_counter, ws.row_tau, sm, dyn_smem, a.first_wait_cap, ws.status,
-                       row_of, cnt, finish);
+  auto noise = [&](int b, int f) -> GumbelCtx {
+    GumbelCtx g = a.draw;
+    g.c2 = 0x40000000u + 4096u * (uint32_t)b + (uint32_t)pid;
+    return g;
+  };
+  scan_pieces<T, true, GUMBEL>(p, a.V, a.K, a.B, ws.partials, ws.row_counter, ws.row_tau, sm, dyn_smem,
+                               a.first_wait_cap, ws.status, row_of, cnt, finish, noise);
 }
 
 }  // namespace
@@ -206,18 +225,22 @@ int row_pass_smax(int K) { return std::min(64, kCandCap / K); }
 
 static size_t row_smem_bytes() { return (size_t)kScanSmemBytes; }
 
-cudaError_t init_tree_attributes() {
-  const int smem = (int)row_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(expand_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(expand_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+template <typename T, bool G>
+static cudaError_t set_expand_attributes(int smem) {
+  cudaError_t e = cudaFuncSetAttribute(expand_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   // all of the unified L1 as shared memory, so that 4 CTAs fit on an SM
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(expand_kernel<uint16_t>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(expand_kernel<T, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(expand_kernel<float>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
+cudaError_t init_tree_attributes() {
+  const int smem = (int)row_smem_bytes();
+  cudaError_t e = set_expand_attributes<uint16_t, false>(smem);
+  if (e == cudaSuccess) e = set_expand_attributes<float, false>(smem);
+  if (e == cudaSuccess) e = set_expand_attributes<uint16_t, true>(smem);
+  if (e == cudaSuccess) e = set_expand_attributes<float, true>(smem);
   return e;
 }
 
@@ -239,7 +262,8 @@ cudaError_t launch_select_frontier(dt_handle* h, const int32_t* width, int width
   return cudaGetLastError();
 }
 
-cudaError_t launch_expand(dt_handle* h, const void* logits, int64_t ld, int F, cudaStream_t s) {
+cudaError_t launch_expand(dt_handle* h, const void* logits, int64_t ld, int F, cudaStream_t s, bool draw,
+                          uint64_t seed, uint64_t round) {
   const int d = h->depth + 1;
   ExpandArgs a;
   a.ws = h->ws;
@@ -257,12 +281,16 @@ cudaError_t launch_expand(dt_handle* h, const void* logits, int64_t ld, int F, c
   a.Smax = row_pass_smax(h->cfg.K);
   a.base = d == 1 ? 1 : 1 + h->cfg.K + (d - 2) * h->LW;
   a.first_wait_cap = (h->cfg.flags & DT_FLAG_TEST_TIMEOUT) ? 0u : kSpinCap;
+  a.draw = GumbelCtx{(uint32_t)seed, (uint32_t)(seed >> 32), (uint32_t)round, (uint32_t)(round >> 32), 0u};
   const unsigned grid = (unsigned)row_pass_grid(h);
   const size_t smem = row_smem_bytes();
-  if (h->cfg.dtype == DT_BF16)
-    launch_k(expand_kernel<uint16_t>, dim3(grid), dim3(kRowThreads), smem, s, a);
-  else
-    launch_k(expand_kernel<float>, dim3(grid), dim3(kRowThreads), smem, s, a);
+  if (h->cfg.dtype == DT_BF16) {
+    if (draw) launch_k(expand_kernel<uint16_t, true>, dim3(grid), dim3(kRowThreads), smem, s, a);
+    else launch_k(expand_kernel<uint16_t, false>, dim3(grid), dim3(kRowThreads), smem, s, a);
+  } else {
+    if (draw) launch_k(expand_kernel<float, true>, dim3(grid), dim3(kRowThreads), smem, s, a);
+    else launch_k(expand_kernel<float, false>, dim3(grid), dim3(kRowThreads), smem, s, a);
+  }
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) h->depth = d;
   return e;

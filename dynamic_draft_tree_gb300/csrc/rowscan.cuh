@@ -377,11 +377,38 @@ __device__ __forceinline__ float warp_kth_largest(float v, int K) {
 
 // Pushes into the warp's candidate buffer the elements of the warp's first nb chunk stages (resident
 // in its ring, stage u in buffer u) whose value is >= tv and not -inf and whose key exceeds tk.
-// Lanes without `scan` push nothing. Out of line: one copy serves every call site.
-template <typename T>
+// Draw noise of sampled drafts (children drawn without replacement by Gumbel-top-K): token v of the
+// row of node n of request b gets G_v = -log(-log u_v), u_v = (k + 1/2) 2^-23 with k the top 23 bits
+// of word v & 3 of Philox4x32-10(key = seed; counter = (round_lo, round_hi, c2, v >> 2)),
+// c2 = 0x40000000 + 4096 b + n. The row's keys are then x_v + G_v instead of x_v.
+struct GumbelCtx {
+  uint32_t k0, k1, r0, r1, c2;
+};
+
+__device__ __forceinline__ float gumbel_of_word(uint32_t w) {
+  const float u = ((float)(w >> 9) + 0.5f) * 1.1920928955078125e-07f;  // 2^-23
+  return -logf(-logf(u));
+}
+
+// G of token id, reusing the Philox block of the previous call when id is in the same group of four.
+struct GumbelCursor {
+  uint32_t group = 0xFFFFFFFFu;
+  Philox4 w;
+  __device__ __forceinline__ float at(const GumbelCtx& g, uint32_t id) {
+    if ((id >> 2) != group) {
+      group = id >> 2;
+      w = philox4x32_10(g.r0, g.r1, g.c2, group, g.k0, g.k1);
+    }
+    return gumbel_of_word(w.v[id & 3u]);
+  }
+};
+
+// Lanes without `scan` push nothing. Out of line: one copy serves every call site. With GUMBEL the
+// tested value of token id is x + G(id).
+template <typename T, bool GUMBEL>
 static __device__ __noinline__ void push_batch_candidates(WarpRing& rg, const uint8_t* my_stages, int nb,
                                                           int64_t wbytes, int64_t we0, float tv, uint64_t tk,
-                                                          bool scan) {
+                                                          bool scan, GumbelCtx gc) {
   constexpr int VEC = Elt<T>::kVec;
   constexpr int ESZ = (int)sizeof(T);
   constexpr int QV = kStageBytes / 16 / 32;
@@ -395,11 +422,14 @@ static __device__ __noinline__ void push_batch_candidates(WarpRing& rg, const ui
         const int vi = q * 32 + lane;
         if (vi * 16 >= st_bytes) break;
         const uint4 w = *reinterpret_cast<const uint4*>(sp + (size_t)vi * 16);
+        GumbelCursor gcur;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
+          const uint32_t id = (uint32_t)(st_e0 + (int64_t)(vi * VEC + e));
           const float x = vec_elt<T>(w, e);
-          if (x >= tv && x != -INFINITY) {
-            const uint64_t k = make_key(x, (uint32_t)(st_e0 + (int64_t)(vi * VEC + e)));
+          const float y = GUMBEL ? x + gcur.at(gc, id) : x;
+          if (y >= tv && x != -INFINITY) {
+            const uint64_t k = make_key(y, id);
             if (k > tk) {
               const int pos = atomicAdd(&rg.cnt, 1);
               if (pos < kWarpCand) rg.cand[pos] = k;
@@ -413,10 +443,12 @@ static __device__ __noinline__ void push_batch_candidates(WarpRing& rg, const ui
 }
 
 // Scans elements [s0, s1) of `row`. K <= kMaxK. `stages` is kScanWarps * kWarpStages * kStageBytes of
-// shared memory (dynamic). All threads of the CTA call it.
-template <typename T, bool SOFTMAX>
+// shared memory (dynamic). All threads of the CTA call it. With GUMBEL the keys (top-K, thresholds)
+// are x + G of the draw noise gc; the softmax statistics stay those of x.
+template <typename T, bool SOFTMAX, bool GUMBEL = false>
 __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1, int K, ScanSmem& sm,
-                               uint8_t* stages, uint32_t first_wait_cap, unsigned long long* gtau) {
+                               uint8_t* stages, uint32_t first_wait_cap, unsigned long long* gtau,
+                               GumbelCtx gc = GumbelCtx{}) {
   constexpr int VEC = Elt<T>::kVec;
   constexpr int ESZ = (int)sizeof(T);
   const int tid = threadIdx.x;
@@ -474,7 +506,10 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
     }
     // its key joins the warp list only after streaming: the strict tie test of later stages relies on
     // the list holding earlier (smaller) ids of this warp's own chunk
-    if (!(x != x)) ht_key = make_key(x, (uint32_t)idx);
+    if (!(x != x)) {
+      GumbelCursor gcur;
+      ht_key = make_key(GUMBEL ? x + gcur.at(gc, (uint32_t)idx) : x, (uint32_t)idx);
+    }
   }
   __syncwarp();
 
@@ -596,6 +631,28 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
       }
     }
 
+    // the filter's maxima: of x, or with GUMBEL of x + G (every element's noise, lane by lane)
+    float flm = lm;
+    if (GUMBEL) {
+      flm = -INFINITY;
+      GumbelCursor gcur;
+#pragma unroll 1
+      for (int q = 0; q < QV; ++q) {
+        float vm = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const int v = q * VEC + e;  // value index within the lane's stage values
+          float x;
+          if (ESZ == 2) x = (v & 1) ? bf16_hi(wv[v >> 1]) : bf16_lo(wv[v >> 1]);
+          else x = __uint_as_float(wv[v]);
+          const uint32_t id = (uint32_t)(st_e0 + (int64_t)((q * 32 + lane) * VEC + e));
+          if (x != -INFINITY) vm = fmaxf(vm, x + gcur.at(gc, id));
+        }
+        vmax[q] = vm;
+        flm = fmaxf(flm, vm);
+      }
+    }
+
     // The rarely taken candidate paths below read the stage from shared memory with rolled loops:
     // straight-line code over all NV register values would be large and, being rarely executed,
     // always cold in the instruction cache. Vector q of this lane is stage vector q * 32 + lane; its
@@ -611,7 +668,7 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
     };
 
     if (t < nb) {
-      bmax = fmaxf(bmax, lm);
+      bmax = fmaxf(bmax, flm);
       if (t + 1 < nb) continue;  // the next batch stage
       // Threshold: the K-th largest lane maximum (K lanes hold an element at or above it, so no
       // element below it is in the top-K), or the row's shared threshold if larger. The warp has
@@ -619,7 +676,7 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
       uint64_t tk = gt;
       float tv = fmaxf(warp_kth_largest(bmax, K), gt ? key_value(gt) : -INFINITY);
       if (__any_sync(0xFFFFFFFFu, bmax >= tv)) {
-        push_batch_candidates<T>(rg, my_stages, nb, wbytes, we0, tv, tk, bmax >= tv);
+        push_batch_candidates<T, GUMBEL>(rg, my_stages, nb, wbytes, we0, tv, tk, bmax >= tv, gc);
         bool overflow = merge(false);
         // An overflowed buffer still raised the list's K-th key: filter again above it (keys already
         // in the list are dropped by the merge). The key rises every round.
@@ -630,7 +687,7 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
           }
           tk = tau_key;
           tv = tau_val;
-          push_batch_candidates<T>(rg, my_stages, nb, wbytes, we0, tv, tk, bmax >= tv);
+          push_batch_candidates<T, GUMBEL>(rg, my_stages, nb, wbytes, we0, tv, tk, bmax >= tv, gc);
           overflow = merge(true);
         }
         if (gtau && lane == 0 && nl == K) atomicMax(gtau, (unsigned long long)tau_key);
@@ -654,7 +711,7 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
         }
         const float tv = tk ? key_value(tk) : -INFINITY;
         const bool strict = t > 0 && own;
-        const bool hot = strict ? (lm > tv) : (lm >= tv);
+        const bool hot = strict ? (flm > tv) : (flm >= tv);
         if (!__any_sync(0xFFFFFFFFu, hot)) break;
         if (hot) {
           unsigned vm = 0u;  // vectors that may hold candidates
@@ -666,11 +723,13 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
             vm &= vm - 1;
             uint4 w;
             if (!vec_at(q, w)) break;
+            GumbelCursor gcur;
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
               const float x = vec_elt<T>(w, e);
-              if (x >= tv && x != -INFINITY) {
-                const uint64_t k = make_key(x, id_of(q, e));
+              const float y = GUMBEL ? x + gcur.at(gc, id_of(q, e)) : x;
+              if (y >= tv && x != -INFINITY) {
+                const uint64_t k = make_key(y, id_of(q, e));
                 if (k > tk) push(k);
               }
             }
@@ -875,13 +934,14 @@ __device__ void plan_rows(RowPlan& p, int B, int64_t V, int Smax, int esz, Cnt c
 // Scans this CTA's pieces in order (all threads). row_of(b, i) gives row i of request b, or nullptr
 // when that row is not to be read (its pieces leave empty partials); it is called when a piece
 // starts, so it may also start loads the row's finish will need. When a piece completes its row,
+// noise(b, i) gives the draw noise of row (b, i) when GUMBEL (called after row_of(b, i)).
 // finish(b, i, st) runs on all threads with the row's merged top-K in sm.topk and its softmax
 // statistics st (max and sum for softmax passes; the best key's value otherwise). After a timed-out copy wait the CTA reads nothing more (empty partials), so
 // that every row still completes its count.
-template <typename T, bool SOFTMAX, class RowOf, class Cnt, class Finish>
+template <typename T, bool SOFTMAX, bool GUMBEL = false, class RowOf, class Cnt, class Finish, class Noise>
 __device__ void scan_pieces(const RowPlan& p, int64_t V, int K, int B, Partial* partials, int32_t* counter,
                             unsigned long long* row_tau, ScanSmem& sm, uint8_t* stages, uint32_t first_wait_cap,
-                            int32_t* status, RowOf row_of, Cnt cnt, Finish finish) {
+                            int32_t* status, RowOf row_of, Cnt cnt, Finish finish, Noise noise) {
   const int tid = threadIdx.x;
   const int64_t c = blockIdx.x;
   if (tid == 0) sm.cand = reinterpret_cast<uint64_t*>(stages);
@@ -910,7 +970,8 @@ __device__ void scan_pieces(const RowPlan& p, int64_t V, int K, int B, Partial* 
     const bool scan = row != nullptr && !halted && e1 > e0;
     SegOut so;
     if (scan) {
-      so = scan_segment<T, SOFTMAX>(row, e0, e1, K, sm, stages, first_wait_cap, row_tau ? row_tau + j : nullptr);
+      so = scan_segment<T, SOFTMAX, GUMBEL>(row, e0, e1, K, sm, stages, first_wait_cap,
+                                            row_tau ? row_tau + j : nullptr, GUMBEL ? noise(b, i) : GumbelCtx{});
     } else {
       so.m = -INFINITY;
       so.s_hi = so.s_lo = 0.0f;

@@ -25,7 +25,8 @@ import torch
 
 from . import (Handle, Meta, Template, make_prune_params, make_prune_out, dt_tree_reset, dt_select_frontier,
                dt_expand_layer, dt_expand_prune_select, dt_cast_prune, dt_cast_prune_select, dt_cast_verify_rerank, dt_rerank, dt_graft_retrieve, dt_build_tree_meta, dt_verify, dt_verify_rows,
-               dt_verify_accept, dt_adj_update, dt_block_expand, DT_GREEDY, DT_SAMPLE, DT_VERIFY_PACKED,
+               dt_verify_accept, dt_adj_update, dt_block_expand, dt_expand_layer_sampled, dt_verify_sampled,
+               DT_GREEDY, DT_SAMPLE, DT_VERIFY_PACKED,
                DT_POLICY_CAST_WIDTH_DEPTH, DT_POLICY_CAST_VERIFY, DT_POLICY_GRAFT_CHECKPOINT, DT_POLICY_NONE,
                DT_ANCHOR_ROOT, DT_ANCHOR_TAIL)
 
@@ -34,15 +35,22 @@ class RoundRunner:
     """Device buffers and call sequence of one round for a policy ('eagle' | 'cast' | 'graft')."""
 
     def __init__(self, policy, B, V, K, k, D, P, D_path, m, dtype, T=0, cast=None, cast_tables=None,
-                 graft=None, template=None, flags=0, device="cuda", fused=True, packed=False, block=False):
+                 graft=None, template=None, flags=0, device="cuda", fused=True, packed=False, block=False,
+                 draw=False):
         """``fused``: each layer's expansion, pruning and next frontier as one call
         (dt_expand_prune_select), and CAST's verify count + rerank as one (dt_cast_verify_rerank),
         instead of the separate calls. ``packed``: the target rows are padding-free
         (DT_VERIFY_PACKED): ``target_rows`` returns them at meta.row_off[b] + i. ``block`` (Graft):
-        the D draft layers come from a block drafter's rows in one dt_block_expand call."""
+        the D draft layers come from a block drafter's rows in one dt_block_expand call. ``draw``
+        (EAGLE-2 with T = 1): sampled drafts, the children drawn from the draft rows
+        (dt_expand_layer_sampled), every drawn node verified (dt_verify_sampled); ``draft_rows`` must
+        then return views of one [D][B][k][V] buffer, layer d at index d - 1, which is handed to the
+        verify as ``self.draft_rows``."""
         self.fused = fused
         self.packed = packed
         self.block = block
+        self.draw = draw
+        self.draft_rows = None
         self.policy, self.B, self.V, self.K, self.k, self.D = policy, B, V, K, k, D
         self.P, self.D_path, self.T = P, D_path, T
         self.h = Handle(B, V, K, k, D, P, dtype, flags)
@@ -132,6 +140,15 @@ class RoundRunner:
             if d > 1 and not self.fused:
                 dt_select_frontier(h, self.width, self.stop, self.frontier_token)
             logits = draft_rows(d, self.frontier_token)
+            if self.draw:  # sampled drafts: draws from every frontier row, no pruning (EAGLE-2 frontier)
+                if timing is not None:
+                    timing.start("expand")
+                dt_expand_layer_sampled(h, logits, self.k, seed, rnd)
+                if timing is not None:
+                    timing.stop("expand")
+                if d < self.D:
+                    dt_select_frontier(h, self.width, None, self.frontier_token)
+                continue
             if not self.fused:
                 dt_expand_layer(h, logits, F)
                 if pol in ("cast", "graft"):
@@ -174,7 +191,14 @@ class RoundRunner:
             dt_build_tree_meta(h, self.selected, self.m_cap, self.meta, self.pos_offset)
         logits = target_rows(self.meta)
         mode = (DT_SAMPLE if self.T == 1 else DT_GREEDY) | (DT_VERIFY_PACKED if self.packed else 0)
-        if timing is not None:
+        if self.draw:
+            if timing is not None:
+                timing.start("verify_sampled")
+            dt_verify_sampled(h, self.meta, logits, self.draft_rows, seed, rnd, self.accept_len, self.accept_path,
+                              self.bonus, packed=self.packed)
+            if timing is not None:
+                timing.stop("verify_sampled")
+        elif timing is not None:
             timing.start("verify_rows")
             dt_verify_rows(h, self.meta, logits, mode, self.top8 is not None)
             timing.stop("verify_rows")

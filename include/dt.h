@@ -260,6 +260,19 @@ int dt_expand_prune_select(dt_handle* h, const void* logits, int64_t ld, int32_t
 int dt_block_expand(dt_handle* h, const void* logits, int64_t ld, int32_t L, const dt_prune_params* p,
                     const dt_prune_out* out, cudaStream_t s);
 
+/* Sampled drafts (EAGLE-2 page, §先把投机解码的账本摆清楚: drafted tokens drawn from the draft
+ * distribution q and tested with min(1, p/q)): dt_expand_layer with the K children of each expanded
+ * node drawn from softmax(row) without replacement, i.e. the first K tokens by x_v + G_v (ties: lower
+ * id), G_v = -log(-log u_v), u_v = (k + 1/2) 2^-23 with k the top 23 bits of word v & 3 of
+ * Philox4x32-10(key seed; counter (round lo, round hi, 0x40000000 + 4096 b + node, v >> 2)); the
+ * children are in draw order (rank r = the r-th draw), log c = log softmax(row)[token]. Each expanded
+ * node records its row's slot and softmax statistics for dt_verify_sampled. Needs N <= 4096.
+ * For dt_verify_sampled the rows of every layer must stay in one buffer draft_rows [D_max][B][W][ld_d]:
+ * pass logits = draft_rows + (d - 1) * B * W * ld_d and F = W for layer d (layer 1 too; rows past the
+ * frontier are not read). */
+int dt_expand_layer_sampled(dt_handle* h, const void* logits, int64_t ld, int32_t F, uint64_t seed, uint64_t round,
+                            cudaStream_t s);
+
 /* a3 + a2 in one launch: exactly dt_cast_prune(h, DT_POLICY_CAST_WIDTH_DEPTH, p, out, s) followed by
  * dt_select_frontier(h, out->width, 1, out->stop, frontier_token, s): CAST width and grow/stop after
  * the newest layer, then the next layer's frontier (none for stopped requests). One kernel instead of
@@ -337,6 +350,22 @@ int dt_verify_rows(dt_handle* h, const dt_tree_meta* meta, const void* logits, i
 int dt_verify_accept(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int32_t mode,
                      uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* accept_path, int32_t* bonus,
                      int32_t* top8, cudaStream_t s);
+
+/* Verify of a tree of sampled drafts (EAGLE-2 page, §先把投机解码的账本摆清楚, §无损性…): every drawn
+ * node must be in the tree (dt_rerank with m = every node: dropping drawn nodes by value is not
+ * lossless). From the root, the children of the current position, in position order (= draw order),
+ * are tested: child j, drawn from q_j = q without the earlier children (renormalised), q = softmax of
+ * the row its parent's children were drawn from, against the residual r_j (r_0 = softmax(target row)):
+ * accepted with probability min(1, r_j(t)/q_j(t)), u as in dt_verify; on rejection r_{j+1} =
+ * norm(max(0, r_j - q_j)) (one pass over both rows per rejection). An accepted child becomes the
+ * current position; when all children are rejected, or there are none, the bonus is the Gumbel-max
+ * draw of dt_verify from the last residual (token 0 if the residual is empty). mode: 0 or
+ * DT_VERIFY_PACKED (target row layout as dt_verify). draft_rows: the [D_max][B][W][ld_d] buffer of
+ * dt_expand_layer_sampled. Per-element arithmetic in fp32, sums and the tests in fp64. Two launches
+ * (the streaming pass over the target rows, then one CTA per request). */
+int dt_verify_sampled(dt_handle* h, const dt_tree_meta* meta, const void* logits, int64_t ld, int32_t mode,
+                      const void* draft_rows, int64_t ld_d, uint64_t seed, uint64_t round, int32_t* accept_len,
+                      int32_t* accept_path, int32_t* bonus, cudaStream_t s);
 
 /* a10 (Graft step (3)): M[b][token_i][0..7] = top8[b][i][0..7] for every used position i with a
  * valid token; when a token repeats the highest position wins. M: device [B][V][8]. */

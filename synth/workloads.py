@@ -69,6 +69,10 @@ WORKLOADS = {
                         graft=dict(ckpt_layers=list(range(16)), tau=[0.05] * 4 + [0.1] * 12,
                                    k_draft=[min(60, 4 * (j + 1)) for j in range(16)], K_total=60, anchor="tail",
                                    template_shape=(8, 8))),
+    # sampled drafts (T = 1): EAGLE-2 tree of the PR1 shape whose children are drawn from the draft
+    # rows (Gumbel-top-K); every drawn node is verified (84 nodes); Vicuna-like Zipf rows
+    "sampled": dict(policy="eagle", draft_sampling=True, B=4, V=32000, dtype=BF16, K=4, k=4, D=6, m=84, T=1,
+                    seed=7, rounds=200, recipe=dict(kind=1, sigma=0.5, zipf_s=1.1, depthkey=True)),
     # large-batch stress: fp32, half low-entropy (peak +U[6,12]) and half high-entropy (+U[0,2]), T = 1
     "stress": dict(policy="eagle", B=64, V=128256, dtype=F32, K=8, k=8, D=10, m=64, T=1, seed=5, rounds=500,
                    recipe=dict(kind=0, sigma=2 ** 0.5, peak=None, per_request_height=False, depthkey=True)),
@@ -113,6 +117,8 @@ def geometry(w):
         return dict(W=w["k"], D_max=w["D"], P=K_total + 1, D_path=max(w["D"], depth) + 2, m_cap=min(K_total, nodes),
                     R_cap=K_total)
     m_cap = w["cast"]["m_cap"] if pol == "cast" else w["m"]
+    if w.get("draft_sampling"):  # every drawn node is verified
+        m_cap = w["K"] + (w["D"] - 1) * w["k"] * w["K"]
     return dict(W=w["k"], D_max=w["D"], P=m_cap + 1, D_path=w["D"] + 1, m_cap=m_cap, R_cap=0)
 
 

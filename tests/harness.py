@@ -90,6 +90,7 @@ def oracle_cfg(w):
     if w["policy"] == "graft":
         c["graft"] = dict(w["graft"], template=graft_template(w))
         c["block"] = bool(w.get("block", False))
+    c["draft_sampling"] = bool(w.get("draft_sampling", False))
     return c
 
 
@@ -159,11 +160,15 @@ class GpuRound:
         if w["policy"] == "graft":
             kw = dict(graft=w["graft"], template=graft_template(w), block=bool(w.get("block", False)))
         self.packed = packed
+        self.draw = bool(w.get("draft_sampling", False))
         self.run = RoundRunner(w["policy"], B, V, w["K"], k, g["D_max"], g["P"], g["D_path"], g["m_cap"],
-                               self.spec.dtype, T=w["T"], flags=flags, fused=fused, packed=packed, **kw)
+                               self.spec.dtype, T=w["T"], flags=flags, fused=fused, packed=packed, draw=self.draw, **kw)
         dt = torch.int16 if self.spec.dtype == synth.BF16 else torch.float32
         self.block = bool(w.get("block", False))
         self.dbuf = torch.zeros((B, w["D"] if self.block else k, V), dtype=dt, device="cuda")
+        if self.draw:  # every layer's rows kept for the sampled verify: [D][B][k][V]
+            self.dbuf = torch.zeros((w["D"], B, k, V), dtype=dt, device="cuda")
+            self.run.draft_rows = self.dbuf
         self.tbuf = torch.zeros((B, g["P"], V), dtype=dt, device="cuda")
         self.M = None
         if w["policy"] == "graft":
@@ -185,6 +190,11 @@ class GpuRound:
                                    depth_dev=pos if dk else None, rows_per_b=L, salts_dev=salts_dev)
                 return self.dbuf
             F = 1 if d == 1 else k
+            if self.draw:  # layer d's rows at [d - 1], row (b, f) at b * k + f (only the frontier's read)
+                ctx = ftok.contiguous().view(-1)
+                synth.gen_rows_gpu(torch, self.spec, w["seed"], salt, synth.DRAFT, ctx, self.dbuf[d - 1], V,
+                                   depth_add=d if dk else 0, rows_per_b=k, salts_dev=salts_dev)
+                return self.dbuf[d - 1]
             ctx = ftok[:, :F].contiguous().view(-1)
             synth.gen_rows_gpu(torch, self.spec, w["seed"], salt, synth.DRAFT, ctx, self.dbuf, V,
                                depth_add=d if dk else 0, rows_per_b=F, salts_dev=salts_dev)
