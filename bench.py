@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "draft-tree rounds/s (expand+rerank+verify) at B=8,V=128256; logits HBM GB/s"
 UNIT = "rounds/s"
 HEADLINE = "cast"
-OTHERS = ["pr1", "vicuna", "vicuna_t1", "graft", "stress", "cast_req", "graft_block"]
+OTHERS = ["pr1", "vicuna", "vicuna_t1", "graft", "stress", "cast_req", "graft_block", "sampled"]
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--min-replay-s", type=float, default=1.0, help="time the K-step graph for at least this long")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--record-rounds", type=int, default=0,
+                    help="recorded rounds replayed (0: enough for 3x L2 of inputs); small values for profiling runs")
     return ap.parse_args()
 
 
@@ -162,7 +164,9 @@ class Clocks:
 
 # DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte of the streaming
 # kernels, from the captures summarised in profiles/ (None while no capture of the current kernel exists).
-TRAFFIC_PER_ALGO_BYTE = {"expand": None, "verify_rows": None}
+# DRAM bytes (read + write) per algorithmic byte from the ncu captures of the current kernels (CAST
+# workload, small case: expand layers 1-2, verify passes of two rounds); summaries under profiles/
+TRAFFIC_PER_ALGO_BYTE = {"expand": 1.0115, "verify_rows": 1.0266}
 
 
 def measured_peaks():
@@ -223,13 +227,16 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
     if graft:
         kw = dict(graft=w["graft"], template=graft_template(w), block=bool(w.get("block", False)))
     packed = bool(w.get("packed", False))
+    draw = bool(w.get("draft_sampling", False))
     run = RoundRunner(w["policy"], B, V, w["K"], k, D, P, g["D_path"], g["m_cap"], spec.dtype, T=w["T"],
-                      packed=packed, **kw)
+                      packed=packed, draw=draw, **kw)
     dt = torch.int16 if spec.dtype == synth.BF16 else torch.float32
     esz = 2 if spec.dtype == synth.BF16 else 4
     round_bytes = (D * B * k + B * P) * V * esz
     # recorded rounds: at least 16 (a mix of rounds) and at least 3x L2 of inputs, at most 48 GiB
     R = int(max(2, min(max(16, math.ceil(3 * L2_BYTES / round_bytes)), 256, (48 << 30) // round_bytes)))
+    if args.record_rounds > 0:
+        R = args.record_rounds
     block = bool(w.get("block", False))
     # a block drafter's rows: one [B][L][V] set per round (L = D), at rec_draft[r, 0]
     rec_draft = torch.empty((R, 1, B, D, V) if block else (R, D, B, k, V), dtype=dt, device="cuda")
@@ -257,9 +264,13 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
                     widths.append(np.full(B, D))
                 return rec_draft[slot, 0]
             F = 1 if d == 1 else k
-            ctx = ftok[:, :F].contiguous().view(-1)
             if widths is not None:
                 widths.append((ftok[:, :F] >= 0).sum(1).cpu().numpy())
+            if draw:  # every layer kept for the sampled verify: row (b, f) of layer d at rec_draft[slot, d - 1, b, f]
+                synth.gen_rows_gpu(torch, spec, w["seed"], salt, synth.DRAFT, ftok.contiguous().view(-1),
+                                   rec_draft[slot, d - 1], V, depth_add=d if dk else 0, rows_per_b=k)
+                return rec_draft[slot, d - 1]
+            ctx = ftok[:, :F].contiguous().view(-1)
             synth.gen_rows_gpu(torch, spec, w["seed"], salt, synth.DRAFT, ctx, rec_draft[slot, d - 1], V,
                                depth_add=d if dk else 0, rows_per_b=F)
             return rec_draft[slot, d - 1]
@@ -275,6 +286,7 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
                                rows_per_b=P)
             return rec_target[slot]
 
+        run.draft_rows = rec_draft[slot]
         run.run(roots[slot], draft_rows, target_rows, seed=w["seed"], rnd=r, M=M, n0=512 * (1 + r % 16))
 
     # Graft: the configured warm-up rounds seed M, then more until it no longer changes (a steady M, so
@@ -303,6 +315,7 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
 
     # ---- timed replay: the path only, on recorded inputs, captured as one CUDA graph ----
     def replay(r, timing=None):
+        run.draft_rows = rec_draft[r]
         run.run(roots[r], lambda d, ftok: rec_draft[r, d - 1], lambda meta: rec_target[r], seed=w["seed"], rnd=r,
                 M=M, n0=512 * (1 + r % 16), timing=timing)
 
@@ -365,7 +378,7 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
     exp_bytes = sum(sum(rows_expand[s % R]) for s in range(steps)) * V * esz
     ver_bytes = sum(rows_verify[s % R] for s in range(steps)) * V * esz
     for kind, nbytes in (("expand", exp_bytes), ("prune_select", None), ("verify_rows", ver_bytes),
-                         ("verify_accept", None)):
+                         ("verify_accept", None), ("verify_sampled", ver_bytes)):
         t = timing.ms(kind)
         if not t:
             continue
@@ -379,11 +392,13 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
         lay = sum(timing.ms("expand")) + sum(timing.ms("prune_select"))
         kern["expand_layer"] = {"avg_us": 1e3 * lay / len(timing.ms("expand")),
                                 "gbs": exp_bytes / (lay / 1e3) / 1e9}
-    streaming = [k_ for k_ in ("expand", "verify_rows") if k_ in kern]
+    streaming = [k_ for k_ in ("expand", "verify_rows", "verify_sampled") if k_ in kern]
     top = max(streaming, key=lambda k_: kern[k_]["total_us_per_round"])
     tr = TRAFFIC_PER_ALGO_BYTE.get(top)
     names = {"expand": "expand_kernel (vocab softmax + top-K of the frontier rows, children, layer order)",
-             "verify_rows": "verify_stream_kernel (argmax / softmax pieces of the used target rows)"}
+             "verify_rows": "verify_stream_kernel (argmax / softmax pieces of the used target rows)",
+             "verify_sampled": "verify_stream_kernel + verify_sampled_kernel (target-row statistics, then the "
+                               "recursive-residual walk; bytes: the used target rows)"}
     roofline = {"bound": "hbm", "achieved": kern[top]["gbs"], "peak": peak, "unit": "GB/s", "frac": kern[top]["frac"],
                 "traffic": None if tr is None else tr * kern[top]["bytes_per_launch"], "kernel": names[top],
                 "peak_source": peak_kind, "bytes_per_launch": kern[top]["bytes_per_launch"],
@@ -398,6 +413,8 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
         (3 if w["T"] == 1 else 2) + (1 if graft else 0)
     if block:  # reset, the block expansion, rerank, retrieval, meta, the verify, the M refresh
         launches = 5 + (3 if w["T"] == 1 else 2) + 1
+    if draw:  # the sampled verify: the streaming pass and the walk (which draws the bonus itself)
+        launches -= 1
 
     out = {"label": label, "value": value, "unit": UNIT, "ms_per_step": ms / steps, "steps": steps,
            "dtype": "bf16" if spec.dtype == synth.BF16 else "f32",
@@ -435,13 +452,14 @@ def kv_commit_run(torch, run, rec_out, steps, R):
 
     B, P = run.meta.tokens.shape
     Dp = run.accept_path.shape[1]
-    L = steps * Dp
+    L = max(steps, 3) * Dp  # room for the warm-up calls and for each replay's `steps` calls
     tmp = torch.empty((B, P, KV_ROW_BYTES), dtype=torch.uint8, device="cuda")
     cache = torch.empty((B, L, KV_ROW_BYTES), dtype=torch.uint8, device="cuda")
     cache_len = torch.zeros((B,), dtype=torch.int32, device="cuda")
     rows = sum(int((rec_out[s % R][0] + 1).sum()) for s in range(steps))
     for s in range(3):  # warm-up
         dt_commit_kv(run.h, tmp, cache, cache_len, rec_out[s % R][0], rec_out[s % R][3])
+    cache_len.zero_()
     torch.cuda.synchronize()
     # the calls of `steps` rounds captured as one CUDA graph (device time, not the host's call rate),
     # each replay starting again from an empty cache
