@@ -73,9 +73,11 @@ enum {
   DT_DEV_KV_FULL = 32      /* dt_commit_kv: a request's rows would pass the cache's capacity   */
 };
 /* dt_config.flags */
-enum { DT_FLAG_TEST_TIMEOUT = 1 }; /* test only: the streaming row passes (expansion and verify)
-                                      behave as if their reads had timed out: they read nothing, leave
-                                      empty results and set DT_DEV_TIMEOUT, exercising that path */
+enum { DT_FLAG_TEST_TIMEOUT = 1 }; /* test only: the expansion row scans (dt_expand_layer and the
+                                      calls built on it, dt_block_expand) give their first bounded
+                                      copy wait a limit of zero, so it runs out; the verify streaming
+                                      pass behaves as if its reads had timed out (reads nothing).
+                                      Either way empty results and DT_DEV_TIMEOUT, no fault */
 
 typedef struct dt_handle dt_handle;
 
@@ -409,8 +411,9 @@ int dt_commit_kv(dt_handle* h, const void* tmp_kv, int64_t tmp_pos_stride, int64
  * The counters must be zero when a call starts: they are zero when the library is loaded and each
  * call leaves them zero. The partials need no initial value.
  * The first call on each device does a one-time set-up (cudaGetSymbolAddress of the scratch,
- * the SM count, the kernels' shared-memory limit); make that first call outside any stream
- * capture. Every call on a device shares the one scratch: two calls that may overlap in time
+ * the SM count, the kernels' shared-memory limit), cached per device index for the life of the
+ * process; make that first call outside any stream capture. A device reset (cudaDeviceReset)
+ * invalidates that set-up and is not supported: calls after it may fail with DT_ERR_CUDA. Every call on a device shares the one scratch: two calls that may overlap in time
  * (different streams with no ordering between them) race and corrupt each other's results;
  * issue them on one stream or order them with events. */
 int dt_row_topk_static(const void* logits, int64_t ld, int32_t rows, int32_t V, int32_t K, int32_t dtype,
