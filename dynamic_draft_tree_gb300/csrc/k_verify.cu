@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
   __shared__ int32_t s_tok[kMaxP], s_par[kMaxP], s_amax[kMaxP], s_depth[kMaxP];
   __shared__ uint8_t s_reach[kMaxP], s_haschild[kMaxP];
   __shared__ unsigned long long s_best;
-  __shared__ int32_t s_cur, s_len, s_nrej, s_state;
+  __shared__ int32_t s_cur, s_len, s_nrej, s_state, s_nkids, s_jpos;
   __shared__ double s_sres;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
@@ -277,54 +277,77 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
     st.s = s_S;
     st.amax = -1;
     const double S = st.s;
-    __syncthreads();
+    // the children of cur in position order, each one's e = exp(x_t - M) and acceptance uniform
+    // loaded in parallel; the tests then only compare them (one thread, in order)
     if (tid == 0) {
+      int n = 0;
+      for (int c = s_first_child[cur]; c >= 0 && n < kMaxP; c = s_next_sib[c]) s_amax[n++] = c;
+      s_nkids = n;
       s_nrej = 0;
       s_sres = S;
     }
+    __syncthreads();
+    const int nk = s_nkids;
+    float2* ev = reinterpret_cast<float2*>(s_key);  // (e, u) per child (s_key serves the greedy walk only)
+    for (int j = tid; j < nk; j += blockDim.x) {
+      const int c = s_amax[j];
+      const int t = s_tok[c];
+      float e = 0.0f;
+      if (t >= 0 && t < a.V) e = ex2((load_logit(a.logits, a.dtype, (lrow0 + cur) * a.ld + t) - st.m) * kLog2e);
+      const Philox4 w = philox4x32_10(a.r0, a.r1, (uint32_t)(512 * b + c), 0x80000000u, a.key0, a.key1);
+      ev[j] = make_float2(e, (float)(w.v[0] >> 8) * 5.9604644775390625e-08f);  // u: 24 bits x 2^-24, exact
+    }
+    __syncthreads();
     double s_ref = S;
-    int child = s_first_child[cur];
+    int child = -1;
     bool moved = false;
-    while (child >= 0) {
-      __syncthreads();  // every thread is done with the previous step's shared state
+    for (int j0 = 0, pass = 0; pass <= kMaxP; ++pass) {
       if (tid == 0) {
-        const int t = s_tok[child];
-        bool skip = t < 0;
-        if (t >= a.V) {
-          set_status(ws.status, DT_DEV_BAD_TOKEN);
-          skip = true;
+        // 0: every child tested; 1: child j accepted; 4: the running residual lost too much to
+        // cancellation before child j
+        int state = 0, j = j0, nrej = s_nrej;
+        double sres = s_sres;
+        for (; j < nk; ++j) {
+          const int t = s_tok[s_amax[j]];
+          bool skip = t < 0;
+          if (t >= a.V) {
+            set_status(ws.status, DT_DEV_BAD_TOKEN);
+            skip = true;
+          }
+          for (int r = 0; r < nrej && !skip; ++r) skip = s_rej[r] == t;
+          if (skip) continue;
+          if (sres < s_ref * 0.125) {
+            state = 4;
+            break;
+          }
+          const float2 eu = ev[j];
+          if ((double)eu.y * sres < (double)eu.x) {  // u < e / S_res = P_res(x), without the division
+            state = 1;
+            break;
+          }
+          s_rej[nrej++] = t;
+          sres -= (double)eu.x;
         }
-        for (int j = 0; j < s_nrej && !skip; ++j) skip = s_rej[j] == t;
-        s_state = skip ? 3 : (s_sres < s_ref * 0.125 ? 4 : 0);
+        s_nrej = nrej;
+        s_sres = sres;
+        s_state = state;
+        s_jpos = j;
       }
       __syncthreads();
-      const int st0 = s_state;
-      if (st0 == 4) {  // the running residual lost too much to cancellation: recompute it exactly
+      const int state = s_state;
+      j0 = s_jpos;
+      if (state == 4) {  // recompute the residual exactly, then test the same child again
         const double v = residual_rescan(a, lrow0 + cur, st.m, s_rej, s_nrej);
         if (tid == 0) s_sres = v;
         s_ref = v;
+        __syncthreads();
+        continue;
       }
-      __syncthreads();
-      if (tid == 0 && st0 != 3) {
-        const int t = s_tok[child];
-        const float x = load_logit(a.logits, a.dtype, (lrow0 + cur) * a.ld + t);
-        const float e = ex2((x - st.m) * kLog2e);
-        const Philox4 w = philox4x32_10(a.r0, a.r1, (uint32_t)(512 * b + child), 0x80000000u, a.key0, a.key1);
-        const double u = (double)(w.v[0] >> 8) * 5.9604644775390625e-08;  // 2^-24
-        if (u * s_sres < (double)e) {  // u < e / S_res = P_res(x), without the division
-          s_state = 1;
-        } else {
-          s_rej[s_nrej] = t;
-          s_nrej = s_nrej + 1;
-          s_sres = s_sres - (double)e;
-        }
-      }
-      __syncthreads();
-      if (s_state == 1) {
+      if (state == 1) {
         moved = true;
-        break;
+        child = s_amax[j0];
       }
-      child = s_next_sib[child];
+      break;
     }
     if (moved) {
       if (tid == 0) {

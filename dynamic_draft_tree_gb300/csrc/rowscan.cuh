@@ -390,16 +390,28 @@ __device__ __forceinline__ float gumbel_of_word(uint32_t w) {
   return -logf(-logf(u));
 }
 
-// G of token id, reusing the Philox block of the previous call when id is in the same group of four.
+// G of the four tokens of one Philox block. Out of line: one copy serves every call site.
+static __device__ __noinline__ float4 gumbel_group4(GumbelCtx g, uint32_t group) {
+  const Philox4 w = philox4x32_10(g.r0, g.r1, g.c2, group, g.k0, g.k1);
+  return make_float4(gumbel_of_word(w.v[0]), gumbel_of_word(w.v[1]), gumbel_of_word(w.v[2]), gumbel_of_word(w.v[3]));
+}
+
+// G of token id, reusing the block of the previous call when id is in the same group of four (the
+// four values are kept in registers: no indexed array).
 struct GumbelCursor {
   uint32_t group = 0xFFFFFFFFu;
-  Philox4 w;
+  float g0 = 0.0f, g1 = 0.0f, g2 = 0.0f, g3 = 0.0f;
   __device__ __forceinline__ float at(const GumbelCtx& g, uint32_t id) {
     if ((id >> 2) != group) {
       group = id >> 2;
-      w = philox4x32_10(g.r0, g.r1, g.c2, group, g.k0, g.k1);
+      const float4 v = gumbel_group4(g, group);
+      g0 = v.x;
+      g1 = v.y;
+      g2 = v.z;
+      g3 = v.w;
     }
-    return gumbel_of_word(w.v[id & 3u]);
+    const uint32_t s = id & 3u;
+    return s == 0u ? g0 : (s == 1u ? g1 : (s == 2u ? g2 : g3));
   }
 };
 
@@ -636,7 +648,7 @@ __device__ SegOut scan_segment(const T* __restrict__ row, int64_t s0, int64_t s1
     if (GUMBEL) {
       flm = -INFINITY;
       GumbelCursor gcur;
-#pragma unroll 1
+#pragma unroll
       for (int q = 0; q < QV; ++q) {
         float vm = -INFINITY;
 #pragma unroll
