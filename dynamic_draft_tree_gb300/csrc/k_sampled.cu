@@ -10,6 +10,8 @@
 // the bonus token is a Gumbel-max draw from the last residual.
 #include <algorithm>
 
+#include <cooperative_groups.h>
+
 #include "rowstream.cuh"
 
 namespace dt {
@@ -17,6 +19,10 @@ namespace {
 
 constexpr int kSampThreads = 512;
 constexpr int kSampWarps = kSampThreads / 32;
+// A request's walk runs on a thread-block cluster: every CTA follows the same walk (the decisions are
+// computed identically from the same data), each pass over the vocabulary is split across the CTAs,
+// and the partial sums and the bonus candidates meet through distributed shared memory.
+constexpr int kSampCluster = 8;
 constexpr int kMaxKids = kMaxK;  // children of a node <= K <= 32
 
 struct SampledArgs {
@@ -64,9 +70,15 @@ __device__ __forceinline__ float residual_at(const Resid& s, float p, float q, i
   return r;
 }
 
-// One CTA per request.
+// One cluster of kSampCluster CTAs per request.
 __global__ void __launch_bounds__(kSampThreads) verify_sampled_kernel(SampledArgs a) {
   pdl_begin();
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int ncta = (int)cluster.num_blocks();
+  __shared__ double s_zpart[2];               // this CTA's partial Z of a pass (slot = pass parity)
+  __shared__ unsigned long long s_bkey;       // this CTA's best bonus key
   __shared__ uint64_t s_mbuf[256];
   __shared__ uint64_t s_mtop[kMaxK];
   __shared__ int32_t s_tok[kMaxP], s_par[kMaxP], s_dep[kMaxP], s_node[kMaxP];
@@ -78,8 +90,12 @@ __global__ void __launch_bounds__(kSampThreads) verify_sampled_kernel(SampledArg
   __shared__ int64_t s_A, s_base;
   __shared__ int32_t s_cur, s_len, s_state;
   __shared__ double s_Q;  // q mass of the children tested so far at the current node
-  const int b = blockIdx.x;
+  const int b = blockIdx.x / ncta;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // this CTA's slice of the vocabulary, in groups of four tokens (one Philox block each)
+  const int64_t slice = ((((int64_t)a.V + ncta - 1) / ncta) + 3) / 4 * 4;
+  const int64_t v_lo = min((int64_t)a.V, rank * slice), v_hi = min((int64_t)a.V, v_lo + slice);
+  int npass = 0;
   Workspace& ws = a.ws;
   const int P = a.P;
   const int Dp = a.meta.D_path;
@@ -104,7 +120,8 @@ __global__ void __launch_bounds__(kSampThreads) verify_sampled_kernel(SampledArg
   __syncthreads();
   const int64_t rowA = s_A, rowbase = s_base;
   const PieceMap pm(rowA, a.V, stream_warps(rowA, a.V, a.dtype == DT_BF16 ? 2 : 4, a.Gtot, a.maxp), a.vecel);
-  for (int p = tid; p < npos; p += blockDim.x) ws.row_tau[rowbase + p] = 0ull;  // the pass is over
+  if (rank == 0)
+    for (int p = tid; p < npos; p += blockDim.x) ws.row_tau[rowbase + p] = 0ull;  // the pass is over
   if (tid == 0) {
     for (int p = 0; p < P; ++p) {
       s_first_child[p] = -1;
@@ -146,7 +163,7 @@ __global__ void __launch_bounds__(kSampThreads) verify_sampled_kernel(SampledArg
         warp_merge_row(ws.partials + rp.slot0, rp.S, 1, s_mbuf, 256, s_mtop, true, M, sh, sl);
       }
       if (lane == 0) {
-        if (sh != sh || !(M > -INFINITY) || M == INFINITY || !(sh > 0.0f) || sh == INFINITY)
+        if (rank == 0 && (sh != sh || !(M > -INFINITY) || M == INFINITY || !(sh > 0.0f) || sh == INFINITY))
           set_status(ws.status, DT_DEV_BAD_LOGITS);
         s_res.Mp = M;
         s_res.invSp = (float)(1.0 / ((double)sh + (double)sl));
@@ -174,7 +191,7 @@ __global__ void __launch_bounds__(kSampThreads) verify_sampled_kernel(SampledArg
         const int n = s_res.nrej;
         s_state = 0;
         if (t < 0 || t >= a.V || n >= kMaxKids) {
-          set_status(ws.status, t >= a.V || n >= kMaxKids ? DT_DEV_BAD_TOKEN : DT_DEV_BAD_TREE);
+          if (rank == 0) set_status(ws.status, t >= a.V || n >= kMaxKids ? DT_DEV_BAD_TOKEN : DT_DEV_BAD_TREE);
           s_state = 2;
         } else {
           const double p_t = exp((double)load_elt(prow, a.dtype, t) - (double)s_res.Mp) * (double)s_res.invSp;
@@ -205,11 +222,12 @@ __global__ void __launch_bounds__(kSampThreads) verify_sampled_kernel(SampledArg
         break;
       }
       if (st == 0) {
-        // rejected: Z_{n+1} = sum_v max(0, r_n(v) - q_n(v)), one pass over both rows
+        // rejected: Z_{n+1} = sum_v max(0, r_n(v) - q_n(v)), one pass over both rows, split across the
+        // cluster's CTAs
         Resid& R = s_res;
         const int n = R.nrej;  // the rejected child is draw index n
         double part = 0.0;
-        for (int64_t v = tid; v < a.V; v += blockDim.x) {
+        for (int64_t v = v_lo + tid; v < v_hi; v += blockDim.x) {
           const float xp = load_elt(prow, a.dtype, v), xq = load_elt(qrow, a.dtype, v);
           const float p = __expf(xp - R.Mp) * R.invSp, q = __expf(xq - R.Mq) * R.invSq;
           const float r = residual_at(R, p, q, (int32_t)v);
@@ -221,12 +239,22 @@ __global__ void __launch_bounds__(kSampThreads) verify_sampled_kernel(SampledArg
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
         if (lane == 0) s_red[warp] = part;
         __syncthreads();
+        const int slot = npass & 1;
+        if (tid == 0) {
+          double z = 0.0;
+          for (int w = 0; w < kSampWarps; ++w) z += s_red[w];
+          s_zpart[slot] = z;
+        }
+        // every CTA adds the cluster's partials in rank order (the same Z everywhere); a slot is written
+        // again two passes later, after every CTA has passed the next pass's barrier
+        cluster.sync();
         if (tid == 0) {
           double Z = 0.0;
-          for (int w = 0; w < kSampWarps; ++w) Z += s_red[w];
+          for (int r = 0; r < ncta; ++r) Z += *cluster.map_shared_rank(&s_zpart[slot], r);
           R.invZ[n + 1] = Z > 0.0 ? (float)(1.0 / Z) : 0.0f;
           R.nrej = n + 1;
         }
+        ++npass;
         __syncthreads();
       }
       child = s_next_sib[child];
@@ -246,12 +274,12 @@ __global__ void __launch_bounds__(kSampThreads) verify_sampled_kernel(SampledArg
     {
       const Resid& R = s_res;
       unsigned long long best = 0ull;
-      for (int64_t g4 = tid; g4 * 4 < a.V; g4 += blockDim.x) {
+      for (int64_t g4 = v_lo / 4 + tid; g4 * 4 < v_hi; g4 += blockDim.x) {
         const Philox4 w = philox4x32_10(a.r0, a.r1, (uint32_t)(512 * b + cur), (uint32_t)g4, a.key0, a.key1);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int64_t v = g4 * 4 + e;
-          if (v >= a.V) break;
+          if (v >= v_hi) break;
           const float xp = load_elt(prow, a.dtype, v);
           float r;
           if (has_kids) {
@@ -270,16 +298,26 @@ __global__ void __launch_bounds__(kSampThreads) verify_sampled_kernel(SampledArg
       atomicMax(&s_best, best);
     }
     __syncthreads();
-    if (tid == 0) {
-      // no token with r > 0 (an empty residual): token 0, as an argmax over all -inf
-      a.bonus[b] = s_best ? (int32_t)key_id(s_best) : 0;
-      a.accept_len[b] = s_len;
+    if (tid == 0) s_bkey = s_best;
+    cluster.sync();  // every CTA's best key is in place
+    if (rank == 0) {
+      if (tid == 0) {
+        unsigned long long best = 0ull;
+        for (int r = 0; r < ncta; ++r) {
+          const unsigned long long k = *cluster.map_shared_rank(&s_bkey, r);
+          best = k > best ? k : best;
+        }
+        // no token with r > 0 (an empty residual): token 0, as an argmax over all -inf
+        a.bonus[b] = best ? (int32_t)key_id(best) : 0;
+        a.accept_len[b] = s_len;
+      }
+      for (int j = tid; j < Dp; j += blockDim.x) a.accept_path[(int64_t)b * Dp + j] = j <= s_len ? s_path[j] : -1;
     }
-    __syncthreads();
-    for (int j = tid; j < Dp; j += blockDim.x) a.accept_path[(int64_t)b * Dp + j] = j <= s_len ? s_path[j] : -1;
+    cluster.sync();  // no CTA leaves while rank 0 may still read its shared memory
     return;
   }
-  if (tid == 0) set_status(ws.status, DT_DEV_INTERNAL);
+  cluster.sync();  // (never reached in a valid tree) no CTA leaves while another may read its shared memory
+  if (rank == 0 && tid == 0) set_status(ws.status, DT_DEV_INTERNAL);
 }
 
 }  // namespace
@@ -313,7 +351,22 @@ cudaError_t launch_verify_sampled(dt_handle* h, const dt_tree_meta* meta, const 
   a.accept_len = accept_len;
   a.accept_path = accept_path;
   a.bonus = bonus;
-  launch_k(verify_sampled_kernel, dim3(h->B), dim3(kSampThreads), 0, s, a);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kSampCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(h->B * kSampCluster));
+  cfg.blockDim = dim3(kSampThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, verify_sampled_kernel, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
