@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kRowThreads, 4) expand_kernel(ExpandArgs a) {
   auto cnt = [&](int b) -> int { return min(max(ws.frontier_count[b], 0), a.F); };
   if (tid < 32) {
     RowPlan p;
-    plan_rows(p, a.B, a.V, a.Smax, (int)sizeof(T), cnt);
+    plan_rows(p, a.B, a.V, a.Smax, (int)sizeof(T), cnt, GUMBEL ? 1 : 2);
     if (tid == 0) plan = p;
     if (blockIdx.x == 0)  // a frontier wider than the launch's F is a caller error
       for (int b = tid; b < a.B; b += 32)

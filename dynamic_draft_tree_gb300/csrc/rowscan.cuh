@@ -872,11 +872,13 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t E, int64_t G) {
 }
 
 // Warp 0 of every CTA: the layout, this CTA's range and the (b, i) of its first row. A piece holds at
-// least r_min elements: two stages per warp (so that every lane of a warp sees data and the top-K list
-// starts full), and r_min >= (V - 1) / (Smax - 2), so that a row has at most Smax pieces. The first 32
-// counts are read once and kept in a register.
+// least r_min elements: min_stages stages per warp (two for the streaming passes, whose time is the
+// chain of dependent steps; one for compute-heavy passes such as the draw noise of sampled drafts;
+// either way every lane of a warp sees data and the top-K list starts full), and
+// r_min >= (V - 1) / (Smax - 2), so that a row has at most Smax pieces. The first 32 counts are read
+// once and kept in a register.
 template <class Cnt>
-__device__ void plan_rows(RowPlan& p, int B, int64_t V, int Smax, int esz, Cnt cnt) {
+__device__ void plan_rows(RowPlan& p, int B, int64_t V, int Smax, int esz, Cnt cnt, int min_stages = 2) {
   const int lane = threadIdx.x & 31;
   const int head = lane < B ? cnt(lane) : 0;
   int64_t A = 0;
@@ -894,7 +896,8 @@ __device__ void plan_rows(RowPlan& p, int B, int64_t V, int Smax, int esz, Cnt c
   // 32-bit unsigned arithmetic where it suffices (V < 2^31, A and the grid <= 4096): the divisions
   // here are on the launch's critical path
   const uint32_t Vu = (uint32_t)V;
-  const uint32_t r_min = max((uint32_t)(kScanWarps * 2 * kStageBytes / esz), (Vu - 1u + (uint32_t)(Smax - 3)) / (uint32_t)(Smax - 2));
+  const uint32_t r_min = max((uint32_t)(kScanWarps * min_stages * kStageBytes / esz),
+                             (Vu - 1u + (uint32_t)(Smax - 3)) / (uint32_t)(Smax - 2));
   const int64_t c = blockIdx.x;
   if (A <= (int64_t)gridDim.x) {
     const uint32_t Au = (uint32_t)A, cu = (uint32_t)c;
