@@ -429,6 +429,7 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
 
     if with_e2e:
         out["kv_commit"] = kv_commit_run(torch, run, rec_out, steps, R)
+        out["verify_steady"] = verify_steady_run(torch, run, w, rec_target, R, esz)
 
     # ---- end to end through the public API with host buffers ----
     if with_e2e and args.e2e_steps > 0:
@@ -439,6 +440,50 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
     run.h.close()
     torch.cuda.empty_cache()
     return out
+
+
+def verify_steady_run(torch, run, w, rec_target, R, esz, calls=64):
+    """dt_verify (streaming pass + acceptance walk) of the last replayed round's tree against the recorded
+    rounds' target rows, `calls` calls back to back in one CUDA graph (programmatic launch overlap
+    kept), each reading a different round's rows (> L2 apart): the verify's steady state, as in a
+    pipeline that keeps the GPU busy. Bytes = the tree's used rows x V x element size per call."""
+    from dynamic_draft_tree_gb300 import dt_verify, dt_get_status, DT_GREEDY, DT_SAMPLE
+
+    mode = DT_SAMPLE if w["T"] == 1 else DT_GREEDY
+    nbytes = int((run.meta.tokens >= 0).sum()) * w["V"] * esz
+    acc = torch.empty_like(run.accept_len)
+    path = torch.empty_like(run.accept_path)
+    bon = torch.empty_like(run.bonus)
+
+    def call(i):
+        dt_verify(run.h, run.meta, rec_target[i % R], mode, w["seed"], i, acc, path, bon, run.top8)
+
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize()
+    gph = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(gph, stream=cs):
+            for i in range(calls):
+                call(i)
+    torch.cuda.current_stream().wait_stream(cs)
+    times = []
+    for _ in range(6):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        gph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert dt_get_status(run.h) == 0
+    us = float(np.median(times[1:])) * 1e3 / calls
+    peak, _ = measured_peaks()
+    return {"us_per_call": us, "bytes_per_call": nbytes, "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak,
+            "note": "dt_verify (streaming pass + walk) calls back to back in one CUDA graph, median of 5 replays; "
+                    "not part of value"}
 
 
 KV_ROW_BYTES = 32 * 2 * 8 * 128 * 2  # one token's keys and values: 32 layers, 8 KV heads of 128, bf16
@@ -602,7 +647,7 @@ def run_ours(args):
         "roofline": head["roofline"], "kernels": head["kernels"], "replay": head["replay"],
         "e2e": head.get("e2e"), "gpu_launches": head["gpu_launches"],
         "replay_consistent": head["replay_consistent"], "rows_per_round": head["rows_per_round"],
-        "kv_commit": head.get("kv_commit"),
+        "kv_commit": head.get("kv_commit"), "verify_steady": head.get("verify_steady"),
         "clocks": head["clocks"], "per_config": per_config,
     }
     return line

@@ -446,9 +446,12 @@ __device__ void stream_rows(int B, int64_t V, int K, int maxp, int64_t Gtot, War
           // later stages: against the larger of the list's K-th key and the row's shared threshold.
           // Ids grow stage by stage within the piece, so a value equal to the warp's own K-th key's
           // value cannot beat it: strict against the own key, not against another warp's. The
-          // candidates only accumulate in the buffer; they are merged at the end of the piece, or
-          // as soon as the buffer is half full (then the threshold rises and the stage is filtered
-          // again, keys already in the list dropped by the merge).
+          // candidates accumulate in the buffer and are merged at the end of the piece, or as soon as
+          // K of them wait (greedy passes) or the buffer is half full (softmax passes); then the
+          // threshold rises for the stages that follow, and the stage is filtered again, keys already
+          // in the list dropped by the merge. Both limits are the faster one measured for their pass:
+          // merging at K keeps a greedy pass's later stages cold; a softmax pass's stages cost more
+          // than the extra merges save.
           for (int round = 0;; ++round) {
             uint64_t tk = tau_key;
             bool own = true;
@@ -466,7 +469,7 @@ __device__ void stream_rows(int B, int64_t V, int K, int maxp, int64_t Gtot, War
                 if (own ? (vmax[q] > tv) : (vmax[q] >= tv)) qm |= 1u << q;
             }
             push_from_ring<T>(rg, sp, nv, be0, qm, tv, tk);
-            if (rg.cnt < kWarpCand / 2) break;  // deferred: merged later
+            if (rg.cnt < (SOFTMAX ? kWarpCand / 2 : K)) break;  // deferred: merged later
             // a stage filtered again after an overflow pushes keys the list already holds: every
             // merge of deferred keys drops those first
             const bool overflow = merge(true);
