@@ -375,6 +375,39 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
   if (tid == 0) set_status(ws.status, DT_DEV_INTERNAL);
 }
 
+// The top-8 ids of every used row from its pieces (Graft page step (3): every verified row refreshes M
+// with its top-k successors), one warp per row over many CTAs, rows numbered as in the streaming
+// pass; launched before the walk, which then needs only each row's argmax.
+constexpr int kTop8Warps = 8;
+__global__ void __launch_bounds__(32 * kTop8Warps) verify_top8_kernel(WalkArgs a) {
+  pdl_begin();
+  __shared__ uint64_t s_mbuf[kTop8Warps][256];
+  __shared__ uint64_t s_mtop[kTop8Warps][kMaxK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t j = (int64_t)blockIdx.x * kTop8Warps + warp;
+  auto cnt = [&](int bb) -> int { return min(max(a.meta.n_pos[bb], 0), a.P); };
+  const int64_t A = warp_total_rows(a.B, cnt);
+  if (j >= A) return;
+  int b, i;
+  warp_find_row(a.B, j, cnt, b, i);
+  if (b >= a.B) return;
+  const int64_t r = (int64_t)b * a.P + i;
+  if (a.meta.tokens[r] < 0) {
+    if (lane < 8) a.top8[r * 8 + lane] = -1;
+    return;
+  }
+  const PieceMap pm(A, a.V, stream_warps(A, a.V, a.esz, a.Gtot, a.maxp), a.vecel);
+  const RowPieces rp = pm.row(j);
+  if (rp.S > a.maxp) {  // never: the streaming plan bounds the pieces of a row
+    if (lane == 0) set_status(a.ws.status, DT_DEV_INTERNAL);
+    return;
+  }
+  float M, sh, sl;
+  warp_merge_row(a.ws.partials + rp.slot0, rp.S, a.K, s_mbuf[warp], 256, s_mtop[warp], false, M, sh, sl);
+  const uint64_t k = lane < 8 ? s_mtop[warp][lane] : 0ull;
+  if (lane < 8) a.top8[r * 8 + lane] = (lane < a.K && k != 0ull) ? (int32_t)key_id(k) : -1;
+}
+
 struct BonusArgs {
   Workspace ws;
   const void* logits;
@@ -528,6 +561,14 @@ cudaError_t launch_verify_accept(dt_handle* h, const dt_tree_meta* meta, const v
   wa.esz = esz;
   wa.vecel = 16 / esz;
   wa.Gtot = (int64_t)stream_grid(h) * kStreamWarps;
+  if (top8) {  // the top-8 merges on many CTAs first; the walk then takes each row's argmax alone
+    const int64_t rows = (int64_t)h->B * P;
+    launch_k(verify_top8_kernel, dim3((unsigned)((rows + kTop8Warps - 1) / kTop8Warps)), dim3(32 * kTop8Warps), 0, s,
+             wa);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    wa.top8 = nullptr;
+  }
   launch_k(verify_walk_kernel, dim3(h->B), dim3(kWalkThreads), 0, s, wa);
   e = cudaGetLastError();
   if (e != cudaSuccess || mode != DT_SAMPLE) return e;

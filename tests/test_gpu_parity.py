@@ -210,6 +210,13 @@ def test_round_parity_sampling_many_rounds(torch, name, over):
     _run_rounds(torch, with_sizes(name, **over), 24, label=f"T=1 {name} {over}")
 
 
+def test_round_parity_graft_sampling(torch):
+    """Graft with the stochastic verify (T = 1): the M refresh reads the top-8 of every verified row
+    whatever the acceptance rule (Graft page step (3))."""
+    w = with_sizes("graft", V=2003, B=4, T=1)
+    _run_rounds(torch, w, 8, label="graft T=1", chain_roots=False)
+
+
 def test_round_parity_graft_after_warmup(torch):
     """Graft page step (3): every round drafts again from the same root tokens, so the refresh of M
     from the verified positions fills the rows the template reads: after five warm-up rounds
