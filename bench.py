@@ -406,13 +406,15 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
     # kernels of the library launched per round: reset + layer-1 frontier; per layer the expansion and
     # the pruning / frontier kernels (CAST: 1 fused; Graft: checkpoint + frontier; EAGLE: frontier; none
     # after the last layer except CAST's and Graft's pruning); verify count + rerank (CAST) or rerank,
-    # retrieval (Graft), meta, 2 or 3 for the verify (the bonus draw with sampling), the M refresh (Graft)
+    # retrieval (Graft), meta, 2 to 4 for the verify (the top-8 merge with Graft, the bonus draw with sampling),
+    # the M refresh (Graft)
     per_layer = {"cast": 1, "graft": 2, "eagle": 1}[w["policy"]]
     last = 1 if w["policy"] in ("cast", "graft") else 0
+    verify_launches = (3 if w["T"] == 1 else 2) + (1 if graft else 0)  # pass, (top-8,) walk, (bonus)
     launches = 2 + D + per_layer * (D - 1) + last + (2 if w["policy"] == "cast" else 1) + (1 if graft else 0) + 1 + \
-        (3 if w["T"] == 1 else 2) + (1 if graft else 0)
+        verify_launches + (1 if graft else 0)
     if block:  # reset, the block expansion, rerank, retrieval, meta, the verify, the M refresh
-        launches = 5 + (3 if w["T"] == 1 else 2) + 1
+        launches = 5 + verify_launches + 1
     if draw:  # the sampled verify: the streaming pass and the walk (which draws the bonus itself)
         launches -= 1
 
