@@ -434,6 +434,12 @@ static __device__ __noinline__ void push_batch_candidates(WarpRing& rg, const ui
         const int vi = q * 32 + lane;
         if (vi * 16 >= st_bytes) break;
         const uint4 w = *reinterpret_cast<const uint4*>(sp + (size_t)vi * 16);
+        if (!GUMBEL) {  // a vector whose maximum is below the threshold holds no candidate
+          const uint32_t m2 = ESZ == 2 ? max_nan_bf16x2(max_nan_bf16x2(w.x, w.y), max_nan_bf16x2(w.z, w.w))
+                                       : max_nan_f32u(max_nan_f32u(w.x, w.y), max_nan_f32u(w.z, w.w));
+          const float vm = ESZ == 2 ? max_nan_f32(bf16_lo(m2), bf16_hi(m2)) : __uint_as_float(m2);
+          if (vm < tv) continue;  // (a NaN maximum is not below it: its elements are looked at)
+        }
         GumbelCursor gcur;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
