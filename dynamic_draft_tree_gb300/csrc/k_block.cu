@@ -11,7 +11,6 @@
 #include <algorithm>
 
 #include "rowscan.cuh"
-#include "cast_block.cuh"
 
 namespace dt {
 namespace {

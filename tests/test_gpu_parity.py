@@ -149,6 +149,30 @@ def test_host_argument_errors(torch):
         dt.dt_expand_layer(h, x, 1, ld=999)             # ld < V
     with pytest.raises(dt.DtError):
         dt.dt_tree_reset(h, torch.zeros(3, dtype=torch.int32, device="cuda"))  # B > B_max
+    # the entry points of the extensions refuse bad arguments on the host, before any launch
+    blk = torch.zeros((2, 4, 1000), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dt.DtError):
+        dt.dt_block_expand(h, blk, 4)                   # L > D_max
+    dt.dt_expand_layer(h, x, 1)
+    with pytest.raises(dt.DtError):
+        dt.dt_block_expand(h, blk, 2)                   # not right after a reset
+    meta = dt.Meta(2, 9, 4)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    out = [torch.zeros(2, **i32), torch.zeros((2, 4), **i32), torch.zeros(2, **i32)]
+    tgt = torch.zeros((2, 9, 1000), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dt.DtError):                    # sampled verify: mode is 0 or DT_VERIFY_PACKED only
+        lib_mode = dt.lib.dt_verify_sampled(h.h, dt.ctypes.byref(meta.c), tgt.data_ptr(), 1000, dt.DT_SAMPLE,
+                                            tgt.data_ptr(), 1000, 0, 0, out[0].data_ptr(), out[1].data_ptr(),
+                                            out[2].data_ptr(), None)
+        dt.check(lib_mode)
+    tpl = dt.Template([-1, 0], [0, 0], anchor=dt.DT_ANCHOR_TAIL)
+    M = torch.full((2, 1000, 8), -1, **i32)
+    with pytest.raises(dt.DtError):                    # a tail anchor needs the kept nodes
+        dt.dt_graft_retrieve(h, M, tpl, 4, torch.zeros((2, 4), **i32), torch.zeros((2, 4), **i32), out[0])
+    kv = torch.zeros((2, 9, 24), dtype=torch.uint8, device="cuda")   # 24-byte rows: not a multiple of 16
+    cache = torch.zeros((2, 16, 24), dtype=torch.uint8, device="cuda")
+    with pytest.raises(dt.DtError):
+        dt.dt_commit_kv(h, kv, cache, out[0], out[0], out[1])
     h.close()
 
 
