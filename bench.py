@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--per-config-steps", type=int, default=100)
     ap.add_argument("--min-replay-s", type=float, default=1.0, help="time the K-step graph for at least this long")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-gather-blocks", type=int, default=32,
+                    help="CTAs of the kernel that reads the host rows for e2e (0: one DMA copy per row block)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--record-rounds", type=int, default=0,
                     help="recorded rounds replayed (0: enough for 3x L2 of inputs); small values for profiling runs")
@@ -436,7 +438,7 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
     # ---- end to end through the public API with host buffers ----
     if with_e2e and args.e2e_steps > 0:
         out["e2e"] = e2e_run(torch, run, w, rec_draft, rec_target, roots, rec_out, act_rec, npos_rec, esz, M,
-                             args.e2e_steps, world)
+                             args.e2e_steps, world, args.e2e_gather_blocks)
     assert dt_get_status(run.h) == 0, "device status set during the timed region"
     del rec_draft, rec_target
     run.h.close()
@@ -539,11 +541,15 @@ def kv_commit_run(torch, run, rec_out, steps, R):
                     "not part of the round's graph"}
 
 
-def e2e_run(torch, run, w, rec_draft, rec_target, roots, rec_out, act_rec, npos_rec, esz, M, steps, world):
+def e2e_run(torch, run, w, rec_draft, rec_target, roots, rec_out, act_rec, npos_rec, esz, M, steps, world,
+            gather_blocks=0):
     """The recorded round 0 through the public API from pinned host buffers, every step: the rows the
     round reads (each request's active frontier rows per layer, its used target positions) and the roots
     copied host -> device, the round, and the accepted lengths, paths and bonus tokens copied back.
-    The inputs are double-buffered: step s + 1's copies run on a copy stream while step s runs."""
+    The inputs are double-buffered: step s + 1's copies run on a copy stream while step s runs. With
+    gather_blocks > 0 the copies are one kernel of that many CTAs reading the pinned host memory
+    through its device mapping (checked once against plain copies first); else one DMA copy per row
+    block."""
     B, k, V = w["B"], w["k"], w["V"]
     h_draft = rec_draft[0].cpu().pin_memory()
     h_target = rec_target[0].cpu().pin_memory()
@@ -574,10 +580,33 @@ def e2e_run(torch, run, w, rec_draft, rec_target, roots, rec_out, act_rec, npos_
     copy_stream = torch.cuda.Stream()
     copied = [torch.cuda.Event(), torch.cuda.Event()]
 
+    # the same row blocks as (source, destination, bytes) spans for the gather kernel
+    import synth
+    spans = None
+    if gather_blocks > 0:
+        src0 = [synth.host_device_ptr(t) for t in (h_roots, h_draft, h_target)]
+        if all(p is not None for p in src0):
+            spans = []
+            row_b = V * esz
+            per_layer = hd.shape[1]
+            for r_, dr_, tg_ in bufs:
+                sp = [(src0[0], r_.data_ptr(), h_roots.numel() * 4)]
+                for kind, d, r0, n in chunks:
+                    off = ((d * per_layer + r0) if kind == "d" else r0) * row_b
+                    src_t, dst_t = (h_draft, dr_) if kind == "d" else (h_target, tg_)
+                    assert off + n * row_b <= src_t.numel() * esz and off + n * row_b <= dst_t.numel() * esz
+                    sp.append((src0[1 if kind == "d" else 2] + off, dst_t.data_ptr() + off, n * row_b))
+                spans.append(torch.tensor(sp, dtype=torch.int64, device="cuda"))
+
     def copy_inputs(i):
         r_, dr_, tg_ = bufs[i % 2]
         dd = dr_.view(dr_.shape[0], -1, V)
         tt = tg_.view(-1, V)
+        if spans is not None:
+            with torch.cuda.stream(copy_stream):
+                synth.gather_spans_gpu(torch, spans[i % 2], gather_blocks, copy_stream)
+                copied[i % 2].record(copy_stream)
+            return
         with torch.cuda.stream(copy_stream):
             r_.copy_(h_roots, non_blocking=True)
             for kind, d, r0, n in chunks:
@@ -587,6 +616,19 @@ def e2e_run(torch, run, w, rec_draft, rec_target, roots, rec_out, act_rec, npos_
                     tt[r0:r0 + n].copy_(ht[r0:r0 + n], non_blocking=True)
             copied[i % 2].record(copy_stream)
 
+    if spans is not None:  # the gather's bytes, checked once against plain copies of the same blocks
+        for i in range(2):
+            copy_inputs(i)
+        torch.cuda.synchronize()
+        for r_, dr_, tg_ in bufs:
+            dd = dr_.view(dr_.shape[0], -1, V)
+            tt = tg_.view(-1, V)
+            ok = torch.equal(r_.cpu(), h_roots)
+            for kind, d, r0, n in chunks:
+                ok = ok and (torch.equal(dd[d, r0:r0 + n].cpu(), hd[d, r0:r0 + n]) if kind == "d"
+                             else torch.equal(tt[r0:r0 + n].cpu(), ht[r0:r0 + n]))
+            if not ok:
+                raise RuntimeError("e2e: the host-row gather does not reproduce the copied rows")
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -616,7 +658,9 @@ def e2e_run(torch, run, w, rec_draft, rec_target, roots, rec_out, act_rec, npos_
     return {"value": job_throughput(steps, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": int(bi),
             "d2h_bytes_per_step": int(bo), "double_buffered": True, "consistent": consistent,
             "copies": "the rows the round reads (active frontier rows per layer and request, used target "
-                      "positions), as recorded"}
+                      "positions), as recorded",
+            "h2d_method": (f"one kernel of {gather_blocks} CTAs reading the pinned host rows through their device "
+                           f"mapping" if spans is not None else "one DMA copy per row block")}
 
 
 def run_ours(args):

@@ -110,6 +110,10 @@ def _gpu_lib():
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                            ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p]
         lib.synth_gen_rows_gpu.restype = ctypes.c_int
+        lib.synth_host_device_ptr.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]
+        lib.synth_host_device_ptr.restype = ctypes.c_int
+        lib.synth_gather_spans_gpu.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
+        lib.synth_gather_spans_gpu.restype = ctypes.c_int
         _gpu = lib
     return _gpu
 
@@ -197,6 +201,24 @@ def gen_rows_gpu(torch, spec, seed, salt, stream, ctx_dev, out_dev, ld, depth_de
                                        out_dev.data_ptr(), ld, R, cs)
     if rc != 0:
         raise RuntimeError(f"synth_gen_rows_gpu failed ({rc})")
+
+
+def host_device_ptr(t):
+    """Device address of a pinned host tensor's storage (its mapping for kernels), or None when the
+    memory is not mapped for the device."""
+    dev = ctypes.c_void_p()
+    if _gpu_lib().synth_host_device_ptr(ctypes.c_void_p(t.data_ptr()), ctypes.byref(dev)) != 0 or not dev.value:
+        return None
+    return int(dev.value)
+
+
+def gather_spans_gpu(torch, spans_dev, blocks, cuda_stream=None):
+    """Moves host bytes to the device with a kernel: spans_dev is a device int64 tensor [n][3] of
+    (source address for the device, destination address, bytes)."""
+    cs = (cuda_stream or torch.cuda.current_stream()).cuda_stream
+    rc = _gpu_lib().synth_gather_spans_gpu(spans_dev.data_ptr(), spans_dev.shape[0], blocks, cs)
+    if rc != 0:
+        raise RuntimeError(f"synth_gather_spans_gpu failed ({rc})")
 
 
 def bf16_bits_to_f64(bits):

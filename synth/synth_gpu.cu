@@ -169,3 +169,80 @@ extern "C" int synth_gen_rows_gpu(const synth_spec* sp, uint64_t seed, uint64_t 
                                               row_req, out, ld);
   return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }
+
+// ---- host rows into device buffers by a kernel (end-to-end timing) ----
+// A span moves `bytes` from src (pinned host memory, through its device mapping) to dst (device
+// memory). The SMs read the host memory directly over the host link, many loads in flight, instead of
+// one DMA copy per span.
+extern "C" {
+struct synth_span {
+  const void* src;
+  void* dst;
+  int64_t bytes;
+};
+}
+
+namespace {
+
+constexpr int kGatherThreads = 256;
+constexpr int kGatherMaxSpans = 512;
+constexpr int64_t kGatherUnit = (int64_t)kGatherThreads * 16 * 16;  // bytes of one work item (64 KB)
+
+__global__ void __launch_bounds__(kGatherThreads) gather_spans_kernel(const synth_span* __restrict__ spans, int n) {
+  __shared__ int64_t first[kGatherMaxSpans + 1];  // first work item of each span
+  __shared__ synth_span sp[kGatherMaxSpans];
+  if (threadIdx.x == 0) {
+    int64_t acc = 0;
+    for (int i = 0; i < n; ++i) {
+      sp[i] = spans[i];
+      first[i] = acc;
+      acc += (sp[i].bytes + kGatherUnit - 1) / kGatherUnit;
+    }
+    first[n] = acc;
+  }
+  __syncthreads();
+  const int64_t items = first[n];
+  int span = 0;
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+    while (span + 1 < n && first[span + 1] <= it) ++span;  // items grow, so the span only moves forward
+    const synth_span s = sp[span];
+    const int64_t lo = (it - first[span]) * kGatherUnit;
+    const int64_t hi = lo + kGatherUnit < s.bytes ? lo + kGatherUnit : s.bytes;
+    const char* src = static_cast<const char*>(s.src) + lo;
+    char* dst = static_cast<char*>(s.dst) + lo;
+    const int64_t nb = hi - lo;
+    if ((((uintptr_t)src | (uintptr_t)dst | (uintptr_t)nb) & 15u) == 0) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src);
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      const int n4 = (int)(nb / 16);
+      uint4 v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int q = threadIdx.x + u * kGatherThreads;
+        if (q < n4) v[u] = s4[q];
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int q = threadIdx.x + u * kGatherThreads;
+        if (q < n4) d4[q] = v[u];
+      }
+    } else {
+      for (int64_t q = threadIdx.x; q < nb; q += kGatherThreads) dst[q] = src[q];
+    }
+  }
+}
+
+}  // namespace
+
+// Device address of pinned host memory (0 on success).
+extern "C" int synth_host_device_ptr(void* host, void** dev) {
+  return cudaHostGetDevicePointer(dev, host, 0) == cudaSuccess ? 0 : -1;
+}
+
+// Moves every span (descriptors in device memory) with `blocks` CTAs on stream cs.
+extern "C" int synth_gather_spans_gpu(const synth_span* spans_dev, int32_t n, int32_t blocks, cudaStream_t cs) {
+  if (n <= 0) return 0;
+  if (spans_dev == nullptr || n > kGatherMaxSpans || blocks <= 0) return -1;
+  gather_spans_kernel<<<blocks, kGatherThreads, 0, cs>>>(spans_dev, n);
+  return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}

@@ -20,6 +20,29 @@ def torch():
     return t
 
 
+# ----------------------------------------------------------------- host-row gather ----
+def test_host_row_gather_matches_copies(torch):
+    """The end-to-end timing's host -> device gather kernel moves exactly the bytes of its spans: aligned
+    and unaligned spans, spans shorter and longer than one work item; bytes outside every span stay."""
+    host = torch.from_numpy(np.random.default_rng(5).integers(0, 256, 1 << 21, dtype=np.uint8)).pin_memory()
+    src = synth.host_device_ptr(host)
+    if src is None:
+        pytest.skip("pinned host memory is not mapped for the device")
+    dev = torch.zeros(1 << 21, dtype=torch.uint8, device="cuda")
+    cuts = [(0, 0, 256512 * 3), (1 << 20, 1 << 20, 64 * 1024 + 16), (7, 800000, 1000), (1900001, 1900003, 77),
+            (1950000, 1960000, 16)]
+    spans = torch.tensor([(src + a, dev.data_ptr() + b, n) for a, b, n in cuts], dtype=torch.int64,
+                         device="cuda")
+    for blocks in (1, 3, 32):
+        dev.zero_()
+        synth.gather_spans_gpu(torch, spans, blocks)
+        torch.cuda.synchronize()
+        want = torch.zeros_like(host)
+        for a, b, n in cuts:
+            want[b:b + n] = host[a:a + n]
+        assert torch.equal(dev.cpu(), want), blocks
+
+
 # ----------------------------------------------------------------- generator ----
 @pytest.mark.parametrize("name,over", [("pr1", dict(V=4099)), ("vicuna", dict(V=32000)),
                                        ("cast", dict(V=128256)), ("stress", dict(V=5003, B=6))])
