@@ -165,10 +165,10 @@ class Clocks:
 
 
 # DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte of the streaming
-# kernels, from the captures summarised in profiles/ (None while no capture of the current kernel exists).
-# DRAM bytes (read + write) per algorithmic byte from the ncu captures of the current kernels (CAST
-# workload, small case: expand layers 1-2, verify passes of two rounds); summaries under profiles/
-TRAFFIC_PER_ALGO_BYTE = {"expand": 1.0114, "verify_rows": 1.0267}
+# kernels, from the ncu captures of the current kernels (CAST workload, small case: expand layers 1-2,
+# verify passes of two rounds) summarised under profiles/; a kernel without a capture of its current
+# code has no entry (traffic null).
+TRAFFIC_PER_ALGO_BYTE = {"expand": 1.0117, "verify_rows": 1.0254}
 
 
 def measured_peaks():
