@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE, help="workload of the headline line")
+    ap.add_argument("--sizes", default="", help="sizes replaced in the headline workload, e.g. B=8 (profiling a "
+                    "smaller case; the line then names the case)")
     ap.add_argument("--workloads", default=",".join(OTHERS),
                     help="comma-separated workloads measured for the per_config block ('' for none)")
     ap.add_argument("--per-config-steps", type=int, default=100)
@@ -83,21 +85,36 @@ def job_throughput(units_per_rank, world, ms_max):
     return world * units_per_rank / (ms_max / 1e3)
 
 
-def workload_of(name):
+def workload_of(name, sizes=None):
     """(workload dict, label) of a bench workload name; vicuna_t1 is Vicuna with sampling (T = 1);
-    cast_req is the CAST batch with the per-request rule and padding-free target rows."""
+    cast_req is the CAST batch with the per-request rule and padding-free target rows. `sizes`
+    ({field: int}) replaces sizes of the workload (a smaller case of it, for profiling)."""
     from synth.workloads import WORKLOADS
 
     if name == "vicuna_t1":
         w = dict(WORKLOADS["vicuna"])
         w["T"] = 1
-        return w, "vicuna_t1"
-    if name == "cast_req":
+        label = "vicuna_t1"
+    elif name == "cast_req":
         w = dict(WORKLOADS["cast"])
         w["cast"] = dict(w["cast"], per_request=True)
         w["packed"] = True
-        return w, "cast_req"
-    return dict(WORKLOADS[name]), name
+        label = "cast_req"
+    else:
+        w, label = dict(WORKLOADS[name]), name
+    if sizes:
+        w.update(sizes)
+        label = f"{label} ({', '.join(f'{k_}={v_}' for k_, v_ in sizes.items())})"
+    return w, label
+
+
+def parse_sizes(text):
+    """'B=8,V=4099' -> {'B': 8, 'V': 4099}."""
+    out = {}
+    for part in filter(None, (text or "").split(",")):
+        k_, v_ = part.split("=")
+        out[k_.strip()] = int(v_)
+    return out
 
 
 def workload_config(w, g, label):
@@ -165,10 +182,12 @@ class Clocks:
 
 
 # DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte of the streaming
-# kernels, from the ncu captures of the current kernels (CAST workload, small case: expand layers 1-2,
-# verify passes of two rounds) summarised under profiles/; a kernel without a capture of its current
-# code has no entry (traffic null).
-TRAFFIC_PER_ALGO_BYTE = {"expand": 1.0117, "verify_rows": 1.0254}
+# kernels, per workload, from the ncu captures of the current kernels summarised under profiles/ (CAST:
+# expand layers 1-2 and the verify passes of two rounds; stress: its shape at B=32, expand layer 2 and
+# one verify pass, scaled by the rows a launch reads); a workload or kernel without a capture of its
+# current code has no entry (traffic null).
+TRAFFIC_PER_ALGO_BYTE = {("cast", "expand"): 1.0117, ("cast", "verify_rows"): 1.0254,
+                         ("stress", "expand"): 1.0245, ("stress", "verify_rows"): 1.0032}
 
 
 def measured_peaks():
@@ -216,7 +235,7 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
     from dynamic_draft_tree_gb300 import dt_get_status
     from dynamic_draft_tree_gb300.rounds import RoundRunner
 
-    w, label = workload_of(name)
+    w, label = workload_of(name, parse_sizes(args.sizes) if name == args.workload else None)
     w["seed"] = w["seed"] + 1000 * rank  # independent batch per rank
     g = geometry(w)
     spec = spec_for(w)
@@ -396,7 +415,7 @@ def measure_workload(name, steps, warmup, args, rank, world, local, with_e2e):
                                 "gbs": exp_bytes / (lay / 1e3) / 1e9}
     streaming = [k_ for k_ in ("expand", "verify_rows", "verify_sampled") if k_ in kern]
     top = max(streaming, key=lambda k_: kern[k_]["total_us_per_round"])
-    tr = TRAFFIC_PER_ALGO_BYTE.get(top)
+    tr = TRAFFIC_PER_ALGO_BYTE.get((label, top))
     names = {"expand": "expand_kernel (vocab softmax + top-K of the frontier rows, children, layer order)",
              "verify_rows": "verify_stream_kernel (argmax / softmax pieces of the used target rows)",
              "verify_sampled": "verify_stream_kernel + verify_sampled_kernel (target-row statistics, then the "
@@ -708,7 +727,7 @@ def run_reference(args):
     import harness
     from synth.workloads import geometry
 
-    w, label = workload_of(args.workload)
+    w, label = workload_of(args.workload, parse_sizes(args.sizes))
     g = geometry(w)
     # the oracle's rows come from a warm cache so that only the oracle itself is timed; the run is
     # bounded in time (the oracle takes seconds per round), so at most `budget` seconds of rounds are
@@ -741,14 +760,14 @@ def run_reference(args):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def cpu_baseline_sample(name, seconds=12.0):
+def cpu_baseline_sample(name, seconds=12.0, sizes=None):
     """Oracle rounds/s on the host, single process, rows pre-generated: bounded to ~seconds. Also counts
     the rounds whose oracle decision gaps fall below 1e-5 relative (the parity tests redraw those): the
     sampled rounds are the benchmark's own rounds 0, 1, ... (same seeds, salts and prefix lengths)."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import harness
 
-    w, _ = workload_of(name)
+    w, _ = workload_of(name, sizes)
     n, sec, rnd, redrawn, hit = 0, 0.0, 0, 0, 0
     while sec < seconds and n < 50:
         _, _, rej = harness.oracle_round(w, rnd)
@@ -773,7 +792,7 @@ def main():
     else:
         line = run_ours(args)
         if line is not None and not args.no_cpu_baseline:
-            line["cpu_baseline"], line["seed_redraws"] = cpu_baseline_sample(args.workload)
+            line["cpu_baseline"], line["seed_redraws"] = cpu_baseline_sample(args.workload, sizes=parse_sizes(args.sizes))
     if line is not None:
         print(json.dumps(line))
 
