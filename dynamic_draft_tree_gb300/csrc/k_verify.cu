@@ -76,16 +76,48 @@ __device__ __forceinline__ float load_logit(const void* logits, int dtype, int64
 constexpr int kWalkThreads = 256;
 
 // Exact residual mass of row `r` without the tokens rej[0..n_rej): fixed-point sum of
-// exp(x - M) (2^-46 units), so that subtracting the rejected terms cannot cancel.
-__device__ double residual_rescan(const WalkArgs& a, int64_t r, float M, const int32_t* rej, int n_rej) {
+// exp(x - M) (2^-46 units), so that subtracting the rejected terms cannot cancel. The integer sum
+// does not depend on the order of its terms; the row is read with 16-byte loads, four per thread in
+// flight (the elements before the first 16-byte boundary and after the last one singly).
+static __device__ __noinline__ double residual_rescan(const WalkArgs& a, int64_t r, float M, const int32_t* rej, int n_rej) {
   __shared__ unsigned long long acc;
   if (threadIdx.x == 0) acc = 0ull;
   __syncthreads();
   unsigned long long part = 0ull;
   const float scale = 70368744177664.0f;  // 2^46
-  for (int64_t v = threadIdx.x; v < a.V; v += blockDim.x) {
-    const float e = ex2((load_logit(a.logits, a.dtype, r * a.ld + v) - M) * kLog2e);
-    part += (unsigned long long)__float2ull_rn(e * scale);
+  auto term = [&](float x) -> unsigned long long {
+    return (unsigned long long)__float2ull_rn(ex2((x - M) * kLog2e) * scale);
+  };
+  const int esz = a.dtype == DT_BF16 ? 2 : 4;
+  const int per = 16 / esz;  // elements per vector
+  const char* row = reinterpret_cast<const char*>(a.logits) + r * a.ld * esz;
+  const int64_t head = min((int64_t)a.V, (int64_t)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(row) & 15u)) & 15u) / esz));
+  const int64_t nvec = ((int64_t)a.V - head) / per;
+  const int64_t tail0 = head + nvec * per;
+  for (int64_t v = threadIdx.x; v < head; v += blockDim.x) part += term(load_logit(a.logits, a.dtype, r * a.ld + v));
+  for (int64_t v = tail0 + threadIdx.x; v < a.V; v += blockDim.x)
+    part += term(load_logit(a.logits, a.dtype, r * a.ld + v));
+  const uint4* vp = reinterpret_cast<const uint4*>(row + head * esz);
+  const int64_t bd = blockDim.x;
+  for (int64_t q0 = threadIdx.x; q0 < nvec; q0 += 4 * bd) {
+    uint4 w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (q0 + u * bd < nvec) w[u] = __ldg(vp + q0 + u * bd);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (q0 + u * bd >= nvec) break;
+      const uint32_t wd[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (esz == 2) {
+          part += term(bf16_lo(wd[c]));
+          part += term(bf16_hi(wd[c]));
+        } else {
+          part += term(__uint_as_float(wd[c]));
+        }
+      }
+    }
   }
   atomicAdd(&acc, part);
   __syncthreads();
