@@ -271,3 +271,36 @@ def compare_round(gr, ref, check_tree=True):
         np.testing.assert_array_equal(run.stage.cpu().numpy(), np.asarray(ref["stage"]), err_msg="graft stage")
         np.testing.assert_array_equal(gr.M.cpu().numpy(), ref["M"], err_msg="M after refresh")
     del B
+
+
+def exact_residual_events(w, ref):
+    """Children of a T = 1 round's acceptance walk tested after the children rejected before them at
+    the same node held more than 7/8 of the row's softmax mass: there the device walk replaces its
+    running residual by an exact recomputation over the row. Counted from the oracle round ``ref``."""
+    rows = HostRows(w, spec_for(w), ref["salts"])
+    meta = ref["meta"]
+    V = w["V"]
+    n = 0
+    for b in range(w["B"]):
+        path = [int(p) for p in ref["accept_path"][b] if p >= 0]
+        tok, par, dep = meta["tokens"][b], meta["parents"][b], meta["depth"][b]
+        npos = int(meta["n_pos"][b])
+        for k, cur in enumerate(path):
+            nxt = path[k + 1] if k + 1 < len(path) else None
+            x = rows.target_row(b, int(dep[cur]) + 1, int(tok[cur]))
+            p = np.exp(x - x.max())
+            p /= p.sum()
+            rejected, share = set(), 0.0
+            for j in range(1, npos):
+                if int(par[j]) != cur:
+                    continue
+                t = int(tok[j])
+                if t < 0 or t >= V or t in rejected:
+                    continue  # not tested (the walk skips it)
+                if share > 7.0 / 8.0:
+                    n += 1
+                if j == nxt:
+                    break
+                rejected.add(t)
+                share += float(p[t])
+    return n

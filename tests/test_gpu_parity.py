@@ -205,13 +205,13 @@ SMALL = [("pr1", dict(V=4099)), ("pr1", dict(V=32000)), ("vicuna", dict(V=32000)
          ("vicuna", dict(V=8192, T=1)), ("pr1", dict(V=3001, K=1, k=1, m=1)), ("pr1", dict(V=3001, m=60))]
 
 
-def _run_rounds(torch, w, rounds, label=None, compare_from=0, chain_roots=True, packed=False):
+def _run_rounds(torch, w, rounds, label=None, compare_from=0, chain_roots=True, packed=False, on_ref=None):
     """GPU rounds against the oracle's, element by element; ``rounds`` is a count or the list of
     round indices. Graft chains its rounds: M comes from the previous round, and so does the next
     root (its bonus token) unless ``chain_roots`` is false (then every round drafts from the same
     root tokens). Rounds before ``compare_from`` run on both sides (warm-up) but are compared only
-    through M. ``packed``: padding-free target rows (DT_VERIFY_PACKED). Logs the seed redraws under
-    ``label``."""
+    through M. ``packed``: padding-free target rows (DT_VERIFY_PACKED). ``on_ref(ref)`` is called with
+    every compared oracle round. Logs the seed redraws under ``label``."""
     import harness
     from dynamic_draft_tree_gb300 import dt_get_status
 
@@ -230,6 +230,8 @@ def _run_rounds(torch, w, rounds, label=None, compare_from=0, chain_roots=True, 
         assert dt_get_status(gr.run.h) == 0
         if n >= compare_from:
             harness.compare_round(gr, ref)
+            if on_ref is not None:
+                on_ref(ref)
         elif w["policy"] == "graft":  # warm-up: the refreshed M must still agree
             np.testing.assert_array_equal(gr.M.cpu().numpy(), ref["M"], err_msg="M after warm-up round")
         if w["policy"] == "graft":
@@ -252,9 +254,19 @@ def test_round_parity_small(torch, name, over):
 # Stochastic verify (T = 1): 24 rounds each of a Vicuna-shaped and a stress-shaped batch at reduced
 # V, so that a few hundred acceptance tests and residual draws are compared (EAGLE-2 page,
 # §无损性为什么没有被动态树破坏).
+# The stress shape's low-entropy requests also reject children that hold most of a row's mass, which
+# sends the device walk through its exact residual recomputation: that branch must be among the
+# compared decisions.
 @pytest.mark.parametrize("name,over", [("vicuna", dict(V=4096, T=1)), ("stress", dict(V=3001, B=8, D=5))])
 def test_round_parity_sampling_many_rounds(torch, name, over):
-    _run_rounds(torch, with_sizes(name, **over), 24, label=f"T=1 {name} {over}")
+    import harness
+
+    w = with_sizes(name, **over)
+    events = []
+    _run_rounds(torch, w, 24, label=f"T=1 {name} {over}",
+                on_ref=lambda ref: events.append(harness.exact_residual_events(w, ref)))
+    if name == "stress":
+        assert sum(events) > 0, "no exact residual recomputation among the compared rounds"
 
 
 def test_round_parity_graft_sampling(torch):
