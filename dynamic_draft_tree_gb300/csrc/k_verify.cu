@@ -130,15 +130,14 @@ static __device__ __noinline__ double residual_rescan(const WalkArgs& a, int64_t
   return (double)tot * 1.4210854715202004e-14;  // 2^-46
 }
 
-constexpr int kWalkWarps = kWalkThreads / 32;
-
 // One CTA per request. The statistics of the target rows come from the streaming pass's pieces:
-// greedy verify merges every used row first (argmax, and the top-8 ids for the Graft refresh);
+// greedy verify merges every used row's argmax first (the top-8 ids for the Graft refresh are merged
+// before the walk by verify_top8_kernel);
 // sampling merges the softmax statistics of each row the walk visits.
 __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
   pdl_begin();
-  __shared__ uint64_t s_mbuf[kWalkWarps][256];  // per-warp merge scratch (pieces x keys <= 32 x 8)
-  __shared__ uint64_t s_mtop[kWalkWarps][kMaxK];
+  __shared__ uint64_t s_mbuf[256];  // merge scratch of warp 0 (pieces x keys <= 32 x 8)
+  __shared__ uint64_t s_mtop[kMaxK];
   __shared__ uint64_t s_key[kMaxP];
   __shared__ int64_t s_A, s_base;
   __shared__ float s_m;
@@ -186,39 +185,20 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
   const PieceMap pm(rowA, a.V, G, a.vecel);
   for (int p = tid; p < npos; p += blockDim.x) ws.row_tau[rowbase + p] = 0ull;  // the pass is over
   if (a.mode == DT_GREEDY) {
-    if (a.top8 == nullptr) {
-      // argmax of every used row: the best of its pieces' keys (one load per piece)
-      for (int p = tid; p < npos; p += blockDim.x) {
-        if (s_tok[p] < 0) continue;
-        const RowPieces rp = pm.row(rowbase + p);
-        uint64_t best = 0ull;
-        for (int q0 = 0; q0 < rp.S; q0 += 8) {  // independent loads, eight at a time
-          uint64_t k8[8];
+    // argmax of every used row: the best of its pieces' keys (one load per piece; the top-8 output of
+    // the Graft refresh is merged by verify_top8_kernel before this walk)
+    for (int p = tid; p < npos; p += blockDim.x) {
+      if (s_tok[p] < 0) continue;
+      const RowPieces rp = pm.row(rowbase + p);
+      uint64_t best = 0ull;
+      for (int q0 = 0; q0 < rp.S; q0 += 8) {  // independent loads, eight at a time
+        uint64_t k8[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) k8[u] = q0 + u < rp.S ? ws.partials[rp.slot0 + q0 + u].keys[0] : 0ull;
+        for (int u = 0; u < 8; ++u) k8[u] = q0 + u < rp.S ? ws.partials[rp.slot0 + q0 + u].keys[0] : 0ull;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) best = k8[u] > best ? k8[u] : best;
-        }
-        s_key[p] = best;
+        for (int u = 0; u < 8; ++u) best = k8[u] > best ? k8[u] : best;
       }
-    } else {
-      // the top-8 of every used row (the Graft refresh) and its argmax: one warp per row
-      for (int p = warp; p < npos; p += kWalkWarps) {
-        if (s_tok[p] < 0) {
-          if (lane < 8) a.top8[(rb + p) * 8 + lane] = -1;
-          continue;
-        }
-        const RowPieces rp = pm.row(rowbase + p);
-        float M, sh, sl;
-        if (rp.S > a.maxp) {  // never: the streaming plan bounds the pieces of a row
-          if (lane == 0) set_status(ws.status, DT_DEV_INTERNAL);
-          continue;
-        }
-        warp_merge_row(ws.partials + rp.slot0, rp.S, a.K, s_mbuf[warp], 256, s_mtop[warp], false, M, sh, sl);
-        const uint64_t k = lane < 8 ? s_mtop[warp][lane] : 0ull;
-        if (lane < 8) a.top8[(rb + p) * 8 + lane] = (lane < a.K && k != 0ull) ? (int32_t)key_id(k) : -1;
-        if (lane == 0) s_key[p] = s_mtop[warp][0];
-      }
+      s_key[p] = best;
     }
     __syncthreads();
     for (int p = tid; p < npos; p += blockDim.x) {
@@ -294,7 +274,7 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(WalkArgs a) {
       if (s_tok[cur] < 0 || rp.S > a.maxp) {
         if (lane == 0) set_status(ws.status, s_tok[cur] < 0 ? DT_DEV_BAD_TOKEN : DT_DEV_INTERNAL);
       } else {
-        warp_merge_row(ws.partials + rp.slot0, rp.S, a.K, s_mbuf[0], 256, s_mtop[0], true, M, sh, sl);
+        warp_merge_row(ws.partials + rp.slot0, rp.S, a.K, s_mbuf, 256, s_mtop, true, M, sh, sl);
       }
       if (lane == 0) {
         if (sh != sh || !(M > -INFINITY) || M == INFINITY || !(sh > 0.0f) || sh == INFINITY)
